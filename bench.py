@@ -1,0 +1,530 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of libgemm.so on GB300: TFLOP/s = 2*M*N*K / time.
+
+Default workload (one step = one call of the C ABI): FP16 TN GEMM with
+M = N = K = 8192, A row-major, B column-major, C column-major, FP32
+accumulation, entries N(0,1)*0.1 (seed 2).  The line also reports BF16 and
+FP8-E4M3 at 8192^3 and the FP32 SIMT path at 4096^3, each against its dense
+peak, the end-to-end rate with host buffers, the kernel's roofline fraction,
+the SM clocks seen while timing, and the CPU oracle timed on a bounded sample.
+
+Timing: W untimed warm-up steps, then exactly K steps between a barrier and a
+synchronize on each side, timed with CUDA events on the launching stream.
+Steps rotate over three input sets (3 x 384 MiB, far above the 129 MB L2), so
+no step finds its operands in L2; no flush kernel runs.  Under torchrun each
+rank runs its own replica (weak scaling: the GEMM does not need a collective),
+the time is the maximum over ranks and `value` counts every rank's work.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--sweep]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (2MNK/time) FP16 TN 8192³, BF16, FP8; % of GB300 dense peak"
+UNIT = "TFLOP/s"
+# Best FP16 TN 8192^3 figure on the pages: the tuned 192x224 kernel on an
+# RX 9070 XT, FP16 accumulation ("FP16 GEMM Optimization on AMD RDNA 3 and
+# RDNA 4", "Tuning Further", Table 17).  Another machine: context only.
+PAGES_FP16_8192_TFLOPS = 142.30
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+SETS = 3
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """Largest `value` over all ranks (the job's time is its slowest rank's)."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank's work over the slowest rank's time."""
+    return flops_per_step * steps * world / (max_ms * 1e-3) / 1e12
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling (every 100 ms) around a timed region."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._reader = threading.Thread(target=self._read, daemon=True)
+            self._reader.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.05 <= r[0] <= self.t1 + 0.15]
+        use = inside or rows
+        sm = [float(p[2]) for _, p in use if p[2].replace(".", "").isdigit()]
+        mx = [float(p[3]) for _, p in use if p[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, p in use for i in range(4) if p[6 + i] == "Active"})
+        power = [float(p[4]) for _, p in use if p[4].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons,
+                "samples": len(use), "samples_in_window": len(inside),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------- our implementation
+
+def tn_sets(kind, M, N, K, seed, sigma, nsets, device):
+    """Seeded operands for a TN call, copied into `nsets` distinct buffer sets."""
+    import torch
+
+    import synthetic_inputs as si
+
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=seed, sigma=sigma)
+    out_dt = torch.float16 if kind == "f16" else torch.bfloat16
+    sets = []
+    for _ in range(nsets):
+        a = ops["A"].to(device)
+        b = ops["B"].to(device)
+        c = torch.empty((N, M), dtype=out_dt, device=device)
+        sets.append((a, b, c))
+    return ops, sets
+
+
+def tn_call(kind, M, N, K, scale_a, scale_b, stream_h):
+    from dense_gemm_tcgen05_gb300 import capi
+
+    fns = {"f16": capi.gemm_f16_tn, "bf16": capi.gemm_bf16_tn}
+
+    def call(a, b, c):
+        if kind == "e4m3":
+            st = capi.gemm_fp8_tn(M, N, K, a.data_ptr(), K, b.data_ptr(), K, scale_a, scale_b,
+                                  c.data_ptr(), M, stream_h)
+        else:
+            st = fns[kind](M, N, K, a.data_ptr(), K, b.data_ptr(), K, c.data_ptr(), M, stream_h)
+        if st != 0:
+            raise RuntimeError("gemm call failed: %s" % capi.status_text(st))
+
+    return call
+
+
+def timed_loop(call, sets, steps, warmup, stream, dist=None, sampler=None):
+    """W warm-up steps, then K timed steps; returns (total_ms, mean_launch_ms)."""
+    import torch
+
+    for i in range(warmup):
+        call(*sets[i % len(sets)])
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark(True)
+    t_begin.record(stream)
+    for i in range(steps):
+        starts[i].record(stream)
+        call(*sets[i % len(sets)])
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark(False)
+    barrier(dist)
+    total = t_begin.elapsed_time(t_end)
+    launches = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return total, sum(launches) / len(launches)
+
+
+def e2e_loop(kind, M, N, K, ops, steps, warmup, stream, stream_h):
+    """End to end through the C ABI with host buffers: every step copies A and
+    B from pinned host memory, runs the GEMM and copies C back."""
+    import torch
+
+    ha = ops["A"].pin_memory()
+    hb = ops["B"].pin_memory()
+    out_dt = torch.float16 if kind == "f16" else torch.bfloat16
+    hc = torch.empty((N, M), dtype=out_dt).pin_memory()
+    da = torch.empty_like(ha, device="cuda")
+    db = torch.empty_like(hb, device="cuda")
+    dc = torch.empty((N, M), dtype=out_dt, device="cuda")
+    call = tn_call(kind, M, N, K, ops["scale_a"], ops["scale_b"], stream_h)
+
+    def step():
+        da.copy_(ha, non_blocking=True)
+        db.copy_(hb, non_blocking=True)
+        call(da, db, dc)
+        hc.copy_(dc, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    h2d = ha.numel() * ha.element_size() + hb.numel() * hb.element_size()
+    d2h = hc.numel() * hc.element_size()
+    return ms, h2d, d2h
+
+
+def f32_bench(n, steps, warmup, stream, stream_h):
+    import torch
+
+    import synthetic_inputs as si
+    from dense_gemm_tcgen05_gb300 import capi
+
+    ops = si.f32_operands(n, n, n, dist="uniform", seed=1)
+    sets = [(ops["A"].cuda(), ops["B"].cuda(), torch.empty((n, n), device="cuda"))
+            for _ in range(SETS)]
+
+    def call(a, b, c):
+        st = capi.gemm_f32(n, n, n, a.data_ptr(), n, b.data_ptr(), n, c.data_ptr(), n, stream_h)
+        if st != 0:
+            raise RuntimeError(capi.status_text(st))
+
+    with torch.cuda.stream(stream):
+        total, launch = timed_loop(call, sets, steps, warmup, stream)
+    return launch
+
+
+def cublas_context(M, N, K, dtype, steps, stream):
+    """torch.matmul (cuBLAS) on the same problem, for context only."""
+    import torch
+
+    a = torch.randn((M, K), device="cuda").to(dtype)
+    b = torch.randn((N, K), device="cuda").to(dtype)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            torch.matmul(a, b.t())
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            torch.matmul(a, b.t())
+        t1.record(stream)
+        torch.cuda.synchronize()
+    return 2.0 * M * N * K / (t0.elapsed_time(t1) / steps * 1e-3) / 1e12
+
+
+def sm_count():
+    import torch
+
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def fp32_alu_peak_tflops(sms: int, mhz: float) -> float:
+    """FFMA peak: SMs x 128 FP32 lanes x 2 flops x clock."""
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def cpu_baseline(kind="f16", M=8192, N=8192, K=8192, seed=2, sigma=0.1, budget_s=12.0):
+    """The oracle, as it stands, on a bounded sample of the workload: random
+    output elements of the same problem, each one K-long FP64 dot product."""
+    import oracle
+    import synthetic_inputs as si
+
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=seed, sigma=sigma)
+    a, b = si.codes(ops["A"]), si.codes(ops["B"])
+    count = 512
+    elapsed = 0.0
+    while True:
+        ms, ns = si.sample_positions(M, N, count, seed=seed, edges=False)
+        t0 = time.perf_counter()
+        oracle.gemm_tn_sampled(kind, K, a, K, b, K, ms, ns)
+        elapsed = time.perf_counter() - t0
+        if elapsed >= budget_s or count >= 1 << 26:
+            break
+        count = int(count * min(16.0, max(2.0, budget_s / max(elapsed, 1e-3))))
+    tflops = 2.0 * K * count / elapsed / 1e12
+    return {"value": tflops, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d random output elements of the %s TN %dx%dx%d problem (each a %d-long "
+                      "FP64 dot product), %.1f s" % (count, kind, M, N, K, K, elapsed)}
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    from dense_gemm_tcgen05_gb300 import build as libbuild
+    from dense_gemm_tcgen05_gb300 import capi
+
+    if rank == 0 or world == 1:
+        libbuild.build()
+    barrier(dist)
+    capi.lib()
+    peaks, peak_src = load_peaks()
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    stream = torch.cuda.Stream()
+    stream_h = stream.cuda_stream
+    M = N = K = 8192
+    flops = 2.0 * M * N * K
+
+    ops, sets = tn_sets("f16", M, N, K, seed=2, sigma=0.1, nsets=SETS, device="cuda")
+    call = tn_call("f16", M, N, K, 1.0, 1.0, stream_h)
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        total_ms, launch_ms = timed_loop(call, sets, args.steps, args.warmup, stream, dist,
+                                         sampler)
+    clocks = sampler.stop() if sampler else None
+    max_ms = max_over_ranks(dist, total_ms, device="cuda")
+    value = aggregate_tflops(flops, args.steps, world, max_ms)
+    achieved = flops / (launch_ms * 1e-3) / 1e12
+    del sets
+    torch.cuda.empty_cache()
+
+    result = None
+    if rank == 0 and args.only_main:
+        result = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+                  "steps": args.steps, "warmup": args.warmup,
+                  "ms_per_step": round(max_ms / args.steps, 5), "higher_is_better": True,
+                  "scaling": "weak", "note": "--only-main: main workload only (profiling runs)",
+                  "roofline": {"achieved": round(achieved, 1), "peak": burst}}
+    elif rank == 0:
+        per = {}
+        sub_steps = max(10, min(args.steps, 50))
+        for kind, peak in (("bf16", burst), ("e4m3", burst * FP8_OVER_BF16)):
+            o, s = tn_sets(kind, M, N, K, seed=4 if kind == "e4m3" else 3,
+                           sigma=1.0 if kind == "e4m3" else 0.05, nsets=SETS, device="cuda")
+            c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h)
+            with torch.cuda.stream(stream):
+                _, lm = timed_loop(c, s, sub_steps, 3, stream)
+            tf = flops / (lm * 1e-3) / 1e12
+            per[kind + "_tn_8192"] = {"tflops": round(tf, 1), "peak": round(peak, 1),
+                                      "frac": round(tf / peak, 4)}
+            del s
+            torch.cuda.empty_cache()
+        lm = f32_bench(4096, sub_steps, 3, stream, stream_h)
+        tf = 2.0 * 4096 ** 3 / (lm * 1e-3) / 1e12
+        clk = clocks.get("sm_max_mhz") if clocks and clocks.get("sm_max_mhz") else 2070.0
+        fpk = fp32_alu_peak_tflops(sm_count(), clk)
+        per["f32_simt_4096"] = {"tflops": round(tf, 2), "peak": round(fpk, 1),
+                                "frac": round(tf / fpk, 4), "bound": "alu"}
+        per["cublas_context_f16_8192"] = round(cublas_context(M, N, K, torch.float16, 20, stream), 1)
+        if args.sweep:
+            per.update(sweep(stream, stream_h, burst))
+
+        e2e_steps = max(3, min(args.steps, 20))
+        e_ms, h2d, d2h = e2e_loop("f16", M, N, K, ops, e2e_steps, 2, stream, stream_h)
+        traffic = load_traffic()
+        result = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5),
+            "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": round(value / PAGES_FP16_8192_TFLOPS, 2),
+            "dtype": "f16", "data": "synthetic",
+            "config": {"workload": "fp16_tn_8192x8192x8192", "M": M, "N": N, "K": K,
+                       "layout": "TN: A row-major, B column-major, C column-major (ld=M)",
+                       "accumulate": "f32", "values": "N(0,1)*0.1, seed 2",
+                       "l2": "3 rotating input sets (1.1 GiB total) >> 129 MB L2, no flush",
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "vs_baseline_ref": "pages' best FP16 8192^3: 142.30 TFLOP/s, RX 9070 XT"},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": burst,
+                         "unit": UNIT, "frac": round(achieved / burst, 4),
+                         "traffic": traffic, "peak_source": peak_src + " bf16 burst (fp16 rate)"},
+            "e2e": {"value": round(flops / (e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "per_dtype": per,
+        }
+        if not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline()
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def sweep(stream, stream_h, burst):
+    """The BF16 and FP8 shape sweeps (configs 4 and 5), one line each."""
+    import torch
+
+    out = {}
+    shapes = [("bf16", (4096, 4096, 4096)), ("bf16", (4096, 14336, 4096)),
+              ("bf16", (4096, 4096, 14336)), ("bf16", (8191, 8191, 8191)),
+              ("e4m3", (4096, 14336, 4096)), ("e4m3", (16384, 4096, 4096))]
+    for kind, (M, N, K) in shapes:
+        o, s = tn_sets(kind, M, N, K, seed=4 if kind == "e4m3" else 3,
+                       sigma=1.0 if kind == "e4m3" else 0.05, nsets=SETS, device="cuda")
+        c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h)
+        with torch.cuda.stream(stream):
+            _, lm = timed_loop(c, s, 20, 3, stream)
+        tf = 2.0 * M * N * K / (lm * 1e-3) / 1e12
+        peak = burst * (FP8_OVER_BF16 if kind == "e4m3" else 1.0)
+        out["%s_%dx%dx%d" % (kind, M, N, K)] = {"tflops": round(tf, 1), "frac": round(tf / peak, 4)}
+        del s
+        torch.cuda.empty_cache()
+    return out
+
+
+def load_traffic():
+    """DRAM bytes per launch of the main kernel from the committed ncu summary
+    (profiles/tc_gemm_f16_8192.txt), or None when there is none."""
+    path = os.path.join(ROOT, "profiles", "tc_gemm_f16_8192.txt")
+    try:
+        for line in open(path):
+            if line.startswith("traffic_bytes_per_launch:"):
+                return int(float(line.split(":", 1)[1].strip()))
+    except OSError:
+        pass
+    return None
+
+
+# -------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The oracle on the host cores, on the same metric and workload: each step
+    is a bounded sample of the FP16 8192^3 problem."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    import synthetic_inputs as si
+
+    M = N = K = 8192
+    ops = si.tn_operands("f16", M, N, K, dist="normal", seed=2, sigma=0.1)
+    a, b = si.codes(ops["A"]), si.codes(ops["B"])
+    per_step = 2048
+    times = []
+    for i in range(args.warmup + args.steps):
+        ms, ns = si.sample_positions(M, N, per_step, seed=100 + i, edges=False)
+        t0 = time.perf_counter()
+        oracle.gemm_tn_sampled("f16", K, a, K, b, K, ms, ns)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = 2.0 * K * per_step * len(times) / total / 1e12
+    sample = ("%d random output elements per step of the f16 TN 8192^3 problem (each an "
+              "8192-long FP64 dot product)" % per_step)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total / len(times) * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "fp16_tn_8192x8192x8192", "M": M, "N": N, "K": K},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sweep", action="store_true", help="add the BF16/FP8 shape sweeps")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-main", action="store_true",
+                    help="time the main workload only (for profiler runs)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        out = run_reference(args)
+    else:
+        out = run_ours(args)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

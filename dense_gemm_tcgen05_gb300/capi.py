@@ -1,0 +1,124 @@
+"""ctypes binding of libgemm.so with the C ABI's own names and arguments.
+
+Argument marshalling only: every function forwards integers, floats and raw
+device pointers (Python ints) to the library and returns its status code.  The
+library must have been built (``dense_gemm_tcgen05_gb300.build``); loading
+fails loudly otherwise -- there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from . import build as _build
+
+LIB_PATH = _build.LIB
+HEADER = os.path.join(_build.INCLUDE, "gemm.h")
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_DIM = 1
+GEMM_ERR_INVALID_LD = 2
+GEMM_ERR_NULL_PTR = 3
+GEMM_ERR_MISALIGNED = 4
+GEMM_ERR_UNSUPPORTED_DEVICE = 5
+GEMM_ERR_LAUNCH = 6
+GEMM_ERR_TIMEOUT = 7
+GEMM_ERR_INVALID_OPTION = 8
+
+_lock = threading.Lock()
+_lib = None
+
+_i64, _f32, _vp, _int = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
+_SIGNATURES = {
+    "gemm_f32": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp], _int),
+    "gemm_f16_tn": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp], _int),
+    "gemm_bf16_tn": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp], _int),
+    "gemm_fp8_tn": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _f32, _f32, _vp, _i64, _vp], _int),
+    "gemm_status_string": ([_int], ctypes.c_char_p),
+    "gemm_read_watchdog": ([_int], _int),
+    "gemm_set_option": ([ctypes.c_char_p, _i64], _int),
+    "gemm_tile_coord": ([_i64, _i64, _i64, _i64, ctypes.POINTER(_i64), ctypes.POINTER(_i64)], _int),
+    "gemm_watchdog_selftest": ([_i64, _vp], _int),
+}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        super().__init__("%s failed: status %d (%s)" % (where or "gemm", status, status_text(status)))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library.  Raises if libgemm.so has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    "libgemm.so is missing (%s); build it with "
+                    "`python -m dense_gemm_tcgen05_gb300.build`" % LIB_PATH)
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (args, res) in _SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = handle
+        return _lib
+
+
+def declared_symbols() -> list[str]:
+    """Function names declared in include/gemm.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(gemm_\w+)\s*\(", text, re.M)))
+
+
+def status_text(status: int) -> str:
+    try:
+        return lib().gemm_status_string(int(status)).decode()
+    except Exception:  # pragma: no cover - library not loadable
+        return "status %d" % status
+
+
+def _p(x) -> int | None:
+    return None if x is None else int(x)
+
+
+def gemm_f32(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
+    return lib().gemm_f32(M, N, K, _p(A), lda, _p(B), ldb, _p(C), ldc, _p(stream))
+
+
+def gemm_f16_tn(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
+    return lib().gemm_f16_tn(M, N, K, _p(A), lda, _p(B), ldb, _p(C), ldc, _p(stream))
+
+
+def gemm_bf16_tn(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
+    return lib().gemm_bf16_tn(M, N, K, _p(A), lda, _p(B), ldb, _p(C), ldc, _p(stream))
+
+
+def gemm_fp8_tn(M, N, K, A, lda, B, ldb, scale_a, scale_b, C, ldc, stream=None) -> int:
+    return lib().gemm_fp8_tn(M, N, K, _p(A), lda, _p(B), ldb, float(scale_a), float(scale_b),
+                             _p(C), ldc, _p(stream))
+
+
+def gemm_status_string(status: int) -> str:
+    return status_text(status)
+
+
+def gemm_read_watchdog(reset: int = 0) -> int:
+    return lib().gemm_read_watchdog(int(reset))
+
+
+def gemm_set_option(name: str, value: int) -> int:
+    return lib().gemm_set_option(name.encode(), int(value))
+
+
+def gemm_tile_coord(t: int, tiles_m: int, tiles_n: int, group: int):
+    tm, tn = _i64(), _i64()
+    st = lib().gemm_tile_coord(t, tiles_m, tiles_n, group, ctypes.byref(tm), ctypes.byref(tn))
+    return st, tm.value, tn.value
+
+
+def gemm_watchdog_selftest(limit_ns: int, stream=None) -> int:
+    return lib().gemm_watchdog_selftest(int(limit_ns), _p(stream))

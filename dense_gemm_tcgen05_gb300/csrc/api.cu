@@ -1,0 +1,326 @@
+// api.cu -- the C ABI of libgemm.so (declared in include/gemm.h): argument
+// validation, device checks, path choice, TMA tensor-map encoding and launch.
+//
+// Nothing here allocates device memory.  Tensor maps are encoded on the host
+// per call (a few hundred nanoseconds) and passed by value as
+// __grid_constant__ kernel parameters.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "common.h"
+#include "gemm.h"
+#include "raster.h"
+
+namespace gb300 {
+cudaError_t tc_launch_f16(bool pair, const TcLaunch& L);
+cudaError_t tc_launch_bf16(bool pair, const TcLaunch& L);
+cudaError_t tc_launch_fp8(bool pair, const TcLaunch& L);
+TcGeometry tc_geometry_f16(bool pair);
+TcGeometry tc_geometry_bf16(bool pair);
+TcGeometry tc_geometry_fp8(bool pair);
+
+TcGeometry tc_geometry(InKind in, bool pair) {
+    switch (in) {
+        case InKind::F16: return tc_geometry_f16(pair);
+        case InKind::BF16: return tc_geometry_bf16(pair);
+        default: return tc_geometry_fp8(pair);
+    }
+}
+
+cudaError_t tc_launch(InKind in, bool pair, const TcLaunch& L) {
+    switch (in) {
+        case InKind::F16: return tc_launch_f16(pair, L);
+        case InKind::BF16: return tc_launch_bf16(pair, L);
+        default: return tc_launch_fp8(pair, L);
+    }
+}
+}  // namespace gb300
+
+using namespace gb300;
+
+// Per-device watchdog word: kernels OR kWatchTimeout into it when a bounded
+// wait runs out.  Its device address is looked up once per device.
+__device__ unsigned int g_gemm_watchdog_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int cc_major = 0, cc_minor = 0, sms = 0;
+    unsigned int* watchdog = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+std::atomic<int> g_opt_pair{-1};
+std::atomic<int> g_opt_group{8};
+std::atomic<int> g_opt_path{0};
+std::atomic<int> g_opt_max_ctas{0};
+std::atomic<int64_t> g_opt_timeout_ns{2000000000LL};
+
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+thread_local char t_status_buf[256];
+
+int fail_cuda(cudaError_t e) {
+    t_last_cuda_error = e;
+    return GEMM_ERR_LAUNCH;
+}
+
+// Looks up (once) the attributes of the current device.  Returns a status.
+int current_device(const DeviceInfo** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (!d.ready) {
+        if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+                cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) !=
+                cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) !=
+                cudaSuccess)
+            return fail_cuda(e);
+        if (d.cc_major == 10 && d.cc_minor == 3) {
+            void* p = nullptr;
+            if ((e = cudaGetSymbolAddress(&p, g_gemm_watchdog_word)) != cudaSuccess)
+                return fail_cuda(e);
+            d.watchdog = static_cast<unsigned int*>(p);
+        }
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q);
+            if (e != cudaSuccess) return fail_cuda(e);
+            if (q != cudaDriverEntryPointSuccess || !fn) return fail_cuda(cudaErrorNotSupported);
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.ready = true;
+    }
+    if (!(d.cc_major == 10 && d.cc_minor == 3)) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    *out = &d;
+    return GEMM_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+constexpr int64_t kMaxDim = 0x7fffffffLL;
+
+// 2D tensor map over a matrix with `outer` rows of `inner` contiguous elements
+// and a row pitch of `pitch_bytes`, copied in boxes of box_inner x box_outer
+// with 128-byte swizzling and zero fill outside the matrix.
+CUresult encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, int64_t inner,
+                   int64_t outer, int64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_bytes)};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+int gemm_tn(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+            const void* B, int64_t ldb, float scale, void* C, int64_t ldc, void* stream_v) {
+    const int es = in == InKind::E4M3 ? 1 : 2;
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return GEMM_ERR_INVALID_DIM;
+    const int64_t kmin = K > 1 ? K : 1;
+    if (lda < kmin || ldb < kmin || ldc < (M > 1 ? M : 1)) return GEMM_ERR_INVALID_LD;
+    if ((M > 0 && K > 0 && !A) || (N > 0 && K > 0 && !B) || (M > 0 && N > 0 && !C))
+        return GEMM_ERR_NULL_PTR;
+    if (!aligned(A, es) || !aligned(B, es) || !aligned(C, 2)) return GEMM_ERR_MISALIGNED;
+    const DeviceInfo* dev = nullptr;
+    int st = current_device(&dev);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    cudaError_t e;
+    if (K == 0) {
+        e = zero_fill_launch(C, N, M, ldc, 2, stream);
+        return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
+    }
+
+    const bool tma_ok = g_opt_path.load() == 0 && aligned(A, 16) && aligned(B, 16) &&
+                        aligned(C, 16) && (lda * es) % 16 == 0 && (ldb * es) % 16 == 0 &&
+                        (ldc * 2) % 16 == 0 && lda * es < (1LL << 40) && ldb * es < (1LL << 40) &&
+                        ldc * 2 < (1LL << 40);
+    if (!tma_ok) {
+        e = tn_fallback_launch(in, M, N, K, A, lda, B, ldb, scale, C, ldc, stream);
+        return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
+    }
+
+    const int opt_pair = g_opt_pair.load();
+    const bool pair = opt_pair == 1;  // automatic choice: one CTA per tile
+    const TcGeometry g = tc_geometry(in, pair);
+    TcLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    const CUtensorMapDataType in_dt = in == InKind::F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                      : in == InKind::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const CUtensorMapDataType out_dt =
+        in == InKind::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    // P = B: N rows of K contiguous elements.  Q = A: M rows of K.  Out = C: N rows of M.
+    CUresult r = encode_2d(&L.map_p, in_dt, B, K, N, ldb * es, g.stage_k, g.load_p);
+    if (r == CUDA_SUCCESS) r = encode_2d(&L.map_q, in_dt, A, K, M, lda * es, g.stage_k, g.load_q);
+    if (r == CUDA_SUCCESS) r = encode_2d(&L.map_out, out_dt, C, M, N, ldc * 2, 64, 32);
+    if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
+
+    const int64_t tiles_p = (N + g.tile_p - 1) / g.tile_p;
+    const int64_t tiles_q = (M + g.tile_q - 1) / g.tile_q;
+    const int64_t tiles = tiles_p * tiles_q;
+    int64_t slots = dev->sms / g.cluster;
+    const int cap = g_opt_max_ctas.load();
+    if (cap > 0 && cap / g.cluster < slots) slots = cap / g.cluster > 0 ? cap / g.cluster : 1;
+    const int64_t ctas = (tiles < slots ? tiles : slots) * g.cluster;
+
+    L.prm.rows_p = static_cast<int32_t>(N);
+    L.prm.rows_q = static_cast<int32_t>(M);
+    L.prm.num_kb = static_cast<int32_t>((K + g.stage_k - 1) / g.stage_k);
+    L.prm.tiles_p = static_cast<int32_t>(tiles_p);
+    L.prm.tiles_q = static_cast<int32_t>(tiles_q);
+    L.prm.group = g_opt_group.load();
+    L.prm.scale = scale;
+    L.prm.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
+    L.prm.watchdog = dev->watchdog;
+    L.prm.out = C;
+    L.prm.ld_out = ldc;
+    L.grid = static_cast<int>(ctas);
+    L.stream = stream;
+    if (std::getenv("GEMM_DEBUG"))
+        std::fprintf(stderr,
+                     "[gemm] tn in=%d M=%lld N=%lld K=%lld pair=%d tiles=%lldx%lld grid=%d\n",
+                     int(in), (long long)M, (long long)N, (long long)K, int(pair),
+                     (long long)tiles_q, (long long)tiles_p, L.grid);
+    e = tc_launch(in, pair, L);
+    return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
+             int64_t ldb, float* C, int64_t ldc, void* stream_v) {
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return GEMM_ERR_INVALID_DIM;
+    const int64_t nmin = N > 1 ? N : 1;
+    if (lda < (K > 1 ? K : 1) || ldb < nmin || ldc < nmin) return GEMM_ERR_INVALID_LD;
+    if ((M > 0 && K > 0 && !A) || (N > 0 && K > 0 && !B) || (M > 0 && N > 0 && !C))
+        return GEMM_ERR_NULL_PTR;
+    if (!aligned(A, 4) || !aligned(B, 4) || !aligned(C, 4)) return GEMM_ERR_MISALIGNED;
+    const DeviceInfo* dev = nullptr;
+    int st = current_device(&dev);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    cudaError_t e = K == 0 ? zero_fill_launch(C, M, N, ldc, 4, stream)
+                           : f32_launch(M, N, K, A, lda, B, ldb, C, ldc, stream);
+    return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
+}
+
+int gemm_f16_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                int64_t ldb, void* C, int64_t ldc, void* stream) {
+    return gemm_tn(InKind::F16, M, N, K, A, lda, B, ldb, 1.0f, C, ldc, stream);
+}
+
+int gemm_bf16_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                 int64_t ldb, void* C, int64_t ldc, void* stream) {
+    return gemm_tn(InKind::BF16, M, N, K, A, lda, B, ldb, 1.0f, C, ldc, stream);
+}
+
+int gemm_fp8_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                int64_t ldb, float scale_a, float scale_b, void* C, int64_t ldc, void* stream) {
+    const float scale = scale_a * scale_b;  // one FP32 product, applied in the epilogue
+    return gemm_tn(InKind::E4M3, M, N, K, A, lda, B, ldb, scale, C, ldc, stream);
+}
+
+const char* gemm_status_string(int status) {
+    switch (status) {
+        case GEMM_OK: return "ok";
+        case GEMM_ERR_INVALID_DIM: return "invalid dimension (negative or above 2^31-1)";
+        case GEMM_ERR_INVALID_LD: return "leading dimension below its minimum";
+        case GEMM_ERR_NULL_PTR: return "null matrix pointer with a nonzero extent";
+        case GEMM_ERR_MISALIGNED: return "pointer not aligned to its element size";
+        case GEMM_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3";
+        case GEMM_ERR_LAUNCH:
+            std::snprintf(t_status_buf, sizeof(t_status_buf), "CUDA error: %s",
+                          cudaGetErrorString(t_last_cuda_error));
+            return t_status_buf;
+        case GEMM_ERR_TIMEOUT: return "a device-side wait ran out of time";
+        case GEMM_ERR_INVALID_OPTION: return "unknown option or value out of range";
+        default: return "unknown status";
+    }
+}
+
+int gemm_read_watchdog(int reset) {
+    const DeviceInfo* dev = nullptr;
+    int st = current_device(&dev);
+    if (st != GEMM_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e);
+    unsigned int word = 0;
+    e = cudaMemcpy(&word, dev->watchdog, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (reset) {
+        e = cudaMemset(dev->watchdog, 0, sizeof(word));
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return fail_cuda(e);
+    }
+    return word ? GEMM_ERR_TIMEOUT : GEMM_OK;
+}
+
+int gemm_set_option(const char* name, int64_t value) {
+    if (!name) return GEMM_ERR_INVALID_OPTION;
+    if (!std::strcmp(name, "pair")) {
+        if (value < -1 || value > 1) return GEMM_ERR_INVALID_OPTION;
+        g_opt_pair.store(static_cast<int>(value));
+    } else if (!std::strcmp(name, "group")) {
+        if (value < 1 || value > 64) return GEMM_ERR_INVALID_OPTION;
+        g_opt_group.store(static_cast<int>(value));
+    } else if (!std::strcmp(name, "path")) {
+        if (value < 0 || value > 1) return GEMM_ERR_INVALID_OPTION;
+        g_opt_path.store(static_cast<int>(value));
+    } else if (!std::strcmp(name, "timeout_ns")) {
+        if (value < 1000000LL || value > 60000000000LL) return GEMM_ERR_INVALID_OPTION;
+        g_opt_timeout_ns.store(value);
+    } else if (!std::strcmp(name, "max_ctas")) {
+        if (value < 0 || value > 1 << 20) return GEMM_ERR_INVALID_OPTION;
+        g_opt_max_ctas.store(static_cast<int>(value));
+    } else {
+        return GEMM_ERR_INVALID_OPTION;
+    }
+    return GEMM_OK;
+}
+
+int gemm_tile_coord(int64_t t, int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t* tm,
+                    int64_t* tn) {
+    if (tiles_m <= 0 || tiles_n <= 0 || group <= 0 || t < 0 || t >= tiles_m * tiles_n || !tm ||
+        !tn)
+        return GEMM_ERR_INVALID_DIM;
+    raster_tile(t, tiles_m, tiles_n, group, tm, tn);
+    return GEMM_OK;
+}
+
+int gemm_watchdog_selftest(int64_t limit_ns, void* stream) {
+    if (limit_ns < 100000LL || limit_ns > 10000000000LL) return GEMM_ERR_INVALID_OPTION;
+    const DeviceInfo* dev = nullptr;
+    int st = current_device(&dev);
+    if (st != GEMM_OK) return st;
+    cudaError_t e = watchdog_selftest_launch(static_cast<uint64_t>(limit_ns), dev->watchdog,
+                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// common.h -- host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gb300 {
+
+enum class InKind : int { F16 = 0, BF16 = 1, E4M3 = 2 };
+
+// Watchdog status bits recorded by kernels whose bounded waits ran out.
+constexpr unsigned int kWatchTimeout = 1u;
+
+// Parameters of the persistent tensor-core kernel.  "P" is the operand whose
+// rows become TMEM lanes (the API's B, rows n), "Q" the operand whose rows
+// become accumulator columns (the API's A, rows m).  The kernel computes
+// D[i][j] = sum_k P[i][k] * Q[j][k] and stores D row-major, which is exactly
+// the column-major C of the TN layout.
+struct TcParams {
+    int32_t rows_p;      // N
+    int32_t rows_q;      // M
+    int32_t num_kb;      // K stages per tile: ceil(K / stage depth)
+    int32_t tiles_p;     // tiles along P
+    int32_t tiles_q;     // tiles along Q (the grouped dimension)
+    int32_t group;       // rasteriser group size, in tiles along Q
+    float scale;         // epilogue scale (FP8 per-tensor scales; 1 otherwise)
+    uint64_t timeout_ns; // limit for every wait
+    unsigned int* watchdog;
+    void* out;           // D (= C) base pointer, for the ragged-edge stores
+    int64_t ld_out;      // D row pitch in elements (= ldc)
+};
+
+struct TcLaunch {
+    CUtensorMap map_p, map_q, map_out;
+    TcParams prm;
+    int grid;
+    cudaStream_t stream;
+};
+
+// Tile geometry of one persistent CTA (or CTA pair), for the host's grid sizing.
+struct TcGeometry {
+    int tile_p, tile_q;    // output tile of one CTA (or CTA pair)
+    int load_q, load_p;    // TMA box rows each CTA loads per stage
+    int stage_k;           // K elements per stage
+    int cluster;           // CTAs per tile
+};
+
+TcGeometry tc_geometry(InKind in, bool pair);
+cudaError_t tc_launch(InKind in, bool pair, const TcLaunch& L);
+
+// CUDA-core fallback for TN operands that TMA cannot address.
+cudaError_t tn_fallback_launch(InKind in, int64_t M, int64_t N, int64_t K, const void* A,
+                               int64_t lda, const void* B, int64_t ldb, float scale, void* C,
+                               int64_t ldc, cudaStream_t stream);
+
+cudaError_t f32_launch(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                       const float* B, int64_t ldb, float* C, int64_t ldc, cudaStream_t stream);
+
+// Writes zeros into a rows x cols block with leading dimension ld (elements of
+// elem_bytes bytes); used for K == 0.
+cudaError_t zero_fill_launch(void* C, int64_t rows, int64_t cols, int64_t ld, int elem_bytes,
+                             cudaStream_t stream);
+
+cudaError_t watchdog_selftest_launch(uint64_t limit_ns, unsigned int* watchdog,
+                                     cudaStream_t stream);
+
+}  // namespace gb300

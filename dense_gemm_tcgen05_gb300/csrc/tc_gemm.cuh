@@ -1,0 +1,457 @@
+// tc_gemm.cuh -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+// Computes D[i][j] = sum_k P[i][k] * Q[j][k] (both operands K-major) with FP32
+// accumulators in tensor memory and stores D row-major.  With P = B (rows n)
+// and Q = A (rows m) this is the TN product C = A x B with C column-major
+// ("FP16 GEMM Optimization on AMD RDNA 3 and RDNA 4", "What We Are
+// Computing"), so the epilogue's contiguous dimension is C's leading one.
+//
+// Structure (one CTA per SM, or one CTA pair per two SMs with cta_group::2):
+//   warp 0      TMA producer: fills a ring of kStages shared-memory stages with
+//               128-byte-swizzled tiles of P and Q; each stage is one 128-byte
+//               swizzle atom deep in K (64 fp16/bf16 or 128 e4m3 values).
+//               Out-of-range rows and K columns are zero-filled by TMA, which
+//               is what makes ragged M, N and K work without special cases.
+//   warp 1      allocates tensor memory; one lane issues tcgen05.mma (4 per
+//               stage) and releases each stage with tcgen05.commit as soon as
+//               its MMAs are issued.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator, conversion (and FP8
+//               scaling) in registers, swizzled shared-memory staging, TMA
+//               store.  Two accumulators (2 x 256 TMEM columns) let the
+//               epilogue of one tile overlap the main loop of the next.
+// Tiles are visited in the grouped order of raster.h.
+//
+// Correspondence with the pages' ladders: the staged shared-memory pipeline
+// stands in for "Step 2: Tiling for Reuse and a Software Pipeline"; TMA's
+// swizzle replaces LDS padding ("Step 3: Avoiding LDS Bank Conflicts"); TMA's
+// zero fill replaces buffer resource descriptors ("Step 4"); one swizzle atom
+// of K per stage, and twice as many FP8 values per stage, follow "Step 5:
+// Trading Tile Area for K Depth" and the FP8 page's deeper-K configurations;
+// the mbarrier handshakes follow the Helios ladder's asynchronous loads and
+// split barriers (Levels 2 and 8), and the staged epilogue its Level 10.
+//
+// Every wait is bounded (see warp_wait): when a limit runs out the kernel
+// records a timeout in the watchdog word, all roles leave their loops, and the
+// CTA waits for its own copies and MMAs before freeing tensor memory.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.h"
+#include "ptx.cuh"
+#include "raster.h"
+
+namespace gb300 {
+
+template <InKind IN, bool PAIR>
+struct TcCfg {
+    static constexpr int kCG = PAIR ? 2 : 1;
+    static constexpr int kElemBytes = IN == InKind::E4M3 ? 1 : 2;
+    static constexpr int kBlockP = 128;              // accumulator rows per CTA (TMEM lanes)
+    static constexpr int kMmaM = PAIR ? 256 : 128;   // M of one MMA instruction
+    static constexpr int kMmaN = 256;                // N of one MMA instruction
+    static constexpr int kTileP = kMmaM;             // P rows per tile (per pair)
+    static constexpr int kTileQ = kMmaN;             // Q rows per tile
+    static constexpr int kLoadQ = PAIR ? 128 : 256;  // Q rows each CTA loads
+    static constexpr int kAtomBytes = 128;           // K bytes per stage row
+    static constexpr int kStageK = kAtomBytes / kElemBytes;
+    static constexpr int kMmaKBytes = 32;            // K bytes per MMA (16 x 16-bit, 32 x 8-bit)
+    static constexpr int kMmasPerStage = kAtomBytes / kMmaKBytes;
+    static constexpr int kBytesP = kBlockP * kAtomBytes;
+    static constexpr int kBytesQ = kLoadQ * kAtomBytes;
+    static constexpr int kStageBytes = kBytesP + kBytesQ;
+    static constexpr int kStages = PAIR ? 6 : 4;
+    static constexpr int kEpiWarps = 4;
+    static constexpr int kEpiCols = 64;                      // columns per staged chunk
+    static constexpr int kEpiBufBytes = 32 * kEpiCols * 2;   // 32 rows x 64 16-bit values
+    static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+    static constexpr int kThreads = 192;
+    static constexpr int kAccCols = kMmaN;
+    static constexpr int kTmemCols = 512;
+    static constexpr int kNumBars = 2 * kStages + 4 + 1;
+    static constexpr int kOffEpi = kStages * kStageBytes;
+    static constexpr int kOffBars = kOffEpi + kEpiBytes;
+    static constexpr int kOffTmemSlot = kOffBars + kNumBars * 8;
+    static constexpr int kOffAbort = kOffTmemSlot + 4;
+    static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
+    static constexpr uint32_t kFormat = IN == InKind::BF16 ? 1u : 0u;
+    static constexpr uint32_t kIdesc = make_idesc(kFormat, kMmaM, kMmaN);
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kStageBytes % 1024 == 0 && kBytesP % 1024 == 0, "1024-byte stage alignment");
+};
+
+// Bounded-wait bookkeeping shared by a CTA's warps.
+struct Watch {
+    volatile int* abort_flag;   // shared memory: set when any warp gives up
+    unsigned int* word;         // global watchdog word read by the host
+    uint64_t limit_ns;
+};
+
+// Warp-collective wait for barrier phase `parity`.  Returns false (on every
+// lane) when the CTA is aborting or this wait exceeded the limit; in the latter
+// case the abort flag and the watchdog word are set.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Watch& w) {
+    uint64_t t0 = 0;
+    for (uint32_t spin = 1;; ++spin) {
+        const bool ok = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, ok)) return true;
+        if ((spin & 63u) == 0) {
+            int give_up = 0;
+            if (lane_idx() == 0) {
+                if (*w.abort_flag) {
+                    give_up = 1;
+                } else {
+                    const uint64_t now = global_timer_ns();
+                    if (t0 == 0) {
+                        t0 = now;
+                    } else if (now - t0 > w.limit_ns) {
+                        *w.abort_flag = 1;
+                        atomicOr(w.word, kWatchTimeout);
+                        give_up = 1;
+                    }
+                }
+            }
+            if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+        }
+    }
+}
+
+// Bounded pause used on the abort path only.
+__device__ __forceinline__ void pause_ns(uint64_t ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < ns) {
+    }
+}
+
+template <int CG>
+__device__ __forceinline__ void commit_to(uint32_t bar, uint16_t mask) {
+    if constexpr (CG == 1)
+        tc_commit(bar);
+    else
+        tc_commit_pair(bar, mask);
+}
+
+template <typename OutT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+template <InKind IN, typename OutT, bool PAIR>
+__global__ void __launch_bounds__(192, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
+                   const __grid_constant__ CUtensorMap map_q,
+                   const __grid_constant__ CUtensorMap map_out, const TcParams prm) {
+    using Cfg = TcCfg<IN, PAIR>;
+    constexpr int S = Cfg::kStages;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+
+    const uint32_t warp = warp_idx();
+    const uint32_t lane = lane_idx();
+    const uint32_t bars = base + Cfg::kOffBars;
+    auto full_bar = [&](uint32_t s) { return bars + 8u * s; };
+    auto empty_bar = [&](uint32_t s) { return bars + 8u * (S + s); };
+    auto accf_bar = [&](uint32_t b) { return bars + 8u * (2 * S + b); };
+    auto acce_bar = [&](uint32_t b) { return bars + 8u * (2 * S + 2 + b); };
+    const uint32_t done_bar = bars + 8u * (2 * S + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Cfg::kOffTmemSlot);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Cfg::kOffAbort);
+
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), (PAIR ? 2 : 1) * Cfg::kEpiWarps);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&map_p);
+        prefetch_tensormap(&map_q);
+        prefetch_tensormap(&map_out);
+    }
+    if (warp == 1) {
+        tmem_alloc<Cfg::kCG>(smem_u32(tmem_slot), Cfg::kTmemCols);
+        tmem_relinquish<Cfg::kCG>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if constexpr (PAIR) cluster_sync();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+    const Watch wd{abort_flag, prm.watchdog, prm.timeout_ns};
+    const int64_t num_tiles = static_cast<int64_t>(prm.tiles_p) * prm.tiles_q;
+    const int64_t first = PAIR ? blockIdx.x / 2 : blockIdx.x;
+    const int64_t stride = PAIR ? gridDim.x / 2 : gridDim.x;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t t = first; ok && t < num_tiles; t += stride) {
+            int64_t tq, tp;
+            raster_tile(t, prm.tiles_q, prm.tiles_p, prm.group, &tq, &tp);
+            const int32_t p0 = static_cast<int32_t>(tp * Cfg::kTileP + rank * Cfg::kBlockP);
+            const int32_t q0 = static_cast<int32_t>(tq * Cfg::kTileQ + rank * Cfg::kLoadQ);
+            for (int32_t kb = 0; kb < prm.num_kb; ++kb, ++it) {
+                const uint32_t s = it % S, ph = (it / S) & 1u;
+                if (!warp_wait(empty_bar(s), ph ^ 1u, wd)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t sp = base + s * Cfg::kStageBytes;
+                    const uint32_t sq = sp + Cfg::kBytesP;
+                    const int32_t kx = kb * Cfg::kStageK;
+                    if constexpr (PAIR) {
+                        const uint32_t fb = mapa_shared(full_bar(s), 0);
+                        if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * Cfg::kStageBytes);
+                        tma_load_2d_pair(sp, &map_p, fb, kx, p0);
+                        tma_load_2d_pair(sq, &map_q, fb, kx, q0);
+                    } else {
+                        mbar_arrive_expect_tx(full_bar(s), Cfg::kStageBytes);
+                        tma_load_2d(sp, &map_p, full_bar(s), kx, p0);
+                        tma_load_2d(sq, &map_q, full_bar(s), kx, q0);
+                    }
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok) {
+            // Aborting: let this CTA's own copies still in flight land before
+            // the CTA can exit.
+            if constexpr (PAIR) {
+                if (lane == 0) pause_ns(200000);
+            } else {
+                const uint32_t outstanding = it < static_cast<uint32_t>(S) ? it : S;
+                const Watch drain{abort_flag, prm.watchdog, prm.timeout_ns};
+                for (uint32_t i = it - outstanding; i < it; ++i) {
+                    uint64_t t0 = global_timer_ns();
+                    while (!__all_sync(0xffffffffu, mbar_try_wait(full_bar(i % S), (i / S) & 1u))) {
+                        if (global_timer_ns() - t0 > drain.limit_ns) break;
+                    }
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (!PAIR || leader) {
+            uint32_t it = 0, lt = 0;
+            bool ok = true;
+            for (int64_t t = first; ok && t < num_tiles; t += stride, ++lt) {
+                const uint32_t b = lt & 1u, aph = (lt >> 1) & 1u;
+                if (!warp_wait(acce_bar(b), aph ^ 1u, wd)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + b * Cfg::kAccCols;
+                for (int32_t kb = 0; kb < prm.num_kb; ++kb, ++it) {
+                    const uint32_t s = it % S, ph = (it / S) & 1u;
+                    if (!warp_wait(full_bar(s), ph, wd)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    if (lane == 0) {
+                        const uint32_t sp = base + s * Cfg::kStageBytes;
+                        const uint64_t adesc = sdesc_kmajor_sw128(sp);
+                        const uint64_t bdesc = sdesc_kmajor_sw128(sp + Cfg::kBytesP);
+#pragma unroll
+                        for (int kk = 0; kk < Cfg::kMmasPerStage; ++kk) {
+                            // advance the start address by 32 bytes of K per MMA
+                            const uint64_t off = static_cast<uint64_t>(kk * (Cfg::kMmaKBytes >> 4));
+                            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+                            if constexpr (IN == InKind::E4M3)
+                                mma_f8<Cfg::kCG>(d_tmem, adesc + off, bdesc + off, Cfg::kIdesc, acc);
+                            else
+                                mma_f16<Cfg::kCG>(d_tmem, adesc + off, bdesc + off, Cfg::kIdesc, acc);
+                        }
+                        commit_to<Cfg::kCG>(empty_bar(s), 0x3);
+                    }
+                    __syncwarp();
+                }
+                if (!ok) break;
+                if (lane == 0) commit_to<Cfg::kCG>(accf_bar(b), 0x3);
+                __syncwarp();
+            }
+            // Every MMA issued here must finish before tensor memory is freed.
+            if (lane == 0) commit_to<Cfg::kCG>(done_bar, 0x1);
+            __syncwarp();
+            uint64_t t0 = global_timer_ns();
+            while (!__all_sync(0xffffffffu, mbar_try_wait(done_bar, 0))) {
+                if (global_timer_ns() - t0 > prm.timeout_ns) {
+                    if (lane == 0) atomicOr(prm.watchdog, kWatchTimeout);
+                    break;
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const uint32_t quarter = warp & 3u;     // TMEM lanes this warp may access
+        const uint32_t ew = warp - 2u;          // staging buffers owned by this warp
+        const uint32_t stage0 = base + Cfg::kOffEpi + ew * 2u * Cfg::kEpiBufBytes;
+        const float scale = prm.scale;
+        uint32_t lt = 0, chunk = 0;
+        for (int64_t t = first; t < num_tiles; t += stride, ++lt) {
+            int64_t tq, tp;
+            raster_tile(t, prm.tiles_q, prm.tiles_p, prm.group, &tq, &tp);
+            const uint32_t b = lt & 1u, aph = (lt >> 1) & 1u;
+            if (!warp_wait(accf_bar(b), aph, wd)) break;
+            tc_fence_after_sync();
+            const int32_t row0 =
+                static_cast<int32_t>(tp * Cfg::kTileP + rank * Cfg::kBlockP + quarter * 32);
+            const int32_t col0 = static_cast<int32_t>(tq * Cfg::kTileQ);
+            const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + b * Cfg::kAccCols;
+#pragma unroll 1
+            for (int c = 0; c < Cfg::kAccCols / Cfg::kEpiCols; ++c) {
+                uint32_t v0[32], v1[32];
+                tmem_ld_32x32b_x32(t_row + c * Cfg::kEpiCols, v0);
+                tmem_ld_32x32b_x32(t_row + c * Cfg::kEpiCols + 32, v1);
+                tmem_wait_ld();
+                if (c == Cfg::kAccCols / Cfg::kEpiCols - 1) {
+                    // The accumulator has been read: hand it back to the MMA warp.
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (PAIR)
+                            mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
+                        else
+                            mbar_arrive(acce_bar(b));
+                    }
+                }
+                uint32_t pk[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    float lo = __uint_as_float(j < 16 ? v0[2 * j] : v1[2 * j - 32]);
+                    float hi = __uint_as_float(j < 16 ? v0[2 * j + 1] : v1[2 * j - 31]);
+                    if constexpr (IN == InKind::E4M3) {
+                        lo *= scale;
+                        hi *= scale;
+                    }
+                    pk[j] = pack2<OutT>(lo, hi);
+                }
+                const int32_t x = col0 + c * Cfg::kEpiCols;
+                const bool in_range = x < prm.rows_q && row0 < prm.rows_p;
+                // A TMA store writes whole 16-byte granules of the contiguous
+                // dimension, so a chunk that ends inside a granule (rows_q not a
+                // multiple of 8) would spill into the caller's padding between
+                // rows_q and ld_out.  That chunk is stored element by element.
+                if (in_range && x + Cfg::kEpiCols > prm.rows_q && (prm.rows_q & 7) != 0) {
+                    const int32_t r = row0 + static_cast<int32_t>(lane);
+                    if (r < prm.rows_p) {
+                        uint16_t* dst = static_cast<uint16_t*>(prm.out) +
+                                        static_cast<int64_t>(r) * prm.ld_out + x;
+                        const int32_t ncols = prm.rows_q - x;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            if (2 * j < ncols) dst[2 * j] = static_cast<uint16_t>(pk[j] & 0xFFFFu);
+                            if (2 * j + 1 < ncols) dst[2 * j + 1] = static_cast<uint16_t>(pk[j] >> 16);
+                        }
+                    }
+                    ++chunk;
+                    continue;
+                }
+                const uint32_t buf = stage0 + (chunk & 1u) * Cfg::kEpiBufBytes;
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+                // Row `lane` of the 32 x 128-byte box; 16-byte chunk j is stored
+                // at chunk j ^ (row % 8), the TMA 128-byte swizzle pattern.
+                const uint32_t row_addr = buf + lane * 128u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
+                                 pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && in_range) {
+                    tma_store_2d(&map_out, buf, x, row0);
+                }
+                if (lane == 0) bulk_commit_group();
+                ++chunk;
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    // ---------------------------------------------------- teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if constexpr (PAIR) cluster_sync();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc<Cfg::kCG>(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+template <InKind IN, typename OutT, bool PAIR>
+cudaError_t tc_launch_impl(const TcLaunch& L) {
+    using Cfg = TcCfg<IN, PAIR>;
+    auto kernel = tc_gemm_kernel<IN, OutT, PAIR>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(L.grid), 1, 1);
+    cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    if (PAIR) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, L.map_p, L.map_q, L.map_out, L.prm);
+}
+
+template <InKind IN, bool PAIR>
+TcGeometry tc_geometry_impl() {
+    using Cfg = TcCfg<IN, PAIR>;
+    return TcGeometry{Cfg::kTileP, Cfg::kTileQ, Cfg::kLoadQ, Cfg::kBlockP, Cfg::kStageK,
+                      PAIR ? 2 : 1};
+}
+
+}  // namespace gb300

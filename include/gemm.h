@@ -1,0 +1,161 @@
+/*
+ * gemm.h -- C ABI of libgemm.so, a dense GEMM library for one NVIDIA GB300
+ * GPU (sm_103a).
+ *
+ * Every entry point computes the plain product C := A x B,
+ *
+ *     C[m][n] = sum_{k < K} a(m, k) * b(k, n),
+ *
+ * with no alpha/beta ("Optimizing GEMM in HIP", section "GEMM fundamentals":
+ * an M x K matrix times a K x N matrix gives the M x N product).
+ *
+ * Conventions shared by all compute entry points
+ * ------------------------------------------------
+ *  - Dimensions and leading dimensions are element counts (int64_t).  M, N and
+ *    K must lie in [0, 2^31 - 1].
+ *  - All matrix pointers are DEVICE pointers on the current CUDA device.  The
+ *    caller owns every buffer; the library allocates no device memory per call.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Work is enqueued on it and the call returns without
+ *    synchronising; results are valid once the stream has been synchronised.
+ *  - All arguments are validated before anything is launched.  On any error
+ *    status nothing is launched and C is not written.
+ *  - M == 0 or N == 0 is a successful no-op.  K == 0 writes C = 0 (the empty
+ *    sum).  C overlapping A or B gives undefined results.
+ *  - Calls may be made from several host threads; the library keeps only
+ *    per-device cached attributes and the options set by gemm_set_option.
+ *
+ * Status codes (return values)
+ * ----------------------------
+ */
+#ifndef DENSE_GEMM_TCGEN05_GB300_GEMM_H
+#define DENSE_GEMM_TCGEN05_GB300_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GEMM_OK 0                     /* success */
+#define GEMM_ERR_INVALID_DIM 1        /* M, N or K negative or above 2^31 - 1 */
+#define GEMM_ERR_INVALID_LD 2         /* a leading dimension below its minimum */
+#define GEMM_ERR_NULL_PTR 3           /* NULL matrix pointer with a nonzero extent */
+#define GEMM_ERR_MISALIGNED 4         /* pointer not aligned to its element size */
+#define GEMM_ERR_UNSUPPORTED_DEVICE 5 /* current device is not compute capability 10.3 */
+#define GEMM_ERR_LAUNCH 6             /* a CUDA runtime error; see gemm_status_string */
+#define GEMM_ERR_TIMEOUT 7            /* a device-side wait ran out (gemm_read_watchdog) */
+#define GEMM_ERR_INVALID_OPTION 8     /* unknown option name or value (gemm_set_option) */
+
+/*
+ * gemm_f32 -- FP32 GEMM, every matrix row-major ("Optimizing GEMM in HIP":
+ * FP32 matrices in row-major layout, Steps 3-6 register tiling, double
+ * buffering, vectorised loads).
+ *
+ *   a(m, k) = A[m*lda + k]   lda >= max(1, K)
+ *   b(k, n) = B[k*ldb + n]   ldb >= max(1, N)
+ *   C[m*ldc + n]             ldc >= max(1, N)
+ *
+ * Products and sums in FP32 (fused multiply-add), one rounding per step.
+ * A, B and C must be 4-byte aligned.
+ */
+int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
+             int64_t ldb, float* C, int64_t ldc, void* stream);
+
+/*
+ * gemm_f16_tn -- FP16 inputs, FP32 accumulation, FP16 output, "TN" layout
+ * ("FP16 GEMM Optimization on AMD RDNA 3 and RDNA 4", section "What We Are
+ * Computing": A row-major, B column-major so both are contiguous along K, and
+ * C column-major with leading dimension M):
+ *
+ *   a(m, k) = A[m*lda + k]   lda >= max(1, K)   (IEEE binary16 codes)
+ *   b(k, n) = B[n*ldb + k]   ldb >= max(1, K)
+ *   C[n*ldc + m]             ldc >= max(1, M)   (binary16, round to nearest even)
+ *
+ * Pointers must be 2-byte aligned.  When A, B and C are 16-byte aligned and
+ * lda*2, ldb*2 and ldc*2 are multiples of 16 bytes the tensor-core (tcgen05,
+ * TMA) kernel runs; otherwise a CUDA-core kernel with per-element loads does.
+ * Both accumulate in FP32; the output is rounded once, to nearest even.
+ */
+int gemm_f16_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                int64_t ldb, void* C, int64_t ldc, void* stream);
+
+/*
+ * gemm_bf16_tn -- as gemm_f16_tn with bfloat16 inputs and a bfloat16 output
+ * ("An Educational GEMM Ladder for Helios GPUs": BF16 inputs and output with
+ * FP32 accumulation).
+ */
+int gemm_bf16_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                 int64_t ldb, void* C, int64_t ldc, void* stream);
+
+/*
+ * gemm_fp8_tn -- FP8 E4M3 inputs with per-tensor FP32 scales, FP32
+ * accumulation, bfloat16 output, TN layout ("FP8 GEMM Optimization on AMD
+ * RDNA 4", section "What Changes at FP8": E4M3 x E4M3 accumulated in FP32;
+ * that page applies no scales, the per-tensor scales here are applied once, in
+ * the epilogue):
+ *
+ *   C[n*ldc + m] = bf16_rne( fp32(scale_a * scale_b) * sum_k qa(m,k) * qb(k,n) )
+ *
+ *   qa(m, k) = A[m*lda + k] (OCP E4M3 codes, one byte)   lda >= max(1, K)
+ *   qb(k, n) = B[n*ldb + k]                              ldb >= max(1, K)
+ *   C: bfloat16, column-major                            ldc >= max(1, M)
+ *
+ * C must be 2-byte aligned.  The tensor-core path needs A, B, C 16-byte
+ * aligned, lda and ldb multiples of 16 and ldc a multiple of 8.
+ */
+int gemm_fp8_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                int64_t ldb, float scale_a, float scale_b, void* C, int64_t ldc, void* stream);
+
+/* Human-readable text for a status code.  For GEMM_ERR_LAUNCH it names the
+ * last CUDA error this thread saw.  The returned string is static. */
+const char* gemm_status_string(int status);
+
+/*
+ * gemm_read_watchdog -- every wait inside the library's kernels gives up after
+ * a time limit (gemm_set_option "timeout_ns"), records GEMM_ERR_TIMEOUT in a
+ * per-device status word and lets its kernel exit cleanly instead of hanging.
+ * This call synchronises the current device, returns GEMM_OK when no wait has
+ * run out since the last reset, GEMM_ERR_TIMEOUT when one has, and
+ * GEMM_ERR_LAUNCH on a CUDA error.  reset != 0 clears the word.
+ */
+int gemm_read_watchdog(int reset);
+
+/*
+ * gemm_set_option -- process-wide tuning and test switches.  Not meant to be
+ * changed while calls are in flight on other host threads.
+ *   "pair"        -1 auto (default), 0 one CTA per tile, 1 a cta_group::2 pair
+ *   "group"       tile-rasteriser group size in tile rows, 1..64 (default 8)
+ *   "path"        0 auto (default), 1 force the CUDA-core fallback kernel
+ *   "timeout_ns"  device wait limit in ns, 1e6..6e10 (default 2e9)
+ *   "max_ctas"    cap on persistent CTAs, 0 = one per SM (default)
+ * Returns GEMM_OK or GEMM_ERR_INVALID_OPTION.
+ */
+int gemm_set_option(const char* name, int64_t value);
+
+/*
+ * gemm_tile_coord -- the persistent kernels' tile rasteriser, exported for
+ * tests (host only, no GPU needed).  Maps work index t in [0, tiles_m*tiles_n)
+ * to an output tile (tm, tn): tiles are handed out in groups of `group` tile
+ * rows, walking down the rows of a group before moving to the next tile column;
+ * the last group is short when group does not divide tiles_m ("FP16 GEMM
+ * Optimization on AMD RDNA 3 and RDNA 4", "Step 6: Block Scheduling for Cache
+ * Reuse").  Returns GEMM_OK, or GEMM_ERR_INVALID_DIM for an index out of range.
+ */
+int gemm_tile_coord(int64_t t, int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t* tm,
+                    int64_t* tn);
+
+/*
+ * gemm_watchdog_selftest -- launches one block that waits on a shared-memory
+ * barrier nothing will ever complete, with the given limit (ns, 1e5..1e10),
+ * so that the wait runs out.  The kernel then records GEMM_ERR_TIMEOUT in the
+ * watchdog word and exits; read it with gemm_read_watchdog.  For tests of the
+ * timeout machinery only.
+ */
+int gemm_watchdog_selftest(int64_t limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_GEMM_TCGEN05_GB300_GEMM_H */

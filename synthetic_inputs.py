@@ -96,12 +96,14 @@ def _pad(t: torch.Tensor, ld: int, kind: str) -> torch.Tensor:
 
 def tn_operands(kind: str, M: int, N: int, K: int, dist: str = "normal", seed: int = 0,
                 sigma: float = 1.0, lda: int | None = None, ldb: int | None = None,
-                dist_b: str | None = None) -> dict:
+                dist_b: str | None = None, quantise: bool = True) -> dict:
     """Operands of a TN GEMM as CPU storage tensors.
 
     Returns {"A": (M, lda) tensor, "B": (N, ldb) tensor, "scale_a", "scale_b",
     "lda", "ldb"}.  a(m, k) is A[m, k]; b(k, n) is B[n, k] (B column-major).
-    ``dist_b`` overrides the distribution of B (e.g. "identity").
+    ``dist_b`` overrides the distribution of B (e.g. "identity").  With
+    ``quantise=False`` e4m3 operands are cast directly (clamped to +-448) and
+    keep scale 1.
     """
     lda = K if lda is None else lda
     ldb = K if ldb is None else ldb
@@ -111,8 +113,11 @@ def tn_operands(kind: str, M: int, N: int, K: int, dist: str = "normal", seed: i
     xb = draw(gen, N, K, db, sigma)  # row n of this is column n of B
     if kind == "e4m3":
         # Exact-valued operands (+-1, ones, identity) keep scale 1; drawn ones are quantised.
-        qa, sa = (xa.to(torch.float8_e4m3fn), 1.0) if dist in _EXACT else _quantise_e4m3(xa)
-        qb, sb = (xb.to(torch.float8_e4m3fn), 1.0) if db in _EXACT else _quantise_e4m3(xb)
+        def direct(x):
+            return x.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn), 1.0
+
+        qa, sa = direct(xa) if (dist in _EXACT or not quantise) else _quantise_e4m3(xa)
+        qb, sb = direct(xb) if (db in _EXACT or not quantise) else _quantise_e4m3(xb)
     else:
         qa, sa = xa.to(_TORCH_DTYPES[kind]), 1.0
         qb, sb = xb.to(_TORCH_DTYPES[kind]), 1.0

@@ -1,0 +1,92 @@
+"""Host-side checks of the C ABI (CPU only, no GPU needed): the library
+builds for sm_103a, loads, exports every function include/gemm.h declares,
+rejects bad arguments before touching the GPU, and its tile rasteriser is a
+bijection with the grouped order the pages describe."""
+import ctypes
+
+import pytest
+
+from dense_gemm_tcgen05_gb300 import build, capi
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    yield
+
+
+def test_exports_every_declared_symbol():
+    names = capi.declared_symbols()
+    assert {"gemm_f32", "gemm_f16_tn", "gemm_bf16_tn", "gemm_fp8_tn",
+            "gemm_status_string"} <= set(names)
+    handle = ctypes.CDLL(capi.LIB_PATH)
+    for name in names:
+        assert hasattr(handle, name), name
+    assert set(names) == set(capi._SIGNATURES)
+
+
+def test_status_strings():
+    for st in range(9):
+        assert capi.status_text(st) and capi.status_text(st) != "unknown status"
+    assert capi.status_text(99) == "unknown status"
+
+
+FNS = ["gemm_f16_tn", "gemm_bf16_tn"]
+
+
+@pytest.mark.parametrize("fn", FNS)
+def test_argument_errors_without_gpu(fn):
+    f = getattr(capi, fn)
+    p = 0x10000  # never dereferenced: validation fails first
+    assert f(-1, 4, 4, p, 4, p, 4, p, 4) == capi.GEMM_ERR_INVALID_DIM
+    assert f(4, 4, 1 << 31, p, 1 << 31, p, 1 << 31, p, 4) == capi.GEMM_ERR_INVALID_DIM
+    assert f(4, 4, 8, p, 7, p, 8, p, 4) == capi.GEMM_ERR_INVALID_LD
+    assert f(4, 4, 8, p, 8, p, 7, p, 4) == capi.GEMM_ERR_INVALID_LD
+    assert f(4, 4, 8, p, 8, p, 8, p, 3) == capi.GEMM_ERR_INVALID_LD
+    assert f(4, 4, 8, None, 8, p, 8, p, 4) == capi.GEMM_ERR_NULL_PTR
+    assert f(4, 4, 8, p, 8, None, 8, p, 4) == capi.GEMM_ERR_NULL_PTR
+    assert f(4, 4, 8, p, 8, p, 8, None, 4) == capi.GEMM_ERR_NULL_PTR
+    assert f(4, 4, 8, p + 1, 8, p, 8, p, 4) == capi.GEMM_ERR_MISALIGNED
+    assert f(4, 4, 8, p, 8, p, 8, p + 1, 4) == capi.GEMM_ERR_MISALIGNED
+
+
+def test_fp8_and_f32_argument_errors_without_gpu():
+    p = 0x10000
+    assert capi.gemm_fp8_tn(4, 4, -2, p, 8, p, 8, 1.0, 1.0, p, 4) == capi.GEMM_ERR_INVALID_DIM
+    assert capi.gemm_fp8_tn(4, 4, 8, p, 8, p, 8, 1.0, 1.0, p + 1, 4) == capi.GEMM_ERR_MISALIGNED
+    # e4m3 operands need no alignment beyond one byte: validation passes them
+    assert capi.gemm_fp8_tn(4, 4, 8, p + 1, 8, p, 8, 1.0, 1.0, p, 3) == capi.GEMM_ERR_INVALID_LD
+    assert capi.gemm_f32(4, 5, 6, p, 5, p, 5, p, 5) == capi.GEMM_ERR_INVALID_LD
+    assert capi.gemm_f32(4, 5, 6, p, 6, p, 4, p, 5) == capi.GEMM_ERR_INVALID_LD
+    assert capi.gemm_f32(4, 5, 6, p + 2, 6, p, 5, p, 5) == capi.GEMM_ERR_MISALIGNED
+    assert capi.gemm_f32(4, 5, 6, None, 6, p, 5, p, 5) == capi.GEMM_ERR_NULL_PTR
+
+
+def test_options():
+    assert capi.gemm_set_option("pair", 1) == 0
+    assert capi.gemm_set_option("pair", -1) == 0
+    assert capi.gemm_set_option("pair", 2) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("group", 0) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("group", 8) == 0
+    assert capi.gemm_set_option("timeout_ns", 10) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("nonsense", 1) == capi.GEMM_ERR_INVALID_OPTION
+
+
+@pytest.mark.parametrize("tiles_m,tiles_n,group", [(1, 1, 8), (32, 64, 8), (16, 12, 8),
+                                                   (17, 5, 8), (7, 9, 3), (5, 5, 64), (64, 3, 1)])
+def test_rasteriser_bijection_and_bands(tiles_m, tiles_n, group):
+    """Every work index maps to a distinct tile; indices t in one band of
+    `group` tile rows stay in that band and walk down its rows first."""
+    seen = set()
+    for t in range(tiles_m * tiles_n):
+        st, tm, tn = capi.gemm_tile_coord(t, tiles_m, tiles_n, group)
+        assert st == 0
+        assert 0 <= tm < tiles_m and 0 <= tn < tiles_n
+        band = t // (group * tiles_n)
+        assert tm // group == band
+        rows = min(group, tiles_m - band * group)
+        local = t - band * group * tiles_n
+        assert tm == band * group + local % rows and tn == local // rows
+        seen.add((tm, tn))
+    assert len(seen) == tiles_m * tiles_n
+    assert capi.gemm_tile_coord(tiles_m * tiles_n, tiles_m, tiles_n, group)[0] != 0

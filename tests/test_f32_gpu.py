@@ -1,0 +1,84 @@
+"""GPU parity of gemm_f32 (SIMT FFMA, all row-major) against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic_inputs as si
+from dense_gemm_tcgen05_gb300 import capi
+from gpu_util import contract_tol
+
+pytestmark = pytest.mark.gpu
+
+
+def run_f32(ops, M, N, K, ldc=None, c_init=None):
+    ldc = N if ldc is None else ldc
+    A, B = ops["A"].cuda(), ops["B"].cuda()
+    C = (torch.full((max(M, 1), ldc), float("nan"), device="cuda") if c_init is None
+         else c_init.cuda())
+    st = capi.gemm_f32(M, N, K, A.data_ptr(), ops["lda"], B.data_ptr(), ops["ldb"],
+                       C.data_ptr(), ldc, torch.cuda.current_stream().cuda_stream)
+    assert st == 0, capi.status_text(st)
+    torch.cuda.synchronize()
+    return C.cpu()
+
+
+def tight_f32(a, b, K):
+    """FP32 FMA chain: |err| <= K * 2^-24 * sum |a||b| (plus slack factor 2)."""
+    return 2.0 * K * 2.0 ** -24 * (np.abs(a) @ np.abs(b)) + 1e-30
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (5, 3, 7), (128, 128, 8), (300, 260, 129),
+                                   (513, 1030, 77), (129, 4, 1000)])
+def test_random_full(shape):
+    M, N, K = shape
+    ops = si.f32_operands(M, N, K, dist="uniform", seed=sum(shape))
+    C = run_f32(ops, M, N, K)[:M, :N].double().numpy()
+    exact = oracle.gemm_f32(M, N, K, ops["A"].numpy(), K, ops["B"].numpy(), N)
+    err = np.abs(C - exact)
+    assert err.max() <= contract_tol("f32", K, 1.0, 1.0)
+    a, b = ops["A"][:, :K].double().numpy(), ops["B"][:, :N].double().numpy()
+    assert np.all(err <= tight_f32(a, b, K))
+
+
+def test_unaligned_and_padded_ld():
+    M, N, K = 257, 130, 70
+    ops = si.f32_operands(M, N, K, dist="uniform", seed=3, lda=K + 1, ldb=N + 3)
+    C = run_f32(ops, M, N, K, ldc=N + 5)
+    exact = oracle.gemm_f32(M, N, K, ops["A"].numpy(), ops["lda"], ops["B"].numpy(), ops["ldb"])
+    got = C[:M, :N].double().numpy()
+    a, b = ops["A"][:, :K].double().numpy(), ops["B"][:, :N].double().numpy()
+    assert np.all(np.abs(got - exact) <= tight_f32(a, b, K))
+    assert torch.all(torch.isnan(C[:M, N:])), "C padding was written"
+
+
+def test_identity_4096_exact():
+    """B = I  =>  C = A exactly ("Optimizing GEMM in HIP": the identity test)."""
+    n = 4096
+    ops = si.f32_operands(n, n, n, dist="uniform", seed=1, dist_b="identity")
+    C = run_f32(ops, n, n, n)
+    assert torch.equal(C, ops["A"])
+
+
+def test_4096_uniform_sampled():
+    """FP32 4096^3, U[-1,1] (seed 1): 4096 samples + edges within 2e-5*K."""
+    n = 4096
+    ops = si.f32_operands(n, n, n, dist="uniform", seed=1)
+    C = run_f32(ops, n, n, n)
+    ms, ns = si.sample_positions(n, n, 4096, seed=1)
+    exact = oracle.gemm_f32_sampled(n, ops["A"].numpy(), n, ops["B"].numpy(), n, ms, ns)
+    got = C[torch.from_numpy(ms), torch.from_numpy(ns)].double().numpy()
+    err = np.abs(got - exact)
+    assert err.max() <= contract_tol("f32", n, 1.0, 1.0)
+    a = ops["A"][torch.from_numpy(ms)].double().numpy()
+    b = ops["B"][:, torch.from_numpy(ns)].double().numpy().T
+    assert np.all(err <= 2.0 * n * 2.0 ** -24 * np.sum(np.abs(a) * np.abs(b), axis=1))
+
+
+def test_k_zero_and_empty():
+    M, N = 33, 17
+    ops = si.f32_operands(M, N, 1, seed=0)
+    C = run_f32(ops, M, N, 0)
+    assert torch.all(C[:M, :N] == 0)
+    init = torch.full((M, N), 5.0)
+    assert torch.equal(run_f32(ops, 0, N, 1, c_init=init), init)

@@ -1,0 +1,225 @@
+"""GPU parity of the TN entry points (gemm_f16_tn, gemm_bf16_tn, gemm_fp8_tn)
+against the CPU oracle, through the C ABI.
+
+Small and mid-size shapes (several tiles, ragged tails in M, N and K) are
+compared element by element; the full-size workloads are compared on 4096
+seeded samples plus corners and edges.  +-1 and identity inputs must match
+bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic_inputs as si
+from dense_gemm_tcgen05_gb300 import capi
+from gpu_util import (assert_codes_equal, check_full, check_sampled, exact_codes, out_codes,
+                      run_tn)
+
+pytestmark = pytest.mark.gpu
+KINDS = ["f16", "bf16", "e4m3"]
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    capi.lib()
+    yield
+
+
+@pytest.fixture(params=[0, 1], ids=["cta1", "pair"])
+def pair_mode(request):
+    assert capi.gemm_set_option("pair", request.param) == 0
+    yield request.param
+    capi.gemm_set_option("pair", -1)
+
+
+# ------------------------------------------------------------ exact checks
+
+def test_pm1_256_f16_bitexact(pair_mode):
+    """FP16 TN 256^3, +-1 entries (seed 0): bit-exact against the oracle."""
+    M = N = K = 256
+    ops = si.tn_operands("f16", M, N, K, dist="pm1", seed=0)
+    C = run_tn("f16", ops, M, N, K)
+    exact = oracle.gemm_tn("f16", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+    assert_codes_equal(out_codes(C, M, N), exact_codes("f16", exact))
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("shape", [(256, 128, 64), (300, 200, 136), (513, 257, 1000)])
+def test_pm1_bitexact(kind, shape, pair_mode):
+    M, N, K = shape
+    ops = si.tn_operands(kind, M, N, K, dist="pm1", seed=11)
+    C = run_tn(kind, ops, M, N, K)
+    exact = oracle.gemm_tn(kind, M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+    assert_codes_equal(out_codes(C, M, N), exact_codes(kind, exact))
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("n", [64, 384, 640])
+def test_identity_bitexact(kind, n, pair_mode):
+    """B = I  =>  C = A exactly (A's values are exact in the output type)."""
+    # e4m3 codes are cast directly (scale 1, |x| <= 448): exact in bf16 output
+    ops = si.tn_operands(kind, n, n, n, dist="normal", seed=5, dist_b="identity",
+                         quantise=False, sigma=4.0 if kind == "e4m3" else 1.0)
+    C = run_tn(kind, ops, n, n, n)
+    exact = oracle.gemm_tn(kind, n, n, n, si.codes(ops["A"]), n, si.codes(ops["B"]), n,
+                           ops["scale_a"], ops["scale_b"])
+    # the oracle's exact result is A itself
+    np.testing.assert_array_equal(exact, ops["A"].to(torch.float64).numpy() * ops["scale_a"])
+    assert_codes_equal(out_codes(C, n, n), exact_codes(kind, exact))
+
+
+def test_fp8_power_of_two_scales_bitexact(pair_mode):
+    M, N, K = 384, 320, 512
+    ops = si.tn_operands("e4m3", M, N, K, dist="pm1", seed=12)
+    ops["scale_a"], ops["scale_b"] = 2.0 ** -3, 2.0 ** 5
+    C = run_tn("e4m3", ops, M, N, K)
+    exact = oracle.gemm_tn("e4m3", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K,
+                           ops["scale_a"], ops["scale_b"])
+    assert_codes_equal(out_codes(C, M, N), exact_codes("e4m3", exact))
+
+
+# --------------------------------------------------- random, full compare
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("shape", [(1, 1, 1), (7, 5, 3), (600, 330, 200), (257, 129, 65),
+                                   (1024, 512, 777), (130, 700, 64)])
+def test_random_full(kind, shape, pair_mode):
+    M, N, K = shape
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=sum(shape), sigma=0.5)
+    C = run_tn(kind, ops, M, N, K)
+    check_full(kind, ops, M, N, K, C)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_padded_ld_and_guards(kind, pair_mode):
+    """Leading dimensions larger than the extents (TMA-aligned); the NaN-coded
+    padding of A and B must never be read, and C's padding rows m in [M, ldc)
+    must stay untouched."""
+    M, N, K = 333, 190, 300
+    lda = ldb = 320 if kind != "e4m3" else 336
+    ldc = 344
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=21, lda=lda, ldb=ldb)
+    C = run_tn(kind, ops, M, N, K, ldc=ldc)
+    check_full(kind, ops, M, N, K, C)
+    pad = C[:N, M:ldc].contiguous().view(torch.int16)
+    sentinel = 0x7E00 if kind == "f16" else 0x7FC0
+    assert torch.all(pad == sentinel), "C padding was written"
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_unaligned_ld_fallback(kind):
+    """Leading dimensions TMA cannot address take the CUDA-core path."""
+    M, N, K = 301, 213, 129
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=31, lda=K, ldb=K + 1)
+    C = run_tn(kind, ops, M, N, K, ldc=M)
+    check_full(kind, ops, M, N, K, C)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_forced_fallback_matches(kind):
+    M, N, K = 200, 150, 96
+    ops = si.tn_operands(kind, M, N, K, dist="pm1", seed=41)
+    assert capi.gemm_set_option("path", 1) == 0
+    try:
+        C = run_tn(kind, ops, M, N, K)
+    finally:
+        capi.gemm_set_option("path", 0)
+    exact = oracle.gemm_tn(kind, M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+    assert_codes_equal(out_codes(C, M, N), exact_codes(kind, exact))
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_k_zero_writes_zeros_and_empty_noop(kind):
+    M, N = 70, 40
+    ops = si.tn_operands(kind, M, N, 1, dist="pm1", seed=1)
+    C = run_tn(kind, ops, M, N, 0)
+    assert torch.all(C[:N, :M].to(torch.float32) == 0)
+    init = torch.full((N, M), 3.0, dtype=torch.bfloat16 if kind != "f16" else torch.float16)
+    C = run_tn(kind, ops, 0, N, 1, c_init=init, ldc=M)
+    assert torch.all(C == init)
+    C = run_tn(kind, ops, M, 0, 1, c_init=init, ldc=M)
+    assert torch.all(C == init)
+
+
+@pytest.mark.parametrize("group", [1, 3, 8, 64])
+def test_group_sizes(group):
+    M, N, K = 1300, 900, 128
+    ops = si.tn_operands("bf16", M, N, K, dist="pm1", seed=group)
+    assert capi.gemm_set_option("group", group) == 0
+    try:
+        C = run_tn("bf16", ops, M, N, K)
+    finally:
+        capi.gemm_set_option("group", 8)
+    exact = oracle.gemm_tn("bf16", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+    assert_codes_equal(out_codes(C, M, N), exact_codes("bf16", exact))
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 37])
+def test_few_persistent_ctas(ctas):
+    """Few CTAs each walk many tiles: exercises the ring and accumulator phases."""
+    M, N, K = 1100, 700, 200
+    ops = si.tn_operands("f16", M, N, K, dist="pm1", seed=ctas)
+    assert capi.gemm_set_option("max_ctas", ctas) == 0
+    try:
+        C = run_tn("f16", ops, M, N, K)
+    finally:
+        capi.gemm_set_option("max_ctas", 0)
+    exact = oracle.gemm_tn("f16", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+    assert_codes_equal(out_codes(C, M, N), exact_codes("f16", exact))
+    assert capi.gemm_read_watchdog(0) == capi.GEMM_OK
+
+
+# ----------------------------------------------------- full-size workloads
+
+def test_f16_8192_normal_sampled(pair_mode):
+    """FP16 TN 8192^3, N(0,1)*0.1 (seed 2): 4096 samples + edges."""
+    M = N = K = 8192
+    ops = si.tn_operands("f16", M, N, K, dist="normal", seed=2, sigma=0.1)
+    C = run_tn("f16", ops, M, N, K)
+    check_sampled("f16", ops, M, N, K, C, seed=2)
+
+
+def test_f16_8192_pm1_k2048_bitexact(pair_mode):
+    M, N, K = 8192, 8192, 2048
+    ops = si.tn_operands("f16", M, N, K, dist="pm1", seed=2)
+    C = run_tn("f16", ops, M, N, K)
+    ms, ns = si.sample_positions(M, N, 4096, seed=2)
+    exact = oracle.gemm_tn_sampled("f16", K, si.codes(ops["A"]), K, si.codes(ops["B"]), K, ms, ns)
+    got = C[torch.from_numpy(ns), torch.from_numpy(ms)].contiguous().view(torch.int16).numpy()
+    assert_codes_equal(got.view(np.uint16), exact_codes("f16", exact))
+
+
+BF16_SHAPES = [(4096, 4096, 4096), (4096, 14336, 4096), (4096, 4096, 14336), (2047, 3001, 1023),
+               (8191, 8191, 8191)]
+
+
+@pytest.mark.parametrize("shape", BF16_SHAPES)
+def test_bf16_sweep_sampled(shape, pair_mode):
+    """BF16 TN sweep, N(0,1)*0.05 (seed 3), tight leading dimensions."""
+    M, N, K = shape
+    ops = si.tn_operands("bf16", M, N, K, dist="normal", seed=3, sigma=0.05)
+    C = run_tn("bf16", ops, M, N, K)
+    check_sampled("bf16", ops, M, N, K, C, seed=3)
+
+
+def test_bf16_ragged_padded_ld_and_full():
+    """The ragged shape with leading dimensions padded to 16-byte rows (TMA
+    path), compared in full."""
+    M, N, K = 2047, 3001, 1023
+    ops = si.tn_operands("bf16", M, N, K, dist="normal", seed=3, sigma=0.05, lda=1024, ldb=1024)
+    C = run_tn("bf16", ops, M, N, K, ldc=2048)
+    check_full("bf16", ops, M, N, K, C)
+
+
+FP8_SHAPES = [(8192, 8192, 8192), (4096, 14336, 4096), (16384, 4096, 4096)]
+
+
+@pytest.mark.parametrize("shape", FP8_SHAPES)
+def test_fp8_sampled(shape, pair_mode):
+    """FP8 E4M3 with per-tensor scales amax/448 (seed 4), bf16 output."""
+    M, N, K = shape
+    ops = si.tn_operands("e4m3", M, N, K, dist="normal", seed=4)
+    C = run_tn("e4m3", ops, M, N, K)
+    check_sampled("e4m3", ops, M, N, K, C, seed=4)
