@@ -17,9 +17,9 @@
 #include "raster.h"
 
 namespace gb300 {
-cudaError_t tc_launch_f16(bool pair, const TcLaunch& L);
-cudaError_t tc_launch_bf16(bool pair, const TcLaunch& L);
-cudaError_t tc_launch_fp8(bool pair, const TcLaunch& L);
+cudaError_t tc_launch_f16(bool pair, Producer prod, const TcLaunch& L);
+cudaError_t tc_launch_bf16(bool pair, Producer prod, const TcLaunch& L);
+cudaError_t tc_launch_fp8(bool pair, Producer prod, const TcLaunch& L);
 TcGeometry tc_geometry_f16(bool pair);
 TcGeometry tc_geometry_bf16(bool pair);
 TcGeometry tc_geometry_fp8(bool pair);
@@ -32,11 +32,11 @@ TcGeometry tc_geometry(InKind in, bool pair) {
     }
 }
 
-cudaError_t tc_launch(InKind in, bool pair, const TcLaunch& L) {
+cudaError_t tc_launch(InKind in, bool pair, Producer prod, const TcLaunch& L) {
     switch (in) {
-        case InKind::F16: return tc_launch_f16(pair, L);
-        case InKind::BF16: return tc_launch_bf16(pair, L);
-        default: return tc_launch_fp8(pair, L);
+        case InKind::F16: return tc_launch_f16(pair, prod, L);
+        case InKind::BF16: return tc_launch_bf16(pair, prod, L);
+        default: return tc_launch_fp8(pair, prod, L);
     }
 }
 }  // namespace gb300
@@ -152,17 +152,22 @@ int gemm_tn(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
         return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
     }
 
-    const bool tma_ok = g_opt_path.load() == 0 && aligned(A, 16) && aligned(B, 16) &&
-                        aligned(C, 16) && (lda * es) % 16 == 0 && (ldb * es) % 16 == 0 &&
-                        (ldc * 2) % 16 == 0 && lda * es < (1LL << 40) && ldb * es < (1LL << 40) &&
-                        ldc * 2 < (1LL << 40);
-    if (!tma_ok) {
+    // Path choice.  TMA needs 16-byte-aligned bases and row pitches; operands
+    // that miss it are read by the load-based producer, and a C that misses it
+    // is written by the epilogue's row-wise stores.  Option "path" = 1 forces
+    // the CUDA-core kernel (a second, independent implementation).
+    if (g_opt_path.load() == 1) {
         e = tn_fallback_launch(in, M, N, K, A, lda, B, ldb, scale, C, ldc, stream);
         return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
     }
-
+    const int64_t lim = 1LL << 40;
+    const bool ab_tma = aligned(A, 16) && aligned(B, 16) && (lda * es) % 16 == 0 &&
+                        (ldb * es) % 16 == 0 && lda * es < lim && ldb * es < lim;
+    const bool c_tma = aligned(C, 16) && (ldc * 2) % 16 == 0 && ldc * 2 < lim;
+    const Producer prod = (ab_tma && g_opt_path.load() != 2) ? Producer::Tma : Producer::Loads;
     const int opt_pair = g_opt_pair.load();
-    const bool pair = opt_pair == 1;  // automatic choice: one CTA per tile
+    // cta_group::2 pairs measured faster on every shape tried; they need TMA.
+    const bool pair = prod == Producer::Tma && opt_pair != 0;
     const TcGeometry g = tc_geometry(in, pair);
     TcLaunch L;
     std::memset(&L, 0, sizeof(L));
@@ -172,9 +177,13 @@ int gemm_tn(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     const CUtensorMapDataType out_dt =
         in == InKind::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     // P = B: N rows of K contiguous elements.  Q = A: M rows of K.  Out = C: N rows of M.
-    CUresult r = encode_2d(&L.map_p, in_dt, B, K, N, ldb * es, g.stage_k, g.load_p);
-    if (r == CUDA_SUCCESS) r = encode_2d(&L.map_q, in_dt, A, K, M, lda * es, g.stage_k, g.load_q);
-    if (r == CUDA_SUCCESS) r = encode_2d(&L.map_out, out_dt, C, M, N, ldc * 2, 64, 32);
+    CUresult r = CUDA_SUCCESS;
+    if (prod == Producer::Tma) {
+        r = encode_2d(&L.map_p, in_dt, B, K, N, ldb * es, g.stage_k, g.load_p);
+        if (r == CUDA_SUCCESS)
+            r = encode_2d(&L.map_q, in_dt, A, K, M, lda * es, g.stage_k, g.load_q);
+    }
+    if (r == CUDA_SUCCESS && c_tma) r = encode_2d(&L.map_out, out_dt, C, M, N, ldc * 2, 64, 32);
     if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
 
     const int64_t tiles_p = (N + g.tile_p - 1) / g.tile_p;
@@ -196,14 +205,22 @@ int gemm_tn(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     L.prm.watchdog = dev->watchdog;
     L.prm.out = C;
     L.prm.ld_out = ldc;
+    L.prm.direct_store = c_tma ? 0 : 1;
+    L.prm.k_bytes = K * es;
+    L.prm.p_ptr = B;
+    L.prm.q_ptr = A;
+    L.prm.ld_p_bytes = ldb * es;
+    L.prm.ld_q_bytes = lda * es;
     L.grid = static_cast<int>(ctas);
     L.stream = stream;
     if (std::getenv("GEMM_DEBUG"))
         std::fprintf(stderr,
-                     "[gemm] tn in=%d M=%lld N=%lld K=%lld pair=%d tiles=%lldx%lld grid=%d\n",
-                     int(in), (long long)M, (long long)N, (long long)K, int(pair),
+                     "[gemm] tn in=%d M=%lld N=%lld K=%lld pair=%d producer=%d direct_store=%d "
+                     "tiles=%lldx%lld grid=%d\n",
+                     int(in), (long long)M, (long long)N, (long long)K, int(pair), int(prod),
+                     L.prm.direct_store,
                      (long long)tiles_q, (long long)tiles_p, L.grid);
-    e = tc_launch(in, pair, L);
+    e = tc_launch(in, pair, prod, L);
     return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
 }
 
@@ -290,7 +307,7 @@ int gemm_set_option(const char* name, int64_t value) {
         if (value < 1 || value > 64) return GEMM_ERR_INVALID_OPTION;
         g_opt_group.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "path")) {
-        if (value < 0 || value > 1) return GEMM_ERR_INVALID_OPTION;
+        if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
         g_opt_path.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "timeout_ns")) {
         if (value < 1000000LL || value > 60000000000LL) return GEMM_ERR_INVALID_OPTION;

@@ -29,6 +29,12 @@ struct TcParams {
     unsigned int* watchdog;
     void* out;           // D (= C) base pointer, for the ragged-edge stores
     int64_t ld_out;      // D row pitch in elements (= ldc)
+    int32_t direct_store;  // 1: no TMA map for D; the epilogue stores rows itself
+    int64_t k_bytes;       // K * element size (row length of P and Q in bytes)
+    const void* p_ptr;     // P (= B) base, for the non-TMA producer
+    const void* q_ptr;     // Q (= A) base, for the non-TMA producer
+    int64_t ld_p_bytes;    // row pitch of P in bytes (= ldb * element size)
+    int64_t ld_q_bytes;    // row pitch of Q in bytes (= lda * element size)
 };
 
 struct TcLaunch {
@@ -46,8 +52,12 @@ struct TcGeometry {
     int cluster;           // CTAs per tile
 };
 
+// Operand producer of the tensor-core kernel: TMA tensor copies, or (for rows
+// TMA cannot address) producer warps using 16-byte-aligned loads.
+enum class Producer : int { Tma = 0, Loads = 1 };
+
 TcGeometry tc_geometry(InKind in, bool pair);
-cudaError_t tc_launch(InKind in, bool pair, const TcLaunch& L);
+cudaError_t tc_launch(InKind in, bool pair, Producer prod, const TcLaunch& L);
 
 // CUDA-core fallback for TN operands that TMA cannot address.
 cudaError_t tn_fallback_launch(InKind in, int64_t M, int64_t N, int64_t K, const void* A,

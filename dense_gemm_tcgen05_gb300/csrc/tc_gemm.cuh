@@ -7,18 +7,25 @@
 // Computing"), so the epilogue's contiguous dimension is C's leading one.
 //
 // Structure (one CTA per SM, or one CTA pair per two SMs with cta_group::2):
-//   warp 0      TMA producer: fills a ring of kStages shared-memory stages with
-//               128-byte-swizzled tiles of P and Q; each stage is one 128-byte
-//               swizzle atom deep in K (64 fp16/bf16 or 128 e4m3 values).
-//               Out-of-range rows and K columns are zero-filled by TMA, which
-//               is what makes ragged M, N and K work without special cases.
+//   producer    fills a ring of kStages shared-memory stages with 128-byte-
+//               swizzled tiles of P and Q; each stage is one 128-byte swizzle
+//               atom deep in K (64 fp16/bf16 or 128 e4m3 values).
+//                 Tma:   warp 0, one lane issues 2D TMA copies; rows and K
+//                        columns outside the matrix are zero-filled by TMA,
+//                        which is what makes ragged M, N and K work.
+//                 Loads: warps 6-17 (for rows TMA cannot address, i.e. rows
+//                        not 16-byte aligned): each thread loads a row's
+//                        window as nine aligned 16-byte chunks, funnel-shifts
+//                        it into place, zeroes what lies outside the matrix and
+//                        writes it to the swizzled stage.
 //   warp 1      allocates tensor memory; one lane issues tcgen05.mma (4 per
 //               stage) and releases each stage with tcgen05.commit as soon as
 //               its MMAs are issued.
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator, conversion (and FP8
-//               scaling) in registers, swizzled shared-memory staging, TMA
-//               store.  Two accumulators (2 x 256 TMEM columns) let the
-//               epilogue of one tile overlap the main loop of the next.
+//               scaling) in registers, swizzled shared-memory staging, then a
+//               TMA store (or, when D's rows are not 16-byte aligned, row-wise
+//               coalesced stores).  Two accumulators (2 x 256 TMEM columns) let
+//               the epilogue of one tile overlap the main loop of the next.
 // Tiles are visited in the grouped order of raster.h.
 //
 // Correspondence with the pages' ladders: the staged shared-memory pipeline
@@ -44,8 +51,9 @@
 
 namespace gb300 {
 
-template <InKind IN, bool PAIR>
+template <InKind IN, bool PAIR, bool LOADS>
 struct TcCfg {
+    static_assert(!(PAIR && LOADS), "the load-based producer runs one CTA per tile");
     static constexpr int kCG = PAIR ? 2 : 1;
     static constexpr int kElemBytes = IN == InKind::E4M3 ? 1 : 2;
     static constexpr int kBlockP = 128;              // accumulator rows per CTA (TMEM lanes)
@@ -66,7 +74,10 @@ struct TcCfg {
     static constexpr int kEpiCols = 64;                      // columns per staged chunk
     static constexpr int kEpiBufBytes = 32 * kEpiCols * 2;   // 32 rows x 64 16-bit values
     static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
-    static constexpr int kThreads = 192;
+    static constexpr int kFirstLoadWarp = 6;
+    static constexpr int kLoadWarps = 12;
+    static constexpr int kThreads = LOADS ? (kFirstLoadWarp + kLoadWarps) * 32 : 192;
+    static constexpr int kFullArrivals = LOADS ? kLoadWarps : 1;
     static constexpr int kAccCols = kMmaN;
     static constexpr int kTmemCols = 512;
     static constexpr int kNumBars = 2 * kStages + 4 + 1;
@@ -79,6 +90,7 @@ struct TcCfg {
     static constexpr uint32_t kIdesc = make_idesc(kFormat, kMmaM, kMmaN);
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kStageBytes % 1024 == 0 && kBytesP % 1024 == 0, "1024-byte stage alignment");
+    static_assert(PAIR || kLoadWarps * 32 == kBlockP + kLoadQ, "load-producer row split");
 };
 
 // Bounded-wait bookkeeping shared by a CTA's warps.
@@ -154,12 +166,78 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-template <InKind IN, typename OutT, bool PAIR>
-__global__ void __launch_bounds__(192, 1)
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// ------------------------------------------------- load-based producer
+//
+// For rows that are not 16-byte aligned.  Work unit: a "quad" of four stage
+// rows whose addresses agree modulo 16 (rows kPeriod = 16 / element-size apart:
+// the row pitch times kPeriod is a multiple of 16 bytes), so the whole warp
+// shares one misalignment delta.  Lanes 8s..8s+7 own row s of the quad and
+// 16-byte chunk c = lane % 8 of its 128-byte K window: each lane loads the two
+// aligned 16-byte chunks that cover its chunk (consecutive lanes read
+// consecutive addresses), funnel-shifts them by delta, zeroes bytes outside
+// the matrix and stores the chunk at its 128-byte-swizzle position.  Only
+// aligned chunks holding at least one byte of the row inside the matrix are
+// loaded, so no load leaves the 16-byte blocks the matrix occupies.
+
+__device__ __forceinline__ uint4 shift_chunk(uint4 lo, uint4 hi, uint32_t delta) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const uint32_t sh = (delta & 3u) * 8u;
+    uint4 o;
+    switch (delta >> 2) {  // uniform across the warp: all rows of a quad share delta
+        case 0:
+            o = make_uint4(__funnelshift_r(w[0], w[1], sh), __funnelshift_r(w[1], w[2], sh),
+                           __funnelshift_r(w[2], w[3], sh), __funnelshift_r(w[3], w[4], sh));
+            break;
+        case 1:
+            o = make_uint4(__funnelshift_r(w[1], w[2], sh), __funnelshift_r(w[2], w[3], sh),
+                           __funnelshift_r(w[3], w[4], sh), __funnelshift_r(w[4], w[5], sh));
+            break;
+        case 2:
+            o = make_uint4(__funnelshift_r(w[2], w[3], sh), __funnelshift_r(w[3], w[4], sh),
+                           __funnelshift_r(w[4], w[5], sh), __funnelshift_r(w[5], w[6], sh));
+            break;
+        default:
+            o = make_uint4(__funnelshift_r(w[3], w[4], sh), __funnelshift_r(w[4], w[5], sh),
+                           __funnelshift_r(w[5], w[6], sh), __funnelshift_r(w[6], w[7], sh));
+            break;
+    }
+    return o;
+}
+
+// Keeps bytes [0, lim) of a 16-byte chunk and zeroes the rest.
+__device__ __forceinline__ uint4 mask_chunk(uint4 v, int32_t lim) {
+    auto m = [](int32_t l) -> uint32_t {
+        return l >= 4 ? 0xFFFFFFFFu : (l <= 0 ? 0u : ((1u << (8 * l)) - 1u));
+    };
+    v.x &= m(lim);
+    v.y &= m(lim - 4);
+    v.z &= m(lim - 8);
+    v.w &= m(lim - 12);
+    return v;
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <InKind IN, typename OutT, bool PAIR, bool LOADS>
+__global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
                    const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_out, const TcParams prm) {
-    using Cfg = TcCfg<IN, PAIR>;
+    using Cfg = TcCfg<IN, PAIR, LOADS>;
     constexpr int S = Cfg::kStages;
 
     extern __shared__ uint8_t smem_raw[];
@@ -183,7 +261,7 @@ __global__ void __launch_bounds__(192, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full_bar(s), 1);
+            mbar_init(full_bar(s), Cfg::kFullArrivals);
             mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -195,9 +273,11 @@ __global__ void __launch_bounds__(192, 1)
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&map_p);
-        prefetch_tensormap(&map_q);
-        prefetch_tensormap(&map_out);
+        if (!LOADS) {
+            prefetch_tensormap(&map_p);
+            prefetch_tensormap(&map_q);
+        }
+        if (!prm.direct_store) prefetch_tensormap(&map_out);
     }
     if (warp == 1) {
         tmem_alloc<Cfg::kCG>(smem_u32(tmem_slot), Cfg::kTmemCols);
@@ -214,7 +294,7 @@ __global__ void __launch_bounds__(192, 1)
     const int64_t first = PAIR ? blockIdx.x / 2 : blockIdx.x;
     const int64_t stride = PAIR ? gridDim.x / 2 : gridDim.x;
 
-    if (warp == 0) {
+    if (warp == 0 && !LOADS) {
         // ------------------------------------------------ TMA producer
         uint32_t it = 0;
         bool ok = true;
@@ -254,15 +334,83 @@ __global__ void __launch_bounds__(192, 1)
                 if (lane == 0) pause_ns(200000);
             } else {
                 const uint32_t outstanding = it < static_cast<uint32_t>(S) ? it : S;
-                const Watch drain{abort_flag, prm.watchdog, prm.timeout_ns};
                 for (uint32_t i = it - outstanding; i < it; ++i) {
-                    uint64_t t0 = global_timer_ns();
+                    const uint64_t t0 = global_timer_ns();
                     while (!__all_sync(0xffffffffu, mbar_try_wait(full_bar(i % S), (i / S) & 1u))) {
-                        if (global_timer_ns() - t0 > drain.limit_ns) break;
+                        if (global_timer_ns() - t0 > prm.timeout_ns) break;
                     }
                 }
             }
             __syncwarp();
+        }
+    } else if (LOADS && warp >= Cfg::kFirstLoadWarp) {
+        // ------------------------------------------------ load-based producer
+        // Producer warp pw owns quads 8pw .. 8pw+7 of the stage.  Quad i of the
+        // warp is stage rows r0 + i + kPeriod * s (s = lane / 8), so the warp
+        // stays within P (pw < 4) or within Q, row pointers advance by one
+        // pitch per quad, and the swizzle row (r % 8) is i.
+        constexpr int kPeriod = 16 / Cfg::kElemBytes;        // rows sharing one delta
+        constexpr int kQuadsPerWarp = 8;
+        static_assert(!LOADS || (Cfg::kBlockP + Cfg::kLoadQ) / 4 == kQuadsPerWarp * Cfg::kLoadWarps,
+                      "quad split");
+        const uint32_t pw = warp - Cfg::kFirstLoadWarp;
+        const uint32_t sub = lane >> 3, c = lane & 7u;
+        const uint32_t qd0 = pw * kQuadsPerWarp;
+        const uint32_t r0 = (qd0 / kPeriod) * (4 * kPeriod) + (qd0 % kPeriod) + kPeriod * sub;
+        const bool is_p = r0 < static_cast<uint32_t>(Cfg::kBlockP);  // warp-uniform
+        const uint8_t* mat = static_cast<const uint8_t*>(is_p ? prm.p_ptr : prm.q_ptr);
+        const int64_t pitch = is_p ? prm.ld_p_bytes : prm.ld_q_bytes;
+        const int64_t rows_lim = is_p ? prm.rows_p : prm.rows_q;
+        const uint32_t srow0 = r0 * Cfg::kAtomBytes;  // P then Q are contiguous, 128 B a row
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t t = first; ok && t < num_tiles; t += stride) {
+            int64_t tq, tp;
+            raster_tile(t, prm.tiles_q, prm.tiles_p, prm.group, &tq, &tp);
+            const int64_t g0 = is_p ? tp * Cfg::kTileP + r0 : tq * Cfg::kTileQ + (r0 - Cfg::kBlockP);
+            const uint8_t* row0 = mat + g0 * pitch;   // address arithmetic only
+            const int64_t rows_left = rows_lim - g0;  // quad i exists iff i < rows_left
+            for (int32_t kb = 0; kb < prm.num_kb; ++kb, ++it) {
+                const uint32_t s = it % S, ph = (it / S) & 1u;
+                const int64_t kb_byte = static_cast<int64_t>(kb) * Cfg::kAtomBytes;
+                const int64_t left = prm.k_bytes - kb_byte;
+                const int32_t win = left > 128 ? 128 : static_cast<int32_t>(left);  // >= 1
+                // Global loads first: they do not touch the stage being refilled.
+                uint4 lo[kQuadsPerWarp], hi[kQuadsPerWarp];
+#pragma unroll
+                for (int i = 0; i < kQuadsPerWarp; ++i) {
+                    const uintptr_t a = reinterpret_cast<uintptr_t>(row0) +
+                                        static_cast<uintptr_t>(i * pitch + kb_byte);
+                    const uint32_t delta = static_cast<uint32_t>(a & 15u);
+                    const uintptr_t al = a - delta + 16u * c;
+                    const int32_t v = i < rows_left ? win : 0;
+                    const int32_t first16 = 16 * static_cast<int32_t>(c) - static_cast<int32_t>(delta);
+                    lo[i] = make_uint4(0u, 0u, 0u, 0u);
+                    hi[i] = make_uint4(0u, 0u, 0u, 0u);
+                    if (first16 < v) lo[i] = ldg_nc_v4(reinterpret_cast<const void*>(al));
+                    if (delta != 0 && first16 + 16 < v)
+                        hi[i] = ldg_nc_v4(reinterpret_cast<const void*>(al + 16u));
+                }
+                if (!warp_wait(empty_bar(s), ph ^ 1u, wd)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sp = base + s * Cfg::kStageBytes + srow0;
+#pragma unroll
+                for (int i = 0; i < kQuadsPerWarp; ++i) {
+                    const uintptr_t a = reinterpret_cast<uintptr_t>(row0) +
+                                        static_cast<uintptr_t>(i * pitch + kb_byte);
+                    uint4 o = shift_chunk(lo[i], hi[i], static_cast<uint32_t>(a & 15u));
+                    const int32_t v = i < rows_left ? win : 0;
+                    if (v < 128) o = mask_chunk(o, v - 16 * static_cast<int32_t>(c));
+                    st_shared_v4(sp + i * Cfg::kAtomBytes + ((c ^ static_cast<uint32_t>(i)) << 4),
+                                 o.x, o.y, o.z, o.w);
+                }
+                // generic-proxy writes -> visible to the tensor core's reads
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full_bar(s));
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
@@ -309,7 +457,7 @@ __global__ void __launch_bounds__(192, 1)
             // Every MMA issued here must finish before tensor memory is freed.
             if (lane == 0) commit_to<Cfg::kCG>(done_bar, 0x1);
             __syncwarp();
-            uint64_t t0 = global_timer_ns();
+            const uint64_t t0 = global_timer_ns();
             while (!__all_sync(0xffffffffu, mbar_try_wait(done_bar, 0))) {
                 if (global_timer_ns() - t0 > prm.timeout_ns) {
                     if (lane == 0) atomicOr(prm.watchdog, kWatchTimeout);
@@ -317,12 +465,13 @@ __global__ void __launch_bounds__(192, 1)
                 }
             }
         }
-    } else {
+    } else if (warp >= 2 && warp < 2 + Cfg::kEpiWarps) {
         // ------------------------------------------------ epilogue
         const uint32_t quarter = warp & 3u;     // TMEM lanes this warp may access
         const uint32_t ew = warp - 2u;          // staging buffers owned by this warp
         const uint32_t stage0 = base + Cfg::kOffEpi + ew * 2u * Cfg::kEpiBufBytes;
         const float scale = prm.scale;
+        uint16_t* const out16 = static_cast<uint16_t*>(prm.out);
         uint32_t lt = 0, chunk = 0;
         for (int64_t t = first; t < num_tiles; t += stride, ++lt) {
             int64_t tq, tp;
@@ -364,15 +513,17 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 const int32_t x = col0 + c * Cfg::kEpiCols;
                 const bool in_range = x < prm.rows_q && row0 < prm.rows_p;
-                // A TMA store writes whole 16-byte granules of the contiguous
-                // dimension, so a chunk that ends inside a granule (rows_q not a
-                // multiple of 8) would spill into the caller's padding between
-                // rows_q and ld_out.  That chunk is stored element by element.
-                if (in_range && x + Cfg::kEpiCols > prm.rows_q && (prm.rows_q & 7) != 0) {
+                const uint32_t buf = stage0 + (chunk & 1u) * Cfg::kEpiBufBytes;
+                ++chunk;
+                if (!prm.direct_store && in_range && x + Cfg::kEpiCols > prm.rows_q &&
+                    (prm.rows_q & 7) != 0) {
+                    // A TMA store writes whole 16-byte granules of the contiguous
+                    // dimension, so a chunk that ends inside a granule (rows_q not
+                    // a multiple of 8) would spill into the caller's padding
+                    // between rows_q and ld_out: store it element by element.
                     const int32_t r = row0 + static_cast<int32_t>(lane);
                     if (r < prm.rows_p) {
-                        uint16_t* dst = static_cast<uint16_t*>(prm.out) +
-                                        static_cast<int64_t>(r) * prm.ld_out + x;
+                        uint16_t* dst = out16 + static_cast<int64_t>(r) * prm.ld_out + x;
                         const int32_t ncols = prm.rows_q - x;
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
@@ -380,12 +531,12 @@ __global__ void __launch_bounds__(192, 1)
                             if (2 * j + 1 < ncols) dst[2 * j + 1] = static_cast<uint16_t>(pk[j] >> 16);
                         }
                     }
-                    ++chunk;
                     continue;
                 }
-                const uint32_t buf = stage0 + (chunk & 1u) * Cfg::kEpiBufBytes;
-                if (lane == 0) bulk_wait_group_read<1>();
-                __syncwarp();
+                if (!prm.direct_store) {
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                }
                 // Row `lane` of the 32 x 128-byte box; 16-byte chunk j is stored
                 // at chunk j ^ (row % 8), the TMA 128-byte swizzle pattern.
                 const uint32_t row_addr = buf + lane * 128u;
@@ -393,16 +544,43 @@ __global__ void __launch_bounds__(192, 1)
                 for (int j = 0; j < 8; ++j)
                     st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
                                  pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0 && in_range) {
-                    tma_store_2d(&map_out, buf, x, row0);
+                if (!prm.direct_store) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (in_range) tma_store_2d(&map_out, buf, x, row0);
+                        bulk_commit_group();
+                    }
+                } else if (in_range) {
+                    // D rows are not 16-byte aligned: the warp writes the box one
+                    // row at a time, lane l storing elements 2l and 2l + 1.
+                    __syncwarp();
+                    const int32_t m = x + 2 * static_cast<int32_t>(lane);
+                    const uint32_t lane_off = ((lane >> 2) << 4) + ((lane & 3u) << 2);
+                    for (int r = 0; r < 32; ++r) {
+                        const int32_t grow = row0 + r;
+                        if (grow >= prm.rows_p) break;
+                        const uint32_t v = ld_shared_u32(
+                            buf + r * 128u + (lane_off ^ ((static_cast<uint32_t>(r) & 7u) << 4)));
+                        uint16_t* dst = out16 + static_cast<int64_t>(grow) * prm.ld_out + m;
+                        if (m + 1 < prm.rows_q) {
+                            if ((reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+                                *reinterpret_cast<uint32_t*>(dst) = v;
+                            } else {
+                                dst[0] = static_cast<uint16_t>(v & 0xFFFFu);
+                                dst[1] = static_cast<uint16_t>(v >> 16);
+                            }
+                        } else if (m < prm.rows_q) {
+                            dst[0] = static_cast<uint16_t>(v & 0xFFFFu);
+                        }
+                    }
+                    __syncwarp();
+                } else {
+                    __syncwarp();
                 }
-                if (lane == 0) bulk_commit_group();
-                ++chunk;
             }
         }
-        if (lane == 0) bulk_wait_group<0>();
+        if (!prm.direct_store && lane == 0) bulk_wait_group<0>();
         __syncwarp();
     }
 
@@ -416,10 +594,10 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-template <InKind IN, typename OutT, bool PAIR>
-cudaError_t tc_launch_impl(const TcLaunch& L) {
-    using Cfg = TcCfg<IN, PAIR>;
-    auto kernel = tc_gemm_kernel<IN, OutT, PAIR>;
+template <InKind IN, typename OutT, bool PAIR, bool LOADS>
+cudaError_t tc_launch_one(const TcLaunch& L) {
+    using Cfg = TcCfg<IN, PAIR, LOADS>;
+    auto kernel = tc_gemm_kernel<IN, OutT, PAIR, LOADS>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -447,11 +625,23 @@ cudaError_t tc_launch_impl(const TcLaunch& L) {
     return cudaLaunchKernelEx(&cfg, kernel, L.map_p, L.map_q, L.map_out, L.prm);
 }
 
-template <InKind IN, bool PAIR>
-TcGeometry tc_geometry_impl() {
-    using Cfg = TcCfg<IN, PAIR>;
-    return TcGeometry{Cfg::kTileP, Cfg::kTileQ, Cfg::kLoadQ, Cfg::kBlockP, Cfg::kStageK,
-                      PAIR ? 2 : 1};
+template <InKind IN, typename OutT>
+cudaError_t tc_launch_impl(bool pair, Producer prod, const TcLaunch& L) {
+    if (prod == Producer::Loads) {
+        if (pair) return cudaErrorInvalidConfiguration;
+        return tc_launch_one<IN, OutT, false, true>(L);
+    }
+    return pair ? tc_launch_one<IN, OutT, true, false>(L) : tc_launch_one<IN, OutT, false, false>(L);
+}
+
+template <InKind IN>
+TcGeometry tc_geometry_impl(bool pair) {
+    if (pair) {
+        using Cfg = TcCfg<IN, true, false>;
+        return TcGeometry{Cfg::kTileP, Cfg::kTileQ, Cfg::kLoadQ, Cfg::kBlockP, Cfg::kStageK, 2};
+    }
+    using Cfg = TcCfg<IN, false, false>;
+    return TcGeometry{Cfg::kTileP, Cfg::kTileQ, Cfg::kLoadQ, Cfg::kBlockP, Cfg::kStageK, 1};
 }
 
 }  // namespace gb300

@@ -72,10 +72,12 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const
  *   b(k, n) = B[n*ldb + k]   ldb >= max(1, K)
  *   C[n*ldc + m]             ldc >= max(1, M)   (binary16, round to nearest even)
  *
- * Pointers must be 2-byte aligned.  When A, B and C are 16-byte aligned and
- * lda*2, ldb*2 and ldc*2 are multiples of 16 bytes the tensor-core (tcgen05,
- * TMA) kernel runs; otherwise a CUDA-core kernel with per-element loads does.
- * Both accumulate in FP32; the output is rounded once, to nearest even.
+ * Pointers must be 2-byte aligned.  The tensor-core (tcgen05) kernel runs for
+ * every alignment: operands whose rows are 16-byte aligned (base and lda*2,
+ * ldb*2) are loaded by TMA, others by producer warps with aligned 16-byte
+ * loads; a C whose rows are 16-byte aligned is written by TMA, otherwise by
+ * row-wise stores.  Accumulation is FP32; the output is rounded once, to
+ * nearest even.
  */
 int gemm_f16_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                 int64_t ldb, void* C, int64_t ldc, void* stream);
@@ -101,8 +103,8 @@ int gemm_bf16_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
  *   qb(k, n) = B[n*ldb + k]                              ldb >= max(1, K)
  *   C: bfloat16, column-major                            ldc >= max(1, M)
  *
- * C must be 2-byte aligned.  The tensor-core path needs A, B, C 16-byte
- * aligned, lda and ldb multiples of 16 and ldc a multiple of 8.
+ * C must be 2-byte aligned.  A and B may have any alignment; TMA loads them
+ * when their bases are 16-byte aligned and lda, ldb are multiples of 16.
  */
 int gemm_fp8_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                 int64_t ldb, float scale_a, float scale_b, void* C, int64_t ldc, void* stream);
@@ -126,7 +128,8 @@ int gemm_read_watchdog(int reset);
  * changed while calls are in flight on other host threads.
  *   "pair"        -1 auto (default), 0 one CTA per tile, 1 a cta_group::2 pair
  *   "group"       tile-rasteriser group size in tile rows, 1..64 (default 8)
- *   "path"        0 auto (default), 1 force the CUDA-core fallback kernel
+ *   "path"        0 auto (default), 1 force the CUDA-core kernel, 2 force the
+ *                 tensor-core kernel's load-based producer (as for unaligned rows)
  *   "timeout_ns"  device wait limit in ns, 1e6..6e10 (default 2e9)
  *   "max_ctas"    cap on persistent CTAs, 0 = one per SM (default)
  * Returns GEMM_OK or GEMM_ERR_INVALID_OPTION.

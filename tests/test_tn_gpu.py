@@ -109,12 +109,69 @@ def test_padded_ld_and_guards(kind, pair_mode):
 
 
 @pytest.mark.parametrize("kind", KINDS)
-def test_unaligned_ld_fallback(kind):
-    """Leading dimensions TMA cannot address take the CUDA-core path."""
+@pytest.mark.parametrize("lds", [(129, 130, 301), (136, 129, 304), (131, 133, 305), (144, 144, 301)])
+def test_unaligned_rows(kind, lds):
+    """Rows that are not 16-byte aligned (odd leading dimensions, a C pitch that
+    is not a multiple of 8) take the load-based producer and/or the row-wise
+    epilogue stores; C's padding must stay untouched."""
     M, N, K = 301, 213, 129
-    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=31, lda=K, ldb=K + 1)
-    C = run_tn(kind, ops, M, N, K, ldc=M)
+    lda, ldb, ldc = lds
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=31, lda=lda, ldb=ldb)
+    C = run_tn(kind, ops, M, N, K, ldc=ldc)
     check_full(kind, ops, M, N, K, C)
+    if ldc > M:
+        pad = C[:N, M:ldc].contiguous().view(torch.int16)
+        assert torch.all(pad == (0x7E00 if kind == "f16" else 0x7FC0)), "C padding was written"
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("offset", [1, 2, 6, 8, 14])
+def test_misaligned_base_pointers(kind, offset):
+    """Base pointers off the 16-byte grid by `offset` elements of A, B and C."""
+    M, N, K = 260, 140, 300
+    es = 1 if kind == "e4m3" else 2
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=offset, lda=K + 16, ldb=K + 16)
+    dt = ops["A"].dtype
+    # shift each matrix by `offset` elements inside a larger buffer
+    fa = torch.zeros(ops["A"].numel() + offset, dtype=dt)
+    fa.view(torch.uint8 if es == 1 else torch.int16)[offset:] = ops["A"].reshape(-1).view(
+        torch.uint8 if es == 1 else torch.int16)
+    fb = torch.zeros(ops["B"].numel() + offset, dtype=dt)
+    fb.view(torch.uint8 if es == 1 else torch.int16)[offset:] = ops["B"].reshape(-1).view(
+        torch.uint8 if es == 1 else torch.int16)
+    A = fa.cuda()
+    B = fb.cuda()
+    out_dt = torch.float16 if kind == "f16" else torch.bfloat16
+    coff = offset % 8 or 1
+    Cbuf = torch.full((N * M + coff,), float("nan"), dtype=out_dt, device="cuda")
+    pa = A.data_ptr() + offset * es
+    pb = B.data_ptr() + offset * es
+    pc = Cbuf.data_ptr() + coff * 2
+    s = torch.cuda.current_stream().cuda_stream
+    if kind == "e4m3":
+        st = capi.gemm_fp8_tn(M, N, K, pa, ops["lda"], pb, ops["ldb"], ops["scale_a"],
+                              ops["scale_b"], pc, M, s)
+    else:
+        fn = capi.gemm_f16_tn if kind == "f16" else capi.gemm_bf16_tn
+        st = fn(M, N, K, pa, ops["lda"], pb, ops["ldb"], pc, M, s)
+    assert st == 0, capi.status_text(st)
+    C = Cbuf.cpu()
+    assert torch.all(torch.isnan(C[:coff].float())), "written before C"
+    check_full(kind, ops, M, N, K, C[coff:].reshape(N, M))
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_forced_load_producer_matches(kind):
+    """The load-based producer on TMA-aligned operands, several K tails."""
+    assert capi.gemm_set_option("path", 2) == 0
+    try:
+        for (M, N, K) in [(256, 128, 64), (513, 300, 1000), (129, 257, 77)]:
+            ops = si.tn_operands(kind, M, N, K, dist="pm1", seed=K)
+            C = run_tn(kind, ops, M, N, K)
+            exact = oracle.gemm_tn(kind, M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+            assert_codes_equal(out_codes(C, M, N), exact_codes(kind, exact))
+    finally:
+        capi.gemm_set_option("path", 0)
 
 
 @pytest.mark.parametrize("kind", KINDS)
@@ -202,6 +259,15 @@ def test_bf16_sweep_sampled(shape, pair_mode):
     ops = si.tn_operands("bf16", M, N, K, dist="normal", seed=3, sigma=0.05)
     C = run_tn("bf16", ops, M, N, K)
     check_sampled("bf16", ops, M, N, K, C, seed=3)
+
+
+def test_bf16_ragged_tight_ld_full():
+    """The ragged shape with tight leading dimensions (rows not 16-byte
+    aligned: load-based producer and row-wise stores), compared in full."""
+    M, N, K = 2047, 3001, 1023
+    ops = si.tn_operands("bf16", M, N, K, dist="normal", seed=3, sigma=0.05)
+    C = run_tn("bf16", ops, M, N, K)
+    check_full("bf16", ops, M, N, K, C)
 
 
 def test_bf16_ragged_padded_ld_and_full():
