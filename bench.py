@@ -455,17 +455,40 @@ def sweep(stream, stream_h, burst):
     return out
 
 
+KERNEL_SOURCES = ("tc_gemm.cuh", "ptx.cuh", "raster.h", "common.h")
+
+
+def kernel_source_hash() -> str:
+    """SHA-256 over the tensor-core kernel's sources, to tell whether committed
+    profiler counters still describe the kernel being timed."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "dense_gemm_tcgen05_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def load_traffic():
     """DRAM bytes per launch of the main kernel from the committed ncu summary
-    (profiles/tc_gemm_f16_8192.txt), or None when there is none."""
+    (profiles/tc_gemm_f16_8192.txt); None when there is none or when the
+    kernel's sources changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "tc_gemm_f16_8192.txt")
+    fields = {}
     try:
         for line in open(path):
-            if line.startswith("traffic_bytes_per_launch:"):
-                return int(float(line.split(":", 1)[1].strip()))
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
     except OSError:
-        pass
-    return None
+        return None
+    if fields.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return int(float(fields["traffic_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
 
 
 # -------------------------------------------------------- reference arm
