@@ -158,14 +158,14 @@ class ClockSampler:
 
 # ------------------------------------------------------- our implementation
 
-def tn_sets(kind, M, N, K, seed, sigma, nsets, device):
+def tn_sets(kind, M, N, K, seed, sigma, nsets, device, out_f32=False):
     """Seeded operands for a TN call, copied into `nsets` distinct buffer sets."""
     import torch
 
     import synthetic_inputs as si
 
     ops = si.tn_operands(kind, M, N, K, dist="normal", seed=seed, sigma=sigma)
-    out_dt = torch.float16 if kind == "f16" else torch.bfloat16
+    out_dt = torch.float32 if out_f32 else (torch.float16 if kind == "f16" else torch.bfloat16)
     sets = []
     for _ in range(nsets):
         a = ops["A"].to(device)
@@ -175,15 +175,16 @@ def tn_sets(kind, M, N, K, seed, sigma, nsets, device):
     return ops, sets
 
 
-def tn_call(kind, M, N, K, scale_a, scale_b, stream_h):
+def tn_call(kind, M, N, K, scale_a, scale_b, stream_h, out_f32=False):
     from dense_gemm_tcgen05_gb300 import capi
 
     fns = {"f16": capi.gemm_f16_tn, "bf16": capi.gemm_bf16_tn}
+    fp8 = capi.gemm_fp8_tn_f32 if out_f32 else capi.gemm_fp8_tn
 
     def call(a, b, c):
         if kind == "e4m3":
-            st = capi.gemm_fp8_tn(M, N, K, a.data_ptr(), K, b.data_ptr(), K, scale_a, scale_b,
-                                  c.data_ptr(), M, stream_h)
+            st = fp8(M, N, K, a.data_ptr(), K, b.data_ptr(), K, scale_a, scale_b, c.data_ptr(), M,
+                     stream_h)
         else:
             st = fns[kind](M, N, K, a.data_ptr(), K, b.data_ptr(), K, c.data_ptr(), M, stream_h)
         if st != 0:
@@ -438,18 +439,27 @@ def sweep(stream, stream_h, burst):
     import torch
 
     out = {}
-    shapes = [("bf16", (4096, 4096, 4096)), ("bf16", (4096, 14336, 4096)),
-              ("bf16", (4096, 4096, 14336)), ("bf16", (8191, 8191, 8191)),
-              ("e4m3", (4096, 14336, 4096)), ("e4m3", (16384, 4096, 4096))]
-    for kind, (M, N, K) in shapes:
+    # BF16 and FP8 configurations (tight leading dimensions: the odd shapes take
+    # the load-based producer), then the pages' transformer shapes -- FP16 on
+    # the FP16 page's wide shape, FP8 with FP32 output as the FP8 page measures.
+    shapes = [("bf16", (4096, 4096, 4096), False), ("bf16", (4096, 14336, 4096), False),
+              ("bf16", (4096, 4096, 14336), False), ("bf16", (2047, 3001, 1023), False),
+              ("bf16", (8191, 8191, 8191), False), ("e4m3", (8192, 8192, 8192), False),
+              ("e4m3", (4096, 14336, 4096), False), ("e4m3", (16384, 4096, 4096), False),
+              ("f16", (8192, 28672, 8192), False), ("e4m3", (8192, 8192, 8192), True),
+              ("e4m3", (8192, 28672, 8192), True), ("e4m3", (8192, 10240, 8192), True),
+              ("e4m3", (3072, 4096, 8192), True)]
+    for kind, (M, N, K), f32 in shapes:
         o, s = tn_sets(kind, M, N, K, seed=4 if kind == "e4m3" else 3,
-                       sigma=1.0 if kind == "e4m3" else 0.05, nsets=SETS, device="cuda")
-        c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h)
+                       sigma=1.0 if kind == "e4m3" else 0.05, nsets=SETS, device="cuda",
+                       out_f32=f32)
+        c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h, out_f32=f32)
         with torch.cuda.stream(stream):
             _, lm = timed_loop(c, s, 20, 3, stream)
         tf = 2.0 * M * N * K / (lm * 1e-3) / 1e12
         peak = burst * (FP8_OVER_BF16 if kind == "e4m3" else 1.0)
-        out["%s_%dx%dx%d" % (kind, M, N, K)] = {"tflops": round(tf, 1), "frac": round(tf / peak, 4)}
+        key = "%s%s_%dx%dx%d" % (kind, "_f32out" if f32 else "", M, N, K)
+        out[key] = {"tflops": round(tf, 1), "frac": round(tf / peak, 4)}
         del s
         torch.cuda.empty_cache()
     return out

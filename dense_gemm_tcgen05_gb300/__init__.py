@@ -46,8 +46,11 @@ def _ld(t: torch.Tensor) -> int:
 
 
 def tn(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None, scale_a: float = 1.0,
-       scale_b: float = 1.0, stream=None) -> torch.Tensor:
-    """C = A x B in the TN layout; returns ``out`` (N, M) holding C column-major."""
+       scale_b: float = 1.0, stream=None, out_dtype: torch.dtype | None = None) -> torch.Tensor:
+    """C = A x B in the TN layout; returns ``out`` (N, M) holding C column-major.
+
+    FP8 inputs give a bfloat16 C, or float32 with ``out_dtype=torch.float32``
+    (``gemm_fp8_tn_f32``)."""
     if a.dtype != b.dtype or a.dtype not in _TN_DTYPES:
         raise TypeError("a and b must both be float16, bfloat16 or float8_e4m3fn")
     _check_2d(a, "a")
@@ -56,16 +59,23 @@ def tn(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None, scale_
     N, Kb = b.shape
     if K != Kb:
         raise ValueError("K mismatch: a has %d columns, b has %d" % (K, Kb))
-    fn_name, out_dtype = _TN_DTYPES[a.dtype]
+    fn_name, default_out = _TN_DTYPES[a.dtype]
+    if out_dtype is None and out is not None:
+        out_dtype = out.dtype
+    out_dtype = default_out if out_dtype is None else out_dtype
+    if fn_name == "gemm_fp8_tn" and out_dtype == torch.float32:
+        fn_name = "gemm_fp8_tn_f32"
+    elif out_dtype != default_out:
+        raise TypeError("output dtype %s is not available for %s inputs" % (out_dtype, a.dtype))
     if out is None:
         out = torch.empty((N, M), dtype=out_dtype, device=a.device)
     _check_2d(out, "out")
     if out.dtype != out_dtype or tuple(out.shape) != (N, M):
         raise ValueError("out must be (N, M) of %s" % out_dtype)
     h = stream_handle(stream)
-    if fn_name == "gemm_fp8_tn":
-        st = capi.gemm_fp8_tn(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), scale_a,
-                              scale_b, out.data_ptr(), _ld(out), h)
+    if fn_name in ("gemm_fp8_tn", "gemm_fp8_tn_f32"):
+        st = getattr(capi, fn_name)(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), scale_a,
+                                    scale_b, out.data_ptr(), _ld(out), h)
     else:
         st = getattr(capi, fn_name)(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b),
                                     out.data_ptr(), _ld(out), h)

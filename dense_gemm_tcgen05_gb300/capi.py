@@ -36,6 +36,7 @@ _SIGNATURES = {
     "gemm_f16_tn": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp], _int),
     "gemm_bf16_tn": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp], _int),
     "gemm_fp8_tn": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _f32, _f32, _vp, _i64, _vp], _int),
+    "gemm_fp8_tn_f32": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _f32, _f32, _vp, _i64, _vp], _int),
     "gemm_status_string": ([_int], ctypes.c_char_p),
     "gemm_read_watchdog": ([_int], _int),
     "gemm_set_option": ([ctypes.c_char_p, _i64], _int),
@@ -100,6 +101,11 @@ def gemm_bf16_tn(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
 def gemm_fp8_tn(M, N, K, A, lda, B, ldb, scale_a, scale_b, C, ldc, stream=None) -> int:
     return lib().gemm_fp8_tn(M, N, K, _p(A), lda, _p(B), ldb, float(scale_a), float(scale_b),
                              _p(C), ldc, _p(stream))
+
+
+def gemm_fp8_tn_f32(M, N, K, A, lda, B, ldb, scale_a, scale_b, C, ldc, stream=None) -> int:
+    return lib().gemm_fp8_tn_f32(M, N, K, _p(A), lda, _p(B), ldb, float(scale_a),
+                                 float(scale_b), _p(C), ldc, _p(stream))
 
 
 def gemm_status_string(status: int) -> str:

@@ -19,7 +19,7 @@
 namespace gb300 {
 cudaError_t tc_launch_f16(bool pair, Producer prod, const TcLaunch& L);
 cudaError_t tc_launch_bf16(bool pair, Producer prod, const TcLaunch& L);
-cudaError_t tc_launch_fp8(bool pair, Producer prod, const TcLaunch& L);
+cudaError_t tc_launch_fp8(bool pair, Producer prod, bool out_f32, const TcLaunch& L);
 TcGeometry tc_geometry_f16(bool pair);
 TcGeometry tc_geometry_bf16(bool pair);
 TcGeometry tc_geometry_fp8(bool pair);
@@ -32,11 +32,11 @@ TcGeometry tc_geometry(InKind in, bool pair) {
     }
 }
 
-cudaError_t tc_launch(InKind in, bool pair, Producer prod, const TcLaunch& L) {
+cudaError_t tc_launch(InKind in, bool pair, Producer prod, bool out_f32, const TcLaunch& L) {
     switch (in) {
         case InKind::F16: return tc_launch_f16(pair, prod, L);
         case InKind::BF16: return tc_launch_bf16(pair, prod, L);
-        default: return tc_launch_fp8(pair, prod, L);
+        default: return tc_launch_fp8(pair, prod, out_f32, L);
     }
 }
 }  // namespace gb300
@@ -131,16 +131,18 @@ CUresult encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, in
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-int gemm_tn(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-            const void* B, int64_t ldb, float scale, void* C, int64_t ldc, void* stream_v) {
+int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void* A,
+            int64_t lda, const void* B, int64_t ldb, float scale, void* C, int64_t ldc,
+            void* stream_v) {
     const int es = in == InKind::E4M3 ? 1 : 2;
+    const int os = out_f32 ? 4 : 2;  // output element size
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return GEMM_ERR_INVALID_DIM;
     const int64_t kmin = K > 1 ? K : 1;
     if (lda < kmin || ldb < kmin || ldc < (M > 1 ? M : 1)) return GEMM_ERR_INVALID_LD;
     if ((M > 0 && K > 0 && !A) || (N > 0 && K > 0 && !B) || (M > 0 && N > 0 && !C))
         return GEMM_ERR_NULL_PTR;
-    if (!aligned(A, es) || !aligned(B, es) || !aligned(C, 2)) return GEMM_ERR_MISALIGNED;
+    if (!aligned(A, es) || !aligned(B, es) || !aligned(C, os)) return GEMM_ERR_MISALIGNED;
     const DeviceInfo* dev = nullptr;
     int st = current_device(&dev);
     if (st != GEMM_OK) return st;
@@ -148,7 +150,7 @@ int gemm_tn(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
     cudaError_t e;
     if (K == 0) {
-        e = zero_fill_launch(C, N, M, ldc, 2, stream);
+        e = zero_fill_launch(C, N, M, ldc, os, stream);
         return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
     }
 
@@ -157,13 +159,13 @@ int gemm_tn(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     // is written by the epilogue's row-wise stores.  Option "path" = 1 forces
     // the CUDA-core kernel (a second, independent implementation).
     if (g_opt_path.load() == 1) {
-        e = tn_fallback_launch(in, M, N, K, A, lda, B, ldb, scale, C, ldc, stream);
+        e = tn_fallback_launch(in, out_f32, M, N, K, A, lda, B, ldb, scale, C, ldc, stream);
         return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
     }
     const int64_t lim = 1LL << 40;
     const bool ab_tma = aligned(A, 16) && aligned(B, 16) && (lda * es) % 16 == 0 &&
                         (ldb * es) % 16 == 0 && lda * es < lim && ldb * es < lim;
-    const bool c_tma = aligned(C, 16) && (ldc * 2) % 16 == 0 && ldc * 2 < lim;
+    const bool c_tma = aligned(C, 16) && (ldc * os) % 16 == 0 && ldc * os < lim;
     const Producer prod = (ab_tma && g_opt_path.load() != 2) ? Producer::Tma : Producer::Loads;
     const int opt_pair = g_opt_pair.load();
     // cta_group::2 pairs measured faster on every shape tried; they need TMA.
@@ -174,8 +176,9 @@ int gemm_tn(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
     const CUtensorMapDataType in_dt = in == InKind::F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                       : in == InKind::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                            : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    const CUtensorMapDataType out_dt =
-        in == InKind::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapDataType out_dt = out_f32            ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                       : in == InKind::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     // P = B: N rows of K contiguous elements.  Q = A: M rows of K.  Out = C: N rows of M.
     CUresult r = CUDA_SUCCESS;
     if (prod == Producer::Tma) {
@@ -183,7 +186,9 @@ int gemm_tn(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
         if (r == CUDA_SUCCESS)
             r = encode_2d(&L.map_q, in_dt, A, K, M, lda * es, g.stage_k, g.load_q);
     }
-    if (r == CUDA_SUCCESS && c_tma) r = encode_2d(&L.map_out, out_dt, C, M, N, ldc * 2, 64, 32);
+    // One staged chunk is one 128-byte row: a box of 128 / os columns x 32 rows.
+    if (r == CUDA_SUCCESS && c_tma)
+        r = encode_2d(&L.map_out, out_dt, C, M, N, ldc * os, 128 / os, 32);
     if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
 
     const int64_t tiles_p = (N + g.tile_p - 1) / g.tile_p;
@@ -220,7 +225,7 @@ int gemm_tn(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t l
                      int(in), (long long)M, (long long)N, (long long)K, int(pair), int(prod),
                      L.prm.direct_store,
                      (long long)tiles_q, (long long)tiles_p, L.grid);
-    e = tc_launch(in, pair, prod, L);
+    e = tc_launch(in, pair, prod, out_f32, L);
     return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
 }
 
@@ -249,18 +254,25 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const
 
 int gemm_f16_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                 int64_t ldb, void* C, int64_t ldc, void* stream) {
-    return gemm_tn(InKind::F16, M, N, K, A, lda, B, ldb, 1.0f, C, ldc, stream);
+    return gemm_tn(InKind::F16, false, M, N, K, A, lda, B, ldb, 1.0f, C, ldc, stream);
 }
 
 int gemm_bf16_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                  int64_t ldb, void* C, int64_t ldc, void* stream) {
-    return gemm_tn(InKind::BF16, M, N, K, A, lda, B, ldb, 1.0f, C, ldc, stream);
+    return gemm_tn(InKind::BF16, false, M, N, K, A, lda, B, ldb, 1.0f, C, ldc, stream);
 }
 
 int gemm_fp8_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                 int64_t ldb, float scale_a, float scale_b, void* C, int64_t ldc, void* stream) {
     const float scale = scale_a * scale_b;  // one FP32 product, applied in the epilogue
-    return gemm_tn(InKind::E4M3, M, N, K, A, lda, B, ldb, scale, C, ldc, stream);
+    return gemm_tn(InKind::E4M3, false, M, N, K, A, lda, B, ldb, scale, C, ldc, stream);
+}
+
+int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                    int64_t ldb, float scale_a, float scale_b, float* C, int64_t ldc,
+                    void* stream) {
+    const float scale = scale_a * scale_b;
+    return gemm_tn(InKind::E4M3, true, M, N, K, A, lda, B, ldb, scale, C, ldc, stream);
 }
 
 const char* gemm_status_string(int status) {

@@ -57,12 +57,14 @@ struct TcGeometry {
 enum class Producer : int { Tma = 0, Loads = 1 };
 
 TcGeometry tc_geometry(InKind in, bool pair);
-cudaError_t tc_launch(InKind in, bool pair, Producer prod, const TcLaunch& L);
+// out_f32: FP32 output (E4M3 inputs only); otherwise the input's 16-bit type
+// (bf16 for E4M3).
+cudaError_t tc_launch(InKind in, bool pair, Producer prod, bool out_f32, const TcLaunch& L);
 
 // CUDA-core fallback for TN operands that TMA cannot address.
-cudaError_t tn_fallback_launch(InKind in, int64_t M, int64_t N, int64_t K, const void* A,
-                               int64_t lda, const void* B, int64_t ldb, float scale, void* C,
-                               int64_t ldc, cudaStream_t stream);
+cudaError_t tn_fallback_launch(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K,
+                               const void* A, int64_t lda, const void* B, int64_t ldb, float scale,
+                               void* C, int64_t ldc, cudaStream_t stream);
 
 cudaError_t f32_launch(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                        const float* B, int64_t ldb, float* C, int64_t ldc, cudaStream_t stream);

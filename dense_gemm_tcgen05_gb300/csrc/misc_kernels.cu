@@ -1,14 +1,15 @@
-// misc_kernels.cu -- the CUDA-core TN fallback, the K == 0 zero fill and the
+// misc_kernels.cu -- a CUDA-core TN kernel, the K == 0 zero fill and the
 // watchdog self-test.
 //
-// The fallback serves TN calls whose pointers or leading dimensions TMA cannot
-// address (a TMA copy needs 16-byte-aligned rows).  It reads elements one by
+// The CUDA-core TN kernel is a second, independent GPU implementation of the
+// TN entry points, selected only by gemm_set_option("path", 1) (tests compare
+// it with the tensor-core kernel and the oracle).  It reads elements one by
 // one, so any alignment works, decodes them to FP32 in shared memory,
-// accumulates in FP32 and rounds the result once to the output type, exactly
-// as the tensor-core kernel does; only the summation order differs.  Like the
-// pages' buffer-descriptor loads ("FP16 GEMM Optimization on AMD RDNA 3 and
-// RDNA 4", "Step 4: Buffer Resource Descriptors for Global Loads"),
-// out-of-range elements read as zero.
+// accumulates in FP32 and rounds the result once to the output type, as the
+// tensor-core kernel does; only the summation order differs.  Like the pages'
+// buffer-descriptor loads ("FP16 GEMM Optimization on AMD RDNA 3 and RDNA 4",
+// "Step 4: Buffer Resource Descriptors for Global Loads"), out-of-range
+// elements read as zero.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -83,7 +84,9 @@ __global__ void __launch_bounds__(kFbThreads)
             if (m >= M) continue;
             float v = acc[i][j];
             if constexpr (IN == InKind::E4M3) v *= scale;
-            if constexpr (sizeof(OutT) == 2 && IN == InKind::F16)
+            if constexpr (sizeof(OutT) == 4)
+                C[n * ldc + m] = v;
+            else if constexpr (IN == InKind::F16)
                 C[n * ldc + m] = __float2half_rn(v);
             else
                 C[n * ldc + m] = __float2bfloat16_rn(v);
@@ -123,9 +126,9 @@ __global__ void watchdog_selftest_kernel(uint64_t limit_ns, unsigned int* watchd
 
 }  // namespace
 
-cudaError_t tn_fallback_launch(InKind in, int64_t M, int64_t N, int64_t K, const void* A,
-                               int64_t lda, const void* B, int64_t ldb, float scale, void* C,
-                               int64_t ldc, cudaStream_t stream) {
+cudaError_t tn_fallback_launch(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K,
+                               const void* A, int64_t lda, const void* B, int64_t ldb, float scale,
+                               void* C, int64_t ldc, cudaStream_t stream) {
     const int64_t tiles_m = (M + kFbBM - 1) / kFbBM, tiles_n = (N + kFbBN - 1) / kFbBN;
     if (tiles_m * tiles_n > 0x7fffffff) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(tiles_m * tiles_n));
@@ -143,9 +146,14 @@ cudaError_t tn_fallback_launch(InKind in, int64_t M, int64_t N, int64_t K, const
                 ldc, tiles_m, tiles_n);
             break;
         case InKind::E4M3:
-            tn_fallback_kernel<InKind::E4M3, __nv_bfloat16><<<grid, kFbThreads, 0, stream>>>(
-                int(M), int(N), int(K), a, lda, b, ldb, scale, static_cast<__nv_bfloat16*>(C),
-                ldc, tiles_m, tiles_n);
+            if (out_f32)
+                tn_fallback_kernel<InKind::E4M3, float><<<grid, kFbThreads, 0, stream>>>(
+                    int(M), int(N), int(K), a, lda, b, ldb, scale, static_cast<float*>(C), ldc,
+                    tiles_m, tiles_n);
+            else
+                tn_fallback_kernel<InKind::E4M3, __nv_bfloat16><<<grid, kFbThreads, 0, stream>>>(
+                    int(M), int(N), int(K), a, lda, b, ldb, scale, static_cast<__nv_bfloat16*>(C),
+                    ldc, tiles_m, tiles_n);
             break;
     }
     return cudaGetLastError();

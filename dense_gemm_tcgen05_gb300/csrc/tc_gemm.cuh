@@ -71,8 +71,7 @@ struct TcCfg {
     static constexpr int kStageBytes = kBytesP + kBytesQ;
     static constexpr int kStages = PAIR ? 6 : 4;
     static constexpr int kEpiWarps = 4;
-    static constexpr int kEpiCols = 64;                      // columns per staged chunk
-    static constexpr int kEpiBufBytes = 32 * kEpiCols * 2;   // 32 rows x 64 16-bit values
+    static constexpr int kEpiBufBytes = 32 * 128;            // 32 rows x one 128-byte row
     static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
     static constexpr int kFirstLoadWarp = 6;
     static constexpr int kLoadWarps = 12;
@@ -467,11 +466,17 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         }
     } else if (warp >= 2 && warp < 2 + Cfg::kEpiWarps) {
         // ------------------------------------------------ epilogue
+        // A staged chunk is one 128-byte row per accumulator row: 64 fp16/bf16
+        // or 32 fp32 output values.
+        constexpr int kOB = static_cast<int>(sizeof(OutT));   // output bytes: 2 or 4
+        constexpr int kCols = 128 / kOB;                        // columns per chunk
+        constexpr int kGran = 16 / kOB;                         // elements per 16-byte granule
+        constexpr int kChunks = Cfg::kAccCols / kCols;
         const uint32_t quarter = warp & 3u;     // TMEM lanes this warp may access
         const uint32_t ew = warp - 2u;          // staging buffers owned by this warp
         const uint32_t stage0 = base + Cfg::kOffEpi + ew * 2u * Cfg::kEpiBufBytes;
         const float scale = prm.scale;
-        uint16_t* const out16 = static_cast<uint16_t*>(prm.out);
+        uint8_t* const out8 = static_cast<uint8_t*>(prm.out);
         uint32_t lt = 0, chunk = 0;
         for (int64_t t = first; t < num_tiles; t += stride, ++lt) {
             int64_t tq, tp;
@@ -484,12 +489,12 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
             const int32_t col0 = static_cast<int32_t>(tq * Cfg::kTileQ);
             const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + b * Cfg::kAccCols;
 #pragma unroll 1
-            for (int c = 0; c < Cfg::kAccCols / Cfg::kEpiCols; ++c) {
+            for (int c = 0; c < kChunks; ++c) {
                 uint32_t v0[32], v1[32];
-                tmem_ld_32x32b_x32(t_row + c * Cfg::kEpiCols, v0);
-                tmem_ld_32x32b_x32(t_row + c * Cfg::kEpiCols + 32, v1);
+                tmem_ld_32x32b_x32(t_row + c * kCols, v0);
+                if constexpr (kOB == 2) tmem_ld_32x32b_x32(t_row + c * kCols + 32, v1);
                 tmem_wait_ld();
-                if (c == Cfg::kAccCols / Cfg::kEpiCols - 1) {
+                if (c == kChunks - 1) {
                     // The accumulator has been read: hand it back to the MMA warp.
                     tc_fence_before_sync();
                     __syncwarp();
@@ -500,35 +505,47 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                             mbar_arrive(acce_bar(b));
                     }
                 }
+                // pk: the chunk's 128 output bytes of this lane's row, as words
                 uint32_t pk[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    float lo = __uint_as_float(j < 16 ? v0[2 * j] : v1[2 * j - 32]);
-                    float hi = __uint_as_float(j < 16 ? v0[2 * j + 1] : v1[2 * j - 31]);
-                    if constexpr (IN == InKind::E4M3) {
-                        lo *= scale;
-                        hi *= scale;
+                    if constexpr (kOB == 2) {
+                        float lo = __uint_as_float(j < 16 ? v0[2 * j] : v1[2 * j - 32]);
+                        float hi = __uint_as_float(j < 16 ? v0[2 * j + 1] : v1[2 * j - 31]);
+                        if constexpr (IN == InKind::E4M3) {
+                            lo *= scale;
+                            hi *= scale;
+                        }
+                        pk[j] = pack2<OutT>(lo, hi);
+                    } else {
+                        float f = __uint_as_float(v0[j]);
+                        if constexpr (IN == InKind::E4M3) f *= scale;
+                        pk[j] = __float_as_uint(f);
                     }
-                    pk[j] = pack2<OutT>(lo, hi);
                 }
-                const int32_t x = col0 + c * Cfg::kEpiCols;
+                const int32_t x = col0 + c * kCols;
                 const bool in_range = x < prm.rows_q && row0 < prm.rows_p;
                 const uint32_t buf = stage0 + (chunk & 1u) * Cfg::kEpiBufBytes;
                 ++chunk;
-                if (!prm.direct_store && in_range && x + Cfg::kEpiCols > prm.rows_q &&
-                    (prm.rows_q & 7) != 0) {
+                if (!prm.direct_store && in_range && x + kCols > prm.rows_q &&
+                    (prm.rows_q % kGran) != 0) {
                     // A TMA store writes whole 16-byte granules of the contiguous
-                    // dimension, so a chunk that ends inside a granule (rows_q not
-                    // a multiple of 8) would spill into the caller's padding
-                    // between rows_q and ld_out: store it element by element.
+                    // dimension, so a chunk that ends inside a granule would
+                    // spill into the caller's padding between rows_q and ld_out:
+                    // store it element by element.
                     const int32_t r = row0 + static_cast<int32_t>(lane);
                     if (r < prm.rows_p) {
-                        uint16_t* dst = out16 + static_cast<int64_t>(r) * prm.ld_out + x;
+                        uint8_t* dst = out8 + (static_cast<int64_t>(r) * prm.ld_out + x) * kOB;
                         const int32_t ncols = prm.rows_q - x;
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            if (2 * j < ncols) dst[2 * j] = static_cast<uint16_t>(pk[j] & 0xFFFFu);
-                            if (2 * j + 1 < ncols) dst[2 * j + 1] = static_cast<uint16_t>(pk[j] >> 16);
+                            if constexpr (kOB == 2) {
+                                uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+                                if (2 * j < ncols) d16[2 * j] = static_cast<uint16_t>(pk[j] & 0xFFFFu);
+                                if (2 * j + 1 < ncols) d16[2 * j + 1] = static_cast<uint16_t>(pk[j] >> 16);
+                            } else {
+                                if (j < ncols) reinterpret_cast<uint32_t*>(dst)[j] = pk[j];
+                            }
                         }
                     }
                     continue;
@@ -553,25 +570,27 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                     }
                 } else if (in_range) {
                     // D rows are not 16-byte aligned: the warp writes the box one
-                    // row at a time, lane l storing elements 2l and 2l + 1.
+                    // row at a time, lane l storing bytes [4l, 4l + 4) of the row
+                    // (elements 2l, 2l + 1 of a 16-bit output, element l of fp32).
                     __syncwarp();
-                    const int32_t m = x + 2 * static_cast<int32_t>(lane);
+                    constexpr int kPerLane = 4 / kOB;
+                    const int32_t m = x + kPerLane * static_cast<int32_t>(lane);
                     const uint32_t lane_off = ((lane >> 2) << 4) + ((lane & 3u) << 2);
                     for (int r = 0; r < 32; ++r) {
                         const int32_t grow = row0 + r;
                         if (grow >= prm.rows_p) break;
                         const uint32_t v = ld_shared_u32(
                             buf + r * 128u + (lane_off ^ ((static_cast<uint32_t>(r) & 7u) << 4)));
-                        uint16_t* dst = out16 + static_cast<int64_t>(grow) * prm.ld_out + m;
-                        if (m + 1 < prm.rows_q) {
+                        uint8_t* dst = out8 + (static_cast<int64_t>(grow) * prm.ld_out + m) * kOB;
+                        if (m + kPerLane - 1 < prm.rows_q) {
                             if ((reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
                                 *reinterpret_cast<uint32_t*>(dst) = v;
                             } else {
-                                dst[0] = static_cast<uint16_t>(v & 0xFFFFu);
-                                dst[1] = static_cast<uint16_t>(v >> 16);
+                                reinterpret_cast<uint16_t*>(dst)[0] = static_cast<uint16_t>(v & 0xFFFFu);
+                                reinterpret_cast<uint16_t*>(dst)[1] = static_cast<uint16_t>(v >> 16);
                             }
-                        } else if (m < prm.rows_q) {
-                            dst[0] = static_cast<uint16_t>(v & 0xFFFFu);
+                        } else if (m < prm.rows_q) {  // 16-bit output only
+                            reinterpret_cast<uint16_t*>(dst)[0] = static_cast<uint16_t>(v & 0xFFFFu);
                         }
                     }
                     __syncwarp();

@@ -109,6 +109,21 @@ int gemm_bf16_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
 int gemm_fp8_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                 int64_t ldb, float scale_a, float scale_b, void* C, int64_t ldc, void* stream);
 
+/*
+ * gemm_fp8_tn_f32 -- as gemm_fp8_tn with an FP32 output, the layout the FP8
+ * page writes ("FP8 GEMM Optimization on AMD RDNA 4", "What Changes at FP8",
+ * "Accumulator type": FP32 C, column-major, leading dimension M):
+ *
+ *   C[n*ldc + m] = fp32(scale_a * scale_b) * sum_k qa(m,k) * qb(k,n)
+ *
+ * (one FP32 multiply of the FP32 accumulator, no further rounding).  C must be
+ * 4-byte aligned; TMA writes it when C is 16-byte aligned and ldc is a multiple
+ * of 4.
+ */
+int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                    int64_t ldb, float scale_a, float scale_b, float* C, int64_t ldc,
+                    void* stream);
+
 /* Human-readable text for a status code.  For GEMM_ERR_LAUNCH it names the
  * last CUDA error this thread saw.  The returned string is static. */
 const char* gemm_status_string(int status);
