@@ -462,6 +462,31 @@ def sweep(stream, stream_h, burst):
         out[key] = {"tflops": round(tf, 1), "frac": round(tf / peak, 4)}
         del s
         torch.cuda.empty_cache()
+    # Skinny and small shapes: HBM-bound, reported in GB/s of compulsory
+    # traffic against the measured copy bandwidth, with a split-K workspace.
+    from dense_gemm_tcgen05_gb300 import capi
+
+    peaks, _ = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    ws = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    capi.gemm_set_workspace(ws.data_ptr(), ws.numel())
+    try:
+        for kind, (M, N, K) in [("bf16", (16, 8192, 8192)), ("bf16", (128, 8192, 8192)),
+                                ("bf16", (64, 14336, 4096)), ("bf16", (1024, 1024, 8192)),
+                                ("e4m3", (128, 8192, 8192))]:
+            o, s = tn_sets(kind, M, N, K, seed=3, sigma=0.05, nsets=SETS, device="cuda")
+            c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h)
+            with torch.cuda.stream(stream):
+                _, lm = timed_loop(c, s, 30, 3, stream)
+            es = 1 if kind == "e4m3" else 2
+            gbs = ((M * K + N * K) * es + M * N * 2) / (lm * 1e-3) / 1e9
+            out["%s_skinny_%dx%dx%d" % (kind, M, N, K)] = {
+                "tflops": round(2.0 * M * N * K / (lm * 1e-3) / 1e12, 1), "gbs": round(gbs),
+                "hbm_frac": round(gbs / hbm, 3), "us": round(lm * 1e3, 1)}
+            del s
+            torch.cuda.empty_cache()
+    finally:
+        capi.gemm_set_workspace(None, 0)
     return out
 
 

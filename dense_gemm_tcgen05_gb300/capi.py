@@ -42,6 +42,8 @@ _SIGNATURES = {
     "gemm_set_option": ([ctypes.c_char_p, _i64], _int),
     "gemm_tile_coord": ([_i64, _i64, _i64, _i64, ctypes.POINTER(_i64), ctypes.POINTER(_i64)], _int),
     "gemm_watchdog_selftest": ([_i64, _vp], _int),
+    "gemm_set_workspace": ([_vp, _i64], _int),
+    "gemm_workspace_bytes": ([_i64, _i64, _i64], _i64),
 }
 
 
@@ -124,6 +126,14 @@ def gemm_tile_coord(t: int, tiles_m: int, tiles_n: int, group: int):
     tm, tn = _i64(), _i64()
     st = lib().gemm_tile_coord(t, tiles_m, tiles_n, group, ctypes.byref(tm), ctypes.byref(tn))
     return st, tm.value, tn.value
+
+
+def gemm_set_workspace(ptr, nbytes: int) -> int:
+    return lib().gemm_set_workspace(_p(ptr), int(nbytes))
+
+
+def gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return lib().gemm_workspace_bytes(M, N, K)
 
 
 def gemm_watchdog_selftest(limit_ns: int, stream=None) -> int:

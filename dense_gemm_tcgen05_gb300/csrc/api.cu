@@ -14,6 +14,7 @@
 
 #include "common.h"
 #include "gemm.h"
+#include "ptx.cuh"
 #include "raster.h"
 
 namespace gb300 {
@@ -55,6 +56,8 @@ struct DeviceInfo {
     bool ready = false;
     int cc_major = 0, cc_minor = 0, sms = 0;
     unsigned int* watchdog = nullptr;
+    void* workspace = nullptr;      // caller-registered split-K scratch (gemm_set_workspace)
+    int64_t workspace_bytes = 0;
 };
 
 std::mutex g_mutex;
@@ -65,6 +68,8 @@ std::atomic<int> g_opt_pair{-1};
 std::atomic<int> g_opt_group{8};
 std::atomic<int> g_opt_path{0};
 std::atomic<int> g_opt_max_ctas{0};
+std::atomic<int> g_opt_splits{0};
+std::atomic<int> g_opt_tile_q{0};
 std::atomic<int64_t> g_opt_timeout_ns{2000000000LL};
 
 thread_local cudaError_t t_last_cuda_error = cudaSuccess;
@@ -114,6 +119,25 @@ int current_device(const DeviceInfo** out) {
 }
 
 bool aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+// Q rows per tile (= MMA N) for a problem with M rows of Q.  Cost = padded
+// MMA columns, ceil(M / t) * t, with narrow tiles charged as 96 columns (below
+// that the per-stage P traffic, not the MMA, sets the pace); ties go to the
+// wider tile, which re-reads P fewer times.
+int choose_tile_q(int64_t M, int max_tile_q) {
+    static const int kChoices[] = {256, 192, 128, 64};
+    int best = max_tile_q;
+    int64_t best_cost = INT64_MAX;
+    for (int t : kChoices) {
+        if (t > max_tile_q) continue;
+        const int64_t cost = ((M + t - 1) / t) * (t > 96 ? t : 96);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = t;
+        }
+    }
+    return best;
+}
 
 constexpr int64_t kMaxDim = 0x7fffffffLL;
 
@@ -180,11 +204,14 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
                                        : in == InKind::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     // P = B: N rows of K contiguous elements.  Q = A: M rows of K.  Out = C: N rows of M.
+    const int opt_tq = g_opt_tile_q.load();
+    const int tile_q = opt_tq ? opt_tq : choose_tile_q(M, g.max_tile_q);
+    const int load_q = tile_q / g.cluster;
     CUresult r = CUDA_SUCCESS;
     if (prod == Producer::Tma) {
         r = encode_2d(&L.map_p, in_dt, B, K, N, ldb * es, g.stage_k, g.load_p);
         if (r == CUDA_SUCCESS)
-            r = encode_2d(&L.map_q, in_dt, A, K, M, lda * es, g.stage_k, g.load_q);
+            r = encode_2d(&L.map_q, in_dt, A, K, M, lda * es, g.stage_k, load_q);
     }
     // One staged chunk is one 128-byte row: a box of 128 / os columns x 32 rows.
     if (r == CUDA_SUCCESS && c_tma)
@@ -192,7 +219,7 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
 
     const int64_t tiles_p = (N + g.tile_p - 1) / g.tile_p;
-    const int64_t tiles_q = (M + g.tile_q - 1) / g.tile_q;
+    const int64_t tiles_q = (M + tile_q - 1) / tile_q;
     const int64_t tiles = tiles_p * tiles_q;
     int64_t slots = dev->sms / g.cluster;
     const int cap = g_opt_max_ctas.load();
@@ -212,18 +239,65 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     L.prm.ld_out = ldc;
     L.prm.direct_store = c_tma ? 0 : 1;
     L.prm.k_bytes = K * es;
+    L.prm.tile_q = tile_q;
+    L.prm.idesc = make_idesc(g.format, static_cast<uint32_t>(g.mma_m), static_cast<uint32_t>(tile_q));
+    L.prm.stage_tx_bytes = static_cast<uint32_t>((g.load_p + load_q) * 128);
     L.prm.p_ptr = B;
     L.prm.q_ptr = A;
     L.prm.ld_p_bytes = ldb * es;
     L.prm.ld_q_bytes = lda * es;
     L.grid = static_cast<int>(ctas);
     L.stream = stream;
+
+    // Split-K (shape-aware): when one wave of tiles cannot occupy the GPU and
+    // a workspace is registered, cut each tile's K range into pieces so that
+    // tiles x pieces fills the SMs; each piece still runs >= 4 K stages.
+    L.prm.splits = 1;
+    L.prm.kb_per_split = L.prm.num_kb;
+    {
+        const int opt = g_opt_splits.load();
+        int64_t want = 1;
+        if (opt >= 2) {
+            want = opt;
+        } else if (opt == 0 && tiles < slots) {
+            want = slots / tiles;
+            const int64_t by_k = L.prm.num_kb / 4;
+            if (want > by_k) want = by_k;
+            if (want > 16) want = 16;
+        }
+        if (want > L.prm.num_kb) want = L.prm.num_kb;
+        if (want >= 2) {
+            const int64_t kb_per = (L.prm.num_kb + want - 1) / want;
+            const int64_t pieces = (L.prm.num_kb + kb_per - 1) / kb_per;
+            const int64_t slices = 4 * g.cluster;                    // 32-row slices per tile
+            const int64_t cnt_bytes = ((tiles * slices * 4 + 255) / 256) * 256;
+            const int64_t part_bytes = tiles * pieces * slices * 32 * 256 * 4;
+            void* ws = nullptr;
+            int64_t ws_bytes = 0;
+            {
+                std::lock_guard<std::mutex> lock(g_mutex);
+                ws = dev->workspace;
+                ws_bytes = dev->workspace_bytes;
+            }
+            if (pieces >= 2 && ws && cnt_bytes + part_bytes <= ws_bytes) {
+                L.prm.splits = static_cast<int32_t>(pieces);
+                L.prm.kb_per_split = static_cast<int32_t>(kb_per);
+                L.prm.ws_counters = static_cast<unsigned int*>(ws);
+                L.prm.ws_partials = reinterpret_cast<float*>(static_cast<char*>(ws) + cnt_bytes);
+                e = cudaMemsetAsync(ws, 0, static_cast<size_t>(cnt_bytes), stream);
+                if (e != cudaSuccess) return fail_cuda(e);
+                const int64_t units = tiles * pieces;
+                const int64_t c2 = (units < slots ? units : slots) * g.cluster;
+                L.grid = static_cast<int>(c2);
+            }
+        }
+    }
     if (std::getenv("GEMM_DEBUG"))
         std::fprintf(stderr,
                      "[gemm] tn in=%d M=%lld N=%lld K=%lld pair=%d producer=%d direct_store=%d "
-                     "tiles=%lldx%lld grid=%d\n",
+                     "splits=%d tile_q=%d tiles=%lldx%lld grid=%d\n",
                      int(in), (long long)M, (long long)N, (long long)K, int(pair), int(prod),
-                     L.prm.direct_store,
+                     L.prm.direct_store, L.prm.splits, L.prm.tile_q,
                      (long long)tiles_q, (long long)tiles_p, L.grid);
     e = tc_launch(in, pair, prod, out_f32, L);
     return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
@@ -324,6 +398,13 @@ int gemm_set_option(const char* name, int64_t value) {
     } else if (!std::strcmp(name, "timeout_ns")) {
         if (value < 1000000LL || value > 60000000000LL) return GEMM_ERR_INVALID_OPTION;
         g_opt_timeout_ns.store(value);
+    } else if (!std::strcmp(name, "splits")) {
+        if (value < 0 || value > 64) return GEMM_ERR_INVALID_OPTION;
+        g_opt_splits.store(static_cast<int>(value));
+    } else if (!std::strcmp(name, "tile_q")) {
+        if (!(value == 0 || value == 64 || value == 128 || value == 192 || value == 256))
+            return GEMM_ERR_INVALID_OPTION;
+        g_opt_tile_q.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "max_ctas")) {
         if (value < 0 || value > 1 << 20) return GEMM_ERR_INVALID_OPTION;
         g_opt_max_ctas.store(static_cast<int>(value));
@@ -331,6 +412,27 @@ int gemm_set_option(const char* name, int64_t value) {
         return GEMM_ERR_INVALID_OPTION;
     }
     return GEMM_OK;
+}
+
+int gemm_set_workspace(void* ptr, int64_t bytes) {
+    if (bytes < 0 || (ptr == nullptr && bytes != 0)) return GEMM_ERR_INVALID_DIM;
+    if (ptr && !aligned(ptr, 256)) return GEMM_ERR_MISALIGNED;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_devices[dev].workspace = ptr;
+    g_devices[dev].workspace_bytes = ptr ? bytes : 0;
+    return GEMM_OK;
+}
+
+int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    // Upper bound over the kernel configurations: 16 pieces of every tile of a
+    // pair (256 x 256) or single CTA (128 x 256), plus the counters.
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    const int64_t tiles = ((N + 127) / 128) * ((M + 255) / 256);
+    return ((tiles * 4 * 4 + 255) / 256) * 256 + tiles * 16 * 4 * 32 * 256 * 4;
 }
 
 int gemm_tile_coord(int64_t t, int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t* tm,

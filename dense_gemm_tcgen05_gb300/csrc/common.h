@@ -35,6 +35,20 @@ struct TcParams {
     const void* q_ptr;     // Q (= A) base, for the non-TMA producer
     int64_t ld_p_bytes;    // row pitch of P in bytes (= ldb * element size)
     int64_t ld_q_bytes;    // row pitch of Q in bytes (= lda * element size)
+    // Split-K: each tile's K range is cut into `splits` pieces of kb_per_split
+    // stages; work unit u is tile u / splits, piece u % splits.  With splits > 1
+    // every piece writes its FP32 partial to ws_partials and the last piece to
+    // finish a 32-row slice (counted in ws_counters) sums them and stores C.
+    int32_t splits;
+    int32_t kb_per_split;
+    float* ws_partials;
+    unsigned int* ws_counters;
+    // Q rows per tile = N of the MMA instruction (64, 128, 192 or 256), chosen
+    // per shape; the instruction descriptor and the per-stage TMA byte count
+    // follow from it.
+    int32_t tile_q;
+    uint32_t idesc;
+    uint32_t stage_tx_bytes;
 };
 
 struct TcLaunch {
@@ -46,10 +60,13 @@ struct TcLaunch {
 
 // Tile geometry of one persistent CTA (or CTA pair), for the host's grid sizing.
 struct TcGeometry {
-    int tile_p, tile_q;    // output tile of one CTA (or CTA pair)
-    int load_q, load_p;    // TMA box rows each CTA loads per stage
+    int tile_p;            // P rows of the output tile of one CTA (or CTA pair)
+    int max_tile_q;        // largest Q tile (MMA N)
+    int load_p;            // P rows each CTA loads per stage
     int stage_k;           // K elements per stage
     int cluster;           // CTAs per tile
+    int mma_m;             // M of the MMA instruction
+    uint32_t format;       // A/B format code of the instruction descriptor
 };
 
 // Operand producer of the tensor-core kernel: TMA tensor copies, or (for rows

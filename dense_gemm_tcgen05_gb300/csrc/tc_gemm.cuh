@@ -60,14 +60,13 @@ struct TcCfg {
     static constexpr int kMmaM = PAIR ? 256 : 128;   // M of one MMA instruction
     static constexpr int kMmaN = 256;                // N of one MMA instruction
     static constexpr int kTileP = kMmaM;             // P rows per tile (per pair)
-    static constexpr int kTileQ = kMmaN;             // Q rows per tile
-    static constexpr int kLoadQ = PAIR ? 128 : 256;  // Q rows each CTA loads
+    static constexpr int kMaxLoadQ = kMmaN / (PAIR ? 2 : 1);  // Q rows a CTA loads, at most
     static constexpr int kAtomBytes = 128;           // K bytes per stage row
     static constexpr int kStageK = kAtomBytes / kElemBytes;
     static constexpr int kMmaKBytes = 32;            // K bytes per MMA (16 x 16-bit, 32 x 8-bit)
     static constexpr int kMmasPerStage = kAtomBytes / kMmaKBytes;
     static constexpr int kBytesP = kBlockP * kAtomBytes;
-    static constexpr int kBytesQ = kLoadQ * kAtomBytes;
+    static constexpr int kBytesQ = kMaxLoadQ * kAtomBytes;
     static constexpr int kStageBytes = kBytesP + kBytesQ;
     static constexpr int kStages = PAIR ? 6 : 4;
     static constexpr int kEpiWarps = 4;
@@ -86,10 +85,9 @@ struct TcCfg {
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
     static constexpr uint32_t kFormat = IN == InKind::BF16 ? 1u : 0u;
-    static constexpr uint32_t kIdesc = make_idesc(kFormat, kMmaM, kMmaN);
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kStageBytes % 1024 == 0 && kBytesP % 1024 == 0, "1024-byte stage alignment");
-    static_assert(PAIR || kLoadWarps * 32 == kBlockP + kLoadQ, "load-producer row split");
+    static_assert(PAIR || kLoadWarps * 32 == kBlockP + kMaxLoadQ, "load-producer row split");
 };
 
 // Bounded-wait bookkeeping shared by a CTA's warps.
@@ -290,6 +288,13 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
 
     const Watch wd{abort_flag, prm.watchdog, prm.timeout_ns};
     const int64_t num_tiles = static_cast<int64_t>(prm.tiles_p) * prm.tiles_q;
+    const int64_t num_units = num_tiles * prm.splits;   // (tile, K piece) work units
+    // K stages of work unit u: [kb_lo, kb_hi)
+    auto unit_kb = [&](int64_t u, int32_t& kb_lo, int32_t& kb_hi) {
+        const int32_t piece = static_cast<int32_t>(u % prm.splits);
+        kb_lo = piece * prm.kb_per_split;
+        kb_hi = kb_lo + prm.kb_per_split < prm.num_kb ? kb_lo + prm.kb_per_split : prm.num_kb;
+    };
     const int64_t first = PAIR ? blockIdx.x / 2 : blockIdx.x;
     const int64_t stride = PAIR ? gridDim.x / 2 : gridDim.x;
 
@@ -297,12 +302,14 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         // ------------------------------------------------ TMA producer
         uint32_t it = 0;
         bool ok = true;
-        for (int64_t t = first; ok && t < num_tiles; t += stride) {
+        for (int64_t u = first; ok && u < num_units; u += stride) {
             int64_t tq, tp;
-            raster_tile(t, prm.tiles_q, prm.tiles_p, prm.group, &tq, &tp);
+            raster_tile(u / prm.splits, prm.tiles_q, prm.tiles_p, prm.group, &tq, &tp);
             const int32_t p0 = static_cast<int32_t>(tp * Cfg::kTileP + rank * Cfg::kBlockP);
-            const int32_t q0 = static_cast<int32_t>(tq * Cfg::kTileQ + rank * Cfg::kLoadQ);
-            for (int32_t kb = 0; kb < prm.num_kb; ++kb, ++it) {
+            const int32_t q0 = static_cast<int32_t>(tq * prm.tile_q + rank * (prm.tile_q / Cfg::kCG));
+            int32_t kb_lo, kb_hi;
+            unit_kb(u, kb_lo, kb_hi);
+            for (int32_t kb = kb_lo; kb < kb_hi; ++kb, ++it) {
                 const uint32_t s = it % S, ph = (it / S) & 1u;
                 if (!warp_wait(empty_bar(s), ph ^ 1u, wd)) {
                     ok = false;
@@ -314,11 +321,11 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                     const int32_t kx = kb * Cfg::kStageK;
                     if constexpr (PAIR) {
                         const uint32_t fb = mapa_shared(full_bar(s), 0);
-                        if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * Cfg::kStageBytes);
+                        if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * prm.stage_tx_bytes);
                         tma_load_2d_pair(sp, &map_p, fb, kx, p0);
                         tma_load_2d_pair(sq, &map_q, fb, kx, q0);
                     } else {
-                        mbar_arrive_expect_tx(full_bar(s), Cfg::kStageBytes);
+                        mbar_arrive_expect_tx(full_bar(s), prm.stage_tx_bytes);
                         tma_load_2d(sp, &map_p, full_bar(s), kx, p0);
                         tma_load_2d(sq, &map_q, full_bar(s), kx, q0);
                     }
@@ -350,7 +357,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         // pitch per quad, and the swizzle row (r % 8) is i.
         constexpr int kPeriod = 16 / Cfg::kElemBytes;        // rows sharing one delta
         constexpr int kQuadsPerWarp = 8;
-        static_assert(!LOADS || (Cfg::kBlockP + Cfg::kLoadQ) / 4 == kQuadsPerWarp * Cfg::kLoadWarps,
+        static_assert(!LOADS || (Cfg::kBlockP + Cfg::kMaxLoadQ) / 4 == kQuadsPerWarp * Cfg::kLoadWarps,
                       "quad split");
         const uint32_t pw = warp - Cfg::kFirstLoadWarp;
         const uint32_t sub = lane >> 3, c = lane & 7u;
@@ -363,13 +370,19 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         const uint32_t srow0 = r0 * Cfg::kAtomBytes;  // P then Q are contiguous, 128 B a row
         uint32_t it = 0;
         bool ok = true;
-        for (int64_t t = first; ok && t < num_tiles; t += stride) {
+        for (int64_t u = first; ok && u < num_units; u += stride) {
             int64_t tq, tp;
-            raster_tile(t, prm.tiles_q, prm.tiles_p, prm.group, &tq, &tp);
-            const int64_t g0 = is_p ? tp * Cfg::kTileP + r0 : tq * Cfg::kTileQ + (r0 - Cfg::kBlockP);
+            raster_tile(u / prm.splits, prm.tiles_q, prm.tiles_p, prm.group, &tq, &tp);
+            const int64_t g0 = is_p ? tp * Cfg::kTileP + r0 : tq * prm.tile_q + (r0 - Cfg::kBlockP);
             const uint8_t* row0 = mat + g0 * pitch;   // address arithmetic only
-            const int64_t rows_left = rows_lim - g0;  // quad i exists iff i < rows_left
-            for (int32_t kb = 0; kb < prm.num_kb; ++kb, ++it) {
+            // quad i exists iff i < rows_left: inside the matrix and, for Q,
+            // inside this tile's tile_q rows (the rest of the stage is unused)
+            int64_t rows_left = rows_lim - g0;
+            if (!is_p && prm.tile_q - static_cast<int64_t>(r0 - Cfg::kBlockP) < rows_left)
+                rows_left = prm.tile_q - static_cast<int64_t>(r0 - Cfg::kBlockP);
+            int32_t kb_lo, kb_hi;
+            unit_kb(u, kb_lo, kb_hi);
+            for (int32_t kb = kb_lo; kb < kb_hi; ++kb, ++it) {
                 const uint32_t s = it % S, ph = (it / S) & 1u;
                 const int64_t kb_byte = static_cast<int64_t>(kb) * Cfg::kAtomBytes;
                 const int64_t left = prm.k_bytes - kb_byte;
@@ -416,7 +429,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         if (!PAIR || leader) {
             uint32_t it = 0, lt = 0;
             bool ok = true;
-            for (int64_t t = first; ok && t < num_tiles; t += stride, ++lt) {
+            for (int64_t u = first; ok && u < num_units; u += stride, ++lt) {
                 const uint32_t b = lt & 1u, aph = (lt >> 1) & 1u;
                 if (!warp_wait(acce_bar(b), aph ^ 1u, wd)) {
                     ok = false;
@@ -424,7 +437,9 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * Cfg::kAccCols;
-                for (int32_t kb = 0; kb < prm.num_kb; ++kb, ++it) {
+                int32_t kb_lo, kb_hi;
+                unit_kb(u, kb_lo, kb_hi);
+                for (int32_t kb = kb_lo; kb < kb_hi; ++kb, ++it) {
                     const uint32_t s = it % S, ph = (it / S) & 1u;
                     if (!warp_wait(full_bar(s), ph, wd)) {
                         ok = false;
@@ -439,11 +454,11 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                         for (int kk = 0; kk < Cfg::kMmasPerStage; ++kk) {
                             // advance the start address by 32 bytes of K per MMA
                             const uint64_t off = static_cast<uint64_t>(kk * (Cfg::kMmaKBytes >> 4));
-                            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+                            const uint32_t acc = (kb != kb_lo || kk != 0) ? 1u : 0u;
                             if constexpr (IN == InKind::E4M3)
-                                mma_f8<Cfg::kCG>(d_tmem, adesc + off, bdesc + off, Cfg::kIdesc, acc);
+                                mma_f8<Cfg::kCG>(d_tmem, adesc + off, bdesc + off, prm.idesc, acc);
                             else
-                                mma_f16<Cfg::kCG>(d_tmem, adesc + off, bdesc + off, Cfg::kIdesc, acc);
+                                mma_f16<Cfg::kCG>(d_tmem, adesc + off, bdesc + off, prm.idesc, acc);
                         }
                         commit_to<Cfg::kCG>(empty_bar(s), 0x3);
                     }
@@ -471,14 +486,134 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         constexpr int kOB = static_cast<int>(sizeof(OutT));   // output bytes: 2 or 4
         constexpr int kCols = 128 / kOB;                        // columns per chunk
         constexpr int kGran = 16 / kOB;                         // elements per 16-byte granule
-        constexpr int kChunks = Cfg::kAccCols / kCols;
+        const int chunks = prm.tile_q / kCols;
+        constexpr int kSlices = (PAIR ? 2 : 1) * Cfg::kEpiWarps;  // 32-row slices per tile
+        constexpr int kSliceFloats = 32 * Cfg::kAccCols;
         const uint32_t quarter = warp & 3u;     // TMEM lanes this warp may access
         const uint32_t ew = warp - 2u;          // staging buffers owned by this warp
         const uint32_t stage0 = base + Cfg::kOffEpi + ew * 2u * Cfg::kEpiBufBytes;
+        const uint32_t slice = rank * Cfg::kEpiWarps + quarter;
         const float scale = prm.scale;
         uint8_t* const out8 = static_cast<uint8_t*>(prm.out);
         uint32_t lt = 0, chunk = 0;
-        for (int64_t t = first; t < num_tiles; t += stride, ++lt) {
+
+        // Converts 32 words' worth of FP32 values (kCols of them) into this
+        // lane's 128 output bytes.
+        auto pack = [&](const float* f, uint32_t (&pk)[32]) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if constexpr (kOB == 2) {
+                    float lo = f[2 * j], hi = f[2 * j + 1];
+                    if constexpr (IN == InKind::E4M3) {
+                        lo *= scale;
+                        hi *= scale;
+                    }
+                    pk[j] = pack2<OutT>(lo, hi);
+                } else {
+                    float v = f[j];
+                    if constexpr (IN == InKind::E4M3) v *= scale;
+                    pk[j] = __float_as_uint(v);
+                }
+            }
+        };
+
+        // Writes this warp's packed chunk (rows row0 + lane, columns [x, x + kCols)).
+        auto emit = [&](const uint32_t (&pk)[32], int32_t x, int32_t row0) {
+            const bool in_range = x < prm.rows_q && row0 < prm.rows_p;
+            const uint32_t buf = stage0 + (chunk & 1u) * Cfg::kEpiBufBytes;
+            ++chunk;
+            if (!prm.direct_store && in_range && x + kCols > prm.rows_q &&
+                (prm.rows_q % kGran) != 0) {
+                // A TMA store writes whole 16-byte granules of the contiguous
+                // dimension, so a chunk that ends inside a granule would spill
+                // into the caller's padding between rows_q and ld_out: store it
+                // element by element.
+                const int32_t r = row0 + static_cast<int32_t>(lane);
+                if (r < prm.rows_p) {
+                    uint8_t* dst = out8 + (static_cast<int64_t>(r) * prm.ld_out + x) * kOB;
+                    const int32_t ncols = prm.rows_q - x;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if constexpr (kOB == 2) {
+                            uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+                            if (2 * j < ncols) d16[2 * j] = static_cast<uint16_t>(pk[j] & 0xFFFFu);
+                            if (2 * j + 1 < ncols) d16[2 * j + 1] = static_cast<uint16_t>(pk[j] >> 16);
+                        } else {
+                            if (j < ncols) reinterpret_cast<uint32_t*>(dst)[j] = pk[j];
+                        }
+                    }
+                }
+                // Keep one bulk group per chunk: the staging buffers alternate
+                // with the chunk count, and the wait before a buffer is reused
+                // counts groups, so a skipped group would let the next chunk
+                // overwrite a buffer an earlier TMA store is still reading.
+                if (lane == 0) bulk_commit_group();
+                __syncwarp();
+                return;
+            }
+            if (!prm.direct_store) {
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+            }
+            // Row `lane` of the 32 x 128-byte box; 16-byte chunk j is stored at
+            // chunk j ^ (row % 8), the TMA 128-byte swizzle pattern.
+            const uint32_t row_addr = buf + lane * 128u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), pk[4 * j],
+                             pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            if (!prm.direct_store) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (in_range) tma_store_2d(&map_out, buf, x, row0);
+                    bulk_commit_group();
+                }
+            } else if (in_range) {
+                // D rows are not 16-byte aligned: the warp writes the box one row
+                // at a time, lane l storing bytes [4l, 4l + 4) of the row
+                // (elements 2l, 2l + 1 of a 16-bit output, element l of fp32).
+                __syncwarp();
+                constexpr int kPerLane = 4 / kOB;
+                const int32_t m = x + kPerLane * static_cast<int32_t>(lane);
+                const uint32_t lane_off = ((lane >> 2) << 4) + ((lane & 3u) << 2);
+                for (int r = 0; r < 32; ++r) {
+                    const int32_t grow = row0 + r;
+                    if (grow >= prm.rows_p) break;
+                    const uint32_t v = ld_shared_u32(
+                        buf + r * 128u + (lane_off ^ ((static_cast<uint32_t>(r) & 7u) << 4)));
+                    uint8_t* dst = out8 + (static_cast<int64_t>(grow) * prm.ld_out + m) * kOB;
+                    if (m + kPerLane - 1 < prm.rows_q) {
+                        if ((reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+                            *reinterpret_cast<uint32_t*>(dst) = v;
+                        } else {
+                            reinterpret_cast<uint16_t*>(dst)[0] = static_cast<uint16_t>(v & 0xFFFFu);
+                            reinterpret_cast<uint16_t*>(dst)[1] = static_cast<uint16_t>(v >> 16);
+                        }
+                    } else if (m < prm.rows_q) {  // 16-bit output only
+                        reinterpret_cast<uint16_t*>(dst)[0] = static_cast<uint16_t>(v & 0xFFFFu);
+                    }
+                }
+                __syncwarp();
+            } else {
+                __syncwarp();
+            }
+        };
+
+        auto release_acc = [&](uint32_t b) {
+            // The accumulator has been read: hand it back to the MMA warp.
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
+                else
+                    mbar_arrive(acce_bar(b));
+            }
+        };
+
+        for (int64_t u = first; u < num_units; u += stride, ++lt) {
+            const int64_t t = u / prm.splits;
             int64_t tq, tp;
             raster_tile(t, prm.tiles_q, prm.tiles_p, prm.group, &tq, &tp);
             const uint32_t b = lt & 1u, aph = (lt >> 1) & 1u;
@@ -486,116 +621,67 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
             tc_fence_after_sync();
             const int32_t row0 =
                 static_cast<int32_t>(tp * Cfg::kTileP + rank * Cfg::kBlockP + quarter * 32);
-            const int32_t col0 = static_cast<int32_t>(tq * Cfg::kTileQ);
+            const int32_t col0 = static_cast<int32_t>(tq * prm.tile_q);
             const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + b * Cfg::kAccCols;
+            if (prm.splits == 1) {
 #pragma unroll 1
-            for (int c = 0; c < kChunks; ++c) {
-                uint32_t v0[32], v1[32];
-                tmem_ld_32x32b_x32(t_row + c * kCols, v0);
-                if constexpr (kOB == 2) tmem_ld_32x32b_x32(t_row + c * kCols + 32, v1);
-                tmem_wait_ld();
-                if (c == kChunks - 1) {
-                    // The accumulator has been read: hand it back to the MMA warp.
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (PAIR)
-                            mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
-                        else
-                            mbar_arrive(acce_bar(b));
-                    }
-                }
-                // pk: the chunk's 128 output bytes of this lane's row, as words
-                uint32_t pk[32];
+                for (int c = 0; c < chunks; ++c) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld_32x32b_x32(t_row + c * kCols, v0);
+                    if constexpr (kCols == 64) tmem_ld_32x32b_x32(t_row + c * kCols + 32, v1);
+                    tmem_wait_ld();
+                    if (c == chunks - 1) release_acc(b);
+                    float f[kCols];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if constexpr (kOB == 2) {
-                        float lo = __uint_as_float(j < 16 ? v0[2 * j] : v1[2 * j - 32]);
-                        float hi = __uint_as_float(j < 16 ? v0[2 * j + 1] : v1[2 * j - 31]);
-                        if constexpr (IN == InKind::E4M3) {
-                            lo *= scale;
-                            hi *= scale;
-                        }
-                        pk[j] = pack2<OutT>(lo, hi);
-                    } else {
-                        float f = __uint_as_float(v0[j]);
-                        if constexpr (IN == InKind::E4M3) f *= scale;
-                        pk[j] = __float_as_uint(f);
-                    }
+                    for (int j = 0; j < kCols; ++j)
+                        f[j] = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
+                    uint32_t pk[32];
+                    pack(f, pk);
+                    emit(pk, col0 + c * kCols, row0);
                 }
-                const int32_t x = col0 + c * kCols;
-                const bool in_range = x < prm.rows_q && row0 < prm.rows_p;
-                const uint32_t buf = stage0 + (chunk & 1u) * Cfg::kEpiBufBytes;
-                ++chunk;
-                if (!prm.direct_store && in_range && x + kCols > prm.rows_q &&
-                    (prm.rows_q % kGran) != 0) {
-                    // A TMA store writes whole 16-byte granules of the contiguous
-                    // dimension, so a chunk that ends inside a granule would
-                    // spill into the caller's padding between rows_q and ld_out:
-                    // store it element by element.
-                    const int32_t r = row0 + static_cast<int32_t>(lane);
-                    if (r < prm.rows_p) {
-                        uint8_t* dst = out8 + (static_cast<int64_t>(r) * prm.ld_out + x) * kOB;
-                        const int32_t ncols = prm.rows_q - x;
+            } else {
+                // This K piece's partial sums -> workspace, column-major within
+                // the slice so that a warp's stores (and loads) are coalesced.
+                const int32_t piece = static_cast<int32_t>(u % prm.splits);
+                float* part = prm.ws_partials +
+                              ((t * prm.splits + piece) * kSlices + slice) * kSliceFloats;
+#pragma unroll 1
+                for (int c = 0; c < prm.tile_q / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(t_row + c * 32, v);
+                    tmem_wait_ld();
+                    if (c == prm.tile_q / 32 - 1) release_acc(b);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            if constexpr (kOB == 2) {
-                                uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
-                                if (2 * j < ncols) d16[2 * j] = static_cast<uint16_t>(pk[j] & 0xFFFFu);
-                                if (2 * j + 1 < ncols) d16[2 * j + 1] = static_cast<uint16_t>(pk[j] >> 16);
-                            } else {
-                                if (j < ncols) reinterpret_cast<uint32_t*>(dst)[j] = pk[j];
-                            }
-                        }
-                    }
-                    continue;
+                    for (int j = 0; j < 32; ++j)
+                        __stcg(part + (c * 32 + j) * 32 + lane, __uint_as_float(v[j]));
                 }
-                if (!prm.direct_store) {
-                    if (lane == 0) bulk_wait_group_read<1>();
-                    __syncwarp();
-                }
-                // Row `lane` of the 32 x 128-byte box; 16-byte chunk j is stored
-                // at chunk j ^ (row % 8), the TMA 128-byte swizzle pattern.
-                const uint32_t row_addr = buf + lane * 128u;
+                __threadfence();
+                __syncwarp();
+                unsigned int prev = 0;
+                unsigned int* counter = prm.ws_counters + t * kSlices + slice;
+                if (lane == 0) prev = atomicAdd(counter, 1u);
+                prev = __shfl_sync(0xffffffffu, prev, 0);
+                if (prev + 1 != static_cast<unsigned int>(prm.splits)) continue;
+                // Last piece of this slice: sum all pieces in piece order (the
+                // result does not depend on which piece finished last).
+                __threadfence();
+                if (lane == 0) *counter = 0u;  // ready for the next call
+                const float* base_part =
+                    prm.ws_partials + (t * prm.splits * kSlices + slice) * kSliceFloats;
+#pragma unroll 1
+                for (int c = 0; c < chunks; ++c) {
+                    float f[kCols];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
-                                 pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                if (!prm.direct_store) {
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (in_range) tma_store_2d(&map_out, buf, x, row0);
-                        bulk_commit_group();
+                    for (int j = 0; j < kCols; ++j) f[j] = 0.f;
+                    for (int32_t pc = 0; pc < prm.splits; ++pc) {
+                        const float* src = base_part + static_cast<int64_t>(pc) * kSlices * kSliceFloats;
+#pragma unroll
+                        for (int j = 0; j < kCols; ++j)
+                            f[j] += __ldcg(src + (c * kCols + j) * 32 + lane);
                     }
-                } else if (in_range) {
-                    // D rows are not 16-byte aligned: the warp writes the box one
-                    // row at a time, lane l storing bytes [4l, 4l + 4) of the row
-                    // (elements 2l, 2l + 1 of a 16-bit output, element l of fp32).
-                    __syncwarp();
-                    constexpr int kPerLane = 4 / kOB;
-                    const int32_t m = x + kPerLane * static_cast<int32_t>(lane);
-                    const uint32_t lane_off = ((lane >> 2) << 4) + ((lane & 3u) << 2);
-                    for (int r = 0; r < 32; ++r) {
-                        const int32_t grow = row0 + r;
-                        if (grow >= prm.rows_p) break;
-                        const uint32_t v = ld_shared_u32(
-                            buf + r * 128u + (lane_off ^ ((static_cast<uint32_t>(r) & 7u) << 4)));
-                        uint8_t* dst = out8 + (static_cast<int64_t>(grow) * prm.ld_out + m) * kOB;
-                        if (m + kPerLane - 1 < prm.rows_q) {
-                            if ((reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
-                                *reinterpret_cast<uint32_t*>(dst) = v;
-                            } else {
-                                reinterpret_cast<uint16_t*>(dst)[0] = static_cast<uint16_t>(v & 0xFFFFu);
-                                reinterpret_cast<uint16_t*>(dst)[1] = static_cast<uint16_t>(v >> 16);
-                            }
-                        } else if (m < prm.rows_q) {  // 16-bit output only
-                            reinterpret_cast<uint16_t*>(dst)[0] = static_cast<uint16_t>(v & 0xFFFFu);
-                        }
-                    }
-                    __syncwarp();
-                } else {
-                    __syncwarp();
+                    uint32_t pk[32];
+                    pack(f, pk);
+                    emit(pk, col0 + c * kCols, row0);
                 }
             }
         }
@@ -657,10 +743,12 @@ template <InKind IN>
 TcGeometry tc_geometry_impl(bool pair) {
     if (pair) {
         using Cfg = TcCfg<IN, true, false>;
-        return TcGeometry{Cfg::kTileP, Cfg::kTileQ, Cfg::kLoadQ, Cfg::kBlockP, Cfg::kStageK, 2};
+        return TcGeometry{Cfg::kTileP, Cfg::kMmaN, Cfg::kBlockP, Cfg::kStageK, 2, Cfg::kMmaM,
+                          Cfg::kFormat};
     }
     using Cfg = TcCfg<IN, false, false>;
-    return TcGeometry{Cfg::kTileP, Cfg::kTileQ, Cfg::kLoadQ, Cfg::kBlockP, Cfg::kStageK, 1};
+    return TcGeometry{Cfg::kTileP, Cfg::kMmaN, Cfg::kBlockP, Cfg::kStageK, 1, Cfg::kMmaM,
+                      Cfg::kFormat};
 }
 
 }  // namespace gb300

@@ -147,9 +147,31 @@ int gemm_read_watchdog(int reset);
  *                 tensor-core kernel's load-based producer (as for unaligned rows)
  *   "timeout_ns"  device wait limit in ns, 1e6..6e10 (default 2e9)
  *   "max_ctas"    cap on persistent CTAs, 0 = one per SM (default)
+ *   "tile_q"      output tile width along M (= MMA N): 0 auto (default, by
+ *                 padding cost), or 64, 128, 192, 256
+ *   "splits"      K pieces per tile: 0 auto (default, needs a workspace), 1 never
+ *                 split, 2..64 split that many ways when the workspace suffices
  * Returns GEMM_OK or GEMM_ERR_INVALID_OPTION.
  */
 int gemm_set_option(const char* name, int64_t value);
+
+/*
+ * gemm_set_workspace -- registers caller-owned device scratch for the current
+ * device (ptr 256-byte aligned, `bytes` long; NULL, 0 unregisters).  With a
+ * workspace registered, TN calls whose output tiles cannot fill the GPU in one
+ * wave split K: each K piece writes its FP32 partial tile to the workspace and
+ * the last piece to finish a 32-row slice sums the pieces in piece order (so
+ * the result does not depend on timing) and stores C.  Calls that split K on
+ * the same device share the workspace, so they must not overlap in time
+ * (issue them on one stream, or register a workspace per device and stream
+ * order them).  The library never frees or reallocates the buffer.  Option
+ * "splits" (gemm_set_option) forces or disables splitting.  Returns GEMM_OK,
+ * GEMM_ERR_MISALIGNED or GEMM_ERR_INVALID_DIM.
+ */
+int gemm_set_workspace(void* ptr, int64_t bytes);
+
+/* Workspace bytes that suffice for any split of an M x N x K TN call. */
+int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
  * gemm_tile_coord -- the persistent kernels' tile rasteriser, exported for

@@ -70,6 +70,18 @@ def test_options():
     assert capi.gemm_set_option("group", 8) == 0
     assert capi.gemm_set_option("timeout_ns", 10) == capi.GEMM_ERR_INVALID_OPTION
     assert capi.gemm_set_option("nonsense", 1) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("splits", 65) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("splits", 0) == 0
+    assert capi.gemm_set_option("tile_q", 96) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("tile_q", 192) == 0
+    assert capi.gemm_set_option("tile_q", 0) == 0
+
+
+def test_workspace_size_bound():
+    # 16 pieces of every 128 x 256 tile, 32 KB per 32-row slice, plus counters
+    tiles = (1024 // 128) * (512 // 256)
+    assert capi.gemm_workspace_bytes(512, 1024, 64) >= tiles * 16 * 4 * 32 * 1024
+    assert capi.gemm_workspace_bytes(0, 1, 1) == 0
 
 
 @pytest.mark.parametrize("tiles_m,tiles_n,group", [(1, 1, 8), (32, 64, 8), (16, 12, 8),

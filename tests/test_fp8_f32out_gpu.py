@@ -118,3 +118,20 @@ def test_page_fp16_shapes_sampled(shape):
     ops = si.tn_operands("f16", M, N, K, dist="normal", seed=2, sigma=0.1)
     C = run_tn("f16", ops, M, N, K)
     check_sampled("f16", ops, M, N, K, C, seed=2)
+
+
+@pytest.mark.parametrize("tile_q", [64, 128, 192, 256])
+@pytest.mark.parametrize("M", [257, 450, 385])
+def test_ragged_chunk_then_more_chunks(tile_q, M):
+    """A ragged last chunk (M not a multiple of the 16-byte granule) followed by
+    out-of-range chunks of the same tile, with TMA-stored C (ldc multiple of 4):
+    the staging buffers must not be reused while a store still reads them."""
+    N, K = 129, 65
+    assert capi.gemm_set_option("tile_q", tile_q) == 0
+    try:
+        ops = si.tn_operands("e4m3", M, N, K, dist="pm1", seed=M + tile_q)
+        C = run(ops, M, N, K, ldc=M + (4 - M % 4) % 4 + 4)
+        exact = oracle.gemm_tn("e4m3", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+        np.testing.assert_array_equal(C[:N, :M].numpy().T, exact.astype(np.float32))
+    finally:
+        capi.gemm_set_option("tile_q", 0)

@@ -289,3 +289,32 @@ def test_fp8_sampled(shape, pair_mode):
     ops = si.tn_operands("e4m3", M, N, K, dist="normal", seed=4)
     C = run_tn("e4m3", ops, M, N, K)
     check_sampled("e4m3", ops, M, N, K, C, seed=4)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("tile_q", [64, 128, 192, 256])
+@pytest.mark.parametrize("mode", ["cta1", "pair", "loads"])
+def test_tile_q_variants(kind, tile_q, mode):
+    """Every output tile width along M, with each producer / CTA grouping."""
+    M, N, K = 450, 300, 333
+    assert capi.gemm_set_option("tile_q", tile_q) == 0
+    assert capi.gemm_set_option("pair", 1 if mode == "pair" else 0) == 0
+    assert capi.gemm_set_option("path", 2 if mode == "loads" else 0) == 0
+    try:
+        ops = si.tn_operands(kind, M, N, K, dist="normal", seed=tile_q, sigma=0.5)
+        C = run_tn(kind, ops, M, N, K)
+        check_full(kind, ops, M, N, K, C)
+    finally:
+        capi.gemm_set_option("tile_q", 0)
+        capi.gemm_set_option("pair", -1)
+        capi.gemm_set_option("path", 0)
+
+
+@pytest.mark.parametrize("M", [1, 16, 64, 100, 128, 200, 300])
+def test_skinny_m_auto_tile(M):
+    """Small M picks a narrow tile; results stay bit-exact on +-1 inputs."""
+    N, K = 1000, 512
+    ops = si.tn_operands("bf16", M, N, K, dist="pm1", seed=M)
+    C = run_tn("bf16", ops, M, N, K)
+    exact = oracle.gemm_tn("bf16", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+    assert_codes_equal(out_codes(C, M, N), exact_codes("bf16", exact))
