@@ -26,6 +26,7 @@ GEMM_ERR_UNSUPPORTED_DEVICE = 5
 GEMM_ERR_LAUNCH = 6
 GEMM_ERR_TIMEOUT = 7
 GEMM_ERR_INVALID_OPTION = 8
+GEMM_ERR_SCRATCH = 9
 
 _lock = threading.Lock()
 _lib = None
@@ -43,6 +44,7 @@ _SIGNATURES = {
     "gemm_tile_coord": ([_i64, _i64, _i64, _i64, ctypes.POINTER(_i64), ctypes.POINTER(_i64)], _int),
     "gemm_watchdog_selftest": ([_i64, _vp], _int),
     "gemm_set_workspace": ([_vp, _i64], _int),
+    "gemm_bf16_tn_noalloc": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i64, _vp], _int),
     "gemm_workspace_bytes": ([_i64, _i64, _i64], _i64),
 }
 
@@ -130,6 +132,11 @@ def gemm_tile_coord(t: int, tiles_m: int, tiles_n: int, group: int):
 
 def gemm_set_workspace(ptr, nbytes: int) -> int:
     return lib().gemm_set_workspace(_p(ptr), int(nbytes))
+
+
+def gemm_bf16_tn_noalloc(M, N, K, A, lda, B, ldb, C, ldc, splits=0, stream=None) -> int:
+    return lib().gemm_bf16_tn_noalloc(M, N, K, _p(A), lda, _p(B), ldb, _p(C), ldc, int(splits),
+                                      _p(stream))
 
 
 def gemm_workspace_bytes(M: int, N: int, K: int) -> int:

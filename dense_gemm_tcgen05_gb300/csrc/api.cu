@@ -155,9 +155,14 @@ CUresult encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, in
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// `ov`, when given, replaces the registered workspace and the "splits" option:
+// the call splits K with that scratch (ov->splits: 0 by the automatic rule,
+// >= 2 forced, 1 never) and fails with GEMM_ERR_SCRATCH when the split it
+// chooses needs more than ov->bytes.  Every public entry point but the
+// no-allocation one passes nullptr.
 int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void* A,
             int64_t lda, const void* B, int64_t ldb, float scale, void* C, int64_t ldc,
-            void* stream_v) {
+            void* stream_v, const ScratchOverride* ov = nullptr) {
     const int es = in == InKind::E4M3 ? 1 : 2;
     const int os = out_f32 ? 4 : 2;  // output element size
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
@@ -255,7 +260,7 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     L.prm.splits = 1;
     L.prm.kb_per_split = L.prm.num_kb;
     {
-        const int opt = g_opt_splits.load();
+        const int opt = ov ? ov->splits : g_opt_splits.load();
         int64_t want = 1;
         if (opt >= 2) {
             want = opt;
@@ -274,7 +279,11 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
             const int64_t part_bytes = tiles * pieces * slices * 32 * 256 * 4;
             void* ws = nullptr;
             int64_t ws_bytes = 0;
-            {
+            if (ov) {
+                ws = ov->ptr;
+                ws_bytes = ov->bytes;
+                if (pieces >= 2 && cnt_bytes + part_bytes > ws_bytes) return GEMM_ERR_SCRATCH;
+            } else {
                 std::lock_guard<std::mutex> lock(g_mutex);
                 ws = dev->workspace;
                 ws_bytes = dev->workspace_bytes;
@@ -304,6 +313,14 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
 }
 
 }  // namespace
+
+namespace gb300 {
+int gemm_tn_with_scratch(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                         const void* B, int64_t ldb, void* C, int64_t ldc, void* stream,
+                         const ScratchOverride& ov) {
+    return gemm_tn(in, false, M, N, K, A, lda, B, ldb, 1.0f, C, ldc, stream, &ov);
+}
+}  // namespace gb300
 
 extern "C" {
 
@@ -363,6 +380,8 @@ const char* gemm_status_string(int status) {
             return t_status_buf;
         case GEMM_ERR_TIMEOUT: return "a device-side wait ran out of time";
         case GEMM_ERR_INVALID_OPTION: return "unknown option or value out of range";
+        case GEMM_ERR_SCRATCH:
+            return "the call needs more split-K scratch than the library's static array holds";
         default: return "unknown status";
     }
 }

@@ -83,6 +83,19 @@ cudaError_t tn_fallback_launch(InKind in, bool out_f32, int64_t M, int64_t N, in
                                const void* A, int64_t lda, const void* B, int64_t ldb, float scale,
                                void* C, int64_t ldc, cudaStream_t stream);
 
+// Scratch supplied by the caller of the internal TN path instead of the
+// registered workspace (see gemm_tn_with_scratch).
+struct ScratchOverride {
+    void* ptr;       // device address, 256-byte aligned
+    int64_t bytes;   // usable bytes at ptr
+    int splits;      // 0 automatic, 1 never split, >= 2 that many K pieces
+};
+
+// The TN path with explicit split-K scratch (16-bit inputs and output).
+int gemm_tn_with_scratch(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                         const void* B, int64_t ldb, void* C, int64_t ldc, void* stream,
+                         const ScratchOverride& ov);
+
 cudaError_t f32_launch(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                        const float* B, int64_t ldb, float* C, int64_t ldc, cudaStream_t stream);
 

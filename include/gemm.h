@@ -46,6 +46,7 @@ extern "C" {
 #define GEMM_ERR_LAUNCH 6             /* a CUDA runtime error; see gemm_status_string */
 #define GEMM_ERR_TIMEOUT 7            /* a device-side wait ran out (gemm_read_watchdog) */
 #define GEMM_ERR_INVALID_OPTION 8     /* unknown option name or value (gemm_set_option) */
+#define GEMM_ERR_SCRATCH 9            /* split needs more than gemm_bf16_tn_noalloc's scratch */
 
 /*
  * gemm_f32 -- FP32 GEMM, every matrix row-major ("Optimizing GEMM in HIP":
@@ -172,6 +173,32 @@ int gemm_set_workspace(void* ptr, int64_t bytes);
 
 /* Workspace bytes that suffice for any split of an M x N x K TN call. */
 int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * gemm_bf16_tn_noalloc -- gemm_bf16_tn with split-K scratch taken from a fixed
+ * array inside the library instead of caller memory, so the call allocates
+ * nothing and needs no registered workspace.  (The pages have no counterpart:
+ * this entry point exists for callers that may not call cudaMalloc -- code
+ * whose device memory belongs to a pooled allocator it must not bypass,
+ * plugins whose host forbids device allocation, latency-critical loops where
+ * an allocation would synchronise the device.)
+ *
+ * Arguments and layouts are those of gemm_bf16_tn, plus `splits`: 0 splits K
+ * by the automatic rule (only when the output tiles cannot fill the GPU), 1
+ * never splits, 2..64 forces that many K pieces.  The array holds
+ * GEMM_NOALLOC_SCRATCH_BYTES (24 MiB) on every GPU that loads the library,
+ * until the library is unloaded; a split whose partial sums need more returns
+ * GEMM_ERR_SCRATCH without launching anything (the automatic rule needs at
+ * most ~20 MiB on a 152-SM GPU).  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current; make
+ * that first call before any stream capture.  All calls share the array and it
+ * keeps the last call's contents (the split counters are zeroed before each
+ * split launch): calls that overlap in time on the GPU race.
+ */
+#define GEMM_NOALLOC_SCRATCH_BYTES (24LL << 20)
+int gemm_bf16_tn_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                         const void* B, int64_t ldb, void* C, int64_t ldc, int64_t splits,
+                         void* stream);
 
 /*
  * gemm_tile_coord -- the persistent kernels' tile rasteriser, exported for

@@ -26,7 +26,7 @@ def test_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for st in range(9):
+    for st in range(10):
         assert capi.status_text(st) and capi.status_text(st) != "unknown status"
     assert capi.status_text(99) == "unknown status"
 
