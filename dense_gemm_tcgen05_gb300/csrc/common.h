@@ -49,10 +49,18 @@ struct TcParams {
     int32_t tile_q;
     uint32_t idesc;
     uint32_t stage_tx_bytes;
+    // Tail splitting: the first full_units units are whole tiles (times K
+    // pieces); the remaining tiles of the last, partial wave are cut into
+    // tail_f narrower units of tile_q / tail_f rows of Q each, loaded through
+    // the tail tensor map with their own instruction descriptor and stage bytes.
+    int64_t full_units;
+    int32_t tail_f;
+    uint32_t idesc_tail;
+    uint32_t stage_tx_tail;
 };
 
 struct TcLaunch {
-    CUtensorMap map_p, map_q, map_out;
+    CUtensorMap map_p, map_q, map_out, map_q_tail;
     TcParams prm;
     int grid;
     cudaStream_t stream;

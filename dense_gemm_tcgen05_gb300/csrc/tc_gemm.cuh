@@ -233,7 +233,8 @@ template <InKind IN, typename OutT, bool PAIR, bool LOADS>
 __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
                    const __grid_constant__ CUtensorMap map_q,
-                   const __grid_constant__ CUtensorMap map_out, const TcParams prm) {
+                   const __grid_constant__ CUtensorMap map_out,
+                   const __grid_constant__ CUtensorMap map_q_tail, const TcParams prm) {
     using Cfg = TcCfg<IN, PAIR, LOADS>;
     constexpr int S = Cfg::kStages;
 
@@ -273,6 +274,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         if (!LOADS) {
             prefetch_tensormap(&map_p);
             prefetch_tensormap(&map_q);
+            if (prm.tail_f > 1) prefetch_tensormap(&map_q_tail);
         }
         if (!prm.direct_store) prefetch_tensormap(&map_out);
     }
@@ -288,12 +290,39 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
 
     const Watch wd{abort_flag, prm.watchdog, prm.timeout_ns};
     const int64_t num_tiles = static_cast<int64_t>(prm.tiles_p) * prm.tiles_q;
-    const int64_t num_units = num_tiles * prm.splits;   // (tile, K piece) work units
-    // K stages of work unit u: [kb_lo, kb_hi)
-    auto unit_kb = [&](int64_t u, int32_t& kb_lo, int32_t& kb_hi) {
-        const int32_t piece = static_cast<int32_t>(u % prm.splits);
-        kb_lo = piece * prm.kb_per_split;
-        kb_hi = kb_lo + prm.kb_per_split < prm.num_kb ? kb_lo + prm.kb_per_split : prm.num_kb;
+    // Work units: whole tiles times K pieces, then the tail tiles cut into
+    // tail_f narrower units each.
+    const int64_t full_tiles = prm.full_units / prm.splits;
+    const int64_t num_units = prm.full_units + (num_tiles - full_tiles) * prm.tail_f;
+    struct Unit {
+        int64_t tile, tq, tp;
+        int32_t q_off;    // first Q row (C column) of the unit
+        int32_t width;    // Q rows of the unit = MMA N
+        int32_t piece;    // K piece (0 unless split)
+        int32_t kb_lo, kb_hi;
+        bool narrow;      // tail unit
+    };
+    auto unit_of = [&](int64_t u) {
+        Unit w;
+        int32_t part = 0;
+        if (u < prm.full_units) {
+            w.tile = u / prm.splits;
+            w.piece = static_cast<int32_t>(u % prm.splits);
+            w.width = prm.tile_q;
+            w.narrow = false;
+        } else {
+            const int64_t v = u - prm.full_units;
+            w.tile = full_tiles + v / prm.tail_f;
+            part = static_cast<int32_t>(v % prm.tail_f);
+            w.piece = 0;
+            w.width = prm.tile_q / prm.tail_f;
+            w.narrow = true;
+        }
+        raster_tile(w.tile, prm.tiles_q, prm.tiles_p, prm.group, &w.tq, &w.tp);
+        w.q_off = static_cast<int32_t>(w.tq * prm.tile_q) + part * w.width;
+        w.kb_lo = w.piece * prm.kb_per_split;
+        w.kb_hi = w.kb_lo + prm.kb_per_split < prm.num_kb ? w.kb_lo + prm.kb_per_split : prm.num_kb;
+        return w;
     };
     const int64_t first = PAIR ? blockIdx.x / 2 : blockIdx.x;
     const int64_t stride = PAIR ? gridDim.x / 2 : gridDim.x;
@@ -303,13 +332,12 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         uint32_t it = 0;
         bool ok = true;
         for (int64_t u = first; ok && u < num_units; u += stride) {
-            int64_t tq, tp;
-            raster_tile(u / prm.splits, prm.tiles_q, prm.tiles_p, prm.group, &tq, &tp);
-            const int32_t p0 = static_cast<int32_t>(tp * Cfg::kTileP + rank * Cfg::kBlockP);
-            const int32_t q0 = static_cast<int32_t>(tq * prm.tile_q + rank * (prm.tile_q / Cfg::kCG));
-            int32_t kb_lo, kb_hi;
-            unit_kb(u, kb_lo, kb_hi);
-            for (int32_t kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+            const Unit w = unit_of(u);
+            const int32_t p0 = static_cast<int32_t>(w.tp * Cfg::kTileP + rank * Cfg::kBlockP);
+            const int32_t q0 = w.q_off + static_cast<int32_t>(rank) * (w.width / Cfg::kCG);
+            const CUtensorMap* mq = w.narrow ? &map_q_tail : &map_q;
+            const uint32_t tx = w.narrow ? prm.stage_tx_tail : prm.stage_tx_bytes;
+            for (int32_t kb = w.kb_lo; kb < w.kb_hi; ++kb, ++it) {
                 const uint32_t s = it % S, ph = (it / S) & 1u;
                 if (!warp_wait(empty_bar(s), ph ^ 1u, wd)) {
                     ok = false;
@@ -321,13 +349,13 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                     const int32_t kx = kb * Cfg::kStageK;
                     if constexpr (PAIR) {
                         const uint32_t fb = mapa_shared(full_bar(s), 0);
-                        if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * prm.stage_tx_bytes);
+                        if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * tx);
                         tma_load_2d_pair(sp, &map_p, fb, kx, p0);
-                        tma_load_2d_pair(sq, &map_q, fb, kx, q0);
+                        tma_load_2d_pair(sq, mq, fb, kx, q0);
                     } else {
-                        mbar_arrive_expect_tx(full_bar(s), prm.stage_tx_bytes);
+                        mbar_arrive_expect_tx(full_bar(s), tx);
                         tma_load_2d(sp, &map_p, full_bar(s), kx, p0);
-                        tma_load_2d(sq, &map_q, full_bar(s), kx, q0);
+                        tma_load_2d(sq, mq, full_bar(s), kx, q0);
                     }
                 }
                 __syncwarp();
@@ -371,18 +399,16 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         uint32_t it = 0;
         bool ok = true;
         for (int64_t u = first; ok && u < num_units; u += stride) {
-            int64_t tq, tp;
-            raster_tile(u / prm.splits, prm.tiles_q, prm.tiles_p, prm.group, &tq, &tp);
-            const int64_t g0 = is_p ? tp * Cfg::kTileP + r0 : tq * prm.tile_q + (r0 - Cfg::kBlockP);
+            const Unit w = unit_of(u);
+            const int64_t g0 =
+                is_p ? w.tp * Cfg::kTileP + r0 : static_cast<int64_t>(w.q_off) + (r0 - Cfg::kBlockP);
             const uint8_t* row0 = mat + g0 * pitch;   // address arithmetic only
             // quad i exists iff i < rows_left: inside the matrix and, for Q,
-            // inside this tile's tile_q rows (the rest of the stage is unused)
+            // inside this unit's rows (the rest of the stage is unused)
             int64_t rows_left = rows_lim - g0;
-            if (!is_p && prm.tile_q - static_cast<int64_t>(r0 - Cfg::kBlockP) < rows_left)
-                rows_left = prm.tile_q - static_cast<int64_t>(r0 - Cfg::kBlockP);
-            int32_t kb_lo, kb_hi;
-            unit_kb(u, kb_lo, kb_hi);
-            for (int32_t kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+            if (!is_p && w.width - static_cast<int64_t>(r0 - Cfg::kBlockP) < rows_left)
+                rows_left = w.width - static_cast<int64_t>(r0 - Cfg::kBlockP);
+            for (int32_t kb = w.kb_lo; kb < w.kb_hi; ++kb, ++it) {
                 const uint32_t s = it % S, ph = (it / S) & 1u;
                 const int64_t kb_byte = static_cast<int64_t>(kb) * Cfg::kAtomBytes;
                 const int64_t left = prm.k_bytes - kb_byte;
@@ -437,9 +463,10 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * Cfg::kAccCols;
-                int32_t kb_lo, kb_hi;
-                unit_kb(u, kb_lo, kb_hi);
-                for (int32_t kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+                const Unit w = unit_of(u);
+                const uint32_t idesc = w.narrow ? prm.idesc_tail : prm.idesc;
+                const int32_t kb_lo = w.kb_lo;
+                for (int32_t kb = w.kb_lo; kb < w.kb_hi; ++kb, ++it) {
                     const uint32_t s = it % S, ph = (it / S) & 1u;
                     if (!warp_wait(full_bar(s), ph, wd)) {
                         ok = false;
@@ -456,9 +483,9 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                             const uint64_t off = static_cast<uint64_t>(kk * (Cfg::kMmaKBytes >> 4));
                             const uint32_t acc = (kb != kb_lo || kk != 0) ? 1u : 0u;
                             if constexpr (IN == InKind::E4M3)
-                                mma_f8<Cfg::kCG>(d_tmem, adesc + off, bdesc + off, prm.idesc, acc);
+                                mma_f8<Cfg::kCG>(d_tmem, adesc + off, bdesc + off, idesc, acc);
                             else
-                                mma_f16<Cfg::kCG>(d_tmem, adesc + off, bdesc + off, prm.idesc, acc);
+                                mma_f16<Cfg::kCG>(d_tmem, adesc + off, bdesc + off, idesc, acc);
                         }
                         commit_to<Cfg::kCG>(empty_bar(s), 0x3);
                     }
@@ -486,7 +513,6 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         constexpr int kOB = static_cast<int>(sizeof(OutT));   // output bytes: 2 or 4
         constexpr int kCols = 128 / kOB;                        // columns per chunk
         constexpr int kGran = 16 / kOB;                         // elements per 16-byte granule
-        const int chunks = prm.tile_q / kCols;
         constexpr int kSlices = (PAIR ? 2 : 1) * Cfg::kEpiWarps;  // 32-row slices per tile
         constexpr int kSliceFloats = 32 * Cfg::kAccCols;
         const uint32_t quarter = warp & 3u;     // TMEM lanes this warp may access
@@ -613,15 +639,15 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         };
 
         for (int64_t u = first; u < num_units; u += stride, ++lt) {
-            const int64_t t = u / prm.splits;
-            int64_t tq, tp;
-            raster_tile(t, prm.tiles_q, prm.tiles_p, prm.group, &tq, &tp);
+            const Unit w = unit_of(u);
+            const int64_t t = w.tile, tp = w.tp;
+            const int chunks = w.width / kCols;
             const uint32_t b = lt & 1u, aph = (lt >> 1) & 1u;
             if (!warp_wait(accf_bar(b), aph, wd)) break;
             tc_fence_after_sync();
             const int32_t row0 =
                 static_cast<int32_t>(tp * Cfg::kTileP + rank * Cfg::kBlockP + quarter * 32);
-            const int32_t col0 = static_cast<int32_t>(tq * prm.tile_q);
+            const int32_t col0 = w.q_off;
             const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + b * Cfg::kAccCols;
             if (prm.splits == 1) {
 #pragma unroll 1
@@ -642,15 +668,15 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
             } else {
                 // This K piece's partial sums -> workspace, column-major within
                 // the slice so that a warp's stores (and loads) are coalesced.
-                const int32_t piece = static_cast<int32_t>(u % prm.splits);
+                const int32_t piece = w.piece;
                 float* part = prm.ws_partials +
                               ((t * prm.splits + piece) * kSlices + slice) * kSliceFloats;
 #pragma unroll 1
-                for (int c = 0; c < prm.tile_q / 32; ++c) {
+                for (int c = 0; c < w.width / 32; ++c) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(t_row + c * 32, v);
                     tmem_wait_ld();
-                    if (c == prm.tile_q / 32 - 1) release_acc(b);
+                    if (c == w.width / 32 - 1) release_acc(b);
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         __stcg(part + (c * 32 + j) * 32 + lane, __uint_as_float(v[j]));
@@ -727,7 +753,7 @@ cudaError_t tc_launch_one(const TcLaunch& L) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kernel, L.map_p, L.map_q, L.map_out, L.prm);
+    return cudaLaunchKernelEx(&cfg, kernel, L.map_p, L.map_q, L.map_out, L.map_q_tail, L.prm);
 }
 
 template <InKind IN, typename OutT>

@@ -1,0 +1,131 @@
+"""Configuration sweep for the tensor-core GEMM: times every combination of the
+library's tuning options on the given shapes and reports the fastest.
+
+The options swept are the ones gemm_set_option exposes -- CTA pairing
+("pair"), the rasteriser's group size ("group"), the output tile width along M
+("tile_q") and split-K ("splits", with a workspace registered) -- so a result
+can be applied directly.  The pages observe that no single tile configuration
+is best everywhere ("FP16 GEMM Optimization on AMD RDNA 3 and RDNA 4",
+"Tuning Further"; "FP8 GEMM Optimization on AMD RDNA 4", "Results"); this
+script measures how far the automatic choices are from the best one found.
+
+  python -m dense_gemm_tcgen05_gb300.tune [--shapes f16:8192x8192x8192,...]
+         [--iters 20] [--quick]
+
+Each timing: 3 warm-up calls, then `iters` calls on the same stream between
+CUDA events, inputs rotating over two sets.  One JSON line per shape is
+printed with every configuration's TFLOP/s, the best one and the automatic
+choice's.
+"""
+from __future__ import annotations
+
+import argparse
+import itertools
+import json
+
+import torch
+
+from . import capi
+
+DEFAULT_SHAPES = ["f16:8192x8192x8192", "bf16:4096x4096x4096", "bf16:4096x14336x4096",
+                  "e4m3:8192x8192x8192", "e4m3:3072x4096x8192", "bf16:128x8192x8192",
+                  "bf16:1024x1024x8192"]
+_DT = {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
+
+
+def _parse(spec: str):
+    kind, dims = spec.split(":")
+    M, N, K = (int(x) for x in dims.lower().split("x"))
+    return kind, M, N, K
+
+
+def _operands(kind, M, N, K, sets=2):
+    out = []
+    for s in range(sets):
+        g = torch.Generator(device="cuda").manual_seed(s)
+        a = torch.randn((M, K), device="cuda", generator=g).to(_DT[kind])
+        b = torch.randn((N, K), device="cuda", generator=g).to(_DT[kind])
+        c = torch.empty((N, M), device="cuda",
+                        dtype=torch.float16 if kind == "f16" else torch.bfloat16)
+        out.append((a, b, c))
+    return out
+
+
+def _call(kind, M, N, K, a, b, c, stream):
+    if kind == "e4m3":
+        return capi.gemm_fp8_tn(M, N, K, a.data_ptr(), K, b.data_ptr(), K, 1.0, 1.0, c.data_ptr(),
+                                M, stream)
+    fn = capi.gemm_f16_tn if kind == "f16" else capi.gemm_bf16_tn
+    return fn(M, N, K, a.data_ptr(), K, b.data_ptr(), K, c.data_ptr(), M, stream)
+
+
+def time_config(kind, M, N, K, ops, iters, stream) -> float:
+    """TFLOP/s of the current option settings (mean over `iters` calls)."""
+    h = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            st = _call(kind, M, N, K, *ops[i % len(ops)], h)
+            if st != 0:
+                raise RuntimeError(capi.status_text(st))
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(iters):
+            _call(kind, M, N, K, *ops[i % len(ops)], h)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / iters
+    return 2.0 * M * N * K / (ms * 1e-3) / 1e12
+
+
+def _set(pair, group, tile_q, splits):
+    for name, value in (("pair", pair), ("group", group), ("tile_q", tile_q), ("splits", splits)):
+        st = capi.gemm_set_option(name, value)
+        if st != 0:
+            raise RuntimeError("option %s=%s: %s" % (name, value, capi.status_text(st)))
+
+
+def tune_shape(spec: str, iters: int, quick: bool) -> dict:
+    kind, M, N, K = _parse(spec)
+    ops = _operands(kind, M, N, K)
+    stream = torch.cuda.Stream()
+    pairs = [0, 1]
+    groups = [8] if quick else [4, 8, 16]
+    tile_qs = [0, 128, 256] if quick else [0, 64, 128, 192, 256]
+    splits = [1, 0]
+    rows = []
+    try:
+        _set(-1, 8, 0, 0)
+        auto = time_config(kind, M, N, K, ops, iters, stream)
+        for p, g, t, s in itertools.product(pairs, groups, tile_qs, splits):
+            _set(p, g, t, s)
+            rows.append({"pair": p, "group": g, "tile_q": t, "splits": s,
+                         "tflops": round(time_config(kind, M, N, K, ops, iters, stream), 1)})
+    finally:
+        _set(-1, 8, 0, 0)
+    best = max(rows, key=lambda r: r["tflops"])
+    return {"shape": spec, "auto_tflops": round(auto, 1), "best": best,
+            "auto_over_best": round(auto / best["tflops"], 4), "configs": rows}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--shapes", default=",".join(DEFAULT_SHAPES))
+    ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--quick", action="store_true", help="fewer group sizes and tile widths")
+    args = ap.parse_args(argv)
+    from . import build
+
+    build.build()
+    capi.lib()
+    ws = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    capi.gemm_set_workspace(ws.data_ptr(), ws.numel())
+    try:
+        for spec in args.shapes.split(","):
+            print(json.dumps(tune_shape(spec.strip(), args.iters, args.quick)), flush=True)
+    finally:
+        capi.gemm_set_workspace(None, 0)
+
+
+if __name__ == "__main__":
+    main()

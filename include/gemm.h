@@ -150,6 +150,9 @@ int gemm_read_watchdog(int reset);
  *   "max_ctas"    cap on persistent CTAs, 0 = one per SM (default)
  *   "tile_q"      output tile width along M (= MMA N): 0 auto (default, by
  *                 padding cost), or 64, 128, 192, 256
+ *   "tail"        the last, partial wave of tiles: 0 auto (default) cuts its tiles
+ *                 into 2 or 4 narrower ones when that ends it sooner, 1 never, 2 or
+ *                 4 always
  *   "splits"      K pieces per tile: 0 auto (default, needs a workspace), 1 never
  *                 split, 2..64 split that many ways when the workspace suffices
  * Returns GEMM_OK or GEMM_ERR_INVALID_OPTION.

@@ -75,6 +75,8 @@ def test_options():
     assert capi.gemm_set_option("tile_q", 96) == capi.GEMM_ERR_INVALID_OPTION
     assert capi.gemm_set_option("tile_q", 192) == 0
     assert capi.gemm_set_option("tile_q", 0) == 0
+    assert capi.gemm_set_option("tail", 3) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("tail", 0) == 0
 
 
 def test_workspace_size_bound():
@@ -102,3 +104,10 @@ def test_rasteriser_bijection_and_bands(tiles_m, tiles_n, group):
         seen.add((tm, tn))
     assert len(seen) == tiles_m * tiles_n
     assert capi.gemm_tile_coord(tiles_m * tiles_n, tiles_m, tiles_n, group)[0] != 0
+
+
+def test_tuner_shape_parser():
+    from dense_gemm_tcgen05_gb300 import tune
+
+    assert tune._parse("f16:8192x28672x8192") == ("f16", 8192, 28672, 8192)
+    assert all(tune._parse(s)[0] in ("f16", "bf16", "e4m3") for s in tune.DEFAULT_SHAPES)

@@ -51,3 +51,16 @@ def test_side_stream_and_tensor_api():
     s.synchronize()
     assert out.shape == (N, M)
     assert torch.all(out.float() == K)
+
+
+def test_tuner_runs_and_restores_defaults():
+    from dense_gemm_tcgen05_gb300 import tune
+
+    res = tune.tune_shape("bf16:512x384x256", iters=2, quick=True)
+    assert res["best"]["tflops"] > 0 and res["auto_tflops"] > 0
+    assert len(res["configs"]) == 2 * 1 * 3 * 2
+    # options are back to their defaults: a normal call still works
+    M, N, K = 256, 256, 128
+    ops = si.tn_operands("bf16", M, N, K, dist="ones", seed=0)
+    C = run_tn("bf16", ops, M, N, K)
+    assert torch.all(C.to(torch.float32) == K)

@@ -318,3 +318,41 @@ def test_skinny_m_auto_tile(M):
     C = run_tn("bf16", ops, M, N, K)
     exact = oracle.gemm_tn("bf16", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
     assert_codes_equal(out_codes(C, M, N), exact_codes("bf16", exact))
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("tail", [2, 4])
+@pytest.mark.parametrize("mode", ["cta1", "pair", "loads"])
+def test_tail_split_variants(kind, tail, mode):
+    """The last partial wave cut into narrower units (forced), few CTAs so that
+    whole tiles and tail units share the persistent loop."""
+    M, N, K = 1100, 700, 300
+    opts = {"tail": tail, "pair": 1 if mode == "pair" else 0, "path": 2 if mode == "loads" else 0,
+            "max_ctas": 10, "tile_q": 256}
+    for k, v in opts.items():
+        assert capi.gemm_set_option(k, v) == 0
+    try:
+        ops = si.tn_operands(kind, M, N, K, dist="normal", seed=tail, sigma=0.5)
+        C = run_tn(kind, ops, M, N, K)
+        check_full(kind, ops, M, N, K, C)
+    finally:
+        for k, v in {"tail": 0, "pair": -1, "path": 0, "max_ctas": 0, "tile_q": 0}.items():
+            capi.gemm_set_option(k, v)
+
+
+def test_tail_split_fp32_out():
+    M, N, K = 1000, 900, 200
+    for k, v in {"tail": 2, "max_ctas": 12}.items():
+        assert capi.gemm_set_option(k, v) == 0
+    try:
+        ops = si.tn_operands("e4m3", M, N, K, dist="pm1", seed=2)
+        A, B = ops["A"].cuda(), ops["B"].cuda()
+        C = torch.full((N, M), float("nan"), device="cuda")
+        st = capi.gemm_fp8_tn_f32(M, N, K, A.data_ptr(), K, B.data_ptr(), K, 1.0, 1.0,
+                                  C.data_ptr(), M, torch.cuda.current_stream().cuda_stream)
+        assert st == 0
+        exact = oracle.gemm_tn("e4m3", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+        np.testing.assert_array_equal(C.cpu().numpy().T, exact.astype(np.float32))
+    finally:
+        for k, v in {"tail": 0, "max_ctas": 0}.items():
+            capi.gemm_set_option(k, v)
