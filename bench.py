@@ -392,6 +392,24 @@ def run_ours(args):
                                       "frac": round(tf / peak, 4)}
             del s
             torch.cuda.empty_cache()
+        # FP16 accumulation (the FP16 page's measured mode), same problem
+        from dense_gemm_tcgen05_gb300 import capi as _capi
+
+        o16, s16 = tn_sets("f16", M, N, K, seed=2, sigma=0.1, nsets=SETS, device="cuda")
+
+        def acc16(a, b, c):
+            st = _capi.gemm_f16_tn_acc16(M, N, K, a.data_ptr(), K, b.data_ptr(), K, c.data_ptr(),
+                                         M, stream_h)
+            if st != 0:
+                raise RuntimeError(_capi.status_text(st))
+
+        with torch.cuda.stream(stream):
+            _, lm = timed_loop(acc16, s16, sub_steps, 3, stream)
+        tf = flops / (lm * 1e-3) / 1e12
+        per["f16_acc16_tn_8192"] = {"tflops": round(tf, 1), "peak": round(burst, 1),
+                                    "frac": round(tf / burst, 4)}
+        del s16
+        torch.cuda.empty_cache()
         lm = f32_bench(4096, sub_steps, 3, stream, stream_h)
         tf = 2.0 * 4096 ** 3 / (lm * 1e-3) / 1e12
         clk = clocks.get("sm_max_mhz") if clocks and clocks.get("sm_max_mhz") else 2070.0

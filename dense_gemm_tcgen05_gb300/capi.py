@@ -36,6 +36,7 @@ _SIGNATURES = {
     "gemm_f32": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp], _int),
     "gemm_f16_tn": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp], _int),
     "gemm_bf16_tn": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp], _int),
+    "gemm_f16_tn_acc16": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp], _int),
     "gemm_fp8_tn": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _f32, _f32, _vp, _i64, _vp], _int),
     "gemm_fp8_tn_f32": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _f32, _f32, _vp, _i64, _vp], _int),
     "gemm_status_string": ([_int], ctypes.c_char_p),
@@ -96,6 +97,10 @@ def gemm_f32(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
 
 def gemm_f16_tn(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
     return lib().gemm_f16_tn(M, N, K, _p(A), lda, _p(B), ldb, _p(C), ldc, _p(stream))
+
+
+def gemm_f16_tn_acc16(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
+    return lib().gemm_f16_tn_acc16(M, N, K, _p(A), lda, _p(B), ldb, _p(C), ldc, _p(stream))
 
 
 def gemm_bf16_tn(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:

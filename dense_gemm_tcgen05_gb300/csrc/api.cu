@@ -163,7 +163,7 @@ CUresult encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, in
 // no-allocation one passes nullptr.
 int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void* A,
             int64_t lda, const void* B, int64_t ldb, float scale, void* C, int64_t ldc,
-            void* stream_v, const ScratchOverride* ov = nullptr) {
+            void* stream_v, const ScratchOverride* ov = nullptr, bool acc16 = false) {
     const int es = in == InKind::E4M3 ? 1 : 2;
     const int os = out_f32 ? 4 : 2;  // output element size
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
@@ -188,7 +188,7 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     // that miss it are read by the load-based producer, and a C that misses it
     // is written by the epilogue's row-wise stores.  Option "path" = 1 forces
     // the CUDA-core kernel (a second, independent implementation).
-    if (g_opt_path.load() == 1) {
+    if (g_opt_path.load() == 1 && !acc16) {
         e = tn_fallback_launch(in, out_f32, M, N, K, A, lda, B, ldb, scale, C, ldc, stream);
         return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
     }
@@ -246,7 +246,10 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     L.prm.direct_store = c_tma ? 0 : 1;
     L.prm.k_bytes = K * es;
     L.prm.tile_q = tile_q;
-    L.prm.idesc = make_idesc(g.format, static_cast<uint32_t>(g.mma_m), static_cast<uint32_t>(tile_q));
+    const uint32_t d_format = acc16 ? 0u : 1u;
+    L.prm.acc16 = acc16 ? 1 : 0;
+    L.prm.idesc = make_idesc(g.format, static_cast<uint32_t>(g.mma_m), static_cast<uint32_t>(tile_q),
+                             d_format);
     L.prm.stage_tx_bytes = static_cast<uint32_t>((g.load_p + load_q) * 128);
     L.prm.p_ptr = B;
     L.prm.q_ptr = A;
@@ -261,7 +264,8 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     L.prm.splits = 1;
     L.prm.kb_per_split = L.prm.num_kb;
     {
-        const int opt = ov ? ov->splits : g_opt_splits.load();
+        // FP16 accumulation never splits K: combining pieces would add FP32 sums.
+        const int opt = acc16 ? 1 : (ov ? ov->splits : g_opt_splits.load());
         int64_t want = 1;
         if (opt >= 2) {
             want = opt;
@@ -346,7 +350,7 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
             L.prm.tail_f = f;
             L.prm.full_units = waves * units_slots;
             L.prm.idesc_tail = make_idesc(g.format, static_cast<uint32_t>(g.mma_m),
-                                          static_cast<uint32_t>(width));
+                                          static_cast<uint32_t>(width), d_format);
             L.prm.stage_tx_tail = static_cast<uint32_t>((g.load_p + load_qt) * 128);
             const int64_t units = L.prm.full_units + (tiles - L.prm.full_units) * f;
             L.grid = static_cast<int>((units < slots ? units : slots) * g.cluster);
@@ -397,6 +401,12 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const
 int gemm_f16_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                 int64_t ldb, void* C, int64_t ldc, void* stream) {
     return gemm_tn(InKind::F16, false, M, N, K, A, lda, B, ldb, 1.0f, C, ldc, stream);
+}
+
+int gemm_f16_tn_acc16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                      int64_t ldb, void* C, int64_t ldc, void* stream) {
+    return gemm_tn(InKind::F16, false, M, N, K, A, lda, B, ldb, 1.0f, C, ldc, stream, nullptr,
+                   true);
 }
 
 int gemm_bf16_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,

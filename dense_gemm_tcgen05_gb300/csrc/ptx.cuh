@@ -282,13 +282,14 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16 / kind::f8f6f4, dense, FP32 accumulator,
-// both operands K-major.  Bits: [4,6) D format (1 = F32), [7,10) A format,
-// [10,13) B format (f16: 0 = F16, 1 = BF16; f8f6f4: 0 = E4M3), [15] / [16]
-// A / B major (0 = K), [17,23) N >> 3, [24,29) M >> 4.
+// Instruction descriptor, kind::f16 / kind::f8f6f4, dense, both operands
+// K-major.  Bits: [4,6) D format (1 = F32, 0 = F16), [7,10) A format, [10,13)
+// B format (f16: 0 = F16, 1 = BF16; f8f6f4: 0 = E4M3), [15] / [16] A / B major
+// (0 = K), [17,23) N >> 3, [24,29) M >> 4.  With an F16 D each accumulator
+// element still takes one 32-bit TMEM column, in its low 16 bits.
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, uint32_t mma_m,
-                                                  uint32_t mma_n) {
-    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((mma_n >> 3) << 17) |
+                                                  uint32_t mma_n, uint32_t d_format = 1) {
+    return (d_format << 4) | (ab_format << 7) | (ab_format << 10) | ((mma_n >> 3) << 17) |
            ((mma_m >> 4) << 24);
 }
 

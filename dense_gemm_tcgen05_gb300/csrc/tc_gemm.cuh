@@ -657,12 +657,22 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                     if constexpr (kCols == 64) tmem_ld_32x32b_x32(t_row + c * kCols + 32, v1);
                     tmem_wait_ld();
                     if (c == chunks - 1) release_acc(b);
-                    float f[kCols];
-#pragma unroll
-                    for (int j = 0; j < kCols; ++j)
-                        f[j] = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
                     uint32_t pk[32];
-                    pack(f, pk);
+                    if (kOB == 2 && prm.acc16) {
+                        // FP16 accumulators: the low halves are the output codes.
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const uint32_t lo = j < 16 ? v0[2 * j] : v1[2 * j - 32];
+                            const uint32_t hi = j < 16 ? v0[2 * j + 1] : v1[2 * j - 31];
+                            pk[j] = (lo & 0xFFFFu) | (hi << 16);
+                        }
+                    } else {
+                        float f[kCols];
+#pragma unroll
+                        for (int j = 0; j < kCols; ++j)
+                            f[j] = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
+                        pack(f, pk);
+                    }
                     emit(pk, col0 + c * kCols, row0);
                 }
             } else {

@@ -84,6 +84,18 @@ int gemm_f16_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, con
                 int64_t ldb, void* C, int64_t ldc, void* stream);
 
 /*
+ * gemm_f16_tn_acc16 -- as gemm_f16_tn, but the tensor core accumulates in FP16,
+ * the mode the FP16 page measures ("FP16 GEMM Optimization on AMD RDNA 3 and
+ * RDNA 4", "The Target": both the kernels and hipBLASLt accumulate in FP16,
+ * HIPBLAS_COMPUTE_16F).  On GB300 it runs at the same tensor rate as FP32
+ * accumulation and is less accurate over long K; it is exact while every
+ * partial sum is an integer FP16 holds (|sum| <= 2048), e.g. for +-1 inputs
+ * with K <= 2048.  Never splits K; option "path" = 1 does not apply.
+ */
+int gemm_f16_tn_acc16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                      int64_t ldb, void* C, int64_t ldc, void* stream);
+
+/*
  * gemm_bf16_tn -- as gemm_f16_tn with bfloat16 inputs and a bfloat16 output
  * ("An Educational GEMM Ladder for Helios GPUs": BF16 inputs and output with
  * FP32 accumulation).
