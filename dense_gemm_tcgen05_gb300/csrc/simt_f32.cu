@@ -6,7 +6,7 @@
 // Design, following "Optimizing GEMM in HIP" Steps 2-6 (shared-memory tiling,
 // register tiling, double buffering, vectorised loads, register budget), made
 // for a Blackwell SM:
-//   - a 128 x 128 block tile, K slices of 8, 256 threads, 8 x 8 outputs per
+//   - a 128 x 128 block tile, K slices of 16, 256 threads, 8 x 8 outputs per
 //     thread held in registers (outer-product FFMAs, 64 per k per thread);
 //   - each thread's 8 x 8 outputs are two 4-row by two 4-column groups 64 apart,
 //     so its shared-memory operand reads are float4 and conflict-free;
@@ -27,7 +27,8 @@
 namespace gb300 {
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kBK = 8, kThreads = 256, kPadA = 4;
+constexpr int kBM = 128, kBN = 128, kBK = 16, kThreads = 256, kPadA = 4;
+constexpr int kLoads = kBK / 8;  // float4 loads of A and of B per thread per slice
 
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -43,8 +44,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int tid = threadIdx.x;
     const int tx = tid & 15, ty = tid >> 4;
 
-    // Global -> register mapping: A tile 128 x 8 (one float4 along k per
-    // thread), B tile 8 x 128 (one float4 along n per thread).
+    // Global -> register mapping: A tile 128 x kBK (float4s along k at k offsets
+    // a_k + 8l), B tile kBK x 128 (float4s along n at rows b_k + 8l).
     const int a_row = tid >> 1, a_k = (tid & 1) * 4;
     const int b_k = tid >> 5, b_col = (tid & 31) * 4;
     const int64_t gm = m0 + a_row;
@@ -82,14 +83,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         return v;
     };
-    auto store_a = [&](int buf, float4 v) {
-        As[buf][a_k + 0][a_row] = v.x;
-        As[buf][a_k + 1][a_row] = v.y;
-        As[buf][a_k + 2][a_row] = v.z;
-        As[buf][a_k + 3][a_row] = v.w;
+    auto store_a = [&](int buf, int l, float4 v) {
+        As[buf][a_k + 8 * l + 0][a_row] = v.x;
+        As[buf][a_k + 8 * l + 1][a_row] = v.y;
+        As[buf][a_k + 8 * l + 2][a_row] = v.z;
+        As[buf][a_k + 8 * l + 3][a_row] = v.w;
     };
-    auto store_b = [&](int buf, float4 v) {
-        *reinterpret_cast<float4*>(&Bs[buf][b_k][b_col]) = v;
+    auto store_b = [&](int buf, int l, float4 v) {
+        *reinterpret_cast<float4*>(&Bs[buf][b_k + 8 * l][b_col]) = v;
     };
 
     float acc[8][8];
@@ -99,17 +100,25 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
     const int ktiles = (K + kBK - 1) / kBK;
-    float4 ra = load_a(0), rb = load_b(0);
-    store_a(0, ra);
-    store_b(0, rb);
+    float4 ra[kLoads], rb[kLoads];
+#pragma unroll
+    for (int l = 0; l < kLoads; ++l) {
+        ra[l] = load_a(8 * l);
+        rb[l] = load_b(8 * l);
+        store_a(0, l, ra[l]);
+        store_b(0, l, rb[l]);
+    }
     __syncthreads();
 
     for (int kt = 0; kt < ktiles; ++kt) {
         const int cur = kt & 1;
         const bool more = kt + 1 < ktiles;
         if (more) {
-            ra = load_a((kt + 1) * kBK);
-            rb = load_b((kt + 1) * kBK);
+#pragma unroll
+            for (int l = 0; l < kLoads; ++l) {
+                ra[l] = load_a((kt + 1) * kBK + 8 * l);
+                rb[l] = load_b((kt + 1) * kBK + 8 * l);
+            }
         }
 #pragma unroll
         for (int k = 0; k < kBK; ++k) {
@@ -125,8 +134,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
         if (more) {
-            store_a(cur ^ 1, ra);
-            store_b(cur ^ 1, rb);
+#pragma unroll
+            for (int l = 0; l < kLoads; ++l) {
+                store_a(cur ^ 1, l, ra[l]);
+                store_b(cur ^ 1, l, rb[l]);
+            }
         }
         __syncthreads();
     }
