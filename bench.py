@@ -489,6 +489,17 @@ def sweep(stream, stream_h, burst):
     ws = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
     capi.gemm_set_workspace(ws.data_ptr(), ws.numel())
     try:
+        # the tight-leading-dimension BF16 configurations again, now repacked
+        for kind, (M, N, K) in [("bf16", (2047, 3001, 1023)), ("bf16", (8191, 8191, 8191))]:
+            o, s = tn_sets(kind, M, N, K, seed=3, sigma=0.05, nsets=SETS, device="cuda")
+            c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h)
+            with torch.cuda.stream(stream):
+                _, lm = timed_loop(c, s, 20, 3, stream)
+            tf = 2.0 * M * N * K / (lm * 1e-3) / 1e12
+            out["%s_%dx%dx%d_ws" % (kind, M, N, K)] = {"tflops": round(tf, 1),
+                                                       "frac": round(tf / burst, 4)}
+            del s
+            torch.cuda.empty_cache()
         for kind, (M, N, K) in [("bf16", (16, 8192, 8192)), ("bf16", (128, 8192, 8192)),
                                 ("bf16", (64, 14336, 4096)), ("bf16", (1024, 1024, 8192)),
                                 ("e4m3", (128, 8192, 8192))]:

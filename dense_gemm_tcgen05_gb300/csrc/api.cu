@@ -71,6 +71,7 @@ std::atomic<int> g_opt_max_ctas{0};
 std::atomic<int> g_opt_splits{0};
 std::atomic<int> g_opt_tile_q{0};
 std::atomic<int> g_opt_tail{0};
+std::atomic<int> g_opt_repack{0};
 std::atomic<int64_t> g_opt_timeout_ns{2000000000LL};
 
 thread_local cudaError_t t_last_cuda_error = cudaSuccess;
@@ -185,17 +186,60 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     }
 
     // Path choice.  TMA needs 16-byte-aligned bases and row pitches; operands
-    // that miss it are read by the load-based producer, and a C that misses it
-    // is written by the epilogue's row-wise stores.  Option "path" = 1 forces
-    // the CUDA-core kernel (a second, independent implementation).
+    // that miss it are repacked into the workspace when there is one (below)
+    // or read by the load-based producer, and a C that misses it is written by
+    // the epilogue's row-wise stores.  Option "path" = 1 forces the CUDA-core
+    // kernel (a second, independent implementation).
     if (g_opt_path.load() == 1 && !acc16) {
         e = tn_fallback_launch(in, out_f32, M, N, K, A, lda, B, ldb, scale, C, ldc, stream);
         return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
     }
     const int64_t lim = 1LL << 40;
-    const bool ab_tma = aligned(A, 16) && aligned(B, 16) && (lda * es) % 16 == 0 &&
-                        (ldb * es) % 16 == 0 && lda * es < lim && ldb * es < lim;
+    bool a_tma = aligned(A, 16) && (lda * es) % 16 == 0 && lda * es < lim;
+    bool b_tma = aligned(B, 16) && (ldb * es) % 16 == 0 && ldb * es < lim;
     const bool c_tma = aligned(C, 16) && (ldc * os) % 16 == 0 && ldc * os < lim;
+
+    // Scratch: the caller's workspace (registered, or the override).
+    char* ws_base = nullptr;
+    int64_t ws_total = 0;
+    if (ov) {
+        ws_base = static_cast<char*>(ov->ptr);
+        ws_total = ov->bytes;
+    } else {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        ws_base = static_cast<char*>(dev->workspace);
+        ws_total = dev->workspace_bytes;
+    }
+    int64_t ws_used = 0;  // bytes at the start of the scratch taken by repacked operands
+
+    // Operands whose rows TMA cannot address are copied once into the scratch
+    // with 16-byte-aligned rows (one pass at memory speed), after which the TMA
+    // path runs at full rate; without room for that, the load-based producer
+    // reads them in place.
+    if ((!a_tma || !b_tma) && g_opt_path.load() == 0 && g_opt_repack.load() == 0 && ws_base) {
+        const int64_t rb = K * es;                       // row bytes
+        const int64_t dp = (rb + 15) / 16 * 16;          // aligned pitch
+        const int64_t need_a = a_tma ? 0 : (M * dp + 255) / 256 * 256;
+        const int64_t need_b = b_tma ? 0 : (N * dp + 255) / 256 * 256;
+        if (need_a + need_b <= ws_total) {
+            if (!a_tma) {
+                e = repack_rows_launch(A, lda * es, ws_base, dp, M, rb, stream);
+                if (e != cudaSuccess) return fail_cuda(e);
+                A = ws_base;
+                lda = dp / es;
+                a_tma = true;
+            }
+            if (!b_tma) {
+                e = repack_rows_launch(B, ldb * es, ws_base + need_a, dp, N, rb, stream);
+                if (e != cudaSuccess) return fail_cuda(e);
+                B = ws_base + need_a;
+                ldb = dp / es;
+                b_tma = true;
+            }
+            ws_used = need_a + need_b;
+        }
+    }
+    const bool ab_tma = a_tma && b_tma;
     const Producer prod = (ab_tma && g_opt_path.load() != 2) ? Producer::Tma : Producer::Loads;
     const int opt_pair = g_opt_pair.load();
     // cta_group::2 pairs measured faster on every shape tried; they need TMA.
@@ -282,17 +326,9 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
             const int64_t slices = 4 * g.cluster;                    // 32-row slices per tile
             const int64_t cnt_bytes = ((tiles * slices * 4 + 255) / 256) * 256;
             const int64_t part_bytes = tiles * pieces * slices * 32 * 256 * 4;
-            void* ws = nullptr;
-            int64_t ws_bytes = 0;
-            if (ov) {
-                ws = ov->ptr;
-                ws_bytes = ov->bytes;
-                if (pieces >= 2 && cnt_bytes + part_bytes > ws_bytes) return GEMM_ERR_SCRATCH;
-            } else {
-                std::lock_guard<std::mutex> lock(g_mutex);
-                ws = dev->workspace;
-                ws_bytes = dev->workspace_bytes;
-            }
+            void* ws = ws_base ? ws_base + ws_used : nullptr;
+            const int64_t ws_bytes = ws_total - ws_used;
+            if (ov && pieces >= 2 && cnt_bytes + part_bytes > ws_bytes) return GEMM_ERR_SCRATCH;
             if (pieces >= 2 && ws && cnt_bytes + part_bytes <= ws_bytes) {
                 L.prm.splits = static_cast<int32_t>(pieces);
                 L.prm.kb_per_split = static_cast<int32_t>(kb_per);
@@ -488,6 +524,9 @@ int gemm_set_option(const char* name, int64_t value) {
     } else if (!std::strcmp(name, "tail")) {
         if (!(value == 0 || value == 1 || value == 2 || value == 4)) return GEMM_ERR_INVALID_OPTION;
         g_opt_tail.store(static_cast<int>(value));
+    } else if (!std::strcmp(name, "repack")) {
+        if (value < 0 || value > 1) return GEMM_ERR_INVALID_OPTION;
+        g_opt_repack.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "max_ctas")) {
         if (value < 0 || value > 1 << 20) return GEMM_ERR_INVALID_OPTION;
         g_opt_max_ctas.store(static_cast<int>(value));
@@ -511,11 +550,14 @@ int gemm_set_workspace(void* ptr, int64_t bytes) {
 }
 
 int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    // Upper bound over the kernel configurations: 16 pieces of every tile of a
-    // pair (256 x 256) or single CTA (128 x 256), plus the counters.
+    // Upper bound over the configurations: aligned copies of A and B (16-bit
+    // elements), then 16 K pieces of every tile of the narrowest layout
+    // (128 rows of N by 64 of M per tile), plus the counters.
     if (M <= 0 || N <= 0 || K <= 0) return 0;
-    const int64_t tiles = ((N + 127) / 128) * ((M + 255) / 256);
-    return ((tiles * 4 * 4 + 255) / 256) * 256 + tiles * 16 * 4 * 32 * 256 * 4;
+    const int64_t dp = (K * 2 + 15) / 16 * 16;
+    const int64_t repack = (M * dp + 255) / 256 * 256 + (N * dp + 255) / 256 * 256;
+    const int64_t tiles = ((N + 127) / 128) * ((M + 63) / 64);
+    return repack + ((tiles * 4 * 4 + 255) / 256) * 256 + tiles * 16 * 4 * 32 * 256 * 4;
 }
 
 int gemm_tile_coord(int64_t t, int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t* tm,

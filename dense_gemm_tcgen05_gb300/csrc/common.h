@@ -110,6 +110,11 @@ int gemm_tn_with_scratch(InKind in, int64_t M, int64_t N, int64_t K, const void*
 cudaError_t f32_launch(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                        const float* B, int64_t ldb, float* C, int64_t ldc, cudaStream_t stream);
 
+// Copies rows of row_bytes bytes from any alignment into 16-byte-aligned rows
+// of pitch dp (a multiple of 16) so that TMA can address them.
+cudaError_t repack_rows_launch(const void* src, int64_t sp, void* dst, int64_t dp, int64_t rows,
+                               int64_t row_bytes, cudaStream_t stream);
+
 // Writes zeros into a rows x cols block with leading dimension ld (elements of
 // elem_bytes bytes); used for K == 0.
 cudaError_t zero_fill_launch(void* C, int64_t rows, int64_t cols, int64_t ld, int elem_bytes,

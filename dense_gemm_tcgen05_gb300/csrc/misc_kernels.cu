@@ -1,5 +1,6 @@
-// misc_kernels.cu -- a CUDA-core TN kernel, the K == 0 zero fill and the
-// watchdog self-test.
+// misc_kernels.cu -- a CUDA-core TN kernel, the row repack used for operands
+// whose rows are not 16-byte aligned, the K == 0 zero fill and the watchdog
+// self-test.
 //
 // The CUDA-core TN kernel is a second, independent GPU implementation of the
 // TN entry points, selected only by gemm_set_option("path", 1) (tests compare
@@ -94,6 +95,38 @@ __global__ void __launch_bounds__(kFbThreads)
     }
 }
 
+// Copies `rows` rows of `row_bytes` bytes from src (row pitch sp, any
+// alignment) to dst (row pitch dp; dst and dp 16-byte aligned, dp >= row_bytes
+// rounded up to 16).  One warp per 512-byte segment of a row: lane l writes the
+// 16-byte chunk at offset 16 l of the segment from the one or two aligned
+// source chunks that cover it (all lanes of a row share the misalignment).
+// Only aligned source chunks holding a byte of the row are read; bytes past the
+// row's end in the last chunk are zeroed.
+__global__ void repack_rows_kernel(const uint8_t* __restrict__ src, int64_t sp,
+                                   uint8_t* __restrict__ dst, int64_t dp, int64_t rows,
+                                   int64_t row_bytes) {
+    const int64_t segs = (row_bytes + 511) / 512;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+    const int lane = threadIdx.x & 31;
+    for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + threadIdx.x / 32;
+         w < rows * segs; w += warps) {
+        const int64_t row = w / segs, seg = w % segs;
+        const int64_t o = seg * 512 + 16 * lane;
+        if (o >= row_bytes) continue;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(src + row * sp + o);
+        const uint32_t delta = static_cast<uint32_t>(a & 15u);
+        const uintptr_t al = a - delta;
+        const int64_t valid = row_bytes - o;  // >= 1
+        const uint4 lo = ldg_nc_v4(reinterpret_cast<const void*>(al));
+        uint4 hi = make_uint4(0u, 0u, 0u, 0u);
+        if (delta != 0 && 16 - static_cast<int64_t>(delta) < valid)
+            hi = ldg_nc_v4(reinterpret_cast<const void*>(al + 16u));
+        uint4 out = shift_chunk(lo, hi, delta);
+        if (valid < 16) out = mask_chunk(out, static_cast<int32_t>(valid));
+        *reinterpret_cast<uint4*>(dst + row * dp + o) = out;
+    }
+}
+
 __global__ void zero_fill_kernel(uint8_t* C, int64_t rows, int64_t cols, int64_t ld,
                                  int elem_bytes) {
     const int64_t total = rows * cols;
@@ -156,6 +189,17 @@ cudaError_t tn_fallback_launch(InKind in, bool out_f32, int64_t M, int64_t N, in
                     ldc, tiles_m, tiles_n);
             break;
     }
+    return cudaGetLastError();
+}
+
+cudaError_t repack_rows_launch(const void* src, int64_t sp, void* dst, int64_t dp, int64_t rows,
+                               int64_t row_bytes, cudaStream_t stream) {
+    if (rows <= 0 || row_bytes <= 0) return cudaSuccess;
+    const int64_t work = rows * ((row_bytes + 511) / 512);
+    int64_t blocks = (work + 7) / 8;  // 8 warps a block
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    repack_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const uint8_t*>(src), sp, static_cast<uint8_t*>(dst), dp, rows, row_bytes);
     return cudaGetLastError();
 }
 

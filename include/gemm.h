@@ -165,6 +165,8 @@ int gemm_read_watchdog(int reset);
  *   "tail"        the last, partial wave of tiles: 0 auto (default) cuts its tiles
  *                 into 2 or 4 narrower ones when that ends it sooner, 1 never, 2 or
  *                 4 always
+ *   "repack"      0 (default): with a workspace, operands whose rows are not 16-byte
+ *                 aligned are first copied into it with aligned rows; 1 never
  *   "splits"      K pieces per tile: 0 auto (default, needs a workspace), 1 never
  *                 split, 2..64 split that many ways when the workspace suffices
  * Returns GEMM_OK or GEMM_ERR_INVALID_OPTION.
@@ -174,8 +176,10 @@ int gemm_set_option(const char* name, int64_t value);
 /*
  * gemm_set_workspace -- registers caller-owned device scratch for the current
  * device (ptr 256-byte aligned, `bytes` long; NULL, 0 unregisters).  With a
- * workspace registered, TN calls whose output tiles cannot fill the GPU in one
- * wave split K: each K piece writes its FP32 partial tile to the workspace and
+ * workspace registered, a TN call whose A or B rows are not 16-byte aligned
+ * first copies that operand into the workspace with aligned rows (when it
+ * fits: rows * K * element size, rounded up), so that the TMA path can run;
+ * and TN calls whose output tiles cannot fill the GPU in one wave split K: each K piece writes its FP32 partial tile to the workspace and
  * the last piece to finish a 32-row slice sums the pieces in piece order (so
  * the result does not depend on timing) and stores C.  Calls that split K on
  * the same device share the workspace, so they must not overlap in time
@@ -186,7 +190,8 @@ int gemm_set_option(const char* name, int64_t value);
  */
 int gemm_set_workspace(void* ptr, int64_t bytes);
 
-/* Workspace bytes that suffice for any split of an M x N x K TN call. */
+/* Workspace bytes that suffice for any M x N x K TN call (aligned copies of A
+ * and B plus the largest split). */
 int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*

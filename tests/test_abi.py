@@ -77,12 +77,15 @@ def test_options():
     assert capi.gemm_set_option("tile_q", 0) == 0
     assert capi.gemm_set_option("tail", 3) == capi.GEMM_ERR_INVALID_OPTION
     assert capi.gemm_set_option("tail", 0) == 0
+    assert capi.gemm_set_option("repack", 2) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("repack", 0) == 0
 
 
 def test_workspace_size_bound():
-    # 16 pieces of every 128 x 256 tile, 32 KB per 32-row slice, plus counters
-    tiles = (1024 // 128) * (512 // 256)
-    assert capi.gemm_workspace_bytes(512, 1024, 64) >= tiles * 16 * 4 * 32 * 1024
+    # aligned copies of A and B, then 16 pieces of every 128 x 64 tile (32 KB a slice)
+    tiles = (1024 // 128) * (512 // 64)
+    repack = (512 + 1024) * 64 * 2
+    assert capi.gemm_workspace_bytes(512, 1024, 64) >= repack + tiles * 16 * 4 * 32 * 1024
     assert capi.gemm_workspace_bytes(0, 1, 1) == 0
 
 
