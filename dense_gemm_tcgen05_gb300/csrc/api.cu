@@ -72,6 +72,7 @@ std::atomic<int> g_opt_splits{0};
 std::atomic<int> g_opt_tile_q{0};
 std::atomic<int> g_opt_tail{0};
 std::atomic<int> g_opt_repack{0};
+std::atomic<int> g_opt_l2hints{0};
 std::atomic<int64_t> g_opt_timeout_ns{2000000000LL};
 
 thread_local cudaError_t t_last_cuda_error = cudaSuccess;
@@ -289,6 +290,7 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     L.prm.ld_out = ldc;
     L.prm.direct_store = c_tma ? 0 : 1;
     L.prm.k_bytes = K * es;
+    L.prm.l2_hints = g_opt_l2hints.load();
     L.prm.tile_q = tile_q;
     const uint32_t d_format = acc16 ? 0u : 1u;
     L.prm.acc16 = acc16 ? 1 : 0;
@@ -524,6 +526,9 @@ int gemm_set_option(const char* name, int64_t value) {
     } else if (!std::strcmp(name, "tail")) {
         if (!(value == 0 || value == 1 || value == 2 || value == 4)) return GEMM_ERR_INVALID_OPTION;
         g_opt_tail.store(static_cast<int>(value));
+    } else if (!std::strcmp(name, "l2_hints")) {
+        if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
+        g_opt_l2hints.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "repack")) {
         if (value < 0 || value > 1) return GEMM_ERR_INVALID_OPTION;
         g_opt_repack.store(static_cast<int>(value));

@@ -60,6 +60,9 @@ struct TcParams {
     // 1: the tensor core accumulates in FP16 (fp16 inputs and output); each
     // accumulator column then holds the final FP16 code in its low half.
     int32_t acc16;
+    // TMA L2 hints: 0 none, 1 Q panels (reused by every tile of a rasteriser
+    // band) evict last and P panels evict first, 2 Q panels evict last only.
+    int32_t l2_hints;
 };
 
 struct TcLaunch {

@@ -331,6 +331,9 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         // ------------------------------------------------ TMA producer
         uint32_t it = 0;
         bool ok = true;
+        const uint64_t pol_p = l2_evict_first_policy();
+        const uint64_t pol_q = l2_evict_last_policy();
+        const bool hints = prm.l2_hints != 0;
         for (int64_t u = first; ok && u < num_units; u += stride) {
             const Unit w = unit_of(u);
             const int32_t p0 = static_cast<int32_t>(w.tp * Cfg::kTileP + rank * Cfg::kBlockP);
@@ -350,12 +353,28 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                     if constexpr (PAIR) {
                         const uint32_t fb = mapa_shared(full_bar(s), 0);
                         if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * tx);
-                        tma_load_2d_pair(sp, &map_p, fb, kx, p0);
-                        tma_load_2d_pair(sq, mq, fb, kx, q0);
+                        if (hints) {
+                            if (prm.l2_hints == 1)
+                                tma_load_2d_pair_hint(sp, &map_p, fb, kx, p0, pol_p);
+                            else
+                                tma_load_2d_pair(sp, &map_p, fb, kx, p0);
+                            tma_load_2d_pair_hint(sq, mq, fb, kx, q0, pol_q);
+                        } else {
+                            tma_load_2d_pair(sp, &map_p, fb, kx, p0);
+                            tma_load_2d_pair(sq, mq, fb, kx, q0);
+                        }
                     } else {
                         mbar_arrive_expect_tx(full_bar(s), tx);
-                        tma_load_2d(sp, &map_p, full_bar(s), kx, p0);
-                        tma_load_2d(sq, mq, full_bar(s), kx, q0);
+                        if (hints) {
+                            if (prm.l2_hints == 1)
+                                tma_load_2d_hint(sp, &map_p, full_bar(s), kx, p0, pol_p);
+                            else
+                                tma_load_2d(sp, &map_p, full_bar(s), kx, p0);
+                            tma_load_2d_hint(sq, mq, full_bar(s), kx, q0, pol_q);
+                        } else {
+                            tma_load_2d(sp, &map_p, full_bar(s), kx, p0);
+                            tma_load_2d(sq, mq, full_bar(s), kx, q0);
+                        }
                     }
                 }
                 __syncwarp();

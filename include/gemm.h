@@ -165,6 +165,10 @@ int gemm_read_watchdog(int reset);
  *   "tail"        the last, partial wave of tiles: 0 auto (default) cuts its tiles
  *                 into 2 or 4 narrower ones when that ends it sooner, 1 never, 2 or
  *                 4 always
+ *   "l2_hints"    L2 eviction hints on the TMA loads: 0 none (default), 1 keep the
+ *                 band-reused A panels and drop the B panels first, 2 keep A only
+ *                 (measured on GB300: 1 raises DRAM reads by half and loses 3-5 %,
+ *                 2 changes nothing measurable)
  *   "repack"      0 (default): with a workspace, operands whose rows are not 16-byte
  *                 aligned are first copied into it with aligned rows; 1 never
  *   "splits"      K pieces per tile: 0 auto (default, needs a workspace), 1 never
