@@ -297,6 +297,18 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     L.prm.idesc = make_idesc(g.format, static_cast<uint32_t>(g.mma_m), static_cast<uint32_t>(tile_q),
                              d_format);
     L.prm.stage_tx_bytes = static_cast<uint32_t>((g.load_p + load_q) * 128);
+    // Ring: as many stages of this width as the stage region holds (narrow
+    // tiles get a deeper ring, i.e. more loads in flight).  The load-based
+    // producer's row split assumes the full-width stage.
+    {
+        const int max_q = g.max_tile_q / g.cluster;
+        const int rows = g.load_p + (prod == Producer::Loads ? max_q : load_q);
+        const int sb = (rows * 128 + 1023) / 1024 * 1024;
+        int st_count = g.stage_region / sb;
+        if (st_count > g.max_stages) st_count = g.max_stages;
+        L.prm.stages = st_count;
+        L.prm.stage_bytes = static_cast<uint32_t>(sb);
+    }
     L.prm.p_ptr = B;
     L.prm.q_ptr = A;
     L.prm.ld_p_bytes = ldb * es;
@@ -397,9 +409,9 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     if (std::getenv("GEMM_DEBUG"))
         std::fprintf(stderr,
                      "[gemm] tn in=%d M=%lld N=%lld K=%lld pair=%d producer=%d direct_store=%d "
-                     "splits=%d tile_q=%d tail=%d tiles=%lldx%lld grid=%d\n",
+                     "splits=%d tile_q=%d tail=%d stages=%d tiles=%lldx%lld grid=%d\n",
                      int(in), (long long)M, (long long)N, (long long)K, int(pair), int(prod),
-                     L.prm.direct_store, L.prm.splits, L.prm.tile_q, L.prm.tail_f,
+                     L.prm.direct_store, L.prm.splits, L.prm.tile_q, L.prm.tail_f, L.prm.stages,
                      (long long)tiles_q, (long long)tiles_p, L.grid);
     e = tc_launch(in, pair, prod, out_f32, L);
     return e == cudaSuccess ? GEMM_OK : fail_cuda(e);

@@ -63,6 +63,10 @@ struct TcParams {
     // TMA L2 hints: 0 none, 1 Q panels (reused by every tile of a rasteriser
     // band) evict last and P panels evict first, 2 Q panels evict last only.
     int32_t l2_hints;
+    // Shared-memory ring: `stages` stages of `stage_bytes` (P tile then Q
+    // tile, a multiple of 1024) in the kernel's fixed stage region.
+    int32_t stages;
+    uint32_t stage_bytes;
 };
 
 struct TcLaunch {
@@ -81,6 +85,8 @@ struct TcGeometry {
     int cluster;           // CTAs per tile
     int mma_m;             // M of the MMA instruction
     uint32_t format;       // A/B format code of the instruction descriptor
+    int stage_region;      // shared-memory bytes for the stage ring
+    int max_stages;        // barrier slots
 };
 
 // Operand producer of the tensor-core kernel: TMA tensor copies, or (for rows

@@ -67,8 +67,10 @@ struct TcCfg {
     static constexpr int kMmasPerStage = kAtomBytes / kMmaKBytes;
     static constexpr int kBytesP = kBlockP * kAtomBytes;
     static constexpr int kBytesQ = kMaxLoadQ * kAtomBytes;
-    static constexpr int kStageBytes = kBytesP + kBytesQ;
-    static constexpr int kStages = PAIR ? 6 : 4;
+    static constexpr int kStageBytes = kBytesP + kBytesQ;    // widest stage
+    static constexpr int kStages = PAIR ? 6 : 4;              // widest stages that fit
+    static constexpr int kStageRegion = kStages * kStageBytes;  // 192 KB either way
+    static constexpr int kMaxStages = 12;  // narrow tiles: more, smaller stages in the region
     static constexpr int kEpiWarps = 4;
     static constexpr int kEpiBufBytes = 32 * 128;            // 32 rows x one 128-byte row
     static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
@@ -78,8 +80,8 @@ struct TcCfg {
     static constexpr int kFullArrivals = LOADS ? kLoadWarps : 1;
     static constexpr int kAccCols = kMmaN;
     static constexpr int kTmemCols = 512;
-    static constexpr int kNumBars = 2 * kStages + 4 + 1;
-    static constexpr int kOffEpi = kStages * kStageBytes;
+    static constexpr int kNumBars = 2 * kMaxStages + 4 + 1;
+    static constexpr int kOffEpi = kStageRegion;
     static constexpr int kOffBars = kOffEpi + kEpiBytes;
     static constexpr int kOffTmemSlot = kOffBars + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -236,7 +238,9 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                    const __grid_constant__ CUtensorMap map_out,
                    const __grid_constant__ CUtensorMap map_q_tail, const TcParams prm) {
     using Cfg = TcCfg<IN, PAIR, LOADS>;
-    constexpr int S = Cfg::kStages;
+    constexpr int SM = Cfg::kMaxStages;                 // barrier slots
+    const uint32_t S = static_cast<uint32_t>(prm.stages);  // ring depth for this call
+    const uint32_t stage_bytes = prm.stage_bytes;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -247,10 +251,10 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
     const uint32_t lane = lane_idx();
     const uint32_t bars = base + Cfg::kOffBars;
     auto full_bar = [&](uint32_t s) { return bars + 8u * s; };
-    auto empty_bar = [&](uint32_t s) { return bars + 8u * (S + s); };
-    auto accf_bar = [&](uint32_t b) { return bars + 8u * (2 * S + b); };
-    auto acce_bar = [&](uint32_t b) { return bars + 8u * (2 * S + 2 + b); };
-    const uint32_t done_bar = bars + 8u * (2 * S + 4);
+    auto empty_bar = [&](uint32_t s) { return bars + 8u * (SM + s); };
+    auto accf_bar = [&](uint32_t b) { return bars + 8u * (2 * SM + b); };
+    auto acce_bar = [&](uint32_t b) { return bars + 8u * (2 * SM + 2 + b); };
+    const uint32_t done_bar = bars + 8u * (2 * SM + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Cfg::kOffTmemSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Cfg::kOffAbort);
 
@@ -258,7 +262,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
     const bool leader = rank == 0;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
+        for (int s = 0; s < SM; ++s) {
             mbar_init(full_bar(s), Cfg::kFullArrivals);
             mbar_init(empty_bar(s), 1);
         }
@@ -329,7 +333,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
 
     if (warp == 0 && !LOADS) {
         // ------------------------------------------------ TMA producer
-        uint32_t it = 0;
+        uint32_t it = 0, rs = 0, rph = 0;   // stages issued; ring slot and phase
         bool ok = true;
         const uint64_t pol_p = l2_evict_first_policy();
         const uint64_t pol_q = l2_evict_last_policy();
@@ -341,13 +345,17 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
             const CUtensorMap* mq = w.narrow ? &map_q_tail : &map_q;
             const uint32_t tx = w.narrow ? prm.stage_tx_tail : prm.stage_tx_bytes;
             for (int32_t kb = w.kb_lo; kb < w.kb_hi; ++kb, ++it) {
-                const uint32_t s = it % S, ph = (it / S) & 1u;
+                const uint32_t s = rs, ph = rph;
+                if (++rs == S) {
+                    rs = 0;
+                    rph ^= 1u;
+                }
                 if (!warp_wait(empty_bar(s), ph ^ 1u, wd)) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
-                    const uint32_t sp = base + s * Cfg::kStageBytes;
+                    const uint32_t sp = base + s * stage_bytes;
                     const uint32_t sq = sp + Cfg::kBytesP;
                     const int32_t kx = kb * Cfg::kStageK;
                     if constexpr (PAIR) {
@@ -415,7 +423,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         const int64_t pitch = is_p ? prm.ld_p_bytes : prm.ld_q_bytes;
         const int64_t rows_lim = is_p ? prm.rows_p : prm.rows_q;
         const uint32_t srow0 = r0 * Cfg::kAtomBytes;  // P then Q are contiguous, 128 B a row
-        uint32_t it = 0;
+        uint32_t rs = 0, rph = 0;   // ring slot and phase
         bool ok = true;
         for (int64_t u = first; ok && u < num_units; u += stride) {
             const Unit w = unit_of(u);
@@ -427,8 +435,12 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
             int64_t rows_left = rows_lim - g0;
             if (!is_p && w.width - static_cast<int64_t>(r0 - Cfg::kBlockP) < rows_left)
                 rows_left = w.width - static_cast<int64_t>(r0 - Cfg::kBlockP);
-            for (int32_t kb = w.kb_lo; kb < w.kb_hi; ++kb, ++it) {
-                const uint32_t s = it % S, ph = (it / S) & 1u;
+            for (int32_t kb = w.kb_lo; kb < w.kb_hi; ++kb) {
+                const uint32_t s = rs, ph = rph;
+                if (++rs == S) {
+                    rs = 0;
+                    rph ^= 1u;
+                }
                 const int64_t kb_byte = static_cast<int64_t>(kb) * Cfg::kAtomBytes;
                 const int64_t left = prm.k_bytes - kb_byte;
                 const int32_t win = left > 128 ? 128 : static_cast<int32_t>(left);  // >= 1
@@ -452,7 +464,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t sp = base + s * Cfg::kStageBytes + srow0;
+                const uint32_t sp = base + s * stage_bytes + srow0;
 #pragma unroll
                 for (int i = 0; i < kQuadsPerWarp; ++i) {
                     const uintptr_t a = reinterpret_cast<uintptr_t>(row0) +
@@ -472,7 +484,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (!PAIR || leader) {
-            uint32_t it = 0, lt = 0;
+            uint32_t lt = 0, rs = 0, rph = 0;   // tiles; ring slot and phase
             bool ok = true;
             for (int64_t u = first; ok && u < num_units; u += stride, ++lt) {
                 const uint32_t b = lt & 1u, aph = (lt >> 1) & 1u;
@@ -485,15 +497,19 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                 const Unit w = unit_of(u);
                 const uint32_t idesc = w.narrow ? prm.idesc_tail : prm.idesc;
                 const int32_t kb_lo = w.kb_lo;
-                for (int32_t kb = w.kb_lo; kb < w.kb_hi; ++kb, ++it) {
-                    const uint32_t s = it % S, ph = (it / S) & 1u;
+                for (int32_t kb = w.kb_lo; kb < w.kb_hi; ++kb) {
+                    const uint32_t s = rs, ph = rph;
+                    if (++rs == S) {
+                        rs = 0;
+                        rph ^= 1u;
+                    }
                     if (!warp_wait(full_bar(s), ph, wd)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
                     if (lane == 0) {
-                        const uint32_t sp = base + s * Cfg::kStageBytes;
+                        const uint32_t sp = base + s * stage_bytes;
                         const uint64_t adesc = sdesc_kmajor_sw128(sp);
                         const uint64_t bdesc = sdesc_kmajor_sw128(sp + Cfg::kBytesP);
 #pragma unroll
@@ -798,12 +814,14 @@ template <InKind IN>
 TcGeometry tc_geometry_impl(bool pair) {
     if (pair) {
         using Cfg = TcCfg<IN, true, false>;
-        return TcGeometry{Cfg::kTileP, Cfg::kMmaN, Cfg::kBlockP, Cfg::kStageK, 2, Cfg::kMmaM,
-                          Cfg::kFormat};
+        return TcGeometry{Cfg::kTileP,  Cfg::kMmaN,    Cfg::kBlockP,      Cfg::kStageK,
+                          2,            Cfg::kMmaM,    Cfg::kFormat,      Cfg::kStageRegion,
+                          Cfg::kMaxStages};
     }
     using Cfg = TcCfg<IN, false, false>;
-    return TcGeometry{Cfg::kTileP, Cfg::kMmaN, Cfg::kBlockP, Cfg::kStageK, 1, Cfg::kMmaM,
-                      Cfg::kFormat};
+    return TcGeometry{Cfg::kTileP,  Cfg::kMmaN,    Cfg::kBlockP,      Cfg::kStageK,
+                      1,            Cfg::kMmaM,    Cfg::kFormat,      Cfg::kStageRegion,
+                      Cfg::kMaxStages};
 }
 
 }  // namespace gb300
