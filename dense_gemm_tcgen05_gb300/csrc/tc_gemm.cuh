@@ -485,6 +485,8 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         // ------------------------------------------------ MMA issuer
         if (!PAIR || leader) {
             uint32_t lt = 0, rs = 0, rph = 0;   // tiles; ring slot and phase
+            const uint64_t adesc0 = sdesc_kmajor_sw128(base);
+            const uint64_t bdesc0 = sdesc_kmajor_sw128(base + Cfg::kBytesP);
             bool ok = true;
             for (int64_t u = first; ok && u < num_units; u += stride, ++lt) {
                 const uint32_t b = lt & 1u, aph = (lt >> 1) & 1u;
@@ -509,9 +511,11 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                     }
                     tc_fence_after_sync();
                     if (lane == 0) {
-                        const uint32_t sp = base + s * stage_bytes;
-                        const uint64_t adesc = sdesc_kmajor_sw128(sp);
-                        const uint64_t bdesc = sdesc_kmajor_sw128(sp + Cfg::kBytesP);
+                        // descriptors of stage s: the ring's first ones advanced by
+                        // s stages (start-address field counts 16-byte units)
+                        const uint64_t soff = static_cast<uint64_t>(s * (stage_bytes >> 4));
+                        const uint64_t adesc = adesc0 + soff;
+                        const uint64_t bdesc = bdesc0 + soff;
 #pragma unroll
                         for (int kk = 0; kk < Cfg::kMmasPerStage; ++kk) {
                             // advance the start address by 32 bytes of K per MMA
