@@ -71,6 +71,7 @@ std::atomic<int> g_opt_max_ctas{0};
 std::atomic<int> g_opt_splits{0};
 std::atomic<int> g_opt_tile_q{0};
 std::atomic<int> g_opt_tail{0};
+std::atomic<int> g_opt_tail_k{0};
 std::atomic<int> g_opt_repack{0};
 std::atomic<int> g_opt_l2hints{0};
 std::atomic<int64_t> g_opt_timeout_ns{2000000000LL};
@@ -357,28 +358,44 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
         }
     }
     // Tail splitting: when the last wave of tiles is partial, cut its tiles
-    // into f narrower units (f = 2 or 4, tile_q / f still a whole number of
-    // epilogue chunks) so that it ends sooner.  Narrow units move more operand
-    // bytes per FLOP and become L2-bound: measured on GB300, a half-width unit
-    // takes about 0.8 of a full tile's time (0.9 for FP8, whose MMA is twice as
-    // fast) and a quarter-width unit about 0.65 (0.8 for FP8).
+    // into f narrower units along M (f = 2 or 4, tile_q / f still a whole
+    // number of epilogue chunks) so that it ends sooner.  Narrow units are
+    // L2-bound; measured on GB300, a half-width unit takes ~0.8 of a full
+    // tile's time (0.9 for FP8), a quarter-width one ~0.65 (0.8 for FP8).
+    // Option "tail_k" = f instead cuts the tail tiles into f K pieces of full
+    // width, combined through the workspace like split-K; it is not chosen
+    // automatically: the last piece's fix-up reads every other piece's partial
+    // slice with one L2 round trip per chunk and piece, which cost more than
+    // the shorter last wave saved (BF16 4096^3: 100 us against 79 us).
     L.prm.full_units = tiles * L.prm.splits;
     L.prm.tail_f = 1;
     L.prm.idesc_tail = L.prm.idesc;
     L.prm.stage_tx_tail = L.prm.stage_tx_bytes;
+    L.prm.tail_ksplit = 0;
+    L.prm.tail_kb_per = L.prm.num_kb;
     {
         const int opt_tail = g_opt_tail.load();
         const int64_t units_slots = slots;
         const int64_t waves = tiles / units_slots, rem = tiles % units_slots;
         const int min_w = 128 / os;  // one epilogue chunk
+        const int64_t slices = 4 * g.cluster;
+        const int64_t cnt_bytes = ((rem * slices * 4 + 255) / 256) * 256;
+        char* ws = ws_base ? ws_base + ws_used : nullptr;
+        const int64_t ws_room = ws_total - ws_used;
         int f = 1;
+        bool ksplit = false;
+        int64_t kb_per_t = L.prm.num_kb;
+        auto narrow_ok = [&](int c) {
+            return tile_q % c == 0 && (tile_q / c) % min_w == 0 && tile_q / c >= 64;
+        };
         if (L.prm.splits == 1 && rem > 0 && opt_tail != 1) {
             if (opt_tail == 2 || opt_tail == 4) {
-                f = opt_tail;
+                f = narrow_ok(opt_tail) ? opt_tail : 1;
             } else {
                 const bool fp8 = in == InKind::E4M3;
                 double best = 1.0;
                 for (int cand : {2, 4}) {
+                    if (!narrow_ok(cand)) continue;
                     const double unit_cost = cand == 2 ? (fp8 ? 0.9 : 0.8) : (fp8 ? 0.8 : 0.65);
                     const double t = static_cast<double>((cand * rem + units_slots - 1) / units_slots) *
                                      unit_cost;
@@ -388,9 +405,28 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
                     }
                 }
             }
-            if (tile_q % f != 0 || (tile_q / f) % min_w != 0 || tile_q / f < 64) f = 1;
+            const int opt_tail_k = g_opt_tail_k.load();
+            if (opt_tail_k >= 2 && !acc16 && ws) {
+                const int64_t kb_per = (L.prm.num_kb + opt_tail_k - 1) / opt_tail_k;
+                const int64_t pieces = (L.prm.num_kb + kb_per - 1) / kb_per;
+                const int64_t need = cnt_bytes + rem * pieces * slices * 32 * 256 * 4;
+                if (pieces >= 2 && need <= ws_room) {
+                    f = static_cast<int>(pieces);
+                    ksplit = true;
+                    kb_per_t = kb_per;
+                }
+            }
         }
-        if (f > 1) {
+        if (f > 1 && ksplit) {
+            L.prm.tail_ksplit = 1;
+            L.prm.tail_f = f;
+            L.prm.tail_kb_per = static_cast<int32_t>(kb_per_t);
+            L.prm.full_units = waves * units_slots;
+            L.prm.ws_counters = reinterpret_cast<unsigned int*>(ws);
+            L.prm.ws_partials = reinterpret_cast<float*>(ws + cnt_bytes);
+            e = cudaMemsetAsync(ws, 0, static_cast<size_t>(cnt_bytes), stream);
+            if (e != cudaSuccess) return fail_cuda(e);
+        } else if (f > 1) {
             const int width = tile_q / f;
             const int load_qt = width / g.cluster;
             if (prod == Producer::Tma) {
@@ -402,6 +438,8 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
             L.prm.idesc_tail = make_idesc(g.format, static_cast<uint32_t>(g.mma_m),
                                           static_cast<uint32_t>(width), d_format);
             L.prm.stage_tx_tail = static_cast<uint32_t>((g.load_p + load_qt) * 128);
+        }
+        if (f > 1) {
             const int64_t units = L.prm.full_units + (tiles - L.prm.full_units) * f;
             L.grid = static_cast<int>((units < slots ? units : slots) * g.cluster);
         }
@@ -409,9 +447,10 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     if (std::getenv("GEMM_DEBUG"))
         std::fprintf(stderr,
                      "[gemm] tn in=%d M=%lld N=%lld K=%lld pair=%d producer=%d direct_store=%d "
-                     "splits=%d tile_q=%d tail=%d stages=%d tiles=%lldx%lld grid=%d\n",
+                     "splits=%d tile_q=%d tail=%d ktail=%d stages=%d tiles=%lldx%lld grid=%d\n",
                      int(in), (long long)M, (long long)N, (long long)K, int(pair), int(prod),
-                     L.prm.direct_store, L.prm.splits, L.prm.tile_q, L.prm.tail_f, L.prm.stages,
+                     L.prm.direct_store, L.prm.splits, L.prm.tile_q, L.prm.tail_f,
+                     L.prm.tail_ksplit, L.prm.stages,
                      (long long)tiles_q, (long long)tiles_p, L.grid);
     e = tc_launch(in, pair, prod, out_f32, L);
     return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
@@ -535,6 +574,9 @@ int gemm_set_option(const char* name, int64_t value) {
         if (!(value == 0 || value == 64 || value == 128 || value == 192 || value == 256))
             return GEMM_ERR_INVALID_OPTION;
         g_opt_tile_q.store(static_cast<int>(value));
+    } else if (!std::strcmp(name, "tail_k")) {
+        if (value < 0 || value > 8 || value == 1) return GEMM_ERR_INVALID_OPTION;
+        g_opt_tail_k.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "tail")) {
         if (!(value == 0 || value == 1 || value == 2 || value == 4)) return GEMM_ERR_INVALID_OPTION;
         g_opt_tail.store(static_cast<int>(value));

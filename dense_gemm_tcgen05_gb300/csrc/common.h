@@ -57,6 +57,10 @@ struct TcParams {
     int32_t tail_f;
     uint32_t idesc_tail;
     uint32_t stage_tx_tail;
+    // 1: the tail tiles keep their width and are cut into tail_f K pieces of
+    // tail_kb_per stages instead, combined through the split-K workspace.
+    int32_t tail_ksplit;
+    int32_t tail_kb_per;
     // 1: the tensor core accumulates in FP16 (fp16 inputs and output); each
     // accumulator column then holds the final FP16 code in its low half.
     int32_t acc16;

@@ -295,37 +295,52 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
     const Watch wd{abort_flag, prm.watchdog, prm.timeout_ns};
     const int64_t num_tiles = static_cast<int64_t>(prm.tiles_p) * prm.tiles_q;
     // Work units: whole tiles times K pieces, then the tail tiles cut into
-    // tail_f narrower units each.
+    // tail_f units each -- narrower along Q, or (tail_ksplit) K pieces.
     const int64_t full_tiles = prm.full_units / prm.splits;
     const int64_t num_units = prm.full_units + (num_tiles - full_tiles) * prm.tail_f;
     struct Unit {
         int64_t tile, tq, tp;
+        int64_t ws_tile;  // the tile's slot in the split-K workspace
         int32_t q_off;    // first Q row (C column) of the unit
         int32_t width;    // Q rows of the unit = MMA N
-        int32_t piece;    // K piece (0 unless split)
+        int32_t piece;    // K piece of the tile (0 unless split)
+        int32_t pieces;   // K pieces of the tile
         int32_t kb_lo, kb_hi;
-        bool narrow;      // tail unit
+        bool narrow;      // narrow tail unit
     };
     auto unit_of = [&](int64_t u) {
         Unit w;
-        int32_t part = 0;
+        int32_t part = 0, kb_per = prm.kb_per_split;
         if (u < prm.full_units) {
             w.tile = u / prm.splits;
             w.piece = static_cast<int32_t>(u % prm.splits);
+            w.pieces = prm.splits;
+            w.ws_tile = w.tile;
             w.width = prm.tile_q;
             w.narrow = false;
         } else {
             const int64_t v = u - prm.full_units;
             w.tile = full_tiles + v / prm.tail_f;
-            part = static_cast<int32_t>(v % prm.tail_f);
-            w.piece = 0;
-            w.width = prm.tile_q / prm.tail_f;
-            w.narrow = true;
+            if (prm.tail_ksplit) {
+                w.piece = static_cast<int32_t>(v % prm.tail_f);
+                w.pieces = prm.tail_f;
+                w.ws_tile = w.tile - full_tiles;
+                w.width = prm.tile_q;
+                w.narrow = false;
+                kb_per = prm.tail_kb_per;
+            } else {
+                part = static_cast<int32_t>(v % prm.tail_f);
+                w.piece = 0;
+                w.pieces = 1;
+                w.ws_tile = 0;
+                w.width = prm.tile_q / prm.tail_f;
+                w.narrow = true;
+            }
         }
         raster_tile(w.tile, prm.tiles_q, prm.tiles_p, prm.group, &w.tq, &w.tp);
         w.q_off = static_cast<int32_t>(w.tq * prm.tile_q) + part * w.width;
-        w.kb_lo = w.piece * prm.kb_per_split;
-        w.kb_hi = w.kb_lo + prm.kb_per_split < prm.num_kb ? w.kb_lo + prm.kb_per_split : prm.num_kb;
+        w.kb_lo = w.piece * kb_per;
+        w.kb_hi = w.kb_lo + kb_per < prm.num_kb ? w.kb_lo + kb_per : prm.num_kb;
         return w;
     };
     const int64_t first = PAIR ? blockIdx.x / 2 : blockIdx.x;
@@ -679,7 +694,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
 
         for (int64_t u = first; u < num_units; u += stride, ++lt) {
             const Unit w = unit_of(u);
-            const int64_t t = w.tile, tp = w.tp;
+            const int64_t tp = w.tp;
             const int chunks = w.width / kCols;
             const uint32_t b = lt & 1u, aph = (lt >> 1) & 1u;
             if (!warp_wait(accf_bar(b), aph, wd)) break;
@@ -688,7 +703,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                 static_cast<int32_t>(tp * Cfg::kTileP + rank * Cfg::kBlockP + quarter * 32);
             const int32_t col0 = w.q_off;
             const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + b * Cfg::kAccCols;
-            if (prm.splits == 1) {
+            if (w.pieces == 1) {
 #pragma unroll 1
                 for (int c = 0; c < chunks; ++c) {
                     uint32_t v0[32], v1[32];
@@ -719,7 +734,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                 // the slice so that a warp's stores (and loads) are coalesced.
                 const int32_t piece = w.piece;
                 float* part = prm.ws_partials +
-                              ((t * prm.splits + piece) * kSlices + slice) * kSliceFloats;
+                              ((w.ws_tile * w.pieces + piece) * kSlices + slice) * kSliceFloats;
 #pragma unroll 1
                 for (int c = 0; c < w.width / 32; ++c) {
                     uint32_t v[32];
@@ -733,22 +748,22 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                 __threadfence();
                 __syncwarp();
                 unsigned int prev = 0;
-                unsigned int* counter = prm.ws_counters + t * kSlices + slice;
+                unsigned int* counter = prm.ws_counters + w.ws_tile * kSlices + slice;
                 if (lane == 0) prev = atomicAdd(counter, 1u);
                 prev = __shfl_sync(0xffffffffu, prev, 0);
-                if (prev + 1 != static_cast<unsigned int>(prm.splits)) continue;
+                if (prev + 1 != static_cast<unsigned int>(w.pieces)) continue;
                 // Last piece of this slice: sum all pieces in piece order (the
                 // result does not depend on which piece finished last).
                 __threadfence();
                 if (lane == 0) *counter = 0u;  // ready for the next call
                 const float* base_part =
-                    prm.ws_partials + (t * prm.splits * kSlices + slice) * kSliceFloats;
+                    prm.ws_partials + (w.ws_tile * w.pieces * kSlices + slice) * kSliceFloats;
 #pragma unroll 1
                 for (int c = 0; c < chunks; ++c) {
                     float f[kCols];
 #pragma unroll
                     for (int j = 0; j < kCols; ++j) f[j] = 0.f;
-                    for (int32_t pc = 0; pc < prm.splits; ++pc) {
+                    for (int32_t pc = 0; pc < w.pieces; ++pc) {
                         const float* src = base_part + static_cast<int64_t>(pc) * kSlices * kSliceFloats;
 #pragma unroll
                         for (int j = 0; j < kCols; ++j)

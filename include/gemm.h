@@ -171,6 +171,9 @@ int gemm_read_watchdog(int reset);
  *                 2 changes nothing measurable)
  *   "repack"      0 (default): with a workspace, operands whose rows are not 16-byte
  *                 aligned are first copied into it with aligned rows; 1 never
+ *   "tail_k"      0 (default), or 2..8: with a workspace, cut the last partial wave's
+ *                 tiles into that many K pieces instead of narrower tiles (slower
+ *                 on the shapes measured: the fix-up is L2-latency-bound)
  *   "splits"      K pieces per tile: 0 auto (default, needs a workspace), 1 never
  *                 split, 2..64 split that many ways when the workspace suffices
  * Returns GEMM_OK or GEMM_ERR_INVALID_OPTION.

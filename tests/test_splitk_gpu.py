@@ -98,3 +98,34 @@ def test_workspace_api_checks():
     ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
     assert capi.gemm_set_workspace(ws.data_ptr() + 8, 512) == capi.GEMM_ERR_MISALIGNED
     assert capi.gemm_workspace_bytes(1024, 1024, 8192) > 0
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("pair", [0, 1])
+def test_tail_k_pieces_full(kind, pair, workspace):
+    """A partial last wave with a workspace: its tiles are cut into K pieces
+    (few CTAs force several waves and a partial last one)."""
+    M, N, K = 1100, 700, 1000
+    for k, v in {"pair": pair, "max_ctas": 10, "tail_k": 3}.items():
+        assert capi.gemm_set_option(k, v) == 0
+    try:
+        ops = si.tn_operands(kind, M, N, K, dist="normal", seed=pair + 11, sigma=0.5)
+        C1 = run_tn(kind, ops, M, N, K)
+        check_full(kind, ops, M, N, K, C1)
+        C2 = run_tn(kind, ops, M, N, K)
+        assert torch.equal(C1.view(torch.int16), C2.view(torch.int16)), "not deterministic"
+    finally:
+        capi.gemm_set_option("max_ctas", 0)
+        capi.gemm_set_option("tail_k", 0)
+
+
+@pytest.mark.parametrize("shape,tail_k", [((4096, 4096, 4096), 2), ((3072, 4096, 8192), 5)])
+def test_tail_k_pieces_large_sampled(shape, tail_k, workspace):
+    M, N, K = shape
+    assert capi.gemm_set_option("tail_k", tail_k) == 0
+    try:
+        ops = si.tn_operands("bf16", M, N, K, dist="normal", seed=3, sigma=0.05)
+        C = run_tn("bf16", ops, M, N, K)
+        check_sampled("bf16", ops, M, N, K, C, seed=3)
+    finally:
+        capi.gemm_set_option("tail_k", 0)
