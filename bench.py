@@ -225,39 +225,78 @@ def timed_loop(call, sets, steps, warmup, stream, dist=None, sampler=None):
 
 def e2e_loop(kind, M, N, K, ops, steps, warmup, stream, stream_h):
     """End to end through the C ABI with host buffers: every step copies A and
-    B from pinned host memory, runs the GEMM and copies C back."""
+    B from pinned host memory, runs the GEMM and copies C back to pinned host
+    memory.  Steps are pipelined the way a throughput-bound caller would run
+    them: two device buffer sets, host-to-device copies on one stream, the GEMM
+    on `stream`, device-to-host copies on a third, so that the copies of steps
+    i + 1 and i - 1 overlap the GEMM of step i; events order each buffer's reuse.
+    The timed region runs from before the first step's input copy to after the
+    last step's output copy.  Returns (pipelined ms per step, serial ms per step,
+    host-to-device bytes per step, device-to-host bytes per step); the serial
+    figure runs copy, GEMM, copy back to back on one stream, for context."""
     import torch
 
     ha = ops["A"].pin_memory()
     hb = ops["B"].pin_memory()
     out_dt = torch.float16 if kind == "f16" else torch.bfloat16
     hc = torch.empty((N, M), dtype=out_dt).pin_memory()
-    da = torch.empty_like(ha, device="cuda")
-    db = torch.empty_like(hb, device="cuda")
-    dc = torch.empty((N, M), dtype=out_dt, device="cuda")
+    da = [torch.empty_like(ha, device="cuda") for _ in range(2)]
+    db = [torch.empty_like(hb, device="cuda") for _ in range(2)]
+    dc = [torch.empty((N, M), dtype=out_dt, device="cuda") for _ in range(2)]
     call = tn_call(kind, M, N, K, ops["scale_a"], ops["scale_b"], stream_h)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: [torch.cuda.Event() for _ in range(2)]  # noqa: E731
+    in_done, gemm_done, out_done = ev(), ev(), ev()
 
-    def step():
-        da.copy_(ha, non_blocking=True)
-        db.copy_(hb, non_blocking=True)
-        call(da, db, dc)
-        hc.copy_(dc, non_blocking=True)
+    def step(i):
+        j = i % 2
+        if i >= 2:
+            s_in.wait_event(gemm_done[j])      # the GEMM of step i - 2 has read slot j
+        with torch.cuda.stream(s_in):
+            da[j].copy_(ha, non_blocking=True)
+            db[j].copy_(hb, non_blocking=True)
+        in_done[j].record(s_in)
+        stream.wait_event(in_done[j])
+        if i >= 2:
+            stream.wait_event(out_done[j])     # C of step i - 2 has left slot j
+        call(da[j], db[j], dc[j])
+        gemm_done[j].record(stream)
+        s_out.wait_event(gemm_done[j])
+        with torch.cuda.stream(s_out):
+            hc.copy_(dc[j], non_blocking=True)
+        out_done[j].record(s_out)
 
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            step()
-        torch.cuda.synchronize()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(steps):
-            step()
-        t1.record(stream)
-        torch.cuda.synchronize()
+    def serial_step():
+        with torch.cuda.stream(stream):
+            da[0].copy_(ha, non_blocking=True)
+            db[0].copy_(hb, non_blocking=True)
+            call(da[0], db[0], dc[0])
+            hc.copy_(dc[0], non_blocking=True)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(s_in)
+    for i in range(steps):
+        step(i)
+    t1.record(s_out)                           # after the last copy back, which follows all
+    torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
+
+    for _ in range(warmup):
+        serial_step()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(steps):
+        serial_step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    serial_ms = t0.elapsed_time(t1) / steps
     h2d = ha.numel() * ha.element_size() + hb.numel() * hb.element_size()
     d2h = hc.numel() * hc.element_size()
-    return ms, h2d, d2h
+    return ms, serial_ms, h2d, d2h
 
 
 def f32_bench(n, steps, warmup, stream, stream_h):
@@ -281,11 +320,23 @@ def f32_bench(n, steps, warmup, stream, stream_h):
 
 
 def cublas_context(M, N, K, dtype, steps, stream):
-    """torch.matmul (cuBLAS) on the same problem, for context only."""
+    """torch.matmul (cuBLAS) on the same problem, for context only.  FP32 runs
+    with TF32 off, i.e. on the CUDA cores like gemm_f32."""
     import torch
 
     a = torch.randn((M, K), device="cuda").to(dtype)
     b = torch.randn((N, K), device="cuda").to(dtype)
+    tf32 = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        return _time_matmul(a, b, M, N, K, steps, stream)
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = tf32
+
+
+def _time_matmul(a, b, M, N, K, steps, stream):
+    import torch
+
     with torch.cuda.stream(stream):
         for _ in range(3):
             torch.matmul(a, b.t())
@@ -350,6 +401,8 @@ def run_ours(args):
     capi.lib()
     peaks, peak_src = load_peaks()
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained",
+                                FALLBACK_PEAKS["bf16_tflops_sustained"]))
     stream = torch.cuda.Stream()
     stream_h = stream.cuda_stream
     M = N = K = 8192
@@ -416,12 +469,15 @@ def run_ours(args):
         fpk = fp32_alu_peak_tflops(sm_count(), clk)
         per["f32_simt_4096"] = {"tflops": round(tf, 2), "peak": round(fpk, 1),
                                 "frac": round(tf / fpk, 4), "bound": "alu"}
+        per["cublas_context_f32_4096"] = round(cublas_context(4096, 4096, 4096, torch.float32,
+                                                              20, stream), 2)
         per["cublas_context_f16_8192"] = round(cublas_context(M, N, K, torch.float16, 20, stream), 1)
         if args.sweep:
             per.update(sweep(stream, stream_h, burst))
 
         e2e_steps = max(3, min(args.steps, 20))
-        e_ms, h2d, d2h = e2e_loop("f16", M, N, K, ops, e2e_steps, 2, stream, stream_h)
+        e_ms, serial_ms, h2d, d2h = e2e_loop("f16", M, N, K, ops, e2e_steps, 2, stream,
+                                             stream_h)
         traffic = load_traffic()
         result = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -435,11 +491,22 @@ def run_ours(args):
                        "l2": "3 rotating input sets (1.1 GiB total) >> 129 MB L2, no flush",
                        "parallelism": "replicas" if world > 1 else "single",
                        "vs_baseline_ref": "pages' best FP16 8192^3: 142.30 TFLOP/s, RX 9070 XT"},
-            "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": burst,
-                         "unit": UNIT, "frac": round(achieved / burst, 4),
-                         "traffic": traffic, "peak_source": peak_src + " bf16 burst (fp16 rate)"},
+            # The main loop is K back-to-back launches (~0.7 s at K = 1000) and runs
+            # under the power cap, so it is held against the sustained peak; the
+            # burst fraction is given beside it.
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": sustained,
+                         "unit": UNIT, "frac": round(achieved / sustained, 4),
+                         "traffic": traffic,
+                         "peak_source": peak_src + " bf16 sustained (fp16 rate): the timed "
+                                        "region is a long back-to-back loop",
+                         "frac_of_burst": round(achieved / burst, 4)},
             "e2e": {"value": round(flops / (e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps,
+                    "how": "pinned host A, B -> device, gemm_f16_tn, C -> pinned host, every "
+                           "step; copies of neighbouring steps overlap the GEMM (two buffer "
+                           "sets, three streams)",
+                    "serial_value": round(flops / (serial_ms * 1e-3) / 1e12, 2)},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "per_dtype": per,

@@ -12,7 +12,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "common.h"
+#include "launch.h"
 #include "gemm.h"
 #include "ptx.cuh"
 #include "raster.h"
@@ -73,6 +73,7 @@ std::atomic<int> g_opt_tile_q{0};
 std::atomic<int> g_opt_tail{0};
 std::atomic<int> g_opt_tail_k{0};
 std::atomic<int> g_opt_repack{0};
+std::atomic<int> g_opt_f32_tail{0};
 std::atomic<int> g_opt_l2hints{0};
 std::atomic<int64_t> g_opt_timeout_ns{2000000000LL};
 
@@ -483,7 +484,8 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const
     if (M == 0 || N == 0) return GEMM_OK;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
     cudaError_t e = K == 0 ? zero_fill_launch(C, M, N, ldc, 4, stream)
-                           : f32_launch(M, N, K, A, lda, B, ldb, C, ldc, stream);
+                           : f32_launch(M, N, K, A, lda, B, ldb, C, ldc, stream,
+                                        g_opt_f32_tail.load());
     return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
 }
 
@@ -583,6 +585,9 @@ int gemm_set_option(const char* name, int64_t value) {
     } else if (!std::strcmp(name, "l2_hints")) {
         if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
         g_opt_l2hints.store(static_cast<int>(value));
+    } else if (!std::strcmp(name, "f32_tail")) {
+        if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
+        g_opt_f32_tail.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "repack")) {
         if (value < 0 || value > 1) return GEMM_ERR_INVALID_OPTION;
         g_opt_repack.store(static_cast<int>(value));

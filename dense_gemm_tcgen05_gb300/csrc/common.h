@@ -1,4 +1,5 @@
-// common.h -- host-side declarations shared by the library's translation units.
+// common.h -- the tensor-core kernel's parameter block and launch interface,
+// shared by the kernel and the host code that launches it.
 #pragma once
 
 #include <cstdint>
@@ -101,39 +102,5 @@ TcGeometry tc_geometry(InKind in, bool pair);
 // out_f32: FP32 output (E4M3 inputs only); otherwise the input's 16-bit type
 // (bf16 for E4M3).
 cudaError_t tc_launch(InKind in, bool pair, Producer prod, bool out_f32, const TcLaunch& L);
-
-// CUDA-core fallback for TN operands that TMA cannot address.
-cudaError_t tn_fallback_launch(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K,
-                               const void* A, int64_t lda, const void* B, int64_t ldb, float scale,
-                               void* C, int64_t ldc, cudaStream_t stream);
-
-// Scratch supplied by the caller of the internal TN path instead of the
-// registered workspace (see gemm_tn_with_scratch).
-struct ScratchOverride {
-    void* ptr;       // device address, 256-byte aligned
-    int64_t bytes;   // usable bytes at ptr
-    int splits;      // 0 automatic, 1 never split, >= 2 that many K pieces
-};
-
-// The TN path with explicit split-K scratch (16-bit inputs and output).
-int gemm_tn_with_scratch(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-                         const void* B, int64_t ldb, void* C, int64_t ldc, void* stream,
-                         const ScratchOverride& ov);
-
-cudaError_t f32_launch(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
-                       const float* B, int64_t ldb, float* C, int64_t ldc, cudaStream_t stream);
-
-// Copies rows of row_bytes bytes from any alignment into 16-byte-aligned rows
-// of pitch dp (a multiple of 16) so that TMA can address them.
-cudaError_t repack_rows_launch(const void* src, int64_t sp, void* dst, int64_t dp, int64_t rows,
-                               int64_t row_bytes, cudaStream_t stream);
-
-// Writes zeros into a rows x cols block with leading dimension ld (elements of
-// elem_bytes bytes); used for K == 0.
-cudaError_t zero_fill_launch(void* C, int64_t rows, int64_t cols, int64_t ld, int elem_bytes,
-                             cudaStream_t stream);
-
-cudaError_t watchdog_selftest_launch(uint64_t limit_ns, unsigned int* watchdog,
-                                     cudaStream_t stream);
 
 }  // namespace gb300

@@ -1,0 +1,47 @@
+// launch.h -- host-side launchers of the library's other kernels and the
+// internal TN entry with caller-supplied scratch.
+#pragma once
+
+#include "common.h"
+
+namespace gb300 {
+
+// CUDA-core fallback for TN operands that TMA cannot address.
+cudaError_t tn_fallback_launch(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K,
+                               const void* A, int64_t lda, const void* B, int64_t ldb, float scale,
+                               void* C, int64_t ldc, cudaStream_t stream);
+
+// Scratch supplied by the caller of the internal TN path instead of the
+// registered workspace (see gemm_tn_with_scratch).
+struct ScratchOverride {
+    void* ptr;       // device address, 256-byte aligned
+    int64_t bytes;   // usable bytes at ptr
+    int splits;      // 0 automatic, 1 never split, >= 2 that many K pieces
+};
+
+// The TN path with explicit split-K scratch (16-bit inputs and output).
+int gemm_tn_with_scratch(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                         const void* B, int64_t ldb, void* C, int64_t ldc, void* stream,
+                         const ScratchOverride& ov);
+
+// tail_mode 0: a last wave of whole tiles that is at most half full runs as
+// half-width tiles in a second grid launched with programmatic dependent launch;
+// 1: whole tiles only; 2: as 0 but two plain launches.
+cudaError_t f32_launch(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                       const float* B, int64_t ldb, float* C, int64_t ldc, cudaStream_t stream,
+                       int tail_mode);
+
+// Copies rows of row_bytes bytes from any alignment into 16-byte-aligned rows
+// of pitch dp (a multiple of 16) so that TMA can address them.
+cudaError_t repack_rows_launch(const void* src, int64_t sp, void* dst, int64_t dp, int64_t rows,
+                               int64_t row_bytes, cudaStream_t stream);
+
+// Writes zeros into a rows x cols block with leading dimension ld (elements of
+// elem_bytes bytes); used for K == 0.
+cudaError_t zero_fill_launch(void* C, int64_t rows, int64_t cols, int64_t ld, int elem_bytes,
+                             cudaStream_t stream);
+
+cudaError_t watchdog_selftest_launch(uint64_t limit_ns, unsigned int* watchdog,
+                                     cudaStream_t stream);
+
+}  // namespace gb300

@@ -15,7 +15,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
-#include "common.h"
+#include "launch.h"
 #include "ptx.cuh"
 #include "tc_gemm.cuh"
 

@@ -20,7 +20,7 @@
 // threads on one device) race on the array.
 #include <mutex>
 
-#include "common.h"
+#include "launch.h"
 #include "gemm.h"
 
 namespace {

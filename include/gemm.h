@@ -174,6 +174,10 @@ int gemm_read_watchdog(int reset);
  *   "tail_k"      0 (default), or 2..8: with a workspace, cut the last partial wave's
  *                 tiles into that many K pieces instead of narrower tiles (slower
  *                 on the shapes measured: the fix-up is L2-latency-bound)
+ *   "f32_tail"    gemm_f32 only: 0 (default) runs the last partial wave of 128 x 128 tiles
+ *                 as 128 x 64 halves where that shortens it, in a second grid started
+ *                 early by programmatic dependent launch; 1 keeps whole tiles; 2 is 0
+ *                 with a plain second launch.  Results are bit-identical in every mode.
  *   "splits"      K pieces per tile: 0 auto (default, needs a workspace), 1 never
  *                 split, 2..64 split that many ways when the workspace suffices
  * Returns GEMM_OK or GEMM_ERR_INVALID_OPTION.

@@ -52,6 +52,39 @@ def test_unaligned_and_padded_ld():
     assert torch.all(torch.isnan(C[:M, N:])), "C padding was written"
 
 
+@pytest.mark.parametrize("shape", [(2304, 2300, 40), (2304, 2204, 19), (2048, 3580, 24),
+                                   (2560, 3000, 33), (1000, 130, 300), (2304, 2304, 48),
+                                   (2048, 3584, 16)])
+def test_half_width_tail(shape):
+    """On 152 SMs with two blocks each: 324 tiles run as 304 whole + 20 halved
+    (with N = 2204 the right halves of the last tile column hold no columns at
+    all); 448 and 480 tiles all whole (remainders 144 and 176); 16 tiles all
+    halved; the last two
+    shapes are multiples of the tile and of the K slice, so they take the
+    variant without bounds checks (whole and half tiles).  Every tail mode
+    ("f32_tail" 0 = halves behind a dependent launch, 1 = whole tiles, 2 = halves
+    in a plain second launch) must give bit-identical C, since each output is
+    the same chain of FMAs in k order; C's padding columns stay untouched."""
+    M, N, K = shape
+    ops = si.f32_operands(M, N, K, dist="uniform", seed=M + K)
+    outs = []
+    try:
+        for mode in (0, 1, 2):
+            assert capi.gemm_set_option("f32_tail", mode) == 0
+            outs.append(run_f32(ops, M, N, K, ldc=N + 7))
+    finally:
+        capi.gemm_set_option("f32_tail", 0)
+    C = outs[0]
+    exact = oracle.gemm_f32(M, N, K, ops["A"].numpy(), K, ops["B"].numpy(), N)
+    got = C[:M, :N].double().numpy()
+    a, b = ops["A"][:, :K].double().numpy(), ops["B"][:, :N].double().numpy()
+    assert np.all(np.abs(got - exact) <= tight_f32(a, b, K))
+    assert torch.all(torch.isnan(C[:M, N:])), "C padding was written"
+    for other in outs[1:]:
+        assert torch.equal(other[:M, :N], C[:M, :N])
+        assert torch.all(torch.isnan(other[:M, N:]))
+
+
 def test_identity_4096_exact():
     """B = I  =>  C = A exactly ("Optimizing GEMM in HIP": the identity test)."""
     n = 4096
