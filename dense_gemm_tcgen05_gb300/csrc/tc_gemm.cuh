@@ -467,11 +467,16 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                                         static_cast<uintptr_t>(i * pitch + kb_byte);
                     const uint32_t delta = static_cast<uint32_t>(a & 15u);
                     const uintptr_t al = a - delta + 16u * c;
+                    // Row bytes [0, v) are valid (v = 0 for a row outside the
+                    // matrix or the unit).  A 16-byte chunk is read only when it
+                    // starts inside them or, for lane 0 of a misaligned row,
+                    // covers their first byte; a chunk that starts inside valid
+                    // bytes never leaves their 16-byte granule, hence their page.
                     const int32_t v = i < rows_left ? win : 0;
                     const int32_t first16 = 16 * static_cast<int32_t>(c) - static_cast<int32_t>(delta);
                     lo[i] = make_uint4(0u, 0u, 0u, 0u);
                     hi[i] = make_uint4(0u, 0u, 0u, 0u);
-                    if (first16 < v) lo[i] = ldg_nc_v4(reinterpret_cast<const void*>(al));
+                    if (v > 0 && first16 < v) lo[i] = ldg_nc_v4(reinterpret_cast<const void*>(al));
                     if (delta != 0 && first16 + 16 < v)
                         hi[i] = ldg_nc_v4(reinterpret_cast<const void*>(al + 16u));
                 }
