@@ -84,7 +84,8 @@ def test_small_workspace_does_not_split_and_stays_correct():
         capi.gemm_set_workspace(None, 0)
 
 
-@pytest.mark.parametrize("shape", [(128, 8192, 8192), (64, 14336, 4096), (1024, 1024, 8192)])
+@pytest.mark.parametrize("shape", [(128, 8192, 8192), (64, 14336, 4096), (1024, 1024, 8192),
+                                   (16, 8192, 8192), (100, 8192, 2048)])
 def test_skinny_sampled(shape, workspace):
     M, N, K = shape
     ops = si.tn_operands("bf16", M, N, K, dist="normal", seed=3, sigma=0.05)
