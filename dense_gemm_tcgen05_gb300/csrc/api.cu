@@ -246,15 +246,25 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     const Producer prod = (ab_tma && g_opt_path.load() != 2) ? Producer::Tma : Producer::Loads;
     const int opt_pair = g_opt_pair.load();
     // cta_group::2 pairs measured faster on every shape with at least a wave
-    // of tiles; they need TMA.  Skinny products (M <= 128, fewer pair tiles of
-    // 256 rows of N than CTA pairs) run one CTA per 128 rows of N with 64-wide
-    // tiles along M instead: twice the tiles, and measured on GB300 5-7 %
-    // faster at N x K = 8192 x 8192 and 14336 x 4096, 31 % at 8192 x 2048.
+    // of tiles; they need TMA.  When the pair tiles (256 rows of N each) fill
+    // less than one wave but single-CTA tiles of 128 rows of N by `small_q`
+    // columns of M (64 for M <= 128, else 128) still fit in one, the smaller
+    // tiles run instead: up to four times the tiles in flight.  Measured on
+    // GB300 against pairs: BF16 M x N x K = 16..128 x 8192 x 8192 5-7 %
+    // faster, 128 x 8192 x 2048 31 %, 256 x 8192 x 8192 17 %, 1024 x 1024 x 8192
+    // 21 % (FP8 45 %), 1024 x 2048 x 4096 30 %; where the small tiles would need
+    // a second wave (512 x 8192 x 8192, 2048^3) pairs stay 10-26 % faster.
     bool pair = prod == Producer::Tma && opt_pair != 0;
-    bool skinny = false;
-    if (pair && opt_pair < 0 && M <= 128 && (N + 255) / 256 < dev->sms / 2) {
-        pair = false;
-        skinny = true;
+    int small_q = 0;
+    if (pair && opt_pair < 0) {
+        const int64_t pair_tiles = ((N + 255) / 256) * ((M + choose_tile_q(M, 256) - 1) /
+                                                        choose_tile_q(M, 256));
+        const int q = M <= 128 ? 64 : 128;
+        const int64_t small_tiles = ((N + 127) / 128) * ((M + q - 1) / q);
+        if (pair_tiles < dev->sms / 2 && small_tiles <= dev->sms) {
+            pair = false;
+            small_q = q;
+        }
     }
     const TcGeometry g = tc_geometry(in, pair);
     TcLaunch L;
@@ -267,7 +277,7 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     // P = B: N rows of K contiguous elements.  Q = A: M rows of K.  Out = C: N rows of M.
     const int opt_tq = g_opt_tile_q.load();
-    const int tile_q = opt_tq ? opt_tq : skinny ? 64 : choose_tile_q(M, g.max_tile_q);
+    const int tile_q = opt_tq ? opt_tq : small_q ? small_q : choose_tile_q(M, g.max_tile_q);
     const int load_q = tile_q / g.cluster;
     CUresult r = CUDA_SUCCESS;
     if (prod == Producer::Tma) {

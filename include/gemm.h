@@ -154,9 +154,9 @@ int gemm_read_watchdog(int reset);
 /*
  * gemm_set_option -- process-wide tuning and test switches.  Not meant to be
  * changed while calls are in flight on other host threads.
- *   "pair"        -1 auto (default: CTA pairs, except one CTA per tile with 64-wide
- *                 tiles along M for M <= 128 when the pair tiles fill less than one
- *                 wave), 0 one CTA per tile, 1 a cta_group::2 pair
+ *   "pair"        -1 auto (default: CTA pairs, except when the pair tiles fill less
+ *                 than one wave and single-CTA tiles 64 (M <= 128) or 128 wide along
+ *                 M fit in one: then those), 0 one CTA per tile, 1 a cta_group::2 pair
  *   "group"       tile-rasteriser group size in tile rows, 1..64 (default 8)
  *   "path"        0 auto (default), 1 force the CUDA-core kernel, 2 force the
  *                 tensor-core kernel's load-based producer (as for unaligned rows)

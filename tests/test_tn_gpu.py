@@ -356,3 +356,21 @@ def test_tail_split_fp32_out():
     finally:
         for k, v in {"tail": 0, "max_ctas": 0}.items():
             capi.gemm_set_option(k, v)
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_subwave_small_tiles(kind):
+    """Pair tiles fill less than a wave (8 x 4 = 32) while single-CTA tiles of
+    128 x 128 fit in one (16 x 8 = 128): the automatic choice runs the small
+    tiles; ragged on both edges."""
+    M, N, K = 1000, 2000, 500
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=7, sigma=0.5)
+    C = run_tn(kind, ops, M, N, K)
+    check_full(kind, ops, M, N, K, C)
+
+
+@pytest.mark.parametrize("kind,shape", [("bf16", (256, 8192, 8192)), ("e4m3", (1024, 1024, 8192))])
+def test_subwave_small_tiles_sampled(kind, shape):
+    M, N, K = shape
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=8, sigma=0.05)
+    C = run_tn(kind, ops, M, N, K)
+    check_sampled(kind, ops, M, N, K, C, seed=8)
