@@ -216,23 +216,38 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     int64_t ws_used = 0;  // bytes at the start of the scratch taken by repacked operands
 
     // Operands whose rows TMA cannot address are copied once into the scratch
-    // with 16-byte-aligned rows (one pass at memory speed), after which the TMA
-    // path runs at full rate; without room for that, the load-based producer
-    // reads them in place.
-    if ((!a_tma || !b_tma) && g_opt_path.load() == 0 && g_opt_repack.load() == 0 && ws_base) {
+    // with 128-byte-aligned rows (one pass at memory speed), after which the
+    // TMA path runs at full rate; without room for that, the load-based
+    // producer reads them in place.  Rows TMA can address but that do not start
+    // on 128-byte boundaries make every 128-byte row segment of a box straddle
+    // two cache lines, which measured on GB300 costs 20-45 % (BF16 4096^3 with
+    // ld = 4104: 107 against 80 us; FP16 8192^3 with ld = 8200: 786 against
+    // 575-646 us).  They are copied too when the product is compute-heavy
+    // enough for the copy (2 (M + N) K element bytes at ~5.8 TB/s) to cost
+    // clearly less: MN / (M + N) >= 1100 x element size.  Measured with the
+    // copy: 6144^3 383 -> 319-358 us, 8192^3 786 -> 662-703 us, 16384^3 6652 ->
+    // 5763-5804 us; at 4096^3 the copy (22 us) and the penalty (27 us) cancel.
+    auto al128 = [&](const void* p, int64_t ld) {
+        return aligned(p, 128) && (ld * es) % 128 == 0;
+    };
+    const bool heavy = static_cast<double>(M) * static_cast<double>(N) /
+                           static_cast<double>(M + N) >= 1100.0 * es;
+    const bool copy_a = !a_tma || (heavy && !al128(A, lda));
+    const bool copy_b = !b_tma || (heavy && !al128(B, ldb));
+    if ((copy_a || copy_b) && g_opt_path.load() == 0 && g_opt_repack.load() == 0 && ws_base) {
         const int64_t rb = K * es;                       // row bytes
-        const int64_t dp = (rb + 15) / 16 * 16;          // aligned pitch
-        const int64_t need_a = a_tma ? 0 : (M * dp + 255) / 256 * 256;
-        const int64_t need_b = b_tma ? 0 : (N * dp + 255) / 256 * 256;
+        const int64_t dp = (rb + 127) / 128 * 128;       // aligned pitch
+        const int64_t need_a = copy_a ? (M * dp + 255) / 256 * 256 : 0;
+        const int64_t need_b = copy_b ? (N * dp + 255) / 256 * 256 : 0;
         if (need_a + need_b <= ws_total) {
-            if (!a_tma) {
+            if (copy_a) {
                 e = repack_rows_launch(A, lda * es, ws_base, dp, M, rb, stream);
                 if (e != cudaSuccess) return fail_cuda(e);
                 A = ws_base;
                 lda = dp / es;
                 a_tma = true;
             }
-            if (!b_tma) {
+            if (copy_b) {
                 e = repack_rows_launch(B, ldb * es, ws_base + need_a, dp, N, rb, stream);
                 if (e != cudaSuccess) return fail_cuda(e);
                 B = ws_base + need_a;
@@ -637,7 +652,7 @@ int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     // elements), then 16 K pieces of every tile of the narrowest layout
     // (128 rows of N by 64 of M per tile), plus the counters.
     if (M <= 0 || N <= 0 || K <= 0) return 0;
-    const int64_t dp = (K * 2 + 15) / 16 * 16;
+    const int64_t dp = (K * 2 + 127) / 128 * 128;
     const int64_t repack = (M * dp + 255) / 256 * 256 + (N * dp + 255) / 256 * 256;
     const int64_t tiles = ((N + 127) / 128) * ((M + 63) / 64);
     return repack + ((tiles * 4 * 4 + 255) / 256) * 256 + tiles * 16 * 4 * 32 * 256 * 4;

@@ -172,7 +172,8 @@ int gemm_read_watchdog(int reset);
  *                 (measured on GB300: 1 raises DRAM reads by half and loses 3-5 %,
  *                 2 changes nothing measurable)
  *   "repack"      0 (default): with a workspace, operands whose rows are not 16-byte
- *                 aligned are first copied into it with aligned rows; 1 never
+ *                 aligned (or, for compute-heavy shapes, not 128-byte aligned) are
+ *                 first copied into it with 128-byte-aligned rows; 1 never
  *   "tail_k"      0 (default), or 2..8: with a workspace, cut the last partial wave's
  *                 tiles into that many K pieces instead of narrower tiles (slower
  *                 on the shapes measured: the fix-up is L2-latency-bound)
@@ -190,8 +191,11 @@ int gemm_set_option(const char* name, int64_t value);
  * gemm_set_workspace -- registers caller-owned device scratch for the current
  * device (ptr 256-byte aligned, `bytes` long; NULL, 0 unregisters).  With a
  * workspace registered, a TN call whose A or B rows are not 16-byte aligned
- * first copies that operand into the workspace with aligned rows (when it
- * fits: rows * K * element size, rounded up), so that the TMA path can run;
+ * first copies that operand into the workspace with 128-byte-aligned rows
+ * (when it fits: rows * K * element size, rounded up), so that the TMA path
+ * can run; rows that are 16-byte but not 128-byte aligned are copied too when
+ * MN / (M + N) >= 1100 x element size, where the copy costs less than the
+ * slower loads would;
  * and TN calls whose output tiles cannot fill the GPU in one wave split K: each K piece writes its FP32 partial tile to the workspace and
  * the last piece to finish a 32-row slice sums the pieces in piece order (so
  * the result does not depend on timing) and stores C.  Calls that split K on

@@ -1,6 +1,6 @@
 """GPU parity of the repack path: with a workspace registered, operands whose
-rows are not 16-byte aligned are copied into it with aligned rows and the TMA
-path runs.  Checked against the CPU oracle through the C ABI; inputs must be
+rows are not 16-byte aligned (or, for compute-heavy shapes, not 128-byte
+aligned) are copied into it with aligned rows and the TMA path runs.  Checked against the CPU oracle through the C ABI; inputs must be
 left unchanged and C's padding untouched."""
 import numpy as np
 import pytest
@@ -81,3 +81,20 @@ def test_bf16_tight_ld_configs_with_workspace(shape, workspace):
     ops = si.tn_operands("bf16", M, N, K, dist="normal", seed=3, sigma=0.05)
     C = run_tn("bf16", ops, M, N, K)
     check_sampled("bf16", ops, M, N, K, C, seed=3)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_128_byte_misaligned_rows_copied(kind, workspace):
+    """Rows 16-byte but not 128-byte aligned (ld = 208 elements) on a shape
+    heavy enough for the copy (MN / (M + N) = 2560 >= 1100 x element size): the
+    copied path must match the oracle and, bit for bit, the same call without
+    the copy (same arithmetic)."""
+    M = N = 5120
+    K = 200
+    ld = 208
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=11, sigma=0.5, lda=ld, ldb=ld)
+    C = run_tn(kind, ops, M, N, K)
+    check_full(kind, ops, M, N, K, C)
+    assert capi.gemm_set_option("repack", 1) == 0
+    C2 = run_tn(kind, ops, M, N, K)
+    assert torch.equal(C.view(torch.int16), C2.view(torch.int16))
