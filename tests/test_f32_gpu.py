@@ -85,6 +85,16 @@ def test_half_width_tail(shape):
         assert torch.all(torch.isnan(other[:M, N:]))
 
 
+def test_pm1_long_k_exact():
+    """FP32 with +-1 entries and K = 65536: every partial sum is an integer below
+    2^24, so each FMA chain is exact and C equals the oracle exactly."""
+    M, N, K = 130, 140, 65536
+    ops = si.f32_operands(M, N, K, dist="pm1", seed=5)
+    C = run_f32(ops, M, N, K)[:M, :N].double().numpy()
+    exact = oracle.gemm_f32(M, N, K, ops["A"].numpy(), K, ops["B"].numpy(), N)
+    assert np.array_equal(C, exact)
+
+
 def test_identity_4096_exact():
     """B = I  =>  C = A exactly ("Optimizing GEMM in HIP": the identity test)."""
     n = 4096

@@ -56,6 +56,21 @@ def test_pm1_bitexact(kind, shape, pair_mode):
 
 
 @pytest.mark.parametrize("kind", KINDS)
+def test_pm1_long_k_bitexact(kind, pair_mode):
+    """K = 65536 (1024 K stages of 64, or 512 of 128 for FP8) with +-1 entries:
+    every partial sum is an integer of magnitude <= 65536 < 2^24, exact in the
+    FP32 accumulator, so the rounded outputs must match the oracle bit for bit
+    (with FP16 output, |sums| above 2048 round, identically on both sides).
+    A K this long also runs the ring's slot/phase counters through many
+    wrap-arounds."""
+    M, N, K = 200, 136, 65536
+    ops = si.tn_operands(kind, M, N, K, dist="pm1", seed=13)
+    C = run_tn(kind, ops, M, N, K)
+    exact = oracle.gemm_tn(kind, M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+    assert_codes_equal(out_codes(C, M, N), exact_codes(kind, exact))
+
+
+@pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("n", [64, 384, 640])
 def test_identity_bitexact(kind, n, pair_mode):
     """B = I  =>  C = A exactly (A's values are exact in the output type)."""
