@@ -74,6 +74,7 @@ std::atomic<int> g_opt_tail{0};
 std::atomic<int> g_opt_tail_k{0};
 std::atomic<int> g_opt_repack{0};
 std::atomic<int> g_opt_f32_tail{0};
+std::atomic<int> g_opt_cluster{0};
 std::atomic<int> g_opt_l2hints{0};
 std::atomic<int64_t> g_opt_timeout_ns{2000000000LL};
 
@@ -145,6 +146,7 @@ int choose_tile_q(int64_t M, int max_tile_q) {
 }
 
 constexpr int64_t kMaxDim = 0x7fffffffLL;
+constexpr int kMcStageRegion = 200 * 1024;  // ring of the multicast kernel (tc_gemm_mc.cuh)
 
 // 2D tensor map over a matrix with `outer` rows of `inner` contiguous elements
 // and a row pitch of `pitch_bytes`, copied in boxes of box_inner x box_outer
@@ -158,6 +160,20 @@ CUresult encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, in
     return g_encode(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// Resident clusters of the multicast kernel per device, input kind and output
+// type, queried once (0 = not yet known).
+std::atomic<int> g_mc_clusters[kMaxDevices][4];
+
+cudaError_t mc_max_clusters(InKind in, bool out_f32, const DeviceInfo* dev, int* n) {
+    const int di = static_cast<int>(dev - g_devices);
+    const int vi = out_f32 ? 3 : static_cast<int>(in);
+    if ((*n = g_mc_clusters[di][vi].load()) > 0) return cudaSuccess;
+    cudaError_t e = tc_mc_max_clusters(in, out_f32, n);
+    if (e != cudaSuccess) return e;
+    g_mc_clusters[di][vi].store(*n);
+    return cudaSuccess;
 }
 
 // `ov`, when given, replaces the registered workspace and the "splits" option:
@@ -479,15 +495,48 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
             L.grid = static_cast<int>((units < slots ? units : slots) * g.cluster);
         }
     }
+    // Clusters of two pairs sharing P tiles through TMA multicast
+    // (tc_gemm_mc.cuh): only for pair tiles without split-K, tail splitting,
+    // FP16 accumulation or row-wise stores.  Option "cluster" = 4 forces it
+    // where it applies, 2 never; 0 (default) chooses it by the rule below.
+    const int opt_cl = g_opt_cluster.load();
+    bool mc = false;
+    if (pair && prod == Producer::Tma && c_tma && !acc16 && L.prm.splits == 1 && opt_cl != 2 &&
+        opt_cl == 4) {
+        int max_cl = 0;
+        e = mc_max_clusters(in, out_f32, dev, &max_cl);
+        if (e != cudaSuccess) return fail_cuda(e);
+        if (max_cl > 0) {
+            mc = true;
+            {
+                // the multicast kernel's ring: 200 KB of stages of this width
+                const int sb = ((g.load_p + load_q) * 128 + 1023) / 1024 * 1024;
+                int st_count = kMcStageRegion / sb;
+                if (st_count > g.max_stages) st_count = g.max_stages;
+                L.prm.stages = st_count;
+                L.prm.stage_bytes = static_cast<uint32_t>(sb);
+            }
+            r = encode_2d(&L.map_p, in_dt, B, K, N, ldb * es, g.stage_k, g.load_p / 2);
+            if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
+            L.prm.tail_f = 1;
+            L.prm.tail_ksplit = 0;
+            L.prm.full_units = tiles;
+            const int64_t units = tiles_p * ((tiles_q + 1) / 2);
+            int64_t clusters = units < max_cl ? units : max_cl;
+            if (cap > 0 && cap / 4 < clusters) clusters = cap / 4 > 0 ? cap / 4 : 1;
+            L.grid = static_cast<int>(clusters * 4);
+        }
+    }
     if (std::getenv("GEMM_DEBUG"))
         std::fprintf(stderr,
                      "[gemm] tn in=%d M=%lld N=%lld K=%lld pair=%d producer=%d direct_store=%d "
-                     "splits=%d tile_q=%d tail=%d ktail=%d stages=%d tiles=%lldx%lld grid=%d\n",
+                     "splits=%d tile_q=%d tail=%d ktail=%d stages=%d tiles=%lldx%lld grid=%d "
+                     "multicast=%d\n",
                      int(in), (long long)M, (long long)N, (long long)K, int(pair), int(prod),
                      L.prm.direct_store, L.prm.splits, L.prm.tile_q, L.prm.tail_f,
                      L.prm.tail_ksplit, L.prm.stages,
-                     (long long)tiles_q, (long long)tiles_p, L.grid);
-    e = tc_launch(in, pair, prod, out_f32, L);
+                     (long long)tiles_q, (long long)tiles_p, L.grid, int(mc));
+    e = mc ? tc_mc_launch(in, out_f32, L) : tc_launch(in, pair, prod, out_f32, L);
     return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
 }
 
@@ -619,6 +668,9 @@ int gemm_set_option(const char* name, int64_t value) {
     } else if (!std::strcmp(name, "l2_hints")) {
         if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
         g_opt_l2hints.store(static_cast<int>(value));
+    } else if (!std::strcmp(name, "cluster")) {
+        if (!(value == 0 || value == 2 || value == 4)) return GEMM_ERR_INVALID_OPTION;
+        g_opt_cluster.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "f32_tail")) {
         if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
         g_opt_f32_tail.store(static_cast<int>(value));

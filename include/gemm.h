@@ -177,6 +177,9 @@ int gemm_read_watchdog(int reset);
  *   "tail_k"      0 (default), or 2..8: with a workspace, cut the last partial wave's
  *                 tiles into that many K pieces instead of narrower tiles (slower
  *                 on the shapes measured: the fix-up is L2-latency-bound)
+ *   "cluster"     0 (default) or 2: CTA pairs as chosen above; 4: clusters of two pairs
+ *                 that share B tiles through TMA multicast (TN path with TMA-aligned
+ *                 operands and C, no split-K; slower or level on the shapes measured)
  *   "f32_tail"    gemm_f32 only: 0 (default) runs the last partial wave of 128 x 128 tiles
  *                 as 128 x 64 halves where that shortens it, in a second grid started
  *                 early by programmatic dependent launch; 1 keeps whole tiles; 2 is 0
