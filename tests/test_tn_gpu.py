@@ -389,3 +389,25 @@ def test_subwave_small_tiles_sampled(kind, shape):
     ops = si.tn_operands(kind, M, N, K, dist="normal", seed=8, sigma=0.05)
     C = run_tn(kind, ops, M, N, K)
     check_sampled(kind, ops, M, N, K, C, seed=8)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("shape", [(1 << 20, 128, 64), (128, 1 << 20, 64)])
+def test_million_row_extents_sampled(kind, shape):
+    """One operand a million rows long: 4096 tiles along one dimension, TMA row
+    coordinates up to 2^20, C of 2^27 elements."""
+    M, N, K = shape
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=9, sigma=0.5)
+    C = run_tn(kind, ops, M, N, K)
+    check_sampled(kind, ops, M, N, K, C, seed=9)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("shape", [(1, 1, 8192), (1, 300, 1), (300, 1, 1), (257, 129, 1)])
+def test_degenerate_shapes_pm1_bitexact(kind, shape):
+    """M = N = 1 with a long K, and K = 1 (a single product per output)."""
+    M, N, K = shape
+    ops = si.tn_operands(kind, M, N, K, dist="pm1", seed=sum(shape))
+    C = run_tn(kind, ops, M, N, K)
+    exact = oracle.gemm_tn(kind, M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+    assert_codes_equal(out_codes(C, M, N), exact_codes(kind, exact))
