@@ -232,8 +232,11 @@ def e2e_loop(kind, M, N, K, ops, steps, warmup, stream, stream_h):
     i + 1 and i - 1 overlap the GEMM of step i; events order each buffer's reuse.
     The timed region runs from before the first step's input copy to after the
     last step's output copy.  Returns (pipelined ms per step, serial ms per step,
-    host-to-device bytes per step, device-to-host bytes per step); the serial
-    figure runs copy, GEMM, copy back to back on one stream, for context."""
+    host-to-device bytes per step, device-to-host bytes per step, copies-only ms
+    per step); the serial figure runs copy, GEMM, copy back to back on one
+    stream, for context.  The copies-only figure runs the same pipelined steps
+    without the GEMM: the host link's own limit on this loop, against which the
+    end-to-end rate is read."""
     import torch
 
     ha = ops["A"].pin_memory()
@@ -248,7 +251,7 @@ def e2e_loop(kind, M, N, K, ops, steps, warmup, stream, stream_h):
     ev = lambda: [torch.cuda.Event() for _ in range(2)]  # noqa: E731
     in_done, gemm_done, out_done = ev(), ev(), ev()
 
-    def step(i):
+    def step(i, gemm=True):
         j = i % 2
         if i >= 2:
             s_in.wait_event(gemm_done[j])      # the GEMM of step i - 2 has read slot j
@@ -259,7 +262,8 @@ def e2e_loop(kind, M, N, K, ops, steps, warmup, stream, stream_h):
         stream.wait_event(in_done[j])
         if i >= 2:
             stream.wait_event(out_done[j])     # C of step i - 2 has left slot j
-        call(da[j], db[j], dc[j])
+        if gemm:
+            call(da[j], db[j], dc[j])
         gemm_done[j].record(stream)
         s_out.wait_event(gemm_done[j])
         with torch.cuda.stream(s_out):
@@ -285,6 +289,13 @@ def e2e_loop(kind, M, N, K, ops, steps, warmup, stream, stream_h):
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
 
+    t0.record(s_in)
+    for i in range(steps):
+        step(i, gemm=False)
+    t1.record(s_out)
+    torch.cuda.synchronize()
+    copy_ms = t0.elapsed_time(t1) / steps
+
     for _ in range(warmup):
         serial_step()
     torch.cuda.synchronize()
@@ -296,7 +307,7 @@ def e2e_loop(kind, M, N, K, ops, steps, warmup, stream, stream_h):
     serial_ms = t0.elapsed_time(t1) / steps
     h2d = ha.numel() * ha.element_size() + hb.numel() * hb.element_size()
     d2h = hc.numel() * hc.element_size()
-    return ms, serial_ms, h2d, d2h
+    return ms, serial_ms, h2d, d2h, copy_ms
 
 
 def f32_bench(n, steps, warmup, stream, stream_h):
@@ -477,7 +488,7 @@ def run_ours(args):
             per.update(sweep(stream, stream_h, burst))
 
         e2e_steps = max(3, min(args.steps, 20))
-        e_ms, serial_ms, h2d, d2h = e2e_loop("f16", M, N, K, ops, e2e_steps, 2, stream,
+        e_ms, serial_ms, h2d, d2h, copy_ms = e2e_loop("f16", M, N, K, ops, e2e_steps, 2, stream,
                                              stream_h)
         traffic = load_traffic()
         result = {
@@ -511,7 +522,12 @@ def run_ours(args):
                     "how": "pinned host A, B -> device, gemm_f16_tn, C -> pinned host, every "
                            "step; copies of neighbouring steps overlap the GEMM (two buffer "
                            "sets, three streams)",
-                    "serial_value": round(flops / (serial_ms * 1e-3) / 1e12, 2)},
+                    "serial_value": round(flops / (serial_ms * 1e-3) / 1e12, 2),
+                    # the same pipelined loop with the GEMM left out: the host
+                    # link's ceiling for this metric, and its rate in GB/s
+                    "copies_only_value": round(flops / (copy_ms * 1e-3) / 1e12, 2),
+                    "copies_only_gbs": round((h2d + d2h) / (copy_ms * 1e-3) / 1e9, 1),
+                    "frac_of_copies_only": round(copy_ms / e_ms, 4)},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "per_dtype": per,

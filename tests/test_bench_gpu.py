@@ -33,4 +33,7 @@ def test_bench_line_contract():
     assert e2e["value"] > 0 and e2e["unit"] == "TFLOP/s"
     assert e2e["h2d_bytes_per_step"] == 2 * 8192 * 8192 * 2
     assert e2e["d2h_bytes_per_step"] == 8192 * 8192 * 2
+    # the copies alone bound the end-to-end rate (timing noise aside)
+    assert e2e["copies_only_value"] > 0 and e2e["copies_only_gbs"] > 0
+    assert e2e["value"] <= 1.05 * e2e["copies_only_value"]
     assert "sm_mhz" in line["clocks"] and "reasons" in line["clocks"]
