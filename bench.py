@@ -330,6 +330,37 @@ def f32_bench(n, steps, warmup, stream, stream_h):
     return launch
 
 
+def f32_bf16x6_bench(n, steps, warmup, stream, stream_h):
+    """gemm_f32_bf16x6 on the FP32 leg's operands (U[-1,1], seed 1), with the
+    workspace it needs registered; returns the mean per-call ms (two split
+    launches and the GEMM)."""
+    import torch
+
+    import synthetic_inputs as si
+    from dense_gemm_tcgen05_gb300 import capi
+
+    ops = si.f32_operands(n, n, n, dist="uniform", seed=1)
+    sets = [(ops["A"].cuda(), ops["B"].cuda(), torch.empty((n, n), device="cuda"))
+            for _ in range(SETS)]
+    need = capi.gemm_f32_bf16x6_workspace_bytes(n, n, n)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    assert capi.gemm_set_workspace(ws.data_ptr(), need) == 0
+
+    def call(a, b, c):
+        st = capi.gemm_f32_bf16x6(n, n, n, a.data_ptr(), n, b.data_ptr(), n, c.data_ptr(), n,
+                                  stream_h)
+        if st != 0:
+            raise RuntimeError(capi.status_text(st))
+
+    try:
+        with torch.cuda.stream(stream):
+            total, launch = timed_loop(call, sets, steps, warmup, stream)
+    finally:
+        torch.cuda.synchronize()
+        capi.gemm_set_workspace(None, 0)
+    return launch
+
+
 def cublas_context(M, N, K, dtype, steps, stream):
     """torch.matmul (cuBLAS) on the same problem, for context only.  FP32 runs
     with TF32 off, i.e. on the CUDA cores like gemm_f32."""
@@ -481,6 +512,14 @@ def run_ours(args):
         fpk = fp32_alu_peak_tflops(sm_count(), clk)
         per["f32_simt_4096"] = {"tflops": round(tf, 2), "peak": round(fpk, 1),
                                 "frac": round(tf / fpk, 4), "bound": "alu"}
+        # The same FP32 product on the tensor cores (exact BF16 splits, six
+        # piece products): effective FP32 rate, and the BF16 tensor rate the
+        # GEMM runs at (6 x 2 n^3 over the whole call, splits included).
+        lx = f32_bf16x6_bench(4096, sub_steps, 3, stream, stream_h)
+        tfx = 2.0 * 4096 ** 3 / (lx * 1e-3) / 1e12
+        per["f32_bf16x6_4096"] = {"tflops": round(tfx, 1), "tensor_tflops": round(6 * tfx, 1),
+                                  "peak": round(burst, 1), "frac": round(6 * tfx / burst, 4),
+                                  "bound": "tensor", "over_simt": round(tfx / tf, 2)}
         per["cublas_context_f32_4096"] = round(cublas_context(4096, 4096, 4096, torch.float32,
                                                               20, stream), 2)
         per["cublas_context_f16_8192"] = round(cublas_context(M, N, K, torch.float16, 20, stream), 1)

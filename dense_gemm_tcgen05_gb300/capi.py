@@ -27,6 +27,7 @@ GEMM_ERR_LAUNCH = 6
 GEMM_ERR_TIMEOUT = 7
 GEMM_ERR_INVALID_OPTION = 8
 GEMM_ERR_SCRATCH = 9
+GEMM_ERR_WORKSPACE = 10
 
 _lock = threading.Lock()
 _lib = None
@@ -47,6 +48,8 @@ _SIGNATURES = {
     "gemm_set_workspace": ([_vp, _i64], _int),
     "gemm_bf16_tn_noalloc": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i64, _vp], _int),
     "gemm_workspace_bytes": ([_i64, _i64, _i64], _i64),
+    "gemm_f32_bf16x6": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp], _int),
+    "gemm_f32_bf16x6_workspace_bytes": ([_i64, _i64, _i64], _i64),
 }
 
 
@@ -93,6 +96,14 @@ def _p(x) -> int | None:
 
 def gemm_f32(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
     return lib().gemm_f32(M, N, K, _p(A), lda, _p(B), ldb, _p(C), ldc, _p(stream))
+
+
+def gemm_f32_bf16x6(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
+    return lib().gemm_f32_bf16x6(M, N, K, _p(A), lda, _p(B), ldb, _p(C), ldc, _p(stream))
+
+
+def gemm_f32_bf16x6_workspace_bytes(M: int, N: int, K: int) -> int:
+    return lib().gemm_f32_bf16x6_workspace_bytes(M, N, K)
 
 
 def gemm_f16_tn(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:

@@ -20,6 +20,7 @@
 namespace gb300 {
 cudaError_t tc_launch_f16(bool pair, Producer prod, const TcLaunch& L);
 cudaError_t tc_launch_bf16(bool pair, Producer prod, const TcLaunch& L);
+cudaError_t tc_launch_bf16_f32(bool pair, Producer prod, const TcLaunch& L);
 cudaError_t tc_launch_fp8(bool pair, Producer prod, bool out_f32, const TcLaunch& L);
 TcGeometry tc_geometry_f16(bool pair);
 TcGeometry tc_geometry_bf16(bool pair);
@@ -36,7 +37,8 @@ TcGeometry tc_geometry(InKind in, bool pair) {
 cudaError_t tc_launch(InKind in, bool pair, Producer prod, bool out_f32, const TcLaunch& L) {
     switch (in) {
         case InKind::F16: return tc_launch_f16(pair, prod, L);
-        case InKind::BF16: return tc_launch_bf16(pair, prod, L);
+        case InKind::BF16:
+            return out_f32 ? tc_launch_bf16_f32(pair, prod, L) : tc_launch_bf16(pair, prod, L);
         default: return tc_launch_fp8(pair, prod, out_f32, L);
     }
 }
@@ -394,7 +396,8 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
             const int64_t part_bytes = tiles * pieces * slices * 32 * 256 * 4;
             void* ws = ws_base ? ws_base + ws_used : nullptr;
             const int64_t ws_bytes = ws_total - ws_used;
-            if (ov && pieces >= 2 && cnt_bytes + part_bytes > ws_bytes) return GEMM_ERR_SCRATCH;
+            if (ov && ov->strict && pieces >= 2 && cnt_bytes + part_bytes > ws_bytes)
+                return GEMM_ERR_SCRATCH;
             if (pieces >= 2 && ws && cnt_bytes + part_bytes <= ws_bytes) {
                 L.prm.splits = static_cast<int32_t>(pieces);
                 L.prm.kb_per_split = static_cast<int32_t>(kb_per);
@@ -502,7 +505,7 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     const int opt_cl = g_opt_cluster.load();
     bool mc = false;
     if (pair && prod == Producer::Tma && c_tma && !acc16 && L.prm.splits == 1 && opt_cl != 2 &&
-        opt_cl == 4) {
+        opt_cl == 4 && (in == InKind::E4M3 || !out_f32)) {
         int max_cl = 0;
         e = mc_max_clusters(in, out_f32, dev, &max_cl);
         if (e != cudaSuccess) return fail_cuda(e);
@@ -601,6 +604,60 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
     return gemm_tn(InKind::E4M3, true, M, N, K, A, lda, B, ldb, scale, C, ldc, stream);
 }
 
+// The tensor-core FP32 path: three-way BF16 splits of A and B (split_f32.cu)
+// in the caller's workspace, then one BF16 TN GEMM with FP32 output over the
+// six K-segments.  Row-major C = A B is the TN product with the roles of the
+// operands swapped: TN "M" = N with P rows from the split of B, TN "N" = M
+// with Q rows from the split of A, and C[m * ldc + n] its column-major output.
+int64_t gemm_f32_bf16x6_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
+    const int64_t row = 6 * ((K + 63) / 64 * 64) * 2;  // bytes of one split row
+    return (M * row + 255) / 256 * 256 + (N * row + 255) / 256 * 256;
+}
+
+int gemm_f32_bf16x6(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
+                    int64_t ldb, float* C, int64_t ldc, void* stream_v) {
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return GEMM_ERR_INVALID_DIM;
+    const int64_t kp = (K + 63) / 64 * 64;
+    if (6 * kp > kMaxDim) return GEMM_ERR_INVALID_DIM;
+    const int64_t nmin = N > 1 ? N : 1;
+    if (lda < (K > 1 ? K : 1) || ldb < nmin || ldc < nmin) return GEMM_ERR_INVALID_LD;
+    if ((M > 0 && K > 0 && !A) || (N > 0 && K > 0 && !B) || (M > 0 && N > 0 && !C))
+        return GEMM_ERR_NULL_PTR;
+    if (!aligned(A, 4) || !aligned(B, 4) || !aligned(C, 4)) return GEMM_ERR_MISALIGNED;
+    const DeviceInfo* dev = nullptr;
+    int st = current_device(&dev);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    cudaError_t e;
+    if (K == 0) {
+        e = zero_fill_launch(C, M, N, ldc, 4, stream);
+        return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
+    }
+    char* ws = nullptr;
+    int64_t ws_bytes = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        ws = static_cast<char*>(dev->workspace);
+        ws_bytes = dev->workspace_bytes;
+    }
+    const int64_t need = gemm_f32_bf16x6_workspace_bytes(M, N, K);
+    if (!ws || ws_bytes < need) return GEMM_ERR_WORKSPACE;
+    const int64_t a_bytes = (M * 6 * kp * 2 + 255) / 256 * 256;
+    char* sa = ws;             // M rows of 6 kp BF16: the split of A
+    char* sb = ws + a_bytes;   // N rows of 6 kp BF16: the split of B, transposed
+    e = f32_split_rows_launch(A, lda, M, K, kp, sa, dev->sms, stream);
+    if (e == cudaSuccess) e = f32_split_cols_launch(B, ldb, K, N, kp, sb, dev->sms, stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    // What is left of the workspace serves split-K where it fits; otherwise
+    // the GEMM runs unsplit.
+    const ScratchOverride ov{ws + need, ws_bytes - need, 0, 0};
+    return gemm_tn(InKind::BF16, true, N, M, 6 * kp, sb, 6 * kp, sa, 6 * kp, 1.0f, C, ldc,
+                   stream, &ov);
+}
+
 const char* gemm_status_string(int status) {
     switch (status) {
         case GEMM_OK: return "ok";
@@ -617,6 +674,9 @@ const char* gemm_status_string(int status) {
         case GEMM_ERR_INVALID_OPTION: return "unknown option or value out of range";
         case GEMM_ERR_SCRATCH:
             return "the call needs more split-K scratch than the library's static array holds";
+        case GEMM_ERR_WORKSPACE:
+            return "the call needs a registered workspace of at least its "
+                   "gemm_f32_bf16x6_workspace_bytes";
         default: return "unknown status";
     }
 }

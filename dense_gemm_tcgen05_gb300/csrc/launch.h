@@ -24,12 +24,23 @@ struct ScratchOverride {
     void* ptr;       // device address, 256-byte aligned
     int64_t bytes;   // usable bytes at ptr
     int splits;      // 0 automatic, 1 never split, >= 2 that many K pieces
+    int strict = 1;  // 1: a chosen split that does not fit fails with GEMM_ERR_SCRATCH;
+                     // 0: the call runs unsplit instead
 };
 
 // The TN path with explicit split-K scratch (16-bit inputs and output).
 int gemm_tn_with_scratch(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                          const void* B, int64_t ldb, void* C, int64_t ldc, void* stream,
                          const ScratchOverride& ov);
+
+// Operand preparation of the tensor-core FP32 path (split_f32.cu): three-way
+// BF16 splits of FP32 values in six K-segments of Kp columns (Kp a multiple of
+// 64), rows of 6 Kp BF16 values at `out` (256-byte aligned).  Rows: X is
+// rows x K row-major; cols: X is K x N row-major and comes out transposed.
+cudaError_t f32_split_rows_launch(const float* X, int64_t ldx, int64_t rows, int64_t K,
+                                  int64_t Kp, void* out, int sms, cudaStream_t stream);
+cudaError_t f32_split_cols_launch(const float* X, int64_t ldx, int64_t K, int64_t N, int64_t Kp,
+                                  void* out, int sms, cudaStream_t stream);
 
 // tail_mode 0: a last wave of whole tiles that is at most half full runs as
 // half-width tiles in a second grid launched with programmatic dependent launch;

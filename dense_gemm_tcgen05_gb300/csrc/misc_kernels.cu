@@ -174,9 +174,14 @@ cudaError_t tn_fallback_launch(InKind in, bool out_f32, int64_t M, int64_t N, in
                 tiles_m, tiles_n);
             break;
         case InKind::BF16:
-            tn_fallback_kernel<InKind::BF16, __nv_bfloat16><<<grid, kFbThreads, 0, stream>>>(
-                int(M), int(N), int(K), a, lda, b, ldb, scale, static_cast<__nv_bfloat16*>(C),
-                ldc, tiles_m, tiles_n);
+            if (out_f32)
+                tn_fallback_kernel<InKind::BF16, float><<<grid, kFbThreads, 0, stream>>>(
+                    int(M), int(N), int(K), a, lda, b, ldb, scale, static_cast<float*>(C), ldc,
+                    tiles_m, tiles_n);
+            else
+                tn_fallback_kernel<InKind::BF16, __nv_bfloat16><<<grid, kFbThreads, 0, stream>>>(
+                    int(M), int(N), int(K), a, lda, b, ldb, scale,
+                    static_cast<__nv_bfloat16*>(C), ldc, tiles_m, tiles_n);
             break;
         case InKind::E4M3:
             if (out_f32)

@@ -47,6 +47,7 @@ extern "C" {
 #define GEMM_ERR_TIMEOUT 7            /* a device-side wait ran out (gemm_read_watchdog) */
 #define GEMM_ERR_INVALID_OPTION 8     /* unknown option name or value (gemm_set_option) */
 #define GEMM_ERR_SCRATCH 9            /* split needs more than gemm_bf16_tn_noalloc's scratch */
+#define GEMM_ERR_WORKSPACE 10         /* gemm_f32_bf16x6 without a large enough workspace */
 
 /*
  * gemm_f32 -- FP32 GEMM, every matrix row-major ("Optimizing GEMM in HIP":
@@ -62,6 +63,46 @@ extern "C" {
  */
 int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
              int64_t ldb, float* C, int64_t ldc, void* stream);
+
+/*
+ * gemm_f32_bf16x6 -- the FP32 GEMM of gemm_f32 (same arguments, layouts and
+ * checks), computed on the tensor cores instead of the CUDA cores.  The pages
+ * compute FP32 GEMMs with FP32 FMAs only ("Optimizing GEMM in HIP"); this is a
+ * library extension for the same product:
+ *
+ *   each FP32 value x is split exactly into three bfloat16 pieces,
+ *   x = x0 + x1 + x2 (x0 = bf16_rne(x), x1 = bf16_rne(x - x0), x2 = x - x0 - x1);
+ *   C = sum of the six piece products a2 b0, a1 b1, a0 b2, a1 b0, a0 b1, a0 b0,
+ *   each formed exactly and summed in the tensor cores' FP32 accumulator, the
+ *   smallest first.
+ *
+ * The three products left out are below 2^-25 |a b|, so the error is that of
+ * an FP32 GEMM: FP32 accumulation over 6 K terms.  Results are not bit-equal
+ * to gemm_f32 (another summation order), but inputs whose products and partial
+ * sums are exact in FP32 (small integers, +-1, an identity operand) give exact
+ * results on both.  Exact splitting needs finite inputs with |x| in about
+ * [2^-100, 2^127); outside that range pieces lose bits, and Inf or NaN inputs
+ * give NaN.
+ *
+ * Workspace: the splits are written to the workspace registered with
+ * gemm_set_workspace for the current device.  The call needs at least
+ * gemm_f32_bf16x6_workspace_bytes(M, N, K) bytes there and returns
+ * GEMM_ERR_WORKSPACE, launching nothing, without them.  Bytes beyond that let
+ * shapes with few output tiles split K as the TN calls do (up to
+ * gemm_workspace_bytes(N, M, 6 * Kp) more, Kp = K rounded up to a multiple of
+ * 64).  The workspace is in use until the call's work on `stream` has ended.
+ * Launches: two split kernels, then the tensor-core GEMM (a zeroing memset
+ * before it when K is split).
+ */
+int gemm_f32_bf16x6(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
+                    int64_t ldb, float* C, int64_t ldc, void* stream);
+
+/*
+ * Workspace bytes gemm_f32_bf16x6 needs for an M x N x K product: two split
+ * operands of (M + N) rows of 6 Kp bfloat16 values, each rounded up to 256
+ * bytes.  0 when M, N or K is 0 or out of range.
+ */
+int64_t gemm_f32_bf16x6_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
  * gemm_f16_tn -- FP16 inputs, FP32 accumulation, FP16 output, "TN" layout
@@ -201,8 +242,9 @@ int gemm_set_option(const char* name, int64_t value);
  * slower loads would;
  * and TN calls whose output tiles cannot fill the GPU in one wave split K: each K piece writes its FP32 partial tile to the workspace and
  * the last piece to finish a 32-row slice sums the pieces in piece order (so
- * the result does not depend on timing) and stores C.  Calls that split K on
- * the same device share the workspace, so they must not overlap in time
+ * the result does not depend on timing) and stores C.  gemm_f32_bf16x6 writes
+ * its split operands there (and needs them to fit).  Calls that use the
+ * workspace on the same device share it, so they must not overlap in time
  * (issue them on one stream, or register a workspace per device and stream
  * order them).  The library never frees or reallocates the buffer.  Option
  * "splits" (gemm_set_option) forces or disables splitting.  Returns GEMM_OK,

@@ -26,7 +26,7 @@ def test_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for st in range(10):
+    for st in range(11):
         assert capi.status_text(st) and capi.status_text(st) != "unknown status"
     assert capi.status_text(99) == "unknown status"
 
@@ -60,6 +60,14 @@ def test_fp8_and_f32_argument_errors_without_gpu():
     assert capi.gemm_f32(4, 5, 6, p, 6, p, 4, p, 5) == capi.GEMM_ERR_INVALID_LD
     assert capi.gemm_f32(4, 5, 6, p + 2, 6, p, 5, p, 5) == capi.GEMM_ERR_MISALIGNED
     assert capi.gemm_f32(4, 5, 6, None, 6, p, 5, p, 5) == capi.GEMM_ERR_NULL_PTR
+    f6 = capi.gemm_f32_bf16x6
+    assert f6(4, 5, -6, p, 6, p, 5, p, 5) == capi.GEMM_ERR_INVALID_DIM
+    # 6 x K rounded up to 64 must stay below 2^31
+    assert f6(4, 5, 1 << 29, p, 1 << 29, p, 5, p, 5) == capi.GEMM_ERR_INVALID_DIM
+    assert f6(4, 5, 6, p, 5, p, 5, p, 5) == capi.GEMM_ERR_INVALID_LD
+    assert f6(4, 5, 6, p, 6, p, 5, p, 4) == capi.GEMM_ERR_INVALID_LD
+    assert f6(4, 5, 6, p, 6, None, 5, p, 5) == capi.GEMM_ERR_NULL_PTR
+    assert f6(4, 5, 6, p, 6, p, 5, p + 2, 5) == capi.GEMM_ERR_MISALIGNED
 
 
 def test_options():
@@ -93,6 +101,20 @@ def test_workspace_size_bound():
     repack = (512 + 1024) * 64 * 2
     assert capi.gemm_workspace_bytes(512, 1024, 64) >= repack + tiles * 16 * 4 * 32 * 1024
     assert capi.gemm_workspace_bytes(0, 1, 1) == 0
+
+
+def test_f32_bf16x6_workspace_size():
+    # two operands of (rows x 6 Kp) bf16 values, Kp = K rounded up to 64, each
+    # rounded up to 256 bytes
+    def expect(M, N, K):
+        kp = (K + 63) // 64 * 64
+        r = lambda n: (n + 255) // 256 * 256  # noqa: E731
+        return r(M * 6 * kp * 2) + r(N * 6 * kp * 2)
+    for shape in [(1, 1, 1), (4096, 4096, 4096), (3, 5, 65), (2047, 3001, 1023)]:
+        assert capi.gemm_f32_bf16x6_workspace_bytes(*shape) == expect(*shape)
+    assert capi.gemm_f32_bf16x6_workspace_bytes(4096, 4096, 4096) == 2 * 4096 * 6 * 4096 * 2
+    assert capi.gemm_f32_bf16x6_workspace_bytes(0, 4, 4) == 0
+    assert capi.gemm_f32_bf16x6_workspace_bytes(4, 4, -1) == 0
 
 
 @pytest.mark.parametrize("tiles_m,tiles_n,group", [(1, 1, 8), (32, 64, 8), (16, 12, 8),
