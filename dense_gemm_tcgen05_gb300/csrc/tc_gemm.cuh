@@ -231,7 +231,10 @@ __device__ __forceinline__ uint4 mask_chunk(uint4 v, int32_t lim) {
 
 // ------------------------------------------------------------------ kernel
 
-template <InKind IN, typename OutT, bool PAIR, bool LOADS>
+// SPLIT: the launch cuts tiles into K pieces (split-K or a K-split tail) and
+// combines them through the workspace.  Launches without K pieces run the
+// instantiation without that code.
+template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT>
 __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
                    const __grid_constant__ CUtensorMap map_q,
@@ -708,7 +711,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                 static_cast<int32_t>(tp * Cfg::kTileP + rank * Cfg::kBlockP + quarter * 32);
             const int32_t col0 = w.q_off;
             const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + b * Cfg::kAccCols;
-            if (w.pieces == 1) {
+            if (!SPLIT || w.pieces == 1) {
 #pragma unroll 1
                 for (int c = 0; c < chunks; ++c) {
                     uint32_t v0[32], v1[32];
@@ -734,9 +737,12 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                     }
                     emit(pk, col0 + c * kCols, row0);
                 }
-            } else {
+            } else if constexpr (SPLIT) {
                 // This K piece's partial sums -> workspace, column-major within
                 // the slice so that a warp's stores (and loads) are coalesced.
+                // The accumulator stays in TMEM until this warp knows whether
+                // it combines the pieces: the last piece to arrive reads its
+                // own sums from there instead of back from memory.
                 const int32_t piece = w.piece;
                 float* part = prm.ws_partials +
                               ((w.ws_tile * w.pieces + piece) * kSlices + slice) * kSliceFloats;
@@ -745,7 +751,6 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(t_row + c * 32, v);
                     tmem_wait_ld();
-                    if (c == w.width / 32 - 1) release_acc(b);
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         __stcg(part + (c * 32 + j) * 32 + lane, __uint_as_float(v[j]));
@@ -756,7 +761,10 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                 unsigned int* counter = prm.ws_counters + w.ws_tile * kSlices + slice;
                 if (lane == 0) prev = atomicAdd(counter, 1u);
                 prev = __shfl_sync(0xffffffffu, prev, 0);
-                if (prev + 1 != static_cast<unsigned int>(w.pieces)) continue;
+                if (prev + 1 != static_cast<unsigned int>(w.pieces)) {
+                    release_acc(b);
+                    continue;
+                }
                 // Last piece of this slice: sum all pieces in piece order (the
                 // result does not depend on which piece finished last).
                 __threadfence();
@@ -769,15 +777,28 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < kCols; ++j) f[j] = 0.f;
                     for (int32_t pc = 0; pc < w.pieces; ++pc) {
-                        const float* src = base_part + static_cast<int64_t>(pc) * kSlices * kSliceFloats;
+                        if (pc == piece) {
+                            uint32_t v0[32], v1[32];
+                            tmem_ld_32x32b_x32(t_row + c * kCols, v0);
+                            if constexpr (kCols == 64)
+                                tmem_ld_32x32b_x32(t_row + c * kCols + 32, v1);
+                            tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < kCols; ++j)
-                            f[j] += __ldcg(src + (c * kCols + j) * 32 + lane);
+                            for (int j = 0; j < kCols; ++j)
+                                f[j] += __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
+                        } else {
+                            const float* src =
+                                base_part + static_cast<int64_t>(pc) * kSlices * kSliceFloats;
+#pragma unroll
+                            for (int j = 0; j < kCols; ++j)
+                                f[j] += __ldcg(src + (c * kCols + j) * 32 + lane);
+                        }
                     }
                     uint32_t pk[32];
                     pack(f, pk);
                     emit(pk, col0 + c * kCols, row0);
                 }
+                release_acc(b);
             }
         }
         if (!prm.direct_store && lane == 0) bulk_wait_group<0>();
@@ -794,10 +815,10 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
     }
 }
 
-template <InKind IN, typename OutT, bool PAIR, bool LOADS>
+template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT>
 cudaError_t tc_launch_one(const TcLaunch& L) {
     using Cfg = TcCfg<IN, PAIR, LOADS>;
-    auto kernel = tc_gemm_kernel<IN, OutT, PAIR, LOADS>;
+    auto kernel = tc_gemm_kernel<IN, OutT, PAIR, LOADS, SPLIT>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -825,13 +846,21 @@ cudaError_t tc_launch_one(const TcLaunch& L) {
     return cudaLaunchKernelEx(&cfg, kernel, L.map_p, L.map_q, L.map_out, L.map_q_tail, L.prm);
 }
 
-template <InKind IN, typename OutT>
-cudaError_t tc_launch_impl(bool pair, Producer prod, const TcLaunch& L) {
+template <InKind IN, typename OutT, bool SPLIT>
+cudaError_t tc_launch_split(bool pair, Producer prod, const TcLaunch& L) {
     if (prod == Producer::Loads) {
         if (pair) return cudaErrorInvalidConfiguration;
-        return tc_launch_one<IN, OutT, false, true>(L);
+        return tc_launch_one<IN, OutT, false, true, SPLIT>(L);
     }
-    return pair ? tc_launch_one<IN, OutT, true, false>(L) : tc_launch_one<IN, OutT, false, false>(L);
+    return pair ? tc_launch_one<IN, OutT, true, false, SPLIT>(L)
+                : tc_launch_one<IN, OutT, false, false, SPLIT>(L);
+}
+
+template <InKind IN, typename OutT>
+cudaError_t tc_launch_impl(bool pair, Producer prod, const TcLaunch& L) {
+    const bool split = L.prm.splits > 1 || L.prm.tail_ksplit != 0;
+    return split ? tc_launch_split<IN, OutT, true>(pair, prod, L)
+                 : tc_launch_split<IN, OutT, false>(pair, prod, L);
 }
 
 template <InKind IN>
