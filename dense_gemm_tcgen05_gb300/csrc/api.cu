@@ -64,6 +64,9 @@ struct DeviceInfo {
 
 std::mutex g_mutex;
 DeviceInfo g_devices[kMaxDevices];
+// Which fixed counter set of the registered workspace the next split launch
+// on each device counts in.
+std::atomic<unsigned int> g_cnt_parity[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 std::atomic<int> g_opt_pair{-1};
@@ -223,14 +226,42 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     // Scratch: the caller's workspace (registered, or the override).
     char* ws_base = nullptr;
     int64_t ws_total = 0;
+    char* cnt_base = nullptr;  // the two fixed split-counter sets, if this scratch has them
+    std::atomic<unsigned int>* cnt_parity = nullptr;
     if (ov) {
         ws_base = static_cast<char*>(ov->ptr);
         ws_total = ov->bytes;
+        cnt_base = static_cast<char*>(ov->counters);
+        cnt_parity = ov->parity;
     } else {
         std::lock_guard<std::mutex> lock(g_mutex);
         ws_base = static_cast<char*>(dev->workspace);
         ws_total = dev->workspace_bytes;
+        if (ws_base && ws_total >= kSplitCounterBytes) {
+            cnt_base = ws_base;
+            cnt_parity = &g_cnt_parity[dev - g_devices];
+            ws_base += kSplitCounterBytes;
+            ws_total -= kSplitCounterBytes;
+        }
     }
+    // Counters for a split launch: a fixed set when there is one large enough
+    // (the launch zeroes the other set for the next split launch), otherwise
+    // `fallback` in the scratch, zeroed on the stream first.
+    auto take_counters = [&](TcParams& prm, int64_t words, char* fallback,
+                             int64_t fallback_bytes) {
+        if (cnt_base && cnt_parity && words <= kCounterSetWords) {
+            const unsigned int p = cnt_parity->fetch_xor(1u) & 1u;
+            prm.ws_counters = reinterpret_cast<unsigned int*>(cnt_base + p * kCounterSetWords * 4);
+            prm.ws_clear =
+                reinterpret_cast<unsigned int*>(cnt_base + (p ^ 1u) * kCounterSetWords * 4);
+            prm.clear_words = static_cast<int32_t>(kCounterSetWords);
+            return cudaSuccess;
+        }
+        prm.ws_counters = reinterpret_cast<unsigned int*>(fallback);
+        prm.ws_clear = nullptr;
+        prm.clear_words = 0;
+        return cudaMemsetAsync(fallback, 0, static_cast<size_t>(fallback_bytes), stream);
+    };
     int64_t ws_used = 0;  // bytes at the start of the scratch taken by repacked operands
 
     // Operands whose rows TMA cannot address are copied once into the scratch
@@ -401,9 +432,8 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
             if (pieces >= 2 && ws && cnt_bytes + part_bytes <= ws_bytes) {
                 L.prm.splits = static_cast<int32_t>(pieces);
                 L.prm.kb_per_split = static_cast<int32_t>(kb_per);
-                L.prm.ws_counters = static_cast<unsigned int*>(ws);
                 L.prm.ws_partials = reinterpret_cast<float*>(static_cast<char*>(ws) + cnt_bytes);
-                e = cudaMemsetAsync(ws, 0, static_cast<size_t>(cnt_bytes), stream);
+                e = take_counters(L.prm, tiles * slices, static_cast<char*>(ws), cnt_bytes);
                 if (e != cudaSuccess) return fail_cuda(e);
                 const int64_t units = tiles * pieces;
                 const int64_t c2 = (units < slots ? units : slots) * g.cluster;
@@ -476,9 +506,8 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
             L.prm.tail_f = f;
             L.prm.tail_kb_per = static_cast<int32_t>(kb_per_t);
             L.prm.full_units = waves * units_slots;
-            L.prm.ws_counters = reinterpret_cast<unsigned int*>(ws);
             L.prm.ws_partials = reinterpret_cast<float*>(ws + cnt_bytes);
-            e = cudaMemsetAsync(ws, 0, static_cast<size_t>(cnt_bytes), stream);
+            e = take_counters(L.prm, rem * slices, ws, cnt_bytes);
             if (e != cudaSuccess) return fail_cuda(e);
         } else if (f > 1) {
             const int width = tile_q / f;
@@ -612,7 +641,7 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
 int64_t gemm_f32_bf16x6_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
     const int64_t row = 6 * ((K + 63) / 64 * 64) * 2;  // bytes of one split row
-    return (M * row + 255) / 256 * 256 + (N * row + 255) / 256 * 256;
+    return kSplitCounterBytes + (M * row + 255) / 256 * 256 + (N * row + 255) / 256 * 256;
 }
 
 int gemm_f32_bf16x6(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
@@ -646,14 +675,16 @@ int gemm_f32_bf16x6(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda
     const int64_t need = gemm_f32_bf16x6_workspace_bytes(M, N, K);
     if (!ws || ws_bytes < need) return GEMM_ERR_WORKSPACE;
     const int64_t a_bytes = (M * 6 * kp * 2 + 255) / 256 * 256;
-    char* sa = ws;             // M rows of 6 kp BF16: the split of A
-    char* sb = ws + a_bytes;   // N rows of 6 kp BF16: the split of B, transposed
+    char* sa = ws + kSplitCounterBytes;  // M rows of 6 kp BF16: the split of A
+    char* sb = sa + a_bytes;             // N rows of 6 kp BF16: the split of B, transposed
     e = f32_split_rows_launch(A, lda, M, K, kp, sa, dev->sms, stream);
     if (e == cudaSuccess) e = f32_split_cols_launch(B, ldb, K, N, kp, sb, dev->sms, stream);
     if (e != cudaSuccess) return fail_cuda(e);
     // What is left of the workspace serves split-K where it fits; otherwise
     // the GEMM runs unsplit.
-    const ScratchOverride ov{ws + need, ws_bytes - need, 0, 0};
+    ScratchOverride ov{ws + need, ws_bytes - need, 0, 0};
+    ov.counters = ws;  // the workspace's own counter sets
+    ov.parity = &g_cnt_parity[dev - g_devices];
     return gemm_tn(InKind::BF16, true, N, M, 6 * kp, sb, 6 * kp, sa, 6 * kp, 1.0f, C, ldc,
                    stream, &ov);
 }
@@ -754,8 +785,16 @@ int gemm_set_workspace(void* ptr, int64_t bytes) {
     if (e != cudaSuccess) return fail_cuda(e);
     if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
     std::lock_guard<std::mutex> lock(g_mutex);
+    if (ptr && bytes >= kSplitCounterBytes) {
+        // The split counters at the start of the workspace start at zero; the
+        // device must hold them before any stream uses the workspace.
+        e = cudaMemset(ptr, 0, static_cast<size_t>(kSplitCounterBytes));
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return fail_cuda(e);
+    }
     g_devices[dev].workspace = ptr;
     g_devices[dev].workspace_bytes = ptr ? bytes : 0;
+    g_cnt_parity[dev].store(0u);
     return GEMM_OK;
 }
 
@@ -767,7 +806,8 @@ int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     const int64_t dp = (K * 2 + 127) / 128 * 128;
     const int64_t repack = (M * dp + 255) / 256 * 256 + (N * dp + 255) / 256 * 256;
     const int64_t tiles = ((N + 127) / 128) * ((M + 63) / 64);
-    return repack + ((tiles * 4 * 4 + 255) / 256) * 256 + tiles * 16 * 4 * 32 * 256 * 4;
+    return kSplitCounterBytes + repack + ((tiles * 4 * 4 + 255) / 256) * 256 +
+           tiles * 16 * 4 * 32 * 256 * 4;
 }
 
 int gemm_tile_coord(int64_t t, int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t* tm,

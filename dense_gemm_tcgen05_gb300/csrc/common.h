@@ -44,6 +44,11 @@ struct TcParams {
     int32_t kb_per_split;
     float* ws_partials;
     unsigned int* ws_counters;
+    // The other of the two fixed counter sets, which this launch zeroes for
+    // the next split launch (nullptr when the counters were zeroed on the
+    // host instead), and its length in words (a multiple of 4).
+    unsigned int* ws_clear;
+    int32_t clear_words;
     // Q rows per tile = N of the MMA instruction (64, 128, 192 or 256), chosen
     // per shape; the instruction descriptor and the per-stage TMA byte count
     // follow from it.

@@ -2,6 +2,8 @@
 // internal TN entry with caller-supplied scratch.
 #pragma once
 
+#include <atomic>
+
 #include "common.h"
 
 namespace gb300 {
@@ -18,6 +20,15 @@ cudaError_t tn_fallback_launch(InKind in, bool out_f32, int64_t M, int64_t N, in
                                const void* A, int64_t lda, const void* B, int64_t ldb, float scale,
                                void* C, int64_t ldc, cudaStream_t stream);
 
+// Split-K counters live in two fixed sets of kCounterSetWords words at the
+// start of each scratch area (the registered workspace, the no-allocation
+// array), kSplitCounterBytes in all, zeroed when the area is set up.  Split
+// launches alternate between the sets: each counts in one and zeroes the other
+// for the next, and the last piece of every slice resets its own counter, so
+// no launch needs a host-side memset in front of it.
+constexpr int64_t kCounterSetWords = 16384;
+constexpr int64_t kSplitCounterBytes = 2 * kCounterSetWords * 4;
+
 // Scratch supplied by the caller of the internal TN path instead of the
 // registered workspace (see gemm_tn_with_scratch).
 struct ScratchOverride {
@@ -26,6 +37,8 @@ struct ScratchOverride {
     int splits;      // 0 automatic, 1 never split, >= 2 that many K pieces
     int strict = 1;  // 1: a chosen split that does not fit fails with GEMM_ERR_SCRATCH;
                      // 0: the call runs unsplit instead
+    void* counters = nullptr;                  // the two counter sets, or nullptr
+    std::atomic<unsigned int>* parity = nullptr;  // which set the next split launch uses
 };
 
 // The TN path with explicit split-K scratch (16-bit inputs and output).

@@ -14,8 +14,10 @@
 // loaded.  Host code cannot use the array's name as a device address: the
 // address is looked up with cudaGetSymbolAddress once per device, on the first
 // call made with that device current, and cached.  All calls share the array
-// and it keeps the last call's contents; the split counters at its start are
-// zeroed before every split launch, the partial sums are overwritten.  Calls
+// and it keeps the last call's contents.  Its first kSplitCounterBytes hold the
+// two split-counter sets (zero when the library loads; each split launch
+// zeroes the set the next one uses, and resets the counters it counted in),
+// the rest the partial sums, which every split launch overwrites.  Calls
 // whose execution overlaps on the GPU (different streams, or different host
 // threads on one device) race on the array.
 #include <mutex>
@@ -33,6 +35,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
+std::atomic<unsigned int> g_parity[kMaxDevices];  // the next split launch's counter set
 
 // Device address of this device's copy of the array, looked up on first use.
 int scratch_address(void** out) {
@@ -60,7 +63,13 @@ extern "C" int gemm_bf16_tn_noalloc(int64_t M, int64_t N, int64_t K, const void*
     void* scratch = nullptr;
     const int st = scratch_address(&scratch);
     if (st != GEMM_OK) return st;
-    const gb300::ScratchOverride ov{scratch, kNoAllocScratchBytes, static_cast<int>(splits)};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_LAUNCH;
+    gb300::ScratchOverride ov{static_cast<char*>(scratch) + gb300::kSplitCounterBytes,
+                              kNoAllocScratchBytes - gb300::kSplitCounterBytes,
+                              static_cast<int>(splits)};
+    ov.counters = scratch;
+    ov.parity = &g_parity[dev];
     return gb300::gemm_tn_with_scratch(gb300::InKind::BF16, M, N, K, A, lda, B, ldb, C, ldc,
                                        stream, ov);
 }

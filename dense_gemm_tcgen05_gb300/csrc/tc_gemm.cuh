@@ -294,6 +294,13 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
     if constexpr (PAIR) cluster_sync();
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    // Launched with programmatic stream serialisation: everything above ran
+    // while the previous grid in the stream may still be finishing; nothing
+    // below may touch global memory before that grid is complete.  Only then
+    // may the next grid be scheduled, so that grids waiting here never hold
+    // SMs an earlier grid still needs.
+    pdl_wait();
+    pdl_trigger();
 
     const Watch wd{abort_flag, prm.watchdog, prm.timeout_ns};
     const int64_t num_tiles = static_cast<int64_t>(prm.tiles_p) * prm.tiles_q;
@@ -584,6 +591,17 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         const float scale = prm.scale;
         uint8_t* const out8 = static_cast<uint8_t*>(prm.out);
         uint32_t lt = 0, chunk = 0;
+        if constexpr (SPLIT) {
+            // Zero the counter set the next split launch will use.  The last
+            // launch that used it is complete (pdl_wait above); this launch
+            // counts in the other set.
+            if (blockIdx.x == 0 && prm.ws_clear) {
+                uint4* clr = reinterpret_cast<uint4*>(prm.ws_clear);
+                for (int32_t i = static_cast<int32_t>(threadIdx.x) - 64; i < prm.clear_words / 4;
+                     i += 32 * Cfg::kEpiWarps)
+                    clr[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
 
         // Converts 32 words' worth of FP32 values (kCols of them) into this
         // lane's 128 output bytes.
@@ -834,14 +852,19 @@ cudaError_t tc_launch_one(const TcLaunch& L) {
     cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = L.stream;
-    cudaLaunchAttribute attr[1];
+    // The kernel starts its prologue while the previous grid in the stream
+    // finishes, and waits for it (pdl_wait) before touching global memory.
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (PAIR) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     return cudaLaunchKernelEx(&cfg, kernel, L.map_p, L.map_q, L.map_out, L.map_q_tail, L.prm);
 }

@@ -243,17 +243,23 @@ int gemm_set_option(const char* name, int64_t value);
  * and TN calls whose output tiles cannot fill the GPU in one wave split K: each K piece writes its FP32 partial tile to the workspace and
  * the last piece to finish a 32-row slice sums the pieces in piece order (so
  * the result does not depend on timing) and stores C.  gemm_f32_bf16x6 writes
- * its split operands there (and needs them to fit).  Calls that use the
- * workspace on the same device share it, so they must not overlap in time
+ * its split operands there (and needs them to fit).  The first 128 KiB of a
+ * workspace of at least that size hold the split counters: registration
+ * zeroes them (a synchronous cudaMemset followed by cudaDeviceSynchronize),
+ * and every split launch zeroes the set the next one uses, so no split call
+ * needs a memset of its own; after a call that ran into GEMM_ERR_TIMEOUT,
+ * register the workspace again before replaying a captured CUDA graph that
+ * splits K.  Calls that use the workspace on the same device share it, so they must not overlap in time
  * (issue them on one stream, or register a workspace per device and stream
  * order them).  The library never frees or reallocates the buffer.  Option
  * "splits" (gemm_set_option) forces or disables splitting.  Returns GEMM_OK,
- * GEMM_ERR_MISALIGNED or GEMM_ERR_INVALID_DIM.
+ * GEMM_ERR_MISALIGNED, GEMM_ERR_INVALID_DIM, or GEMM_ERR_LAUNCH if zeroing the
+ * counters fails.
  */
 int gemm_set_workspace(void* ptr, int64_t bytes);
 
-/* Workspace bytes that suffice for any M x N x K TN call (aligned copies of A
- * and B plus the largest split). */
+/* Workspace bytes that suffice for any M x N x K TN call (the split counters,
+ * aligned copies of A and B, and the largest split). */
 int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
@@ -274,8 +280,9 @@ int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * most ~20 MiB on a 152-SM GPU).  The first call on a device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current; make
  * that first call before any stream capture.  All calls share the array and it
- * keeps the last call's contents (the split counters are zeroed before each
- * split launch): calls that overlap in time on the GPU race.
+ * keeps the last call's contents; its first 128 KiB hold the split counters
+ * (zero at load, and each split launch zeroes the set the next one uses), the
+ * rest the partial sums.  Calls that overlap in time on the GPU race.
  */
 #define GEMM_NOALLOC_SCRATCH_BYTES (24LL << 20)
 int gemm_bf16_tn_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,

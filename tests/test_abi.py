@@ -95,24 +95,29 @@ def test_options():
     assert capi.gemm_set_option("repack", 0) == 0
 
 
+SPLIT_COUNTER_BYTES = 2 * 16384 * 4  # two fixed split-counter sets at the workspace's start
+
+
 def test_workspace_size_bound():
     # aligned copies of A and B, then 16 pieces of every 128 x 64 tile (32 KB a slice)
     tiles = (1024 // 128) * (512 // 64)
     repack = (512 + 1024) * 64 * 2
-    assert capi.gemm_workspace_bytes(512, 1024, 64) >= repack + tiles * 16 * 4 * 32 * 1024
+    assert capi.gemm_workspace_bytes(512, 1024, 64) >= (SPLIT_COUNTER_BYTES + repack +
+                                                         tiles * 16 * 4 * 32 * 1024)
     assert capi.gemm_workspace_bytes(0, 1, 1) == 0
 
 
 def test_f32_bf16x6_workspace_size():
-    # two operands of (rows x 6 Kp) bf16 values, Kp = K rounded up to 64, each
-    # rounded up to 256 bytes
+    # the split-counter sets, then two operands of (rows x 6 Kp) bf16 values,
+    # Kp = K rounded up to 64, each rounded up to 256 bytes
     def expect(M, N, K):
         kp = (K + 63) // 64 * 64
         r = lambda n: (n + 255) // 256 * 256  # noqa: E731
-        return r(M * 6 * kp * 2) + r(N * 6 * kp * 2)
+        return SPLIT_COUNTER_BYTES + r(M * 6 * kp * 2) + r(N * 6 * kp * 2)
     for shape in [(1, 1, 1), (4096, 4096, 4096), (3, 5, 65), (2047, 3001, 1023)]:
         assert capi.gemm_f32_bf16x6_workspace_bytes(*shape) == expect(*shape)
-    assert capi.gemm_f32_bf16x6_workspace_bytes(4096, 4096, 4096) == 2 * 4096 * 6 * 4096 * 2
+    assert (capi.gemm_f32_bf16x6_workspace_bytes(4096, 4096, 4096) ==
+            SPLIT_COUNTER_BYTES + 2 * 4096 * 6 * 4096 * 2)
     assert capi.gemm_f32_bf16x6_workspace_bytes(0, 4, 4) == 0
     assert capi.gemm_f32_bf16x6_workspace_bytes(4, 4, -1) == 0
 

@@ -130,3 +130,107 @@ def test_tail_k_pieces_large_sampled(shape, tail_k, workspace):
         check_sampled("bf16", ops, M, N, K, C, seed=3)
     finally:
         capi.gemm_set_option("tail_k", 0)
+
+
+def _issue(kind, shape, seed, opts, st):
+    """Copies seeded +-1 operands to the GPU and issues one call (no sync)."""
+    M, N, K = shape
+    ops = si.tn_operands(kind, M, N, K, dist="pm1", seed=seed)
+    A, B = ops["A"].cuda(), ops["B"].cuda()
+    C = torch.full((N, M), float("nan"), dtype=torch.bfloat16, device="cuda")
+    try:
+        for k, v in opts.items():
+            if k != "noalloc":
+                assert capi.gemm_set_option(k, v) == 0
+        if opts.get("noalloc"):
+            rc = capi.gemm_bf16_tn_noalloc(M, N, K, A.data_ptr(), K, B.data_ptr(), K,
+                                           C.data_ptr(), M, 0, st)
+        else:
+            rc = capi.gemm_bf16_tn(M, N, K, A.data_ptr(), K, B.data_ptr(), K, C.data_ptr(), M, st)
+        assert rc == 0, capi.status_text(rc)
+    finally:
+        for k in opts:
+            if k != "noalloc":
+                capi.gemm_set_option(k, 0)
+    return ops, shape, (A, B, C)
+
+
+def _check_exact(ops, shape, bufs, what=""):
+    M, N, K = shape
+    exact = oracle.gemm_tn("bf16", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+    got, want = out_codes(bufs[2].cpu(), M, N), exact_codes("bf16", exact)
+    bad = int(np.count_nonzero((got != want) & ((got | want) != 0x8000)))
+    assert bad == 0, "%s %s: %d of %d outputs differ" % (what, shape, bad, M * N)
+    assert_codes_equal(got, want)
+
+
+def test_counter_sets_back_to_back(workspace):
+    """Split launches count in one of the workspace's two counter sets and
+    zero the other for the next; the last piece of each slice resets its own
+    counter.  A run of split calls of several shapes and kinds (automatic
+    split-K, forced pieces, a K-split tail, the no-allocation array's own
+    sets in between), issued back to back on one stream with no host sync,
+    must each match the oracle bit for bit."""
+    st = torch.cuda.current_stream().cuda_stream
+    plan = [((256, 512, 4096), {}), ((600, 330, 1000), {"splits": 3}),
+            ((300, 200, 1000), {}), ((2048, 2048, 2048), {"tail_k": 2}),
+            ((64, 2048, 2048), {"noalloc": 1}), ((64, 2048, 2048), {}),
+            ((600, 330, 1000), {"splits": 7}), ((1024, 1024, 8192), {})] * 2
+    pending = [_issue("bf16", shape, 200 + i, opts, st) for i, (shape, opts) in enumerate(plan)]
+    torch.cuda.synchronize()
+    bad = []
+    for i, item in enumerate(pending):
+        try:
+            _check_exact(*item, what="call %d %s" % (i, plan[i][1]))
+        except AssertionError as exc:
+            bad.append(str(exc).splitlines()[0])
+    assert not bad, "; ".join(bad)
+
+
+def test_registration_zeroes_the_counter_sets():
+    """The counter sets at the start of a workspace are zeroed when it is
+    registered: fill them with garbage, register, and split calls must still be
+    exact (a counter that did not start at zero would let a piece combine the
+    slice before the other pieces wrote their partial sums)."""
+    ws = torch.empty(1 << 27, dtype=torch.uint8, device="cuda")
+    ws[: 2 * 16384 * 4].fill_(0xFF)
+    assert capi.gemm_set_workspace(ws.data_ptr(), ws.numel()) == 0
+    try:
+        st = torch.cuda.current_stream().cuda_stream
+        pending = [_issue("bf16", (256, 512, 4096), 300 + i, {}, st) for i in range(3)]
+        torch.cuda.synchronize()
+        for item in pending:
+            _check_exact(*item)
+    finally:
+        assert capi.gemm_set_workspace(None, 0) == 0
+
+
+def test_more_counters_than_a_set_holds():
+    """Forced pieces over more than 16384 32-row slices (4128 tiles of 128 x
+    256) do not fit a fixed counter set: those counters go to the scratch and
+    are zeroed on the stream instead.  Fixed-set split calls before and after
+    stay exact."""
+    ws = torch.empty(1200 << 20, dtype=torch.uint8, device="cuda")
+    assert capi.gemm_set_workspace(ws.data_ptr(), ws.numel()) == 0
+    try:
+        st = torch.cuda.current_stream().cuda_stream
+        before = _issue("bf16", (256, 512, 4096), 400, {}, st)
+        M, N, K = 8192, 16512, 128
+        ops = si.tn_operands("bf16", M, N, K, dist="pm1", seed=401)
+        A, B = ops["A"].cuda(), ops["B"].cuda()
+        C = torch.full((N, M), float("nan"), dtype=torch.bfloat16, device="cuda")
+        assert capi.gemm_set_option("pair", 0) == 0
+        assert capi.gemm_set_option("splits", 2) == 0
+        try:
+            rc = capi.gemm_bf16_tn(M, N, K, A.data_ptr(), K, B.data_ptr(), K, C.data_ptr(), M, st)
+            assert rc == 0, capi.status_text(rc)
+        finally:
+            capi.gemm_set_option("pair", -1)
+            capi.gemm_set_option("splits", 0)
+        after = _issue("bf16", (256, 512, 4096), 402, {}, st)
+        torch.cuda.synchronize()
+        check_sampled("bf16", ops, M, N, K, C.cpu(), seed=401)
+        for item in (before, after):
+            _check_exact(*item)
+    finally:
+        assert capi.gemm_set_workspace(None, 0) == 0
