@@ -22,15 +22,15 @@ cudaError_t tc_launch_f16(bool pair, Producer prod, const TcLaunch& L);
 cudaError_t tc_launch_bf16(bool pair, Producer prod, const TcLaunch& L);
 cudaError_t tc_launch_bf16_f32(bool pair, Producer prod, const TcLaunch& L);
 cudaError_t tc_launch_fp8(bool pair, Producer prod, bool out_f32, const TcLaunch& L);
-TcGeometry tc_geometry_f16(bool pair);
-TcGeometry tc_geometry_bf16(bool pair);
-TcGeometry tc_geometry_fp8(bool pair);
+TcGeometry tc_geometry_f16(bool pair, bool half);
+TcGeometry tc_geometry_bf16(bool pair, bool half);
+TcGeometry tc_geometry_fp8(bool pair, bool half);
 
-TcGeometry tc_geometry(InKind in, bool pair) {
+TcGeometry tc_geometry(InKind in, bool pair, bool half) {
     switch (in) {
-        case InKind::F16: return tc_geometry_f16(pair);
-        case InKind::BF16: return tc_geometry_bf16(pair);
-        default: return tc_geometry_fp8(pair);
+        case InKind::F16: return tc_geometry_f16(pair, half);
+        case InKind::BF16: return tc_geometry_bf16(pair, half);
+        default: return tc_geometry_fp8(pair, half);
     }
 }
 
@@ -81,6 +81,7 @@ std::atomic<int> g_opt_repack{0};
 std::atomic<int> g_opt_f32_tail{0};
 std::atomic<int> g_opt_cluster{0};
 std::atomic<int> g_opt_l2hints{0};
+std::atomic<int> g_opt_half{0};
 std::atomic<int64_t> g_opt_timeout_ns{2000000000LL};
 
 thread_local cudaError_t t_last_cuda_error = cudaSuccess;
@@ -323,14 +324,14 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     if (pair && opt_pair < 0) {
         const int64_t pair_tiles = ((N + 255) / 256) * ((M + choose_tile_q(M, 256) - 1) /
                                                         choose_tile_q(M, 256));
-        const int q = M <= 128 ? 64 : 128;
+        const int q = M <= 16 ? 16 : M <= 32 ? 32 : M <= 128 ? 64 : 128;
         const int64_t small_tiles = ((N + 127) / 128) * ((M + q - 1) / q);
         if (pair_tiles < dev->sms / 2 && small_tiles <= dev->sms) {
             pair = false;
             small_q = q;
         }
     }
-    const TcGeometry g = tc_geometry(in, pair);
+    TcGeometry g = tc_geometry(in, pair);
     TcLaunch L;
     std::memset(&L, 0, sizeof(L));
     const CUtensorMapDataType in_dt = in == InKind::F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
@@ -340,8 +341,23 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
                                        : in == InKind::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     // P = B: N rows of K contiguous elements.  Q = A: M rows of K.  Out = C: N rows of M.
+    // Tiles narrower than the epilogue's 64-column chunk (16 or 32 columns, MMA
+    // N = 16 / 32) leave room in each ring stage for more of P; they are used
+    // only when M fits in one of them, so that the rest of a chunk lies past M
+    // (the TMA store clips it), and never for CTA pairs.
     const int opt_tq = g_opt_tile_q.load();
-    const int tile_q = opt_tq ? opt_tq : small_q ? small_q : choose_tile_q(M, g.max_tile_q);
+    const int tile_q = [&] {
+        const int t = opt_tq ? opt_tq : small_q ? small_q : choose_tile_q(M, g.max_tile_q);
+        return t < 64 && (pair || M > t) ? 64 : t;
+    }();
+    // 64-row tiles (one CTA each, MMA M = 64), option "half" = 1: they cover
+    // N with twice as many CTAs without cutting K.  Measured on GB300 they have
+    // not beaten 128-row tiles with K split in two on any skinny shape (BF16
+    // 16 x 8192 x 8192: 31.1 against 27.5 us; 16 x 4096 x 8192: 29.7 against
+    // 17.4 us), so they run only when forced, and only for one-CTA TMA tiles
+    // with FP32 accumulation.
+    L.half = g_opt_half.load() == 1 && !pair && prod == Producer::Tma && !acc16;
+    if (L.half) g = tc_geometry(in, false, true);
     const int load_q = tile_q / g.cluster;
     CUresult r = CUDA_SUCCESS;
     if (prod == Producer::Tma) {
@@ -349,9 +365,10 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
         if (r == CUDA_SUCCESS)
             r = encode_2d(&L.map_q, in_dt, A, K, M, lda * es, g.stage_k, load_q);
     }
-    // One staged chunk is one 128-byte row: a box of 128 / os columns x 32 rows.
+    // One staged chunk is one 128-byte row per accumulator row of an
+    // epilogue warp: a box of 128 / os columns x 32 rows (16 for 64-row tiles).
     if (r == CUDA_SUCCESS && c_tma)
-        r = encode_2d(&L.map_out, out_dt, C, M, N, ldc * os, 128 / os, 32);
+        r = encode_2d(&L.map_out, out_dt, C, M, N, ldc * os, 128 / os, L.half ? 16 : 32);
     if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
 
     const int64_t tiles_p = (N + g.tile_p - 1) / g.tile_p;
@@ -408,7 +425,8 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     L.prm.kb_per_split = L.prm.num_kb;
     {
         // FP16 accumulation never splits K: combining pieces would add FP32 sums.
-        const int opt = acc16 ? 1 : (ov ? ov->splits : g_opt_splits.load());
+        // FP16 accumulation and 64-row tiles never split K.
+        const int opt = (acc16 || L.half) ? 1 : (ov ? ov->splits : g_opt_splits.load());
         int64_t want = 1;
         if (opt >= 2) {
             want = opt;
@@ -490,7 +508,7 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
                 }
             }
             const int opt_tail_k = g_opt_tail_k.load();
-            if (opt_tail_k >= 2 && !acc16 && ws) {
+            if (opt_tail_k >= 2 && !acc16 && !L.half && ws) {
                 const int64_t kb_per = (L.prm.num_kb + opt_tail_k - 1) / opt_tail_k;
                 const int64_t pieces = (L.prm.num_kb + kb_per - 1) / kb_per;
                 const int64_t need = cnt_bytes + rem * pieces * slices * 32 * 256 * 4;
@@ -563,11 +581,11 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
         std::fprintf(stderr,
                      "[gemm] tn in=%d M=%lld N=%lld K=%lld pair=%d producer=%d direct_store=%d "
                      "splits=%d tile_q=%d tail=%d ktail=%d stages=%d tiles=%lldx%lld grid=%d "
-                     "multicast=%d\n",
+                     "multicast=%d half=%d\n",
                      int(in), (long long)M, (long long)N, (long long)K, int(pair), int(prod),
                      L.prm.direct_store, L.prm.splits, L.prm.tile_q, L.prm.tail_f,
                      L.prm.tail_ksplit, L.prm.stages,
-                     (long long)tiles_q, (long long)tiles_p, L.grid, int(mc));
+                     (long long)tiles_q, (long long)tiles_p, L.grid, int(mc), int(L.half));
     e = mc ? tc_mc_launch(in, out_f32, L) : tc_launch(in, pair, prod, out_f32, L);
     return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
 }
@@ -747,7 +765,8 @@ int gemm_set_option(const char* name, int64_t value) {
         if (value < 0 || value > 64) return GEMM_ERR_INVALID_OPTION;
         g_opt_splits.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "tile_q")) {
-        if (!(value == 0 || value == 64 || value == 128 || value == 192 || value == 256))
+        if (!(value == 0 || value == 16 || value == 32 || value == 64 || value == 128 ||
+              value == 192 || value == 256))
             return GEMM_ERR_INVALID_OPTION;
         g_opt_tile_q.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "tail_k")) {
@@ -768,6 +787,9 @@ int gemm_set_option(const char* name, int64_t value) {
     } else if (!std::strcmp(name, "repack")) {
         if (value < 0 || value > 1) return GEMM_ERR_INVALID_OPTION;
         g_opt_repack.store(static_cast<int>(value));
+    } else if (!std::strcmp(name, "half")) {
+        if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
+        g_opt_half.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "max_ctas")) {
         if (value < 0 || value > 1 << 20) return GEMM_ERR_INVALID_OPTION;
         g_opt_max_ctas.store(static_cast<int>(value));

@@ -84,6 +84,7 @@ struct TcLaunch {
     TcParams prm;
     int grid;
     cudaStream_t stream;
+    bool half;  // one CTA per 64-row tile (MMA M = 64); unsplit TMA launches only
 };
 
 // Tile geometry of one persistent CTA (or CTA pair), for the host's grid sizing.
@@ -103,9 +104,10 @@ struct TcGeometry {
 // TMA cannot address) producer warps using 16-byte-aligned loads.
 enum class Producer : int { Tma = 0, Loads = 1 };
 
-TcGeometry tc_geometry(InKind in, bool pair);
-// out_f32: FP32 output (E4M3 inputs only); otherwise the input's 16-bit type
-// (bf16 for E4M3).
+// half: one CTA per 64-row tile (MMA M = 64).
+TcGeometry tc_geometry(InKind in, bool pair, bool half = false);
+// out_f32: FP32 output (E4M3 or BF16 inputs); otherwise the input's 16-bit
+// type (bf16 for E4M3).
 cudaError_t tc_launch(InKind in, bool pair, Producer prod, bool out_f32, const TcLaunch& L);
 
 }  // namespace gb300

@@ -51,13 +51,17 @@
 
 namespace gb300 {
 
-template <InKind IN, bool PAIR, bool LOADS>
+// HALF: one CTA per tile of 64 P rows (MMA M = 64).  Its accumulator row
+// 16 q + i sits in TMEM lane 32 q + i (i < 16), so each epilogue warp owns 16
+// rows instead of 32; used for unsplit TMA launches only.
+template <InKind IN, bool PAIR, bool LOADS, bool HALF = false>
 struct TcCfg {
     static_assert(!(PAIR && LOADS), "the load-based producer runs one CTA per tile");
+    static_assert(!(HALF && (PAIR || LOADS)), "64-row tiles: one CTA, TMA producer");
     static constexpr int kCG = PAIR ? 2 : 1;
     static constexpr int kElemBytes = IN == InKind::E4M3 ? 1 : 2;
-    static constexpr int kBlockP = 128;              // accumulator rows per CTA (TMEM lanes)
-    static constexpr int kMmaM = PAIR ? 256 : 128;   // M of one MMA instruction
+    static constexpr int kBlockP = HALF ? 64 : 128;  // accumulator rows per CTA
+    static constexpr int kMmaM = PAIR ? 256 : kBlockP;  // M of one MMA instruction
     static constexpr int kMmaN = 256;                // N of one MMA instruction
     static constexpr int kTileP = kMmaM;             // P rows per tile (per pair)
     static constexpr int kMaxLoadQ = kMmaN / (PAIR ? 2 : 1);  // Q rows a CTA loads, at most
@@ -69,9 +73,11 @@ struct TcCfg {
     static constexpr int kBytesQ = kMaxLoadQ * kAtomBytes;
     static constexpr int kStageBytes = kBytesP + kBytesQ;    // widest stage
     static constexpr int kStages = PAIR ? 6 : 4;              // widest stages that fit
-    static constexpr int kStageRegion = kStages * kStageBytes;  // 192 KB either way
-    static constexpr int kMaxStages = 12;  // narrow tiles: more, smaller stages in the region
+    static constexpr int kStageRegion = 192 * 1024;
+    static_assert(kStages * kStageBytes <= kStageRegion, "widest stages fit the ring");
+    static constexpr int kMaxStages = 20;  // narrow tiles: more, smaller stages in the region
     static constexpr int kEpiWarps = 4;
+    static constexpr int kRowsPerWarp = kBlockP / kEpiWarps;  // accumulator rows per epilogue warp
     static constexpr int kEpiBufBytes = 32 * 128;            // 32 rows x one 128-byte row
     static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
     static constexpr int kFirstLoadWarp = 6;
@@ -89,7 +95,8 @@ struct TcCfg {
     static constexpr uint32_t kFormat = IN == InKind::BF16 ? 1u : 0u;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kStageBytes % 1024 == 0 && kBytesP % 1024 == 0, "1024-byte stage alignment");
-    static_assert(PAIR || kLoadWarps * 32 == kBlockP + kMaxLoadQ, "load-producer row split");
+    static_assert(PAIR || HALF || kLoadWarps * 32 == kBlockP + kMaxLoadQ,
+                  "load-producer row split");
 };
 
 // Bounded-wait bookkeeping shared by a CTA's warps.
@@ -234,13 +241,14 @@ __device__ __forceinline__ uint4 mask_chunk(uint4 v, int32_t lim) {
 // SPLIT: the launch cuts tiles into K pieces (split-K or a K-split tail) and
 // combines them through the workspace.  Launches without K pieces run the
 // instantiation without that code.
-template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT>
-__global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
+template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT, bool HALF>
+__global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
                    const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_out,
                    const __grid_constant__ CUtensorMap map_q_tail, const TcParams prm) {
-    using Cfg = TcCfg<IN, PAIR, LOADS>;
+    using Cfg = TcCfg<IN, PAIR, LOADS, HALF>;
+    static_assert(!(SPLIT && HALF), "64-row tiles never split K");
     constexpr int SM = Cfg::kMaxStages;                 // barrier slots
     const uint32_t S = static_cast<uint32_t>(prm.stages);  // ring depth for this call
     const uint32_t stage_bytes = prm.stage_bytes;
@@ -635,7 +643,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                 // into the caller's padding between rows_q and ld_out: store it
                 // element by element.
                 const int32_t r = row0 + static_cast<int32_t>(lane);
-                if (r < prm.rows_p) {
+                if (static_cast<int>(lane) < Cfg::kRowsPerWarp && r < prm.rows_p) {
                     uint8_t* dst = out8 + (static_cast<int64_t>(r) * prm.ld_out + x) * kOB;
                     const int32_t ncols = prm.rows_q - x;
 #pragma unroll
@@ -683,7 +691,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                 constexpr int kPerLane = 4 / kOB;
                 const int32_t m = x + kPerLane * static_cast<int32_t>(lane);
                 const uint32_t lane_off = ((lane >> 2) << 4) + ((lane & 3u) << 2);
-                for (int r = 0; r < 32; ++r) {
+                for (int r = 0; r < Cfg::kRowsPerWarp; ++r) {
                     const int32_t grow = row0 + r;
                     if (grow >= prm.rows_p) break;
                     const uint32_t v = ld_shared_u32(
@@ -721,12 +729,15 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
         for (int64_t u = first; u < num_units; u += stride, ++lt) {
             const Unit w = unit_of(u);
             const int64_t tp = w.tp;
-            const int chunks = w.width / kCols;
+            // A tile narrower than one chunk (16 or 32 columns) spans all of M, so
+            // the chunk's columns past the tile lie past M and are not stored.
+            const int chunks = (w.width + kCols - 1) / kCols;
             const uint32_t b = lt & 1u, aph = (lt >> 1) & 1u;
             if (!warp_wait(accf_bar(b), aph, wd)) break;
             tc_fence_after_sync();
             const int32_t row0 =
-                static_cast<int32_t>(tp * Cfg::kTileP + rank * Cfg::kBlockP + quarter * 32);
+                static_cast<int32_t>(tp * Cfg::kTileP + rank * Cfg::kBlockP +
+                                     quarter * Cfg::kRowsPerWarp);
             const int32_t col0 = w.q_off;
             const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + b * Cfg::kAccCols;
             if (!SPLIT || w.pieces == 1) {
@@ -765,7 +776,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
                 float* part = prm.ws_partials +
                               ((w.ws_tile * w.pieces + piece) * kSlices + slice) * kSliceFloats;
 #pragma unroll 1
-                for (int c = 0; c < w.width / 32; ++c) {
+                for (int c = 0; c < (w.width + 31) / 32; ++c) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(t_row + c * 32, v);
                     tmem_wait_ld();
@@ -833,10 +844,10 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS>::kThreads, 1)
     }
 }
 
-template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT>
+template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT, bool HALF = false>
 cudaError_t tc_launch_one(const TcLaunch& L) {
-    using Cfg = TcCfg<IN, PAIR, LOADS>;
-    auto kernel = tc_gemm_kernel<IN, OutT, PAIR, LOADS, SPLIT>;
+    using Cfg = TcCfg<IN, PAIR, LOADS, HALF>;
+    auto kernel = tc_gemm_kernel<IN, OutT, PAIR, LOADS, SPLIT, HALF>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -872,8 +883,16 @@ cudaError_t tc_launch_one(const TcLaunch& L) {
 template <InKind IN, typename OutT, bool SPLIT>
 cudaError_t tc_launch_split(bool pair, Producer prod, const TcLaunch& L) {
     if (prod == Producer::Loads) {
-        if (pair) return cudaErrorInvalidConfiguration;
+        if (pair || L.half) return cudaErrorInvalidConfiguration;
         return tc_launch_one<IN, OutT, false, true, SPLIT>(L);
+    }
+    if (L.half) {
+        if constexpr (SPLIT) {
+            return cudaErrorInvalidConfiguration;
+        } else {
+            if (pair) return cudaErrorInvalidConfiguration;
+            return tc_launch_one<IN, OutT, false, false, false, true>(L);
+        }
     }
     return pair ? tc_launch_one<IN, OutT, true, false, SPLIT>(L)
                 : tc_launch_one<IN, OutT, false, false, SPLIT>(L);
@@ -887,7 +906,13 @@ cudaError_t tc_launch_impl(bool pair, Producer prod, const TcLaunch& L) {
 }
 
 template <InKind IN>
-TcGeometry tc_geometry_impl(bool pair) {
+TcGeometry tc_geometry_impl(bool pair, bool half) {
+    if (half) {
+        using Cfg = TcCfg<IN, false, false, true>;
+        return TcGeometry{Cfg::kTileP,  Cfg::kMmaN,    Cfg::kBlockP,      Cfg::kStageK,
+                          1,            Cfg::kMmaM,    Cfg::kFormat,      Cfg::kStageRegion,
+                          Cfg::kMaxStages};
+    }
     if (pair) {
         using Cfg = TcCfg<IN, true, false>;
         return TcGeometry{Cfg::kTileP,  Cfg::kMmaN,    Cfg::kBlockP,      Cfg::kStageK,

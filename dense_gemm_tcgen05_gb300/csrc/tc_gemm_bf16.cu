@@ -10,6 +10,8 @@ cudaError_t tc_launch_bf16(bool pair, Producer prod, const TcLaunch& L) {
     return tc_launch_impl<InKind::BF16, __nv_bfloat16>(pair, prod, L);
 }
 
-TcGeometry tc_geometry_bf16(bool pair) { return tc_geometry_impl<InKind::BF16>(pair); }
+TcGeometry tc_geometry_bf16(bool pair, bool half) {
+    return tc_geometry_impl<InKind::BF16>(pair, half);
+}
 
 }  // namespace gb300

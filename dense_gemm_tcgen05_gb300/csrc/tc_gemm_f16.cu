@@ -10,6 +10,8 @@ cudaError_t tc_launch_f16(bool pair, Producer prod, const TcLaunch& L) {
     return tc_launch_impl<InKind::F16, __half>(pair, prod, L);
 }
 
-TcGeometry tc_geometry_f16(bool pair) { return tc_geometry_impl<InKind::F16>(pair); }
+TcGeometry tc_geometry_f16(bool pair, bool half) {
+    return tc_geometry_impl<InKind::F16>(pair, half);
+}
 
 }  // namespace gb300

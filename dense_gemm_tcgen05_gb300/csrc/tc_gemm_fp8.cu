@@ -12,6 +12,8 @@ cudaError_t tc_launch_fp8(bool pair, Producer prod, bool out_f32, const TcLaunch
                    : tc_launch_impl<InKind::E4M3, __nv_bfloat16>(pair, prod, L);
 }
 
-TcGeometry tc_geometry_fp8(bool pair) { return tc_geometry_impl<InKind::E4M3>(pair); }
+TcGeometry tc_geometry_fp8(bool pair, bool half) {
+    return tc_geometry_impl<InKind::E4M3>(pair, half);
+}
 
 }  // namespace gb300

@@ -204,7 +204,12 @@ int gemm_read_watchdog(int reset);
  *   "timeout_ns"  device wait limit in ns, 1e6..6e10 (default 2e9)
  *   "max_ctas"    cap on persistent CTAs, 0 = one per SM (default)
  *   "tile_q"      output tile width along M (= MMA N): 0 auto (default, by
- *                 padding cost), or 64, 128, 192, 256
+ *                 padding cost; 16 or 32 when all of M fits in one such tile and
+ *                 single-CTA tiles run), or 16, 32, 64, 128, 192, 256 (16 and 32
+ *                 only apply when M fits in one tile and CTAs do not pair; else 64)
+ *   "half"        64-row tiles (one CTA per 64 rows of N, MMA M = 64): 0 or 2
+ *                 never (default), 1 wherever single-CTA TMA tiles with FP32
+ *                 accumulation run; they never split K
  *   "tail"        the last, partial wave of tiles: 0 auto (default) cuts its tiles
  *                 into 2 or 4 narrower ones when that ends it sooner, 1 never, 2 or
  *                 4 always
