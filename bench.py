@@ -43,6 +43,7 @@ PAGES_FP16_8192_TFLOPS = 142.30
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 SETS = 3
+WORKSPACE_BYTES = 1 << 30   # the library workspace the bench registers (1 GiB)
 
 
 # ---------------------------------------------------------------- helpers
@@ -332,8 +333,8 @@ def f32_bench(n, steps, warmup, stream, stream_h):
 
 def f32_bf16x6_bench(n, steps, warmup, stream, stream_h):
     """gemm_f32_bf16x6 on the FP32 leg's operands (U[-1,1], seed 1), with the
-    workspace it needs registered; returns the mean per-call ms (two split
-    launches and the GEMM)."""
+    splits in the bench's registered workspace; returns the mean per-call ms
+    (two split launches and the GEMM)."""
     import torch
 
     import synthetic_inputs as si
@@ -342,9 +343,8 @@ def f32_bf16x6_bench(n, steps, warmup, stream, stream_h):
     ops = si.f32_operands(n, n, n, dist="uniform", seed=1)
     sets = [(ops["A"].cuda(), ops["B"].cuda(), torch.empty((n, n), device="cuda"))
             for _ in range(SETS)]
-    need = capi.gemm_f32_bf16x6_workspace_bytes(n, n, n)
-    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
-    assert capi.gemm_set_workspace(ws.data_ptr(), need) == 0
+    # the bench's registered workspace holds the splits
+    assert capi.gemm_f32_bf16x6_workspace_bytes(n, n, n) <= WORKSPACE_BYTES
 
     def call(a, b, c):
         st = capi.gemm_f32_bf16x6(n, n, n, a.data_ptr(), n, b.data_ptr(), n, c.data_ptr(), n,
@@ -352,12 +352,8 @@ def f32_bf16x6_bench(n, steps, warmup, stream, stream_h):
         if st != 0:
             raise RuntimeError(capi.status_text(st))
 
-    try:
-        with torch.cuda.stream(stream):
-            total, launch = timed_loop(call, sets, steps, warmup, stream)
-    finally:
-        torch.cuda.synchronize()
-        capi.gemm_set_workspace(None, 0)
+    with torch.cuda.stream(stream):
+        total, launch = timed_loop(call, sets, steps, warmup, stream)
     return launch
 
 
@@ -447,6 +443,13 @@ def run_ours(args):
                                 FALLBACK_PEAKS["bf16_tflops_sustained"]))
     stream = torch.cuda.Stream()
     stream_h = stream.cuda_stream
+    # The library's recommended setup: one caller-owned workspace, registered
+    # once (split-K for shapes that cannot fill the GPU, a last wave cut into K
+    # pieces for long tiles, and the FP32 tensor-core leg's operand splits).
+    from dense_gemm_tcgen05_gb300 import capi as _capi_ws
+    workspace = torch.empty(WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+    if _capi_ws.gemm_set_workspace(workspace.data_ptr(), workspace.numel()) != 0:
+        raise RuntimeError("could not register the workspace")
     M = N = K = 8192
     flops = 2.0 * M * N * K
 
@@ -524,7 +527,7 @@ def run_ours(args):
                                                               20, stream), 2)
         per["cublas_context_f16_8192"] = round(cublas_context(M, N, K, torch.float16, 20, stream), 1)
         if args.sweep:
-            per.update(sweep(stream, stream_h, burst))
+            per.update(sweep(stream, stream_h, burst, workspace))
 
         e2e_steps = max(3, min(args.steps, 20))
         e_ms, serial_ms, h2d, d2h, copy_ms = e2e_loop("f16", M, N, K, ops, e2e_steps, 2, stream,
@@ -542,6 +545,7 @@ def run_ours(args):
                        "layout": "TN: A row-major, B column-major, C column-major (ld=M)",
                        "accumulate": "f32", "values": "N(0,1)*0.1, seed 2",
                        "l2": "3 rotating input sets (1.1 GiB total) >> 129 MB L2, no flush",
+                       "workspace_bytes": WORKSPACE_BYTES,
                        "parallelism": "replicas" if world > 1 else "single",
                        "pages_context": "best FP16 8192^3 on the pages: 142.30 TFLOP/s (RX 9070 "
                                         "XT, FP16 accumulation); compare per_dtype."
@@ -579,11 +583,17 @@ def run_ours(args):
     return result
 
 
-def sweep(stream, stream_h, burst):
-    """The BF16 and FP8 shape sweeps (configs 4 and 5), one line each."""
+def sweep(stream, stream_h, burst, workspace):
+    """The BF16 and FP8 shape sweeps (configs 4 and 5), one line each.  The
+    first part runs without a registered workspace (the odd shapes' tight
+    leading dimensions then take the load-based producer); the rest, and
+    whatever follows, with the bench's `workspace` registered."""
     import torch
 
+    from dense_gemm_tcgen05_gb300 import capi
+
     out = {}
+    capi.gemm_set_workspace(None, 0)
     # BF16 and FP8 configurations (tight leading dimensions: the odd shapes take
     # the load-based producer), then the pages' transformer shapes -- FP16 on
     # the FP16 page's wide shape, FP8 with FP32 output as the FP8 page measures.
@@ -608,41 +618,36 @@ def sweep(stream, stream_h, burst):
         del s
         torch.cuda.empty_cache()
     # Skinny and small shapes: HBM-bound, reported in GB/s of compulsory
-    # traffic against the measured copy bandwidth, with a split-K workspace.
-    from dense_gemm_tcgen05_gb300 import capi
-
+    # traffic against the measured copy bandwidth, with the workspace again.
     peaks, _ = load_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    ws = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
-    capi.gemm_set_workspace(ws.data_ptr(), ws.numel())
-    try:
-        # the tight-leading-dimension BF16 configurations again, now repacked
-        for kind, (M, N, K) in [("bf16", (2047, 3001, 1023)), ("bf16", (8191, 8191, 8191))]:
-            o, s = tn_sets(kind, M, N, K, seed=3, sigma=0.05, nsets=SETS, device="cuda")
-            c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h)
-            with torch.cuda.stream(stream):
-                _, lm = timed_loop(c, s, 20, 3, stream)
-            tf = 2.0 * M * N * K / (lm * 1e-3) / 1e12
-            out["%s_%dx%dx%d_ws" % (kind, M, N, K)] = {"tflops": round(tf, 1),
-                                                       "frac": round(tf / burst, 4)}
-            del s
-            torch.cuda.empty_cache()
-        for kind, (M, N, K) in [("bf16", (16, 8192, 8192)), ("bf16", (128, 8192, 8192)),
-                                ("bf16", (64, 14336, 4096)), ("bf16", (1024, 1024, 8192)),
-                                ("e4m3", (128, 8192, 8192))]:
-            o, s = tn_sets(kind, M, N, K, seed=3, sigma=0.05, nsets=SETS, device="cuda")
-            c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h)
-            with torch.cuda.stream(stream):
-                _, lm = timed_loop(c, s, 30, 3, stream)
-            es = 1 if kind == "e4m3" else 2
-            gbs = ((M * K + N * K) * es + M * N * 2) / (lm * 1e-3) / 1e9
-            out["%s_skinny_%dx%dx%d" % (kind, M, N, K)] = {
-                "tflops": round(2.0 * M * N * K / (lm * 1e-3) / 1e12, 1), "gbs": round(gbs),
-                "hbm_frac": round(gbs / hbm, 3), "us": round(lm * 1e3, 1)}
-            del s
-            torch.cuda.empty_cache()
-    finally:
-        capi.gemm_set_workspace(None, 0)
+    if capi.gemm_set_workspace(workspace.data_ptr(), workspace.numel()) != 0:
+        raise RuntimeError("could not register the workspace")
+    # the tight-leading-dimension BF16 configurations again, now repacked
+    for kind, (M, N, K) in [("bf16", (2047, 3001, 1023)), ("bf16", (8191, 8191, 8191))]:
+        o, s = tn_sets(kind, M, N, K, seed=3, sigma=0.05, nsets=SETS, device="cuda")
+        c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h)
+        with torch.cuda.stream(stream):
+            _, lm = timed_loop(c, s, 20, 3, stream)
+        tf = 2.0 * M * N * K / (lm * 1e-3) / 1e12
+        out["%s_%dx%dx%d_ws" % (kind, M, N, K)] = {"tflops": round(tf, 1),
+                                                   "frac": round(tf / burst, 4)}
+        del s
+        torch.cuda.empty_cache()
+    for kind, (M, N, K) in [("bf16", (16, 8192, 8192)), ("bf16", (128, 8192, 8192)),
+                            ("bf16", (64, 14336, 4096)), ("bf16", (1024, 1024, 8192)),
+                            ("e4m3", (128, 8192, 8192))]:
+        o, s = tn_sets(kind, M, N, K, seed=3, sigma=0.05, nsets=SETS, device="cuda")
+        c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h)
+        with torch.cuda.stream(stream):
+            _, lm = timed_loop(c, s, 30, 3, stream)
+        es = 1 if kind == "e4m3" else 2
+        gbs = ((M * K + N * K) * es + M * N * 2) / (lm * 1e-3) / 1e9
+        out["%s_skinny_%dx%dx%d" % (kind, M, N, K)] = {
+            "tflops": round(2.0 * M * N * K / (lm * 1e-3) / 1e12, 1), "gbs": round(gbs),
+            "hbm_frac": round(gbs / hbm, 3), "us": round(lm * 1e3, 1)}
+        del s
+        torch.cuda.empty_cache()
     return out
 
 

@@ -464,11 +464,15 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     // number of epilogue chunks) so that it ends sooner.  Narrow units are
     // L2-bound; measured on GB300, a half-width unit takes ~0.8 of a full
     // tile's time (0.9 for FP8), a quarter-width one ~0.65 (0.8 for FP8).
-    // Option "tail_k" = f instead cuts the tail tiles into f K pieces of full
-    // width, combined through the workspace like split-K; it is not chosen
-    // automatically: the last piece's fix-up reads every other piece's partial
-    // slice with one L2 round trip per chunk and piece, which cost more than
-    // the shorter last wave saved (BF16 4096^3: 100 us against 79 us).
+    // Cutting the tail tiles into K pieces of full width instead, combined
+    // through the workspace like split-K, pays a fix-up per tile that long
+    // tiles amortise: measured at the power cap against narrowing, two pieces
+    // are 2.7 % faster at BF16 4096 x 4096 x 14336 (224 K stages), level at
+    // FP16 8192^3 (128: +0.35 % back to back, but 4 % more cycles in a single
+    // profiled launch), 1.2 % slower at BF16 4096^3 (64).  So with the tail
+    // left to the automatic rule they are taken when the tiles have at least
+    // 192 K stages and the doubled tail still fits in one wave; option
+    // "tail_k" = f forces f pieces.
     L.prm.full_units = tiles * L.prm.splits;
     L.prm.tail_f = 1;
     L.prm.idesc_tail = L.prm.idesc;
@@ -507,9 +511,11 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
                     }
                 }
             }
-            const int opt_tail_k = g_opt_tail_k.load();
-            if (opt_tail_k >= 2 && !acc16 && !L.half && ws) {
-                const int64_t kb_per = (L.prm.num_kb + opt_tail_k - 1) / opt_tail_k;
+            int want_k = g_opt_tail_k.load();
+            if (want_k == 0 && opt_tail == 0 && L.prm.num_kb >= 192 && 2 * rem <= units_slots)
+                want_k = 2;
+            if (want_k >= 2 && !acc16 && !L.half && ws) {
+                const int64_t kb_per = (L.prm.num_kb + want_k - 1) / want_k;
                 const int64_t pieces = (L.prm.num_kb + kb_per - 1) / kb_per;
                 const int64_t need = cnt_bytes + rem * pieces * slices * 32 * 256 * 4;
                 if (pieces >= 2 && need <= ws_room) {

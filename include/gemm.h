@@ -221,8 +221,10 @@ int gemm_read_watchdog(int reset);
  *                 aligned (or, for compute-heavy shapes, not 128-byte aligned) are
  *                 first copied into it with 128-byte-aligned rows; 1 never
  *   "tail_k"      0 (default), or 2..8: with a workspace, cut the last partial wave's
- *                 tiles into that many K pieces instead of narrower tiles (slower
- *                 on the shapes measured: the fix-up is L2-latency-bound)
+ *                 tiles into that many K pieces instead of narrower tiles.  With 0
+ *                 and "tail" 0 the library takes two pieces by itself when the
+ *                 tiles have at least 192 K stages (K >= 12288 for 16-bit inputs,
+ *                 24576 for e4m3) and the doubled tail still fits in one wave
  *   "cluster"     0 (default) or 2: CTA pairs as chosen above; 4: clusters of two pairs
  *                 that share B tiles through TMA multicast (TN path with TMA-aligned
  *                 operands and C, no split-K; slower or level on the shapes measured)

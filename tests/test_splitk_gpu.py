@@ -234,3 +234,30 @@ def test_more_counters_than_a_set_holds():
             _check_exact(*item)
     finally:
         assert capi.gemm_set_workspace(None, 0) == 0
+
+
+def test_automatic_k_split_tail(workspace, capfd):
+    """96 pair tiles of 256 x 256 with 192 K stages each (BF16, K = 12288): one
+    wave of 76 and a last wave of 20, which the automatic rule cuts into two K
+    pieces per tile (20 x 2 units still fit in one wave).  With "tail" = 2 the
+    last wave is narrowed instead; both exact."""
+    import os
+    M, N, K = 2048, 3072, 12288
+    ops = si.tn_operands("bf16", M, N, K, dist="pm1", seed=81)
+    exact = exact_codes("bf16", oracle.gemm_tn("bf16", M, N, K, si.codes(ops["A"]), K,
+                                               si.codes(ops["B"]), K))
+    lines = {}
+    os.environ["GEMM_DEBUG"] = "1"
+    try:
+        for tail in (0, 2):
+            assert capi.gemm_set_option("tail", tail) == 0
+            capfd.readouterr()
+            C = run_tn("bf16", ops, M, N, K)
+            lines[tail] = [ln for ln in capfd.readouterr().err.splitlines()
+                           if ln.startswith("[gemm] tn")][-1]
+            assert_codes_equal(out_codes(C, M, N), exact)
+    finally:
+        del os.environ["GEMM_DEBUG"]
+        capi.gemm_set_option("tail", 0)
+    assert "ktail=1" in lines[0] and "tail=2" in lines[0], lines[0]
+    assert "ktail=0" in lines[2] and "tail=2" in lines[2], lines[2]
