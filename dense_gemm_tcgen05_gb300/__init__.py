@@ -20,7 +20,7 @@ import torch
 from . import capi
 from .capi import GemmError  # noqa: F401
 
-__all__ = ["tn", "f32", "capi", "GemmError", "stream_handle"]
+__all__ = ["tn", "f32", "f32_bf16x6", "register_workspace", "capi", "GemmError", "stream_handle"]
 
 _TN_DTYPES = {
     torch.float16: ("gemm_f16_tn", torch.float16),
@@ -103,3 +103,40 @@ def f32(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
     if st != capi.GEMM_OK:
         raise GemmError(st, "gemm_f32")
     return out
+
+
+def f32_bf16x6(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """The FP32 product of ``f32`` on the tensor cores (gemm_f32_bf16x6): exact
+    three-way BF16 splits of A and B, six piece products summed in FP32.  Needs
+    a registered workspace of at least gemm_f32_bf16x6_workspace_bytes(M, N, K)
+    (see ``register_workspace``)."""
+    if a.dtype != torch.float32 or b.dtype != torch.float32:
+        raise TypeError("a and b must be float32")
+    _check_2d(a, "a")
+    _check_2d(b, "b")
+    M, K = a.shape
+    Kb, N = b.shape
+    if K != Kb:
+        raise ValueError("K mismatch")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    _check_2d(out, "out")
+    st = capi.gemm_f32_bf16x6(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b),
+                              out.data_ptr(), _ld(out), stream_handle(stream))
+    if st != capi.GEMM_OK:
+        raise GemmError(st, "gemm_f32_bf16x6")
+    return out
+
+
+def register_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """Allocates ``nbytes`` of device memory and registers it as the library's
+    workspace for that device (gemm_set_workspace).  Returns the buffer: the
+    caller keeps it alive for as long as calls may use it, and registers
+    ``None`` (``capi.gemm_set_workspace(None, 0)``) before freeing it."""
+    buf = torch.empty(int(nbytes), dtype=torch.uint8, device=device or "cuda")
+    with torch.cuda.device(buf.device):
+        st = capi.gemm_set_workspace(buf.data_ptr(), buf.numel())
+    if st != capi.GEMM_OK:
+        raise GemmError(st, "gemm_set_workspace")
+    return buf
