@@ -91,8 +91,8 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const
  * shapes with few output tiles split K as the TN calls do (up to
  * gemm_workspace_bytes(N, M, 6 * Kp) more, Kp = K rounded up to a multiple of
  * 64).  The workspace is in use until the call's work on `stream` has ended.
- * Launches: two split kernels, then the tensor-core GEMM (a zeroing memset
- * before it when K is split).
+ * Launches: two split kernels, then the tensor-core GEMM (the split counters
+ * in the workspace need no memset; see gemm_set_workspace).
  */
 int gemm_f32_bf16x6(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
                     int64_t ldb, float* C, int64_t ldc, void* stream);
