@@ -88,7 +88,8 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const
  * gemm_set_workspace for the current device.  The call needs at least
  * gemm_f32_bf16x6_workspace_bytes(M, N, K) bytes there and returns
  * GEMM_ERR_WORKSPACE, launching nothing, without them.  Bytes beyond that let
- * shapes with few output tiles split K as the TN calls do (up to
+ * shapes with few output tiles split K, and long tiles cut their last wave
+ * into K pieces, as the TN calls do (up to
  * gemm_workspace_bytes(N, M, 6 * Kp) more, Kp = K rounded up to a multiple of
  * 64).  The workspace is in use until the call's work on `stream` has ended.
  * Launches: two split kernels, then the tensor-core GEMM (the split counters
