@@ -154,6 +154,286 @@ int choose_tile_q(int64_t M, int max_tile_q) {
 constexpr int64_t kMaxDim = 0x7fffffffLL;
 constexpr int kMcStageRegion = 200 * 1024;  // ring of the multicast kernel (tc_gemm_mc.cuh)
 
+// What a TN call is given, for planning: shapes, what TMA can address, the
+// scratch available, and the device.
+struct TnPlanIn {
+    InKind in;
+    bool out_f32, acc16;
+    int64_t M, N, K;
+    bool a_tma, b_tma, c_tma;   // rows TMA can address (16-byte bases and pitches)
+    bool a_al128, b_al128;      // rows starting on 128-byte boundaries
+    bool has_scratch;           // a registered workspace or an override
+    int64_t ws_total;           // its bytes for repacks and partial sums
+    int ov_splits;              // -1: option "splits" applies; else the override's value
+    bool strict;                // a chosen split that does not fit fails
+    int sms;                    // SMs of the device
+    int mc_clusters;            // resident clusters of four of the multicast kernel
+};
+
+// Everything gemm_tn decides before it encodes tensor maps and launches.
+struct TnPlan {
+    int status = GEMM_OK;       // GEMM_ERR_SCRATCH when a strict split does not fit
+    bool copy_a = false, copy_b = false;  // repacked into the scratch
+    int64_t dp = 0;             // repacked row pitch in bytes
+    int64_t ws_used = 0;        // scratch bytes taken by the repacks
+    Producer prod = Producer::Tma;
+    bool pair = false, half = false, mc = false;
+    int tile_q = 0, load_q = 0;
+    TcGeometry g{};
+    int64_t tiles_p = 0, tiles_q = 0, tiles = 0, slots = 0;
+    int num_kb = 0, stages = 0, stage_bytes = 0;
+    int splits = 1, kb_per_split = 0;
+    int64_t split_cnt_bytes = 0;  // counter bytes ahead of the split partials
+    int tail_f = 1, tail_kb_per = 0;
+    bool tail_ksplit = false;
+    int64_t full_units = 0;
+    int64_t tail_cnt_bytes = 0;   // counter bytes ahead of the K-split tail's partials
+    int grid = 0;
+};
+
+// The planning half of gemm_tn: a pure function of its input and the
+// process-wide options, so that the rules can be checked without a GPU
+// (gemm_tn_plan).  Each rule is measured on GB300; the numbers are with the
+// rules below.
+TnPlan plan_tn(const TnPlanIn& a) {
+    TnPlan p;
+    const int es = a.in == InKind::E4M3 ? 1 : 2;
+    const int os = a.out_f32 ? 4 : 2;
+    const int64_t M = a.M, N = a.N, K = a.K;
+    bool a_tma = a.a_tma, b_tma = a.b_tma;
+
+    // Operands whose rows TMA cannot address are copied once into the scratch
+    // with 128-byte-aligned rows (one pass at memory speed), after which the
+    // TMA path runs at full rate; without room for that, the load-based
+    // producer reads them in place.  Rows TMA can address but that do not start
+    // on 128-byte boundaries make every 128-byte row segment of a box straddle
+    // two cache lines, which measured on GB300 costs 20-45 % (BF16 4096^3 with
+    // ld = 4104: 107 against 80 us; FP16 8192^3 with ld = 8200: 786 against
+    // 575-646 us).  They are copied too when the product is compute-heavy
+    // enough for the copy (2 (M + N) K element bytes at ~5.8 TB/s) to cost
+    // clearly less: MN / (M + N) >= 1100 x element size.  Measured with the
+    // copy: 6144^3 383 -> 319-358 us, 8192^3 786 -> 662-703 us, 16384^3 6652 ->
+    // 5763-5804 us; at 4096^3 the copy (22 us) and the penalty (27 us) cancel.
+    const bool heavy = static_cast<double>(M) * static_cast<double>(N) /
+                           static_cast<double>(M + N) >= 1100.0 * es;
+    const bool copy_a = !a_tma || (heavy && !a.a_al128);
+    const bool copy_b = !b_tma || (heavy && !a.b_al128);
+    if ((copy_a || copy_b) && g_opt_path.load() == 0 && g_opt_repack.load() == 0 &&
+        a.has_scratch) {
+        const int64_t rb = K * es;                       // row bytes
+        const int64_t dp = (rb + 127) / 128 * 128;       // aligned pitch
+        const int64_t need_a = copy_a ? (M * dp + 255) / 256 * 256 : 0;
+        const int64_t need_b = copy_b ? (N * dp + 255) / 256 * 256 : 0;
+        if (need_a + need_b <= a.ws_total) {
+            p.copy_a = copy_a;
+            p.copy_b = copy_b;
+            p.dp = dp;
+            if (copy_a) a_tma = true;
+            if (copy_b) b_tma = true;
+            p.ws_used = need_a + need_b;
+        }
+    }
+    const bool ab_tma = a_tma && b_tma;
+    p.prod = (ab_tma && g_opt_path.load() != 2) ? Producer::Tma : Producer::Loads;
+    const int opt_pair = g_opt_pair.load();
+    // cta_group::2 pairs measured faster on every shape with at least a wave
+    // of tiles; they need TMA.  When the pair tiles (256 rows of N each) fill
+    // less than one wave but single-CTA tiles of 128 rows of N by `small_q`
+    // columns of M (16 or 32 when M fits, 64 for M <= 128, else 128) still fit
+    // in one, the smaller tiles run instead: up to four times the tiles in
+    // flight.  Measured on GB300 against pairs: BF16 M x N x K = 16..128 x 8192
+    // x 8192 5-7 % faster, 128 x 8192 x 2048 31 %, 256 x 8192 x 8192 17 %,
+    // 1024 x 1024 x 8192 21 % (FP8 45 %), 1024 x 2048 x 4096 30 %; where the
+    // small tiles would need a second wave (512 x 8192 x 8192, 2048^3) pairs
+    // stay 10-26 % faster.
+    p.pair = p.prod == Producer::Tma && opt_pair != 0;
+    int small_q = 0;
+    if (p.pair && opt_pair < 0) {
+        const int64_t pair_tiles = ((N + 255) / 256) * ((M + choose_tile_q(M, 256) - 1) /
+                                                        choose_tile_q(M, 256));
+        const int q = M <= 16 ? 16 : M <= 32 ? 32 : M <= 128 ? 64 : 128;
+        const int64_t small_tiles = ((N + 127) / 128) * ((M + q - 1) / q);
+        if (pair_tiles < a.sms / 2 && small_tiles <= a.sms) {
+            p.pair = false;
+            small_q = q;
+        }
+    }
+    p.g = tc_geometry(a.in, p.pair);
+    // Tiles narrower than the epilogue's 64-column chunk (16 or 32 columns, MMA
+    // N = 16 / 32) leave room in each ring stage for more of P; they are used
+    // only when M fits in one of them, so that the rest of a chunk lies past M
+    // (the TMA store clips it), and never for CTA pairs.
+    const int opt_tq = g_opt_tile_q.load();
+    {
+        const int t = opt_tq ? opt_tq : small_q ? small_q : choose_tile_q(M, p.g.max_tile_q);
+        p.tile_q = t < 64 && (p.pair || M > t) ? 64 : t;
+    }
+    // 64-row tiles (one CTA each, MMA M = 64), option "half" = 1: they cover
+    // N with twice as many CTAs without cutting K.  Measured on GB300 they have
+    // not beaten 128-row tiles with K split in two on any skinny shape (BF16
+    // 16 x 8192 x 8192: 31.1 against 27.5 us; 16 x 4096 x 8192: 29.7 against
+    // 17.4 us), so they run only when forced, and only for one-CTA TMA tiles
+    // with FP32 accumulation.
+    p.half = g_opt_half.load() == 1 && !p.pair && p.prod == Producer::Tma && !a.acc16;
+    if (p.half) p.g = tc_geometry(a.in, false, true);
+    const TcGeometry& g = p.g;
+    p.load_q = p.tile_q / g.cluster;
+    p.tiles_p = (N + g.tile_p - 1) / g.tile_p;
+    p.tiles_q = (M + p.tile_q - 1) / p.tile_q;
+    p.tiles = p.tiles_p * p.tiles_q;
+    p.slots = a.sms / g.cluster;
+    const int cap = g_opt_max_ctas.load();
+    if (cap > 0 && cap / g.cluster < p.slots) p.slots = cap / g.cluster > 0 ? cap / g.cluster : 1;
+    const int64_t tiles = p.tiles, slots = p.slots;
+    p.grid = static_cast<int>((tiles < slots ? tiles : slots) * g.cluster);
+    p.num_kb = static_cast<int>((K + g.stage_k - 1) / g.stage_k);
+    // Ring: as many stages of this width as the stage region holds (narrow
+    // tiles get a deeper ring, i.e. more loads in flight).  The load-based
+    // producer's row split assumes the full-width stage.
+    {
+        const int max_q = g.max_tile_q / g.cluster;
+        const int rows = g.load_p + (p.prod == Producer::Loads ? max_q : p.load_q);
+        const int sb = (rows * 128 + 1023) / 1024 * 1024;
+        int st_count = g.stage_region / sb;
+        if (st_count > g.max_stages) st_count = g.max_stages;
+        p.stages = st_count;
+        p.stage_bytes = sb;
+    }
+
+    // Split-K (shape-aware): when one wave of tiles cannot occupy the GPU and
+    // there is scratch, cut each tile's K range into pieces so that tiles x
+    // pieces fills the SMs; each piece still runs >= 4 K stages.  FP16
+    // accumulation (combining pieces would add FP32 sums) and 64-row tiles
+    // never split K.
+    p.kb_per_split = p.num_kb;
+    {
+        const int opt = (a.acc16 || p.half) ? 1 : (a.ov_splits >= 0 ? a.ov_splits
+                                                                     : g_opt_splits.load());
+        int64_t want = 1;
+        if (opt >= 2) {
+            want = opt;
+        } else if (opt == 0 && tiles < slots) {
+            want = slots / tiles;
+            const int64_t by_k = p.num_kb / 4;
+            if (want > by_k) want = by_k;
+            if (want > 16) want = 16;
+        }
+        if (want > p.num_kb) want = p.num_kb;
+        if (want >= 2) {
+            const int64_t kb_per = (p.num_kb + want - 1) / want;
+            const int64_t pieces = (p.num_kb + kb_per - 1) / kb_per;
+            const int64_t slices = 4 * g.cluster;                    // 32-row slices per tile
+            const int64_t cnt_bytes = ((tiles * slices * 4 + 255) / 256) * 256;
+            const int64_t part_bytes = tiles * pieces * slices * 32 * 256 * 4;
+            const int64_t room = a.ws_total - p.ws_used;
+            if (a.strict && pieces >= 2 && cnt_bytes + part_bytes > room) {
+                p.status = GEMM_ERR_SCRATCH;
+                return p;
+            }
+            if (pieces >= 2 && a.has_scratch && cnt_bytes + part_bytes <= room) {
+                p.splits = static_cast<int>(pieces);
+                p.kb_per_split = static_cast<int>(kb_per);
+                p.split_cnt_bytes = cnt_bytes;
+                const int64_t units = tiles * pieces;
+                p.grid = static_cast<int>((units < slots ? units : slots) * g.cluster);
+            }
+        }
+    }
+    // Tail splitting: when the last wave of tiles is partial, cut its tiles
+    // into f narrower units along M (f = 2 or 4, tile_q / f still a whole
+    // number of epilogue chunks) so that it ends sooner.  Narrow units are
+    // L2-bound; measured on GB300, a half-width unit takes ~0.8 of a full
+    // tile's time (0.9 for FP8), a quarter-width one ~0.65 (0.8 for FP8).
+    // Cutting the tail tiles into K pieces of full width instead, combined
+    // through the workspace like split-K, pays a fix-up per tile that long
+    // tiles amortise: measured at the power cap against narrowing, two pieces
+    // are 2.7 % faster at BF16 4096 x 4096 x 14336 (224 K stages), level at
+    // FP16 8192^3 (128: +0.35 % back to back, but 4 % more cycles in a single
+    // profiled launch), 1.2 % slower at BF16 4096^3 (64).  So with the tail
+    // left to the automatic rule they are taken when the tiles have at least
+    // 192 K stages and the doubled tail still fits in one wave; option
+    // "tail_k" = f forces f pieces.
+    p.full_units = tiles * p.splits;
+    p.tail_kb_per = p.num_kb;
+    {
+        const int opt_tail = g_opt_tail.load();
+        const int64_t waves = tiles / slots, rem = tiles % slots;
+        const int min_w = 128 / os;  // one epilogue chunk
+        const int64_t slices = 4 * g.cluster;
+        const int64_t cnt_bytes = ((rem * slices * 4 + 255) / 256) * 256;
+        const int64_t room = a.ws_total - p.ws_used;
+        int f = 1;
+        bool ksplit = false;
+        int64_t kb_per_t = p.num_kb;
+        auto narrow_ok = [&](int c) {
+            return p.tile_q % c == 0 && (p.tile_q / c) % min_w == 0 && p.tile_q / c >= 64;
+        };
+        if (p.splits == 1 && rem > 0 && opt_tail != 1) {
+            if (opt_tail == 2 || opt_tail == 4) {
+                f = narrow_ok(opt_tail) ? opt_tail : 1;
+            } else {
+                const bool fp8 = a.in == InKind::E4M3;
+                double best = 1.0;
+                for (int cand : {2, 4}) {
+                    if (!narrow_ok(cand)) continue;
+                    const double unit_cost = cand == 2 ? (fp8 ? 0.9 : 0.8) : (fp8 ? 0.8 : 0.65);
+                    const double t =
+                        static_cast<double>((cand * rem + slots - 1) / slots) * unit_cost;
+                    if (t < best - 0.02) {
+                        best = t;
+                        f = cand;
+                    }
+                }
+            }
+            int want_k = g_opt_tail_k.load();
+            if (want_k == 0 && opt_tail == 0 && p.num_kb >= 192 && 2 * rem <= slots) want_k = 2;
+            if (want_k >= 2 && !a.acc16 && !p.half && a.has_scratch) {
+                const int64_t kb_per = (p.num_kb + want_k - 1) / want_k;
+                const int64_t pieces = (p.num_kb + kb_per - 1) / kb_per;
+                const int64_t need = cnt_bytes + rem * pieces * slices * 32 * 256 * 4;
+                if (pieces >= 2 && need <= room) {
+                    f = static_cast<int>(pieces);
+                    ksplit = true;
+                    kb_per_t = kb_per;
+                }
+            }
+        }
+        if (f > 1) {
+            p.tail_f = f;
+            p.tail_ksplit = ksplit;
+            p.full_units = waves * slots;
+            if (ksplit) {
+                p.tail_kb_per = static_cast<int>(kb_per_t);
+                p.tail_cnt_bytes = cnt_bytes;
+            }
+            const int64_t units = p.full_units + (tiles - p.full_units) * f;
+            p.grid = static_cast<int>((units < slots ? units : slots) * g.cluster);
+        }
+    }
+    // Clusters of two pairs sharing P tiles through TMA multicast
+    // (tc_gemm_mc.cuh), option "cluster" = 4: only for pair tiles without
+    // split-K, tail splitting, FP16 accumulation or row-wise stores.
+    const int opt_cl = g_opt_cluster.load();
+    if (p.pair && p.prod == Producer::Tma && a.c_tma && !a.acc16 && p.splits == 1 &&
+        opt_cl == 4 && (a.in == InKind::E4M3 || !a.out_f32) && a.mc_clusters > 0) {
+        p.mc = true;
+        // the multicast kernel's ring: 200 KB of stages of this width
+        const int sb = ((g.load_p + p.load_q) * 128 + 1023) / 1024 * 1024;
+        int st_count = kMcStageRegion / sb;
+        if (st_count > g.max_stages) st_count = g.max_stages;
+        p.stages = st_count;
+        p.stage_bytes = sb;
+        p.tail_f = 1;
+        p.tail_ksplit = false;
+        p.full_units = tiles;
+        const int64_t units = p.tiles_p * ((p.tiles_q + 1) / 2);
+        int64_t clusters = units < a.mc_clusters ? units : a.mc_clusters;
+        if (cap > 0 && cap / 4 < clusters) clusters = cap / 4 > 0 ? cap / 4 : 1;
+        p.grid = static_cast<int>(clusters * 4);
+    }
+    return p;
+}
+
 // 2D tensor map over a matrix with `outer` rows of `inner` contiguous elements
 // and a row pitch of `pitch_bytes`, copied in boxes of box_inner x box_outer
 // with 128-byte swizzling and zero fill outside the matrix.
@@ -263,77 +543,56 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
         prm.clear_words = 0;
         return cudaMemsetAsync(fallback, 0, static_cast<size_t>(fallback_bytes), stream);
     };
-    int64_t ws_used = 0;  // bytes at the start of the scratch taken by repacked operands
+    // Plan the call (pure: shapes, alignment, scratch, options, device), then
+    // carry it out.
+    TnPlanIn pin;
+    pin.in = in;
+    pin.out_f32 = out_f32;
+    pin.acc16 = acc16;
+    pin.M = M;
+    pin.N = N;
+    pin.K = K;
+    pin.a_tma = a_tma;
+    pin.b_tma = b_tma;
+    pin.c_tma = c_tma;
+    pin.a_al128 = aligned(A, 128) && (lda * es) % 128 == 0;
+    pin.b_al128 = aligned(B, 128) && (ldb * es) % 128 == 0;
+    pin.has_scratch = ws_base != nullptr;
+    pin.ws_total = ws_base ? ws_total : 0;
+    pin.ov_splits = ov ? ov->splits : -1;
+    pin.strict = ov && ov->strict;
+    pin.sms = dev->sms;
+    pin.mc_clusters = 0;
+    if (g_opt_cluster.load() == 4 && (in == InKind::E4M3 || !out_f32)) {
+        e = mc_max_clusters(in, out_f32, dev, &pin.mc_clusters);
+        if (e != cudaSuccess) return fail_cuda(e);
+    }
+    const TnPlan pl = plan_tn(pin);
+    if (pl.status != GEMM_OK) return pl.status;
 
-    // Operands whose rows TMA cannot address are copied once into the scratch
-    // with 128-byte-aligned rows (one pass at memory speed), after which the
-    // TMA path runs at full rate; without room for that, the load-based
-    // producer reads them in place.  Rows TMA can address but that do not start
-    // on 128-byte boundaries make every 128-byte row segment of a box straddle
-    // two cache lines, which measured on GB300 costs 20-45 % (BF16 4096^3 with
-    // ld = 4104: 107 against 80 us; FP16 8192^3 with ld = 8200: 786 against
-    // 575-646 us).  They are copied too when the product is compute-heavy
-    // enough for the copy (2 (M + N) K element bytes at ~5.8 TB/s) to cost
-    // clearly less: MN / (M + N) >= 1100 x element size.  Measured with the
-    // copy: 6144^3 383 -> 319-358 us, 8192^3 786 -> 662-703 us, 16384^3 6652 ->
-    // 5763-5804 us; at 4096^3 the copy (22 us) and the penalty (27 us) cancel.
-    auto al128 = [&](const void* p, int64_t ld) {
-        return aligned(p, 128) && (ld * es) % 128 == 0;
-    };
-    const bool heavy = static_cast<double>(M) * static_cast<double>(N) /
-                           static_cast<double>(M + N) >= 1100.0 * es;
-    const bool copy_a = !a_tma || (heavy && !al128(A, lda));
-    const bool copy_b = !b_tma || (heavy && !al128(B, ldb));
-    if ((copy_a || copy_b) && g_opt_path.load() == 0 && g_opt_repack.load() == 0 && ws_base) {
-        const int64_t rb = K * es;                       // row bytes
-        const int64_t dp = (rb + 127) / 128 * 128;       // aligned pitch
-        const int64_t need_a = copy_a ? (M * dp + 255) / 256 * 256 : 0;
-        const int64_t need_b = copy_b ? (N * dp + 255) / 256 * 256 : 0;
-        if (need_a + need_b <= ws_total) {
-            if (copy_a) {
-                e = repack_rows_launch(A, lda * es, ws_base, dp, M, rb, stream);
-                if (e != cudaSuccess) return fail_cuda(e);
-                A = ws_base;
-                lda = dp / es;
-                a_tma = true;
-            }
-            if (copy_b) {
-                e = repack_rows_launch(B, ldb * es, ws_base + need_a, dp, N, rb, stream);
-                if (e != cudaSuccess) return fail_cuda(e);
-                B = ws_base + need_a;
-                ldb = dp / es;
-                b_tma = true;
-            }
-            ws_used = need_a + need_b;
+    // Repacks into the scratch: 128-byte-aligned rows of pitch pl.dp.
+    if (pl.copy_a || pl.copy_b) {
+        const int64_t rb = K * es;  // row bytes
+        const int64_t need_a = pl.copy_a ? (M * pl.dp + 255) / 256 * 256 : 0;
+        if (pl.copy_a) {
+            e = repack_rows_launch(A, lda * es, ws_base, pl.dp, M, rb, stream);
+            if (e != cudaSuccess) return fail_cuda(e);
+            A = ws_base;
+            lda = pl.dp / es;
+        }
+        if (pl.copy_b) {
+            e = repack_rows_launch(B, ldb * es, ws_base + need_a, pl.dp, N, rb, stream);
+            if (e != cudaSuccess) return fail_cuda(e);
+            B = ws_base + need_a;
+            ldb = pl.dp / es;
         }
     }
-    const bool ab_tma = a_tma && b_tma;
-    const Producer prod = (ab_tma && g_opt_path.load() != 2) ? Producer::Tma : Producer::Loads;
-    const int opt_pair = g_opt_pair.load();
-    // cta_group::2 pairs measured faster on every shape with at least a wave
-    // of tiles; they need TMA.  When the pair tiles (256 rows of N each) fill
-    // less than one wave but single-CTA tiles of 128 rows of N by `small_q`
-    // columns of M (64 for M <= 128, else 128) still fit in one, the smaller
-    // tiles run instead: up to four times the tiles in flight.  Measured on
-    // GB300 against pairs: BF16 M x N x K = 16..128 x 8192 x 8192 5-7 %
-    // faster, 128 x 8192 x 2048 31 %, 256 x 8192 x 8192 17 %, 1024 x 1024 x 8192
-    // 21 % (FP8 45 %), 1024 x 2048 x 4096 30 %; where the small tiles would need
-    // a second wave (512 x 8192 x 8192, 2048^3) pairs stay 10-26 % faster.
-    bool pair = prod == Producer::Tma && opt_pair != 0;
-    int small_q = 0;
-    if (pair && opt_pair < 0) {
-        const int64_t pair_tiles = ((N + 255) / 256) * ((M + choose_tile_q(M, 256) - 1) /
-                                                        choose_tile_q(M, 256));
-        const int q = M <= 16 ? 16 : M <= 32 ? 32 : M <= 128 ? 64 : 128;
-        const int64_t small_tiles = ((N + 127) / 128) * ((M + q - 1) / q);
-        if (pair_tiles < dev->sms / 2 && small_tiles <= dev->sms) {
-            pair = false;
-            small_q = q;
-        }
-    }
-    TcGeometry g = tc_geometry(in, pair);
+    const Producer prod = pl.prod;
+    const bool pair = pl.pair;
+    const TcGeometry& g = pl.g;
     TcLaunch L;
     std::memset(&L, 0, sizeof(L));
+    L.half = pl.half;
     const CUtensorMapDataType in_dt = in == InKind::F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                       : in == InKind::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                            : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -341,27 +600,12 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
                                        : in == InKind::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     // P = B: N rows of K contiguous elements.  Q = A: M rows of K.  Out = C: N rows of M.
-    // Tiles narrower than the epilogue's 64-column chunk (16 or 32 columns, MMA
-    // N = 16 / 32) leave room in each ring stage for more of P; they are used
-    // only when M fits in one of them, so that the rest of a chunk lies past M
-    // (the TMA store clips it), and never for CTA pairs.
-    const int opt_tq = g_opt_tile_q.load();
-    const int tile_q = [&] {
-        const int t = opt_tq ? opt_tq : small_q ? small_q : choose_tile_q(M, g.max_tile_q);
-        return t < 64 && (pair || M > t) ? 64 : t;
-    }();
-    // 64-row tiles (one CTA each, MMA M = 64), option "half" = 1: they cover
-    // N with twice as many CTAs without cutting K.  Measured on GB300 they have
-    // not beaten 128-row tiles with K split in two on any skinny shape (BF16
-    // 16 x 8192 x 8192: 31.1 against 27.5 us; 16 x 4096 x 8192: 29.7 against
-    // 17.4 us), so they run only when forced, and only for one-CTA TMA tiles
-    // with FP32 accumulation.
-    L.half = g_opt_half.load() == 1 && !pair && prod == Producer::Tma && !acc16;
-    if (L.half) g = tc_geometry(in, false, true);
-    const int load_q = tile_q / g.cluster;
+    const int tile_q = pl.tile_q, load_q = pl.load_q;
     CUresult r = CUDA_SUCCESS;
     if (prod == Producer::Tma) {
-        r = encode_2d(&L.map_p, in_dt, B, K, N, ldb * es, g.stage_k, g.load_p);
+        // the multicast kernel loads half of each pair's P block per CTA
+        r = encode_2d(&L.map_p, in_dt, B, K, N, ldb * es, g.stage_k,
+                      pl.mc ? g.load_p / 2 : g.load_p);
         if (r == CUDA_SUCCESS)
             r = encode_2d(&L.map_q, in_dt, A, K, M, lda * es, g.stage_k, load_q);
     }
@@ -371,17 +615,10 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
         r = encode_2d(&L.map_out, out_dt, C, M, N, ldc * os, 128 / os, L.half ? 16 : 32);
     if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
 
-    const int64_t tiles_p = (N + g.tile_p - 1) / g.tile_p;
-    const int64_t tiles_q = (M + tile_q - 1) / tile_q;
-    const int64_t tiles = tiles_p * tiles_q;
-    int64_t slots = dev->sms / g.cluster;
-    const int cap = g_opt_max_ctas.load();
-    if (cap > 0 && cap / g.cluster < slots) slots = cap / g.cluster > 0 ? cap / g.cluster : 1;
-    const int64_t ctas = (tiles < slots ? tiles : slots) * g.cluster;
-
+    const int64_t tiles_p = pl.tiles_p, tiles_q = pl.tiles_q, tiles = pl.tiles;
     L.prm.rows_p = static_cast<int32_t>(N);
     L.prm.rows_q = static_cast<int32_t>(M);
-    L.prm.num_kb = static_cast<int32_t>((K + g.stage_k - 1) / g.stage_k);
+    L.prm.num_kb = pl.num_kb;
     L.prm.tiles_p = static_cast<int32_t>(tiles_p);
     L.prm.tiles_q = static_cast<int32_t>(tiles_q);
     L.prm.group = g_opt_group.load();
@@ -399,190 +636,50 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     L.prm.idesc = make_idesc(g.format, static_cast<uint32_t>(g.mma_m), static_cast<uint32_t>(tile_q),
                              d_format);
     L.prm.stage_tx_bytes = static_cast<uint32_t>((g.load_p + load_q) * 128);
-    // Ring: as many stages of this width as the stage region holds (narrow
-    // tiles get a deeper ring, i.e. more loads in flight).  The load-based
-    // producer's row split assumes the full-width stage.
-    {
-        const int max_q = g.max_tile_q / g.cluster;
-        const int rows = g.load_p + (prod == Producer::Loads ? max_q : load_q);
-        const int sb = (rows * 128 + 1023) / 1024 * 1024;
-        int st_count = g.stage_region / sb;
-        if (st_count > g.max_stages) st_count = g.max_stages;
-        L.prm.stages = st_count;
-        L.prm.stage_bytes = static_cast<uint32_t>(sb);
-    }
+    L.prm.stages = pl.stages;
+    L.prm.stage_bytes = static_cast<uint32_t>(pl.stage_bytes);
     L.prm.p_ptr = B;
     L.prm.q_ptr = A;
     L.prm.ld_p_bytes = ldb * es;
     L.prm.ld_q_bytes = lda * es;
-    L.grid = static_cast<int>(ctas);
+    L.grid = pl.grid;
     L.stream = stream;
 
-    // Split-K (shape-aware): when one wave of tiles cannot occupy the GPU and
-    // a workspace is registered, cut each tile's K range into pieces so that
-    // tiles x pieces fills the SMs; each piece still runs >= 4 K stages.
-    L.prm.splits = 1;
-    L.prm.kb_per_split = L.prm.num_kb;
-    {
-        // FP16 accumulation never splits K: combining pieces would add FP32 sums.
-        // FP16 accumulation and 64-row tiles never split K.
-        const int opt = (acc16 || L.half) ? 1 : (ov ? ov->splits : g_opt_splits.load());
-        int64_t want = 1;
-        if (opt >= 2) {
-            want = opt;
-        } else if (opt == 0 && tiles < slots) {
-            want = slots / tiles;
-            const int64_t by_k = L.prm.num_kb / 4;
-            if (want > by_k) want = by_k;
-            if (want > 16) want = 16;
-        }
-        if (want > L.prm.num_kb) want = L.prm.num_kb;
-        if (want >= 2) {
-            const int64_t kb_per = (L.prm.num_kb + want - 1) / want;
-            const int64_t pieces = (L.prm.num_kb + kb_per - 1) / kb_per;
-            const int64_t slices = 4 * g.cluster;                    // 32-row slices per tile
-            const int64_t cnt_bytes = ((tiles * slices * 4 + 255) / 256) * 256;
-            const int64_t part_bytes = tiles * pieces * slices * 32 * 256 * 4;
-            void* ws = ws_base ? ws_base + ws_used : nullptr;
-            const int64_t ws_bytes = ws_total - ws_used;
-            if (ov && ov->strict && pieces >= 2 && cnt_bytes + part_bytes > ws_bytes)
-                return GEMM_ERR_SCRATCH;
-            if (pieces >= 2 && ws && cnt_bytes + part_bytes <= ws_bytes) {
-                L.prm.splits = static_cast<int32_t>(pieces);
-                L.prm.kb_per_split = static_cast<int32_t>(kb_per);
-                L.prm.ws_partials = reinterpret_cast<float*>(static_cast<char*>(ws) + cnt_bytes);
-                e = take_counters(L.prm, tiles * slices, static_cast<char*>(ws), cnt_bytes);
-                if (e != cudaSuccess) return fail_cuda(e);
-                const int64_t units = tiles * pieces;
-                const int64_t c2 = (units < slots ? units : slots) * g.cluster;
-                L.grid = static_cast<int>(c2);
-            }
-        }
+    // Split-K: partial sums after the counters in the scratch.
+    char* ws = ws_base ? ws_base + pl.ws_used : nullptr;
+    const int64_t slices = 4 * g.cluster;  // 32-row slices per tile
+    L.prm.splits = pl.splits;
+    L.prm.kb_per_split = pl.kb_per_split;
+    if (pl.splits > 1) {
+        L.prm.ws_partials = reinterpret_cast<float*>(ws + pl.split_cnt_bytes);
+        e = take_counters(L.prm, tiles * slices, ws, pl.split_cnt_bytes);
+        if (e != cudaSuccess) return fail_cuda(e);
     }
-    // Tail splitting: when the last wave of tiles is partial, cut its tiles
-    // into f narrower units along M (f = 2 or 4, tile_q / f still a whole
-    // number of epilogue chunks) so that it ends sooner.  Narrow units are
-    // L2-bound; measured on GB300, a half-width unit takes ~0.8 of a full
-    // tile's time (0.9 for FP8), a quarter-width one ~0.65 (0.8 for FP8).
-    // Cutting the tail tiles into K pieces of full width instead, combined
-    // through the workspace like split-K, pays a fix-up per tile that long
-    // tiles amortise: measured at the power cap against narrowing, two pieces
-    // are 2.7 % faster at BF16 4096 x 4096 x 14336 (224 K stages), level at
-    // FP16 8192^3 (128: +0.35 % back to back, but 4 % more cycles in a single
-    // profiled launch), 1.2 % slower at BF16 4096^3 (64).  So with the tail
-    // left to the automatic rule they are taken when the tiles have at least
-    // 192 K stages and the doubled tail still fits in one wave; option
-    // "tail_k" = f forces f pieces.
-    L.prm.full_units = tiles * L.prm.splits;
-    L.prm.tail_f = 1;
+    // The last wave: narrower units (a tail tensor map, instruction descriptor
+    // and stage byte count of their own) or K pieces through the scratch.
+    L.prm.full_units = pl.full_units;
+    L.prm.tail_f = pl.tail_f;
     L.prm.idesc_tail = L.prm.idesc;
     L.prm.stage_tx_tail = L.prm.stage_tx_bytes;
-    L.prm.tail_ksplit = 0;
-    L.prm.tail_kb_per = L.prm.num_kb;
-    {
-        const int opt_tail = g_opt_tail.load();
-        const int64_t units_slots = slots;
-        const int64_t waves = tiles / units_slots, rem = tiles % units_slots;
-        const int min_w = 128 / os;  // one epilogue chunk
-        const int64_t slices = 4 * g.cluster;
-        const int64_t cnt_bytes = ((rem * slices * 4 + 255) / 256) * 256;
-        char* ws = ws_base ? ws_base + ws_used : nullptr;
-        const int64_t ws_room = ws_total - ws_used;
-        int f = 1;
-        bool ksplit = false;
-        int64_t kb_per_t = L.prm.num_kb;
-        auto narrow_ok = [&](int c) {
-            return tile_q % c == 0 && (tile_q / c) % min_w == 0 && tile_q / c >= 64;
-        };
-        if (L.prm.splits == 1 && rem > 0 && opt_tail != 1) {
-            if (opt_tail == 2 || opt_tail == 4) {
-                f = narrow_ok(opt_tail) ? opt_tail : 1;
-            } else {
-                const bool fp8 = in == InKind::E4M3;
-                double best = 1.0;
-                for (int cand : {2, 4}) {
-                    if (!narrow_ok(cand)) continue;
-                    const double unit_cost = cand == 2 ? (fp8 ? 0.9 : 0.8) : (fp8 ? 0.8 : 0.65);
-                    const double t = static_cast<double>((cand * rem + units_slots - 1) / units_slots) *
-                                     unit_cost;
-                    if (t < best - 0.02) {
-                        best = t;
-                        f = cand;
-                    }
-                }
-            }
-            int want_k = g_opt_tail_k.load();
-            if (want_k == 0 && opt_tail == 0 && L.prm.num_kb >= 192 && 2 * rem <= units_slots)
-                want_k = 2;
-            if (want_k >= 2 && !acc16 && !L.half && ws) {
-                const int64_t kb_per = (L.prm.num_kb + want_k - 1) / want_k;
-                const int64_t pieces = (L.prm.num_kb + kb_per - 1) / kb_per;
-                const int64_t need = cnt_bytes + rem * pieces * slices * 32 * 256 * 4;
-                if (pieces >= 2 && need <= ws_room) {
-                    f = static_cast<int>(pieces);
-                    ksplit = true;
-                    kb_per_t = kb_per;
-                }
-            }
-        }
-        if (f > 1 && ksplit) {
-            L.prm.tail_ksplit = 1;
-            L.prm.tail_f = f;
-            L.prm.tail_kb_per = static_cast<int32_t>(kb_per_t);
-            L.prm.full_units = waves * units_slots;
-            L.prm.ws_partials = reinterpret_cast<float*>(ws + cnt_bytes);
-            e = take_counters(L.prm, rem * slices, ws, cnt_bytes);
-            if (e != cudaSuccess) return fail_cuda(e);
-        } else if (f > 1) {
-            const int width = tile_q / f;
-            const int load_qt = width / g.cluster;
-            if (prod == Producer::Tma) {
-                r = encode_2d(&L.map_q_tail, in_dt, A, K, M, lda * es, g.stage_k, load_qt);
-                if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
-            }
-            L.prm.tail_f = f;
-            L.prm.full_units = waves * units_slots;
-            L.prm.idesc_tail = make_idesc(g.format, static_cast<uint32_t>(g.mma_m),
-                                          static_cast<uint32_t>(width), d_format);
-            L.prm.stage_tx_tail = static_cast<uint32_t>((g.load_p + load_qt) * 128);
-        }
-        if (f > 1) {
-            const int64_t units = L.prm.full_units + (tiles - L.prm.full_units) * f;
-            L.grid = static_cast<int>((units < slots ? units : slots) * g.cluster);
-        }
-    }
-    // Clusters of two pairs sharing P tiles through TMA multicast
-    // (tc_gemm_mc.cuh): only for pair tiles without split-K, tail splitting,
-    // FP16 accumulation or row-wise stores.  Option "cluster" = 4 forces it
-    // where it applies, 2 never; 0 (default) chooses it by the rule below.
-    const int opt_cl = g_opt_cluster.load();
-    bool mc = false;
-    if (pair && prod == Producer::Tma && c_tma && !acc16 && L.prm.splits == 1 && opt_cl != 2 &&
-        opt_cl == 4 && (in == InKind::E4M3 || !out_f32)) {
-        int max_cl = 0;
-        e = mc_max_clusters(in, out_f32, dev, &max_cl);
+    L.prm.tail_ksplit = pl.tail_ksplit ? 1 : 0;
+    L.prm.tail_kb_per = pl.tail_kb_per;
+    if (pl.tail_f > 1 && pl.tail_ksplit) {
+        const int64_t rem = tiles % pl.slots;
+        L.prm.ws_partials = reinterpret_cast<float*>(ws + pl.tail_cnt_bytes);
+        e = take_counters(L.prm, rem * slices, ws, pl.tail_cnt_bytes);
         if (e != cudaSuccess) return fail_cuda(e);
-        if (max_cl > 0) {
-            mc = true;
-            {
-                // the multicast kernel's ring: 200 KB of stages of this width
-                const int sb = ((g.load_p + load_q) * 128 + 1023) / 1024 * 1024;
-                int st_count = kMcStageRegion / sb;
-                if (st_count > g.max_stages) st_count = g.max_stages;
-                L.prm.stages = st_count;
-                L.prm.stage_bytes = static_cast<uint32_t>(sb);
-            }
-            r = encode_2d(&L.map_p, in_dt, B, K, N, ldb * es, g.stage_k, g.load_p / 2);
+    } else if (pl.tail_f > 1) {
+        const int width = tile_q / pl.tail_f;
+        const int load_qt = width / g.cluster;
+        if (prod == Producer::Tma) {
+            r = encode_2d(&L.map_q_tail, in_dt, A, K, M, lda * es, g.stage_k, load_qt);
             if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
-            L.prm.tail_f = 1;
-            L.prm.tail_ksplit = 0;
-            L.prm.full_units = tiles;
-            const int64_t units = tiles_p * ((tiles_q + 1) / 2);
-            int64_t clusters = units < max_cl ? units : max_cl;
-            if (cap > 0 && cap / 4 < clusters) clusters = cap / 4 > 0 ? cap / 4 : 1;
-            L.grid = static_cast<int>(clusters * 4);
         }
+        L.prm.idesc_tail = make_idesc(g.format, static_cast<uint32_t>(g.mma_m),
+                                      static_cast<uint32_t>(width), d_format);
+        L.prm.stage_tx_tail = static_cast<uint32_t>((g.load_p + load_qt) * 128);
     }
+    const bool mc = pl.mc;
     if (std::getenv("GEMM_DEBUG"))
         std::fprintf(stderr,
                      "[gemm] tn in=%d M=%lld N=%lld K=%lld pair=%d producer=%d direct_store=%d "
@@ -711,6 +808,58 @@ int gemm_f32_bf16x6(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda
     ov.parity = &g_cnt_parity[dev - g_devices];
     return gemm_tn(InKind::BF16, true, N, M, 6 * kp, sb, 6 * kp, sa, 6 * kp, 1.0f, C, ldc,
                    stream, &ov);
+}
+
+int gemm_tn_plan(int kind, int64_t M, int64_t N, int64_t K, int flags, int64_t workspace_bytes,
+                 int sms, int mc_clusters, int64_t* out, int nout) {
+    if (kind < GEMM_PLAN_F16 || kind > GEMM_PLAN_FP8_F32OUT || !out || nout < GEMM_PLAN_FIELDS)
+        return GEMM_ERR_INVALID_OPTION;
+    if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || sms <= 0 ||
+        workspace_bytes < 0 || mc_clusters < 0)
+        return GEMM_ERR_INVALID_DIM;
+    TnPlanIn pin;
+    pin.in = kind == GEMM_PLAN_BF16 ? InKind::BF16
+             : (kind == GEMM_PLAN_FP8 || kind == GEMM_PLAN_FP8_F32OUT) ? InKind::E4M3
+                                                                       : InKind::F16;
+    pin.out_f32 = kind == GEMM_PLAN_FP8_F32OUT;
+    pin.acc16 = kind == GEMM_PLAN_F16_ACC16;
+    pin.M = M;
+    pin.N = N;
+    pin.K = K;
+    pin.a_tma = (flags & GEMM_PLAN_A_TMA) != 0;
+    pin.b_tma = (flags & GEMM_PLAN_B_TMA) != 0;
+    pin.c_tma = (flags & GEMM_PLAN_C_TMA) != 0;
+    pin.a_al128 = (flags & GEMM_PLAN_A_128) != 0;
+    pin.b_al128 = (flags & GEMM_PLAN_B_128) != 0;
+    // as gemm_tn sees a registered workspace: the counter sets come off the top
+    pin.has_scratch = workspace_bytes > 0;
+    pin.ws_total = workspace_bytes >= kSplitCounterBytes ? workspace_bytes - kSplitCounterBytes
+                                                         : workspace_bytes;
+    pin.ov_splits = -1;
+    pin.strict = false;
+    pin.sms = sms;
+    pin.mc_clusters = mc_clusters;
+    const TnPlan pl = plan_tn(pin);
+    const int64_t v[GEMM_PLAN_FIELDS] = {pl.status,
+                                         pl.pair,
+                                         static_cast<int64_t>(pl.prod),
+                                         pl.tile_q,
+                                         pl.half,
+                                         pl.splits,
+                                         pl.tail_f,
+                                         pl.tail_ksplit,
+                                         pl.stages,
+                                         pl.grid,
+                                         pl.copy_a,
+                                         pl.copy_b,
+                                         pl.mc,
+                                         pl.tiles_p,
+                                         pl.tiles_q,
+                                         pl.kb_per_split,
+                                         pl.tail_kb_per,
+                                         pl.stage_bytes};
+    for (int i = 0; i < GEMM_PLAN_FIELDS; ++i) out[i] = v[i];
+    return GEMM_OK;
 }
 
 const char* gemm_status_string(int status) {

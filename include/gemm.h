@@ -179,6 +179,49 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                     int64_t ldb, float scale_a, float scale_b, float* C, int64_t ldc,
                     void* stream);
 
+/*
+ * gemm_tn_plan -- what a TN call would run, decided on the host without a GPU
+ * (for tests and tuning; nothing is launched and no device is touched).  The
+ * calls plan with exactly this function, reading the same options
+ * (gemm_set_option).
+ *
+ *   kind             GEMM_PLAN_F16 (gemm_f16_tn), GEMM_PLAN_BF16, GEMM_PLAN_FP8,
+ *                    GEMM_PLAN_F16_ACC16 (gemm_f16_tn_acc16), GEMM_PLAN_FP8_F32OUT
+ *   M, N, K          as for the call (all > 0)
+ *   flags            GEMM_PLAN_A_TMA / _B_TMA / _C_TMA: that matrix's base and row
+ *                    pitch are 16-byte aligned (TMA can address its rows);
+ *                    GEMM_PLAN_A_128 / _B_128: A's or B's rows start on 128-byte
+ *                    boundaries (base and pitch)
+ *   workspace_bytes  the registered workspace (0: none)
+ *   sms              the device's SM count (152 on GB300)
+ *   mc_clusters      resident clusters of four CTAs of the multicast kernel (36 on
+ *                    GB300; used only with option "cluster" = 4)
+ *   out[nout]        nout >= GEMM_PLAN_FIELDS; receives, in this order: status
+ *                    (GEMM_OK), CTA pairs (0/1), producer (0 TMA, 1 load-based),
+ *                    tile width along M, 64-row tiles (0/1), K pieces per tile,
+ *                    last-wave units per tile (1: untouched), last wave cut along K
+ *                    (0/1; else along M), ring stages, grid (CTAs), A repacked,
+ *                    B repacked, multicast kernel (0/1), tiles along N, tiles
+ *                    along M, K stages per piece, K stages per last-wave piece,
+ *                    ring stage bytes.
+ *
+ * Returns GEMM_OK, GEMM_ERR_INVALID_DIM or GEMM_ERR_INVALID_OPTION (kind, out
+ * or nout).
+ */
+#define GEMM_PLAN_F16 0
+#define GEMM_PLAN_BF16 1
+#define GEMM_PLAN_FP8 2
+#define GEMM_PLAN_F16_ACC16 3
+#define GEMM_PLAN_FP8_F32OUT 4
+#define GEMM_PLAN_A_TMA 1
+#define GEMM_PLAN_B_TMA 2
+#define GEMM_PLAN_C_TMA 4
+#define GEMM_PLAN_A_128 8
+#define GEMM_PLAN_B_128 16
+#define GEMM_PLAN_FIELDS 18
+int gemm_tn_plan(int kind, int64_t M, int64_t N, int64_t K, int flags, int64_t workspace_bytes,
+                 int sms, int mc_clusters, int64_t* out, int nout);
+
 /* Human-readable text for a status code.  For GEMM_ERR_LAUNCH it names the
  * last CUDA error this thread saw.  The returned string is static. */
 const char* gemm_status_string(int status);

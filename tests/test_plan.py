@@ -1,0 +1,178 @@
+"""The TN calls' planning rules, checked on the CPU through gemm_tn_plan (the
+same host function every TN call plans with; no GPU needed).  Each case pins
+one rule measured on GB300: tile shape, producer and repacks, narrow Q tiles,
+split-K, the last wave's treatment, and the opt-in kernels."""
+import pytest
+
+from dense_gemm_tcgen05_gb300 import build, capi
+
+WS = 1 << 30
+ALIGNED = capi.PLAN_ALIGNED
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    yield
+
+
+@pytest.fixture
+def options():
+    """Sets library options for one test and restores the defaults after it."""
+    touched = []
+
+    def set_(name, value):
+        assert capi.gemm_set_option(name, value) == 0
+        touched.append(name)
+    yield set_
+    defaults = {"pair": -1, "group": 8}
+    for name in touched:
+        capi.gemm_set_option(name, defaults.get(name, 0))
+
+
+def plan(kind, M, N, K, **kw):
+    st, p = capi.gemm_tn_plan(kind, M, N, K, **kw)
+    assert st == capi.GEMM_OK and p["status"] == capi.GEMM_OK
+    return p
+
+
+def test_square_8192_pairs_and_narrowed_tail():
+    """FP16 8192^3: 32 x 32 pair tiles of 256 x 256 on 76 pairs; the last
+    wave's 36 tiles become 72 half-width units (0.8 of a tile each)."""
+    p = plan("f16", 8192, 8192, 8192, workspace_bytes=WS)
+    assert (p["pair"], p["tile_q"], p["tiles_p"], p["tiles_q"]) == (1, 256, 32, 32)
+    assert (p["splits"], p["tail_f"], p["tail_ksplit"]) == (1, 2, 0)
+    assert (p["stages"], p["stage_bytes"], p["grid"]) == (6, 32 * 1024, 152)
+
+
+def test_long_k_tail_in_k_pieces_only_with_room():
+    """192+ K stages and a tail that fits twice in a wave: K pieces, but only
+    with a workspace; 4096^3 (64 stages) keeps the narrowed tail."""
+    p = plan("bf16", 4096, 4096, 14336, workspace_bytes=WS)
+    assert (p["tail_f"], p["tail_ksplit"], p["tail_kb_per"]) == (2, 1, 112)
+    p = plan("bf16", 4096, 4096, 14336)
+    assert (p["tail_f"], p["tail_ksplit"]) == (2, 0)
+    p = plan("bf16", 4096, 4096, 4096, workspace_bytes=WS)
+    assert (p["tail_f"], p["tail_ksplit"]) == (2, 0)
+
+
+def test_tail_options(options):
+    options("tail", 1)
+    assert plan("f16", 8192, 8192, 8192)["tail_f"] == 1
+    options("tail", 4)
+    assert plan("f16", 8192, 8192, 8192)["tail_f"] == 4
+    options("tail", 0)
+    options("tail_k", 3)
+    p = plan("f16", 8192, 8192, 8192, workspace_bytes=WS)
+    assert (p["tail_f"], p["tail_ksplit"]) == (3, 1)
+
+
+@pytest.mark.parametrize("M,q", [(1, 16), (16, 16), (17, 32), (32, 32), (33, 64), (128, 64),
+                                 (129, 128)])
+def test_skinny_single_cta_tiles_and_width(M, q):
+    """Decode-like shapes: single-CTA 128-row tiles, 16/32 columns when M fits
+    in one such tile, else 64 (M <= 128) or 128."""
+    p = plan("bf16", M, 8192, 8192)
+    assert p["pair"] == 0 and p["tile_q"] == q and p["tiles_p"] == 64
+
+
+def test_skinny_split_k_needs_a_workspace():
+    """64 tiles on 152 SMs: two K pieces each with a workspace (128 CTAs), one
+    wave of 64 CTAs without."""
+    p = plan("bf16", 16, 8192, 8192, workspace_bytes=WS)
+    assert (p["splits"], p["kb_per_split"], p["grid"]) == (2, 64, 128)
+    p = plan("bf16", 16, 8192, 8192)
+    assert (p["splits"], p["grid"]) == (1, 64)
+
+
+def test_narrow_ring_is_deeper():
+    """A 16-column tile's stage holds 16 KB of B and 2 KB of A: 10 stages of
+    18 KB in the 192 KB ring, against 8 of 24 KB at 64 columns."""
+    assert (plan("bf16", 16, 8192, 8192)["stages"], plan("bf16", 16, 8192, 8192)["stage_bytes"]) \
+        == (10, 18 * 1024)
+    assert (plan("bf16", 64, 8192, 8192)["stages"], plan("bf16", 64, 8192, 8192)["stage_bytes"]) \
+        == (8, 24 * 1024)
+
+
+def test_forced_narrow_width_needs_m_to_fit(options):
+    options("tile_q", 16)
+    assert plan("bf16", 16, 8192, 8192)["tile_q"] == 16
+    assert plan("bf16", 40, 8192, 8192)["tile_q"] == 64       # three tiles would overlap
+    options("pair", 1)
+    assert plan("bf16", 16, 8192, 8192)["tile_q"] == 64       # never with CTA pairs
+
+
+def test_sub_wave_rule():
+    """Pair tiles filling less than a wave give way to single-CTA tiles that
+    fit in one (1024 x 1024 x 8192: 64 tiles of 128 x 128, two K pieces with a
+    workspace); where those would need a second wave (2048^2) pairs stay."""
+    p = plan("bf16", 1024, 1024, 8192, workspace_bytes=WS)
+    assert (p["pair"], p["tile_q"], p["splits"], p["grid"]) == (0, 128, 2, 128)
+    assert plan("bf16", 2048, 2048, 8192)["pair"] == 1
+
+
+def test_unaligned_operands_repacked_or_load_producer():
+    """A's rows not 16-byte aligned: copied into the workspace when it has room
+    (TMA path), read by the load-based producer (single CTA) otherwise."""
+    flags = ALIGNED & ~(capi.PLAN_A_TMA | capi.PLAN_A_128)
+    p = plan("bf16", 2047, 3001, 1023, flags=flags)
+    assert (p["producer"], p["pair"], p["copy_a"]) == (1, 0, 0)
+    p = plan("bf16", 2047, 3001, 1023, flags=flags, workspace_bytes=WS)
+    assert (p["producer"], p["copy_a"], p["copy_b"]) == (0, 1, 0)
+    p = plan("bf16", 2047, 3001, 1023, flags=flags, workspace_bytes=1 << 20)   # too small
+    assert (p["producer"], p["copy_a"]) == (1, 0)
+
+
+def test_not_128_byte_aligned_copied_only_when_heavy():
+    """Rows 16- but not 128-byte aligned are copied when MN / (M + N) >= 1100 x
+    element size (8192^3: 4096 >= 2200), not at 4096^3 (2048)."""
+    flags = ALIGNED & ~capi.PLAN_A_128
+    assert plan("f16", 8192, 8192, 8192, flags=flags, workspace_bytes=WS)["copy_a"] == 1
+    assert plan("f16", 4096, 4096, 4096, flags=flags, workspace_bytes=WS)["copy_a"] == 0
+
+
+def test_fp16_accumulation_never_splits():
+    p = plan("f16_acc16", 16, 8192, 8192, workspace_bytes=WS)
+    assert p["splits"] == 1
+    assert plan("f16", 16, 8192, 8192, workspace_bytes=WS)["splits"] == 2
+
+
+def test_fp8_stages_and_tail():
+    """E4M3 stages hold 128 K values: 8192^3 has 64 K stages per tile (no
+    K-split tail); its narrowed tail units cost 0.9 of a tile, still worth it."""
+    p = plan("e4m3", 8192, 8192, 8192, workspace_bytes=WS)
+    assert (p["pair"], p["kb_per_split"], p["tail_f"], p["tail_ksplit"]) == (1, 64, 2, 0)
+
+
+def test_64_row_tiles_only_when_forced(options):
+    assert plan("bf16", 16, 8192, 8192)["half"] == 0
+    options("half", 1)
+    p = plan("bf16", 16, 8192, 8192, workspace_bytes=WS)
+    assert (p["half"], p["tiles_p"], p["splits"], p["grid"]) == (1, 128, 1, 128)
+    assert plan("f16_acc16", 16, 8192, 8192)["half"] == 0
+    assert plan("bf16", 4096, 4096, 4096)["half"] == 0          # CTA pairs
+
+
+def test_multicast_only_when_asked(options):
+    assert plan("f16", 8192, 8192, 8192)["multicast"] == 0
+    options("cluster", 4)
+    p = plan("f16", 8192, 8192, 8192, mc_clusters=36)
+    assert (p["multicast"], p["grid"], p["tail_f"]) == (1, 144, 1)
+    assert plan("f16", 8192, 8192, 8192, mc_clusters=0)["multicast"] == 0
+    assert plan("e4m3_f32out", 8192, 8192, 8192, mc_clusters=36)["multicast"] == 1
+    p = plan("f16", 8192, 8192, 8192, flags=ALIGNED & ~capi.PLAN_C_TMA, mc_clusters=36)
+    assert p["multicast"] == 0                                  # row-wise stores
+
+
+def test_persistent_grid_follows_sms_and_cap(options):
+    assert plan("f16", 8192, 8192, 8192, sms=148)["grid"] == 148
+    options("max_ctas", 64)
+    assert plan("f16", 8192, 8192, 8192)["grid"] == 64
+
+
+def test_argument_errors():
+    assert capi.gemm_tn_plan("f16", 0, 8, 8)[0] == capi.GEMM_ERR_INVALID_DIM
+    assert capi.gemm_tn_plan("f16", 8, 8, 8, sms=0)[0] == capi.GEMM_ERR_INVALID_DIM
+    lib = capi.lib()
+    assert lib.gemm_tn_plan(9, 8, 8, 8, 0, 0, 152, 36, None, 18) == capi.GEMM_ERR_INVALID_OPTION
+    assert lib.gemm_tn_plan(0, 8, 8, 8, 0, 0, 152, 36, None, 18) == capi.GEMM_ERR_INVALID_OPTION
