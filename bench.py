@@ -17,6 +17,7 @@ the time is the maximum over ranks and `value` counts every rank's work.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--sweep]
+  python bench.py --ncu-case bf16:128x8192x8192   (launches for a profiler capture)
 """
 from __future__ import annotations
 
@@ -724,6 +725,33 @@ def run_reference(args):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def ncu_case(spec: str):
+    """A few launches of one TN shape for profiler captures: three rounds of
+    this library's call followed by cuBLAS's (torch.matmul) on the same
+    operands, with the bench workspace registered.  Nothing is timed; the
+    line only names the case.  FP8 runs this library's call alone."""
+    import torch
+
+    from dense_gemm_tcgen05_gb300 import capi
+
+    kind, dims = spec.split(":")
+    M, N, K = (int(x) for x in dims.lower().split("x"))
+    workspace = torch.empty(WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+    assert capi.gemm_set_workspace(workspace.data_ptr(), workspace.numel()) == 0
+    _, sets = tn_sets(kind, M, N, K, 2, 0.1, 2, "cuda")
+    stream = torch.cuda.Stream()
+    call = tn_call(kind, M, N, K, 1.0, 1.0, stream.cuda_stream)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            a, b, c = sets[i % 2]
+            call(a, b, c)
+            if kind != "e4m3":
+                torch.matmul(b, a.T, out=c)      # C column-major = (B A^T) row-major
+    torch.cuda.synchronize()
+    assert capi.gemm_set_workspace(None, 0) == 0
+    return {"ncu_case": spec, "launches_each": 3, "cublas": kind != "e4m3"}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -734,7 +762,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-main", action="store_true",
                     help="time the main workload only (for profiler runs)")
+    ap.add_argument("--ncu-case", metavar="KIND:MxNxK",
+                    help="launch one TN shape three times, and cuBLAS beside it, for ncu")
     args = ap.parse_args(argv)
+    if args.ncu_case:
+        print(json.dumps(ncu_case(args.ncu_case)), flush=True)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":

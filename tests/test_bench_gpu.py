@@ -37,3 +37,12 @@ def test_bench_line_contract():
     assert e2e["copies_only_value"] > 0 and e2e["copies_only_gbs"] > 0
     assert e2e["value"] <= 1.05 * e2e["copies_only_value"]
     assert "sm_mhz" in line["clocks"] and "reasons" in line["clocks"]
+
+
+def test_ncu_case_runs():
+    """The profiler-capture mode launches the shape it is given and exits 0."""
+    out = subprocess.run([sys.executable, "bench.py", "--ncu-case", "bf16:128x1024x512"], cwd=ROOT,
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line == {"ncu_case": "bf16:128x1024x512", "launches_each": 3, "cublas": True}
