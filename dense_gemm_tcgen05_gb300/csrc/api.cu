@@ -152,6 +152,26 @@ int choose_tile_q(int64_t M, int max_tile_q) {
 }
 
 constexpr int64_t kMaxDim = 0x7fffffffLL;
+// Leading dimensions above this many elements cannot address device memory;
+// the bound keeps every pitch and size product below 2^63.
+constexpr int64_t kMaxLd = 1LL << 48;
+// Byte counts for sizes no device can hold saturate here, a quarter of the
+// int64 range, so that a few of them can still be added without overflow.
+constexpr int64_t kSatBytes = INT64_MAX / 4;
+
+// a * b for a, b >= 0, saturating at kSatBytes.
+int64_t sat_mul(int64_t a, int64_t b) {
+    if (a == 0 || b == 0) return 0;
+    return a > kSatBytes / b ? kSatBytes : a * b;
+}
+
+// x rounded up to a multiple of 256, for x in [0, kSatBytes].
+int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
+
+// Whether `need` bytes (possibly a saturated sum) fit in `room`: a saturated
+// size never does, however large the room.
+bool fits(int64_t need, int64_t room) { return need < kSatBytes && need <= room; }
+
 constexpr int kMcStageRegion = 200 * 1024;  // ring of the multicast kernel (tc_gemm_mc.cuh)
 
 // What a TN call is given, for planning: shapes, what TMA can address, the
@@ -222,9 +242,9 @@ TnPlan plan_tn(const TnPlanIn& a) {
         a.has_scratch) {
         const int64_t rb = K * es;                       // row bytes
         const int64_t dp = (rb + 127) / 128 * 128;       // aligned pitch
-        const int64_t need_a = copy_a ? (M * dp + 255) / 256 * 256 : 0;
-        const int64_t need_b = copy_b ? (N * dp + 255) / 256 * 256 : 0;
-        if (need_a + need_b <= a.ws_total) {
+        const int64_t need_a = copy_a ? round256(sat_mul(M, dp)) : 0;
+        const int64_t need_b = copy_b ? round256(sat_mul(N, dp)) : 0;
+        if (fits(need_a + need_b, a.ws_total)) {
             p.copy_a = copy_a;
             p.copy_b = copy_b;
             p.dp = dp;
@@ -323,14 +343,15 @@ TnPlan plan_tn(const TnPlanIn& a) {
             const int64_t kb_per = (p.num_kb + want - 1) / want;
             const int64_t pieces = (p.num_kb + kb_per - 1) / kb_per;
             const int64_t slices = 4 * g.cluster;                    // 32-row slices per tile
-            const int64_t cnt_bytes = ((tiles * slices * 4 + 255) / 256) * 256;
-            const int64_t part_bytes = tiles * pieces * slices * 32 * 256 * 4;
+            const int64_t cnt_bytes = round256(sat_mul(tiles, slices * 4));
+            const int64_t part_bytes = sat_mul(sat_mul(tiles, pieces), slices * 32 * 256 * 4);
             const int64_t room = a.ws_total - p.ws_used;
-            if (a.strict && pieces >= 2 && cnt_bytes + part_bytes > room) {
+            const bool fit = fits(cnt_bytes + part_bytes, room);
+            if (a.strict && pieces >= 2 && !fit) {
                 p.status = GEMM_ERR_SCRATCH;
                 return p;
             }
-            if (pieces >= 2 && a.has_scratch && cnt_bytes + part_bytes <= room) {
+            if (pieces >= 2 && a.has_scratch && fit) {
                 p.splits = static_cast<int>(pieces);
                 p.kb_per_split = static_cast<int>(kb_per);
                 p.split_cnt_bytes = cnt_bytes;
@@ -391,7 +412,7 @@ TnPlan plan_tn(const TnPlanIn& a) {
                 const int64_t kb_per = (p.num_kb + want_k - 1) / want_k;
                 const int64_t pieces = (p.num_kb + kb_per - 1) / kb_per;
                 const int64_t need = cnt_bytes + rem * pieces * slices * 32 * 256 * 4;
-                if (pieces >= 2 && need <= room) {
+                if (pieces >= 2 && fits(need, room)) {
                     f = static_cast<int>(pieces);
                     ksplit = true;
                     kb_per_t = kb_per;
@@ -475,7 +496,9 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return GEMM_ERR_INVALID_DIM;
     const int64_t kmin = K > 1 ? K : 1;
-    if (lda < kmin || ldb < kmin || ldc < (M > 1 ? M : 1)) return GEMM_ERR_INVALID_LD;
+    if (lda < kmin || ldb < kmin || ldc < (M > 1 ? M : 1) || lda > kMaxLd || ldb > kMaxLd ||
+        ldc > kMaxLd)
+        return GEMM_ERR_INVALID_LD;
     if ((M > 0 && K > 0 && !A) || (N > 0 && K > 0 && !B) || (M > 0 && N > 0 && !C))
         return GEMM_ERR_NULL_PTR;
     if (!aligned(A, es) || !aligned(B, es) || !aligned(C, os)) return GEMM_ERR_MISALIGNED;
@@ -710,7 +733,9 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return GEMM_ERR_INVALID_DIM;
     const int64_t nmin = N > 1 ? N : 1;
-    if (lda < (K > 1 ? K : 1) || ldb < nmin || ldc < nmin) return GEMM_ERR_INVALID_LD;
+    if (lda < (K > 1 ? K : 1) || ldb < nmin || ldc < nmin || lda > kMaxLd || ldb > kMaxLd ||
+        ldc > kMaxLd)
+        return GEMM_ERR_INVALID_LD;
     if ((M > 0 && K > 0 && !A) || (N > 0 && K > 0 && !B) || (M > 0 && N > 0 && !C))
         return GEMM_ERR_NULL_PTR;
     if (!aligned(A, 4) || !aligned(B, 4) || !aligned(C, 4)) return GEMM_ERR_MISALIGNED;
@@ -762,7 +787,7 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
 int64_t gemm_f32_bf16x6_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
     const int64_t row = 6 * ((K + 63) / 64 * 64) * 2;  // bytes of one split row
-    return kSplitCounterBytes + (M * row + 255) / 256 * 256 + (N * row + 255) / 256 * 256;
+    return kSplitCounterBytes + round256(sat_mul(M, row)) + round256(sat_mul(N, row));
 }
 
 int gemm_f32_bf16x6(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
@@ -772,7 +797,9 @@ int gemm_f32_bf16x6(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda
     const int64_t kp = (K + 63) / 64 * 64;
     if (6 * kp > kMaxDim) return GEMM_ERR_INVALID_DIM;
     const int64_t nmin = N > 1 ? N : 1;
-    if (lda < (K > 1 ? K : 1) || ldb < nmin || ldc < nmin) return GEMM_ERR_INVALID_LD;
+    if (lda < (K > 1 ? K : 1) || ldb < nmin || ldc < nmin || lda > kMaxLd || ldb > kMaxLd ||
+        ldc > kMaxLd)
+        return GEMM_ERR_INVALID_LD;
     if ((M > 0 && K > 0 && !A) || (N > 0 && K > 0 && !B) || (M > 0 && N > 0 && !C))
         return GEMM_ERR_NULL_PTR;
     if (!aligned(A, 4) || !aligned(B, 4) || !aligned(C, 4)) return GEMM_ERR_MISALIGNED;
@@ -794,8 +821,8 @@ int gemm_f32_bf16x6(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda
         ws_bytes = dev->workspace_bytes;
     }
     const int64_t need = gemm_f32_bf16x6_workspace_bytes(M, N, K);
-    if (!ws || ws_bytes < need) return GEMM_ERR_WORKSPACE;
-    const int64_t a_bytes = (M * 6 * kp * 2 + 255) / 256 * 256;
+    if (!ws || !fits(need, ws_bytes)) return GEMM_ERR_WORKSPACE;
+    const int64_t a_bytes = round256(sat_mul(M, 6 * kp * 2));
     char* sa = ws + kSplitCounterBytes;  // M rows of 6 kp BF16: the split of A
     char* sb = sa + a_bytes;             // N rows of 6 kp BF16: the split of B, transposed
     e = f32_split_rows_launch(A, lda, M, K, kp, sa, dev->sms, stream);
@@ -866,7 +893,7 @@ const char* gemm_status_string(int status) {
     switch (status) {
         case GEMM_OK: return "ok";
         case GEMM_ERR_INVALID_DIM: return "invalid dimension (negative or above 2^31-1)";
-        case GEMM_ERR_INVALID_LD: return "leading dimension below its minimum";
+        case GEMM_ERR_INVALID_LD: return "leading dimension below its minimum or above 2^48";
         case GEMM_ERR_NULL_PTR: return "null matrix pointer with a nonzero extent";
         case GEMM_ERR_MISALIGNED: return "pointer not aligned to its element size";
         case GEMM_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3";
@@ -976,15 +1003,16 @@ int gemm_set_workspace(void* ptr, int64_t bytes) {
 }
 
 int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    // Upper bound over the configurations: aligned copies of A and B (16-bit
-    // elements), then 16 K pieces of every tile of the narrowest layout
-    // (128 rows of N by 64 of M per tile), plus the counters.
-    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    // Upper bound over the automatic configurations: aligned copies of A and B
+    // (16-bit elements), then 16 K pieces of every tile of the narrowest
+    // layout (128 rows of N by 64 of M per tile), plus the counters.
+    if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
     const int64_t dp = (K * 2 + 127) / 128 * 128;
-    const int64_t repack = (M * dp + 255) / 256 * 256 + (N * dp + 255) / 256 * 256;
+    const int64_t repack = round256(sat_mul(M, dp)) + round256(sat_mul(N, dp));
     const int64_t tiles = ((N + 127) / 128) * ((M + 63) / 64);
-    return kSplitCounterBytes + repack + ((tiles * 4 * 4 + 255) / 256) * 256 +
-           tiles * 16 * 4 * 32 * 256 * 4;
+    const int64_t total = kSplitCounterBytes + repack + round256(sat_mul(tiles, 4 * 4)) +
+                          sat_mul(tiles, 16 * 4 * 32 * 256 * 4);
+    return total < kSatBytes ? total : kSatBytes;
 }
 
 int gemm_tile_coord(int64_t t, int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t* tm,

@@ -12,7 +12,8 @@
  * Conventions shared by all compute entry points
  * ------------------------------------------------
  *  - Dimensions and leading dimensions are element counts (int64_t).  M, N and
- *    K must lie in [0, 2^31 - 1].
+ *    K must lie in [0, 2^31 - 1]; a leading dimension must be at least its
+ *    documented minimum and at most 2^48 (GEMM_ERR_INVALID_LD otherwise).
  *  - All matrix pointers are DEVICE pointers on the current CUDA device.  The
  *    caller owns every buffer; the library allocates no device memory per call.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
@@ -39,7 +40,7 @@ extern "C" {
 
 #define GEMM_OK 0                     /* success */
 #define GEMM_ERR_INVALID_DIM 1        /* M, N or K negative or above 2^31 - 1 */
-#define GEMM_ERR_INVALID_LD 2         /* a leading dimension below its minimum */
+#define GEMM_ERR_INVALID_LD 2         /* a leading dimension below its minimum or above 2^48 */
 #define GEMM_ERR_NULL_PTR 3           /* NULL matrix pointer with a nonzero extent */
 #define GEMM_ERR_MISALIGNED 4         /* pointer not aligned to its element size */
 #define GEMM_ERR_UNSUPPORTED_DEVICE 5 /* current device is not compute capability 10.3 */
@@ -101,7 +102,8 @@ int gemm_f32_bf16x6(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda
 /*
  * Workspace bytes gemm_f32_bf16x6 needs for an M x N x K product: two split
  * operands of (M + N) rows of 6 Kp bfloat16 values, each rounded up to 256
- * bytes.  0 when M, N or K is 0 or out of range.
+ * bytes, plus the 128 KiB of split counters.  0 when M, N or K is 0 or out of
+ * range; sizes that no device could hold are not exact but at least INT64_MAX / 4.
  */
 int64_t gemm_f32_bf16x6_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
@@ -309,8 +311,12 @@ int gemm_set_option(const char* name, int64_t value);
  */
 int gemm_set_workspace(void* ptr, int64_t bytes);
 
-/* Workspace bytes that suffice for any M x N x K TN call (the split counters,
- * aligned copies of A and B, and the largest split). */
+/* Workspace bytes that suffice for any M x N x K TN call under the automatic
+ * rules: the split counters, aligned copies of A and B, and the largest split
+ * those rules choose (16 K pieces of the narrowest tiles).  A split forced with
+ * option "splits" that does not fit in the registered workspace runs unsplit.
+ * 0 when M, N or K is not in [1, 2^31 - 1]; sizes that no device could hold
+ * saturate at INT64_MAX / 4. */
 int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*

@@ -48,6 +48,10 @@ def test_argument_errors_without_gpu(fn):
     assert f(4, 4, 8, p, 8, p, 8, None, 4) == capi.GEMM_ERR_NULL_PTR
     assert f(4, 4, 8, p + 1, 8, p, 8, p, 4) == capi.GEMM_ERR_MISALIGNED
     assert f(4, 4, 8, p, 8, p, 8, p + 1, 4) == capi.GEMM_ERR_MISALIGNED
+    big = (1 << 48) + 8   # above the leading-dimension bound
+    assert f(4, 4, 8, p, big, p, 8, p, 4) == capi.GEMM_ERR_INVALID_LD
+    assert f(4, 4, 8, p, 8, p, big, p, 4) == capi.GEMM_ERR_INVALID_LD
+    assert f(4, 4, 8, p, 8, p, 8, p, big) == capi.GEMM_ERR_INVALID_LD
 
 
 def test_fp8_and_f32_argument_errors_without_gpu():
@@ -68,6 +72,12 @@ def test_fp8_and_f32_argument_errors_without_gpu():
     assert f6(4, 5, 6, p, 6, p, 5, p, 4) == capi.GEMM_ERR_INVALID_LD
     assert f6(4, 5, 6, p, 6, None, 5, p, 5) == capi.GEMM_ERR_NULL_PTR
     assert f6(4, 5, 6, p, 6, p, 5, p + 2, 5) == capi.GEMM_ERR_MISALIGNED
+    big = (1 << 48) + 4
+    for fn in (capi.gemm_f32, f6):
+        assert fn(4, 5, 6, p, big, p, 5, p, 5) == capi.GEMM_ERR_INVALID_LD
+        assert fn(4, 5, 6, p, 6, p, big, p, 5) == capi.GEMM_ERR_INVALID_LD
+        assert fn(4, 5, 6, p, 6, p, 5, p, big) == capi.GEMM_ERR_INVALID_LD
+    assert capi.gemm_fp8_tn(4, 4, 8, p, big, p, 8, 1.0, 1.0, p, 4) == capi.GEMM_ERR_INVALID_LD
 
 
 def test_options():
@@ -107,6 +117,18 @@ def test_workspace_size_bound():
     assert capi.gemm_workspace_bytes(512, 1024, 64) >= (SPLIT_COUNTER_BYTES + repack +
                                                          tiles * 16 * 4 * 32 * 1024)
     assert capi.gemm_workspace_bytes(0, 1, 1) == 0
+    assert capi.gemm_workspace_bytes(1, 1, 1 << 31) == 0          # out of range
+
+
+def test_workspace_sizes_saturate():
+    """Sizes no device could hold saturate instead of wrapping around."""
+    top = (1 << 31) - 1
+    sat = ((1 << 63) - 1) // 4
+    assert capi.gemm_workspace_bytes(top, top, top) == sat
+    assert capi.gemm_workspace_bytes(top, top, 1) == sat            # the split bound alone
+    assert capi.gemm_f32_bf16x6_workspace_bytes(top, top, top) >= sat
+    # the exact figure where it fits in a device
+    assert capi.gemm_workspace_bytes(4096, 4096, 4096) < 1 << 40
 
 
 def test_f32_bf16x6_workspace_size():

@@ -176,3 +176,16 @@ def test_argument_errors():
     lib = capi.lib()
     assert lib.gemm_tn_plan(9, 8, 8, 8, 0, 0, 152, 36, None, 18) == capi.GEMM_ERR_INVALID_OPTION
     assert lib.gemm_tn_plan(0, 8, 8, 8, 0, 0, 152, 36, None, 18) == capi.GEMM_ERR_INVALID_OPTION
+
+
+def test_sizes_beyond_any_device_plan_without_overflow(options):
+    """The largest dimensions with a forced 64-piece split: the partial sums
+    cannot fit in any workspace, so the call stays unsplit (the byte counts
+    saturate instead of wrapping around into a small number)."""
+    top = (1 << 31) - 1
+    options("splits", 64)
+    p = plan("bf16", top, top, top, workspace_bytes=(1 << 62))
+    assert p["splits"] == 1 and p["copy_a"] == 0
+    flags = ALIGNED & ~(capi.PLAN_A_TMA | capi.PLAN_A_128)
+    p = plan("bf16", top, top, top, flags=flags, workspace_bytes=(1 << 62))
+    assert (p["copy_a"], p["producer"]) == (0, 1)   # A's copy cannot fit either
