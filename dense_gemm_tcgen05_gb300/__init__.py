@@ -45,6 +45,22 @@ def _ld(t: torch.Tensor) -> int:
     return max(int(t.stride(0)), int(t.size(1)), 1)
 
 
+def _same_device(*ts: torch.Tensor):
+    dev = ts[0].device
+    for t in ts[1:]:
+        if t.device != dev:
+            raise ValueError("all tensors must be on one device (got %s and %s)" % (dev, t.device))
+
+
+def _check_out(out: torch.Tensor, shape, dtype):
+    """A caller-supplied output must match exactly: the library writes every
+    element of the product, so a smaller tensor would be written past its end."""
+    _check_2d(out, "out")
+    if out.dtype != dtype or tuple(out.shape) != tuple(shape):
+        raise ValueError("out must be %s of %s, got %s of %s" % (tuple(shape), dtype,
+                                                                 tuple(out.shape), out.dtype))
+
+
 def tn(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None, scale_a: float = 1.0,
        scale_b: float = 1.0, stream=None, out_dtype: torch.dtype | None = None) -> torch.Tensor:
     """C = A x B in the TN layout; returns ``out`` (N, M) holding C column-major.
@@ -69,16 +85,16 @@ def tn(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None, scale_
         raise TypeError("output dtype %s is not available for %s inputs" % (out_dtype, a.dtype))
     if out is None:
         out = torch.empty((N, M), dtype=out_dtype, device=a.device)
-    _check_2d(out, "out")
-    if out.dtype != out_dtype or tuple(out.shape) != (N, M):
-        raise ValueError("out must be (N, M) of %s" % out_dtype)
-    h = stream_handle(stream)
-    if fn_name in ("gemm_fp8_tn", "gemm_fp8_tn_f32"):
-        st = getattr(capi, fn_name)(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), scale_a,
-                                    scale_b, out.data_ptr(), _ld(out), h)
-    else:
-        st = getattr(capi, fn_name)(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b),
-                                    out.data_ptr(), _ld(out), h)
+    _check_out(out, (N, M), out_dtype)
+    _same_device(a, b, out)
+    with torch.cuda.device(a.device):
+        h = stream_handle(stream)
+        if fn_name in ("gemm_fp8_tn", "gemm_fp8_tn_f32"):
+            st = getattr(capi, fn_name)(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b),
+                                        scale_a, scale_b, out.data_ptr(), _ld(out), h)
+        else:
+            st = getattr(capi, fn_name)(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b),
+                                        out.data_ptr(), _ld(out), h)
     if st != capi.GEMM_OK:
         raise GemmError(st, fn_name)
     return out
@@ -97,9 +113,11 @@ def f32(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None,
         raise ValueError("K mismatch")
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=a.device)
-    _check_2d(out, "out")
-    st = capi.gemm_f32(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), out.data_ptr(),
-                       _ld(out), stream_handle(stream))
+    _check_out(out, (M, N), torch.float32)
+    _same_device(a, b, out)
+    with torch.cuda.device(a.device):
+        st = capi.gemm_f32(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), out.data_ptr(),
+                           _ld(out), stream_handle(stream))
     if st != capi.GEMM_OK:
         raise GemmError(st, "gemm_f32")
     return out
@@ -121,9 +139,11 @@ def f32_bf16x6(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None
         raise ValueError("K mismatch")
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=a.device)
-    _check_2d(out, "out")
-    st = capi.gemm_f32_bf16x6(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b),
-                              out.data_ptr(), _ld(out), stream_handle(stream))
+    _check_out(out, (M, N), torch.float32)
+    _same_device(a, b, out)
+    with torch.cuda.device(a.device):
+        st = capi.gemm_f32_bf16x6(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b),
+                                  out.data_ptr(), _ld(out), stream_handle(stream))
     if st != capi.GEMM_OK:
         raise GemmError(st, "gemm_f32_bf16x6")
     return out

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import synthetic_inputs as si
-from dense_gemm_tcgen05_gb300 import capi, tn
+from dense_gemm_tcgen05_gb300 import capi, f32, f32_bf16x6, tn
 from gpu_util import run_tn
 
 pytestmark = pytest.mark.gpu
@@ -51,6 +51,27 @@ def test_side_stream_and_tensor_api():
     s.synchronize()
     assert out.shape == (N, M)
     assert torch.all(out.float() == K)
+
+
+def test_tensor_helpers_reject_mismatched_out():
+    """An `out` of the wrong shape or dtype is refused before any launch (the
+    library writes the whole product, so a smaller `out` would overflow)."""
+    a = torch.ones((64, 32), dtype=torch.float32, device="cuda")
+    b = torch.ones((32, 48), dtype=torch.float32, device="cuda")
+    for fn in (f32, f32_bf16x6):
+        short = torch.full((63, 48), 7.0, device="cuda")
+        with pytest.raises(ValueError):
+            fn(a, b, out=short)
+        with pytest.raises(ValueError):
+            fn(a, b, out=torch.empty((64, 48), dtype=torch.float16, device="cuda"))
+        assert torch.all(short == 7.0)
+    ah = torch.ones((64, 32), dtype=torch.float16, device="cuda")
+    bh = torch.ones((48, 32), dtype=torch.float16, device="cuda")
+    with pytest.raises(ValueError):
+        tn(ah, bh, out=torch.empty((47, 64), dtype=torch.float16, device="cuda"))
+    out = f32(a, b, out=torch.empty((64, 48), device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.all(out == 32.0)
 
 
 def test_tuner_runs_and_restores_defaults():
