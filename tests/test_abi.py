@@ -25,6 +25,28 @@ def test_exports_every_declared_symbol():
     assert set(names) == set(capi._SIGNATURES)
 
 
+def test_binding_constants_match_the_header():
+    """Every status code and planner constant the binding hard-codes has the
+    value include/gemm.h defines."""
+    import re
+    defs = {}
+    for line in open(capi.HEADER):
+        m = re.match(r"#define (GEMM_\w+) \(?(\d+)", line)
+        if m:
+            defs[m.group(1)] = int(m.group(2))
+    status = {k: v for k, v in defs.items() if k == "GEMM_OK" or k.startswith("GEMM_ERR_")}
+    assert len(status) == 11
+    for name, value in status.items():
+        assert getattr(capi, name) == value, name
+    kinds = {"GEMM_PLAN_F16": "f16", "GEMM_PLAN_BF16": "bf16", "GEMM_PLAN_FP8": "e4m3",
+             "GEMM_PLAN_F16_ACC16": "f16_acc16", "GEMM_PLAN_FP8_F32OUT": "e4m3_f32out"}
+    for name, key in kinds.items():
+        assert capi.PLAN_KINDS[key] == defs[name], name
+    for flag in ("A_TMA", "B_TMA", "C_TMA", "A_128", "B_128"):
+        assert getattr(capi, "PLAN_" + flag) == defs["GEMM_PLAN_" + flag], flag
+    assert len(capi.PLAN_FIELDS) == defs["GEMM_PLAN_FIELDS"]
+
+
 def test_status_strings():
     for st in range(11):
         assert capi.status_text(st) and capi.status_text(st) != "unknown status"
