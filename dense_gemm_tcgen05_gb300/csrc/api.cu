@@ -488,9 +488,10 @@ cudaError_t mc_max_clusters(InKind in, bool out_f32, const DeviceInfo* dev, int*
 // >= 2 forced, 1 never) and fails with GEMM_ERR_SCRATCH when the split it
 // chooses needs more than ov->bytes.  Every public entry point but the
 // no-allocation one passes nullptr.
-int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void* A,
-            int64_t lda, const void* B, int64_t ldb, float scale, void* C, int64_t ldc,
-            void* stream_v, const ScratchOverride* ov = nullptr, bool acc16 = false) {
+// Argument checks of a TN call, in the order the header documents; nothing
+// here touches the device.
+int validate_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void* A,
+                int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc) {
     const int es = in == InKind::E4M3 ? 1 : 2;
     const int os = out_f32 ? 4 : 2;  // output element size
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
@@ -502,8 +503,18 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     if ((M > 0 && K > 0 && !A) || (N > 0 && K > 0 && !B) || (M > 0 && N > 0 && !C))
         return GEMM_ERR_NULL_PTR;
     if (!aligned(A, es) || !aligned(B, es) || !aligned(C, os)) return GEMM_ERR_MISALIGNED;
+    return GEMM_OK;
+}
+
+int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void* A,
+            int64_t lda, const void* B, int64_t ldb, float scale, void* C, int64_t ldc,
+            void* stream_v, const ScratchOverride* ov = nullptr, bool acc16 = false) {
+    const int es = in == InKind::E4M3 ? 1 : 2;
+    const int os = out_f32 ? 4 : 2;  // output element size
+    int st = validate_tn(in, out_f32, M, N, K, A, lda, B, ldb, C, ldc);
+    if (st != GEMM_OK) return st;
     const DeviceInfo* dev = nullptr;
-    int st = current_device(&dev);
+    st = current_device(&dev);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
@@ -719,6 +730,13 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
 }  // namespace
 
 namespace gb300 {
+int tn_validate(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                const void* B, int64_t ldb, const void* C, int64_t ldc) {
+    return validate_tn(in, false, M, N, K, A, lda, B, ldb, C, ldc);
+}
+
+int tn_record_cuda_error(cudaError_t e) { return fail_cuda(e); }
+
 int gemm_tn_with_scratch(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                          const void* B, int64_t ldb, void* C, int64_t ldc, void* stream,
                          const ScratchOverride& ov) {

@@ -41,6 +41,15 @@ struct ScratchOverride {
     std::atomic<unsigned int>* parity = nullptr;  // which set the next split launch uses
 };
 
+// The argument checks of a TN call with 16-bit output (dimensions, leading
+// dimensions, null pointers, alignment), without touching the device: a
+// gemm.h status.
+int tn_validate(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                const void* B, int64_t ldb, const void* C, int64_t ldc);
+
+// Records a CUDA error for gemm_status_string and returns GEMM_ERR_LAUNCH.
+int tn_record_cuda_error(cudaError_t e);
+
 // The TN path with explicit split-K scratch (16-bit inputs and output).
 int gemm_tn_with_scratch(InKind in, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                          const void* B, int64_t ldb, void* C, int64_t ldc, void* stream,

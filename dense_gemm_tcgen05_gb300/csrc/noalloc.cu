@@ -37,19 +37,23 @@ std::mutex g_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 std::atomic<unsigned int> g_parity[kMaxDevices];  // the next split launch's counter set
 
-// Device address of this device's copy of the array, looked up on first use.
-int scratch_address(void** out) {
+// Device address of this device's copy of the array, looked up on first use,
+// and the device's index.
+int scratch_address(void** out, int* dev_out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_LAUNCH;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return gb300::tn_record_cuda_error(e);
     if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!g_scratch_addr[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
-            return GEMM_ERR_LAUNCH;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return gb300::tn_record_cuda_error(e);
+        if (!p) return gb300::tn_record_cuda_error(cudaErrorInvalidSymbol);
         g_scratch_addr[dev] = p;
     }
     *out = g_scratch_addr[dev];
+    *dev_out = dev;
     return GEMM_OK;
 }
 
@@ -59,12 +63,13 @@ extern "C" int gemm_bf16_tn_noalloc(int64_t M, int64_t N, int64_t K, const void*
                                     const void* B, int64_t ldb, void* C, int64_t ldc,
                                     int64_t splits, void* stream) {
     if (splits < 0 || splits > 64) return GEMM_ERR_INVALID_OPTION;
-    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_DIM;
-    void* scratch = nullptr;
-    const int st = scratch_address(&scratch);
+    // every argument check before the first CUDA call, as for the other entry points
+    int st = gb300::tn_validate(gb300::InKind::BF16, M, N, K, A, lda, B, ldb, C, ldc);
     if (st != GEMM_OK) return st;
+    void* scratch = nullptr;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_LAUNCH;
+    st = scratch_address(&scratch, &dev);
+    if (st != GEMM_OK) return st;
     gb300::ScratchOverride ov{static_cast<char*>(scratch) + gb300::kSplitCounterBytes,
                               kNoAllocScratchBytes - gb300::kSplitCounterBytes,
                               static_cast<int>(splits)};

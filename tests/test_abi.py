@@ -102,6 +102,19 @@ def test_fp8_and_f32_argument_errors_without_gpu():
     assert capi.gemm_fp8_tn(4, 4, 8, p, big, p, 8, 1.0, 1.0, p, 4) == capi.GEMM_ERR_INVALID_LD
 
 
+def test_noalloc_argument_errors_without_gpu():
+    """The no-allocation entry point checks every argument before its first
+    CUDA call (the scratch lookup), like the other entry points."""
+    f = capi.gemm_bf16_tn_noalloc
+    p = 0x10000
+    assert f(4, 4, 8, p, 8, p, 8, p, 4, 65, None) == capi.GEMM_ERR_INVALID_OPTION
+    assert f(-1, 4, 8, p, 8, p, 8, p, 4, 0, None) == capi.GEMM_ERR_INVALID_DIM
+    assert f(4, 4, 8, p, 7, p, 8, p, 4, 0, None) == capi.GEMM_ERR_INVALID_LD
+    assert f(4, 4, 8, p, 8, p, 8, p, 1 << 49, 0, None) == capi.GEMM_ERR_INVALID_LD
+    assert f(4, 4, 8, p, 8, None, 8, p, 4, 0, None) == capi.GEMM_ERR_NULL_PTR
+    assert f(4, 4, 8, p, 8, p + 1, 8, p, 4, 0, None) == capi.GEMM_ERR_MISALIGNED
+
+
 def test_options():
     assert capi.gemm_set_option("pair", 1) == 0
     assert capi.gemm_set_option("pair", -1) == 0
