@@ -50,13 +50,13 @@ __global__ void __launch_bounds__(kFbThreads)
     const int tid = threadIdx.x;
     const int tmi = tid & 15, tni = tid >> 4;
     float acc[4][4] = {};
-    for (int k0 = 0; k0 < K; k0 += kFbBK) {
+    for (int64_t k0 = 0; k0 < K; k0 += kFbBK) {  // 64-bit: K may be 2^31 - 1
 #pragma unroll
         for (int r = 0; r < (kFbBM * kFbBK) / kFbThreads; ++r) {
             const int e = tid + r * kFbThreads;
             const int row = e / kFbBK, kk = e % kFbBK;
             const int64_t m = m0 + row, n = n0 + row;
-            const int k = k0 + kk;
+            const int64_t k = k0 + kk;
             As[kk][row] = (m < M && k < K) ? decode_in<IN>(A, m * lda + k) : 0.f;
             Bs[kk][row] = (n < N && k < K) ? decode_in<IN>(B, n * ldb + k) : 0.f;
         }

@@ -247,7 +247,10 @@ int gemm_read_watchdog(int reset);
  *   "group"       tile-rasteriser group size in tile rows, 1..64 (default 8)
  *   "path"        0 auto (default), 1 force the CUDA-core kernel, 2 force the
  *                 tensor-core kernel's load-based producer (as for unaligned rows)
- *   "timeout_ns"  device wait limit in ns, 1e6..6e10 (default 2e9)
+ *   "timeout_ns"  device wait limit in ns, 1e6..6e10 (default 2e9).  The longest
+ *                 wait lasts one tile's whole K loop (one K piece when K is split),
+ *                 so calls with K in the hundreds of millions and no split-K need
+ *                 a larger limit
  *   "max_ctas"    cap on persistent CTAs, 0 = one per SM (default)
  *   "tile_q"      output tile width along M (= MMA N): 0 auto (default, by
  *                 padding cost; 16 or 32 when all of M fits in one such tile and

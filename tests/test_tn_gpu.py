@@ -70,6 +70,53 @@ def test_pm1_long_k_bitexact(kind, pair_mode):
     assert_codes_equal(out_codes(C, M, N), exact_codes(kind, exact))
 
 
+@pytest.mark.parametrize("kind", ["bf16", "e4m3"])
+def test_max_k_sparse_exact(kind):
+    """K = 2^31 - 1, the largest K the ABI accepts.  A (1 x K) and B (2 x K)
+    are zero except at five k spread over the whole range (0, 1, 2^30, K - 2
+    and K - 1, the last two in the final, ragged K stage), so each output is a
+    sum of at most five products of powers of two, exact in every format.  The
+    element just past K (inside the padded rows) holds a large value that must
+    not be read.  The call splits K over a workspace (16 pieces of 2^21 K
+    stages, 2^20 for FP8), with the device wait limit raised for the pieces'
+    long K loops; every K coordinate stays below 2^31."""
+    K = (1 << 31) - 1
+    M, N, ld, ldc = 1, 2, 1 << 31, 8
+    dt = torch.bfloat16 if kind == "bf16" else torch.float8_e4m3fn
+    A = torch.zeros((M, ld), dtype=dt, device="cuda")
+    B = torch.zeros((N, ld), dtype=dt, device="cuda")
+    for k, v in zip([0, 1, 1 << 30, K - 2, K - 1], [1.0, 2.0, 4.0, 8.0, 16.0]):
+        A[0, k] = v
+        B[0, k] = 1.0
+    B[1, K - 1] = 0.5
+    B[1, 0] = 0.25
+    A[0, K] = 64.0          # past K: outside the matrix
+    B[0, K] = 1.0
+    B[1, K] = 1.0
+    C = torch.full((N, ldc), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    st, plan = capi.gemm_tn_plan(kind, M, N, K, workspace_bytes=ws.numel())
+    assert st == 0 and plan["splits"] == 16
+    assert capi.gemm_set_workspace(ws.data_ptr(), ws.numel()) == 0
+    assert capi.gemm_set_option("timeout_ns", 30_000_000_000) == 0
+    try:
+        if kind == "bf16":
+            st = capi.gemm_bf16_tn(M, N, K, A.data_ptr(), ld, B.data_ptr(), ld, C.data_ptr(),
+                                   ldc, None)
+        else:
+            st = capi.gemm_fp8_tn(M, N, K, A.data_ptr(), ld, B.data_ptr(), ld, 1.0, 1.0,
+                                  C.data_ptr(), ldc, None)
+        assert st == 0
+        torch.cuda.synchronize()
+        assert capi.gemm_read_watchdog(1) == capi.GEMM_OK
+    finally:
+        capi.gemm_set_option("timeout_ns", 2_000_000_000)
+        capi.gemm_set_workspace(None, 0)
+    assert C[0, 0].item() == 31.0           # 1 + 2 + 4 + 8 + 16
+    assert C[1, 0].item() == 8.25           # 16 x 0.5 + 1 x 0.25
+    assert torch.isnan(C[:, 1:].float()).all()   # C's padding past M untouched
+
+
 @pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("n", [64, 384, 640])
 def test_identity_bitexact(kind, n, pair_mode):
