@@ -542,12 +542,9 @@ def run_ours(args):
             # FP32, so it is not the same metric: context below, no ratio here.
             "vs_baseline": None,
             "dtype": "f16", "data": "synthetic",
-            "config": {"workload": "fp16_tn_8192x8192x8192", "M": M, "N": N, "K": K,
-                       "layout": "TN: A row-major, B column-major, C column-major (ld=M)",
-                       "accumulate": "f32", "values": "N(0,1)*0.1, seed 2",
+            "config": {**workload_config(world), "accumulate": "f32",
                        "l2": "3 rotating input sets (1.1 GiB total) >> 129 MB L2, no flush",
                        "workspace_bytes": WORKSPACE_BYTES,
-                       "parallelism": "replicas" if world > 1 else "single",
                        "pages_context": "best FP16 8192^3 on the pages: 142.30 TFLOP/s (RX 9070 "
                                         "XT, FP16 accumulation); compare per_dtype."
                                         "f16_acc16_tn_8192"},
@@ -690,6 +687,14 @@ def load_traffic():
 
 # -------------------------------------------------------- reference arm
 
+def workload_config(world: int) -> dict:
+    """The workload part of the line's config, the same on both arms."""
+    return {"workload": "fp16_tn_8192x8192x8192", "M": 8192, "N": 8192, "K": 8192,
+            "layout": "TN: A row-major, B column-major, C column-major (ld=M)",
+            "values": "N(0,1)*0.1, seed 2",
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 def run_reference(args):
     """The oracle on the host cores, on the same metric and workload: each step
     is a bounded sample of the FP16 8192^3 problem."""
@@ -719,7 +724,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total / len(times) * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "fp16_tn_8192x8192x8192", "M": M, "N": N, "K": K},
+            "config": {**workload_config(world), "accumulate": "f64 (the oracle)"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
