@@ -748,7 +748,9 @@ extern "C" {
 
 int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
              int64_t ldb, float* C, int64_t ldc, void* stream_v) {
-    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    // The SIMT kernel forms K + 7 in 32 bits to count its K slices of 8, so K
+    // stops 7 short of the general limit.
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim - 7)
         return GEMM_ERR_INVALID_DIM;
     const int64_t nmin = N > 1 ? N : 1;
     if (lda < (K > 1 ? K : 1) || ldb < nmin || ldc < nmin || lda > kMaxLd || ldb > kMaxLd ||

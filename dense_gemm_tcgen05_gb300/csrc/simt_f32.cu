@@ -120,8 +120,7 @@ __device__ __forceinline__ void sgemm_tile(int M, int N, int K, const float* __r
 #pragma unroll
         for (int j = 0; j < 2 * kGroups; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
-    // K + kBK - 1 in 64 bits: K may be 2^31 - 1
-    const int ktiles = static_cast<int>((static_cast<int64_t>(K) + kBK - 1) / kBK);
+    const int ktiles = (K + kBK - 1) / kBK;
     store_a(0, load_a(0));
     store_b(0, load_b(0));
     __syncthreads();

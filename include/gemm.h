@@ -60,7 +60,8 @@ extern "C" {
  *   C[m*ldc + n]             ldc >= max(1, N)
  *
  * Products and sums in FP32 (fused multiply-add), one rounding per step.
- * A, B and C must be 4-byte aligned.
+ * A, B and C must be 4-byte aligned.  K is at most 2^31 - 8 here (the kernel
+ * counts K slices of 8 in 32 bits); a larger K returns GEMM_ERR_INVALID_DIM.
  */
 int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
              int64_t ldb, float* C, int64_t ldc, void* stream);

@@ -94,6 +94,9 @@ def test_fp8_and_f32_argument_errors_without_gpu():
     assert f6(4, 5, 6, p, 6, p, 5, p, 4) == capi.GEMM_ERR_INVALID_LD
     assert f6(4, 5, 6, p, 6, None, 5, p, 5) == capi.GEMM_ERR_NULL_PTR
     assert f6(4, 5, 6, p, 6, p, 5, p + 2, 5) == capi.GEMM_ERR_MISALIGNED
+    # the SIMT kernel's K limit is 2^31 - 8
+    assert capi.gemm_f32(4, 5, (1 << 31) - 7, p, 1 << 31, p, 5, p, 5) == capi.GEMM_ERR_INVALID_DIM
+    assert capi.gemm_f32(4, 5, (1 << 31) - 8, p, 1 << 31, p, 5, p, 4) == capi.GEMM_ERR_INVALID_LD
     big = (1 << 48) + 4
     for fn in (capi.gemm_f32, f6):
         assert fn(4, 5, 6, p, big, p, 5, p, 5) == capi.GEMM_ERR_INVALID_LD
