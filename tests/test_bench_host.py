@@ -73,3 +73,34 @@ def test_reference_arm_line(capsys):
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["metric"] == bench.METRIC
+
+
+def test_traffic_only_while_the_kernel_matches_its_profile(tmp_path, monkeypatch):
+    """The line's roofline.traffic comes from the committed ncu summary and is
+    reported only while the kernel's sources hash to the value recorded there;
+    after any change to them it is null."""
+    csrc = tmp_path / "dense_gemm_tcgen05_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for name in bench.KERNEL_SOURCES:
+        (csrc / name).write_text("// %s\n" % name)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "profiles").mkdir()
+    summary = tmp_path / "profiles" / "tc_gemm_f16_8192.txt"
+    summary.write_text("kernel_source_sha256: %s\ntraffic_bytes_per_launch: 1259031552\n"
+                       % bench.kernel_source_hash())
+    assert bench.load_traffic() == 1259031552
+    (csrc / bench.KERNEL_SOURCES[0]).write_text("// changed\n")
+    assert bench.load_traffic() is None
+    summary.unlink()
+    assert bench.load_traffic() is None
+
+
+def test_committed_profile_names_its_traffic():
+    """The committed FP16 8192^3 summary carries the two fields the bench reads."""
+    fields = {}
+    for line in open(os.path.join(bench.ROOT, "profiles", "tc_gemm_f16_8192.txt")):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    assert len(fields["kernel_source_sha256"]) == 64
+    assert int(float(fields["traffic_bytes_per_launch"])) > 384 << 20   # above the compulsory bytes
