@@ -6,7 +6,8 @@ M = N = K = 8192, A row-major, B column-major, C column-major, FP32
 accumulation, entries N(0,1)*0.1 (seed 2).  The line also reports BF16 and
 FP8-E4M3 at 8192^3 and the FP32 SIMT path at 4096^3, each against its dense
 peak, the end-to-end rate with host buffers, the kernel's roofline fraction,
-the SM clocks seen while timing, and the CPU oracle timed on a bounded sample.
+the SM clocks seen while timing, the CPU oracle timed on a bounded sample, and
+the main call's per-launch mean, median and min with L2 warm and flushed.
 
 Timing: W untimed warm-up steps, then exactly K steps between a barrier and a
 synchronize on each side, timed with CUDA events on the launching stream.
@@ -312,6 +313,44 @@ def e2e_loop(kind, M, N, K, ops, steps, warmup, stream, stream_h):
     return ms, serial_ms, h2d, d2h, copy_ms
 
 
+def l2_modes(ops, M, N, K, stream, stream_h, launches=30, warmup=10):
+    """Per-launch CUDA-event times of the main call in two L2 modes: "warm",
+    the same operands at every launch, and "cold", a 512 MiB buffer (four
+    times L2) written between launches, outside the events.  Mean, median
+    and min per launch for each."""
+    import torch
+
+    a = ops["A"].to("cuda")
+    b = ops["B"].to("cuda")
+    c = torch.empty((N, M), dtype=torch.float16, device="cuda")
+    call = tn_call("f16", M, N, K, 1.0, 1.0, stream_h)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    flops = 2.0 * M * N * K
+    out = {"launches": launches, "flush_bytes": flush.numel()}
+    for mode in ("warm", "cold"):
+        events = []
+        with torch.cuda.stream(stream):
+            for i in range(warmup + launches):
+                if mode == "cold":
+                    flush.fill_(i & 0xFF)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call(a, b, c)
+                e1.record(stream)
+                if i >= warmup:
+                    events.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = sorted(e0.elapsed_time(e1) for e0, e1 in events)
+        median = statistics.median(ms)
+        out[mode] = {"mean_ms": round(sum(ms) / len(ms), 4), "median_ms": round(median, 4),
+                     "min_ms": round(ms[0], 4),
+                     "tflops_at_median": round(flops / (median * 1e-3) / 1e12, 1)}
+    del a, b, c, flush
+    torch.cuda.empty_cache()
+    return out
+
+
 def f32_bench(n, steps, warmup, stream, stream_h):
     import torch
 
@@ -533,6 +572,10 @@ def run_ours(args):
         e2e_steps = max(3, min(args.steps, 20))
         e_ms, serial_ms, h2d, d2h, copy_ms = e2e_loop("f16", M, N, K, ops, e2e_steps, 2, stream,
                                              stream_h)
+        try:
+            l2 = l2_modes(ops, M, N, K, stream, stream_h)
+        except Exception as exc:  # an auxiliary figure must not cost the line itself
+            l2 = {"error": "%s: %s" % (type(exc).__name__, exc)}
         traffic = load_traffic()
         result = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -572,6 +615,7 @@ def run_ours(args):
             "gpu_launches": args.steps,
             "clocks": clocks,
             "per_dtype": per,
+            "l2_modes": l2,
         }
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline()

@@ -28,6 +28,11 @@ def test_bench_line_contract():
     assert rf["bound"] == "tensor" and rf["unit"] == "TFLOP/s"
     assert rf["achieved"] > 0 and rf["peak"] > 0
     assert rf["frac"] == pytest.approx(rf["achieved"] / rf["peak"], rel=1e-3)
+    l2 = line["l2_modes"]
+    assert "error" not in l2, l2
+    for mode in ("warm", "cold"):
+        t = l2[mode]
+        assert 0 < t["min_ms"] <= t["median_ms"] and t["min_ms"] <= t["mean_ms"]
     assert rf["traffic"] is None or rf["traffic"] > 0
     e2e = line["e2e"]
     assert e2e["value"] > 0 and e2e["unit"] == "TFLOP/s"
