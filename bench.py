@@ -625,6 +625,12 @@ def run_ours(args):
     return result
 
 
+def compulsory_bytes(kind, M, N, K, out_f32=False) -> int:
+    """Bytes a TN call must move at least: A and B read once, C written once."""
+    es = 1 if kind == "e4m3" else 2
+    return (M * K + N * K) * es + M * N * (4 if out_f32 else 2)
+
+
 def sweep(stream, stream_h, burst, workspace):
     """The BF16 and FP8 shape sweeps (configs 4 and 5), one line each.  The
     first part runs without a registered workspace (the odd shapes' tight
@@ -656,7 +662,8 @@ def sweep(stream, stream_h, burst, workspace):
         tf = 2.0 * M * N * K / (lm * 1e-3) / 1e12
         peak = burst * (FP8_OVER_BF16 if kind == "e4m3" else 1.0)
         key = "%s%s_%dx%dx%d" % (kind, "_f32out" if f32 else "", M, N, K)
-        out[key] = {"tflops": round(tf, 1), "frac": round(tf / peak, 4)}
+        out[key] = {"tflops": round(tf, 1), "frac": round(tf / peak, 4),
+                    "gbs": round(compulsory_bytes(kind, M, N, K, f32) / (lm * 1e-3) / 1e9)}
         del s
         torch.cuda.empty_cache()
     # Skinny and small shapes: HBM-bound, reported in GB/s of compulsory
@@ -672,8 +679,9 @@ def sweep(stream, stream_h, burst, workspace):
         with torch.cuda.stream(stream):
             _, lm = timed_loop(c, s, 20, 3, stream)
         tf = 2.0 * M * N * K / (lm * 1e-3) / 1e12
-        out["%s_%dx%dx%d_ws" % (kind, M, N, K)] = {"tflops": round(tf, 1),
-                                                   "frac": round(tf / burst, 4)}
+        out["%s_%dx%dx%d_ws" % (kind, M, N, K)] = {
+            "tflops": round(tf, 1), "frac": round(tf / burst, 4),
+            "gbs": round(compulsory_bytes(kind, M, N, K) / (lm * 1e-3) / 1e9)}
         del s
         torch.cuda.empty_cache()
     for kind, (M, N, K) in [("bf16", (16, 8192, 8192)), ("bf16", (128, 8192, 8192)),
@@ -683,8 +691,7 @@ def sweep(stream, stream_h, burst, workspace):
         c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h)
         with torch.cuda.stream(stream):
             _, lm = timed_loop(c, s, 30, 3, stream)
-        es = 1 if kind == "e4m3" else 2
-        gbs = ((M * K + N * K) * es + M * N * 2) / (lm * 1e-3) / 1e9
+        gbs = compulsory_bytes(kind, M, N, K) / (lm * 1e-3) / 1e9
         out["%s_skinny_%dx%dx%d" % (kind, M, N, K)] = {
             "tflops": round(2.0 * M * N * K / (lm * 1e-3) / 1e12, 1), "gbs": round(gbs),
             "hbm_frac": round(gbs / hbm, 3), "us": round(lm * 1e3, 1)}

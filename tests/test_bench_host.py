@@ -104,3 +104,14 @@ def test_committed_profile_names_its_traffic():
             fields[k.strip()] = v.strip()
     assert len(fields["kernel_source_sha256"]) == 64
     assert int(float(fields["traffic_bytes_per_launch"])) > 384 << 20   # above the compulsory bytes
+
+
+def test_compulsory_bytes():
+    """A and B read once, C written once: 384 MiB at FP16 8192^3, 256 MiB for
+    FP8 8192^3 with BF16 output, 384 MiB with FP32 output, about 22.6 MB for
+    the ragged BF16 2047 x 3001 x 1023 case."""
+    assert bench.compulsory_bytes("f16", 8192, 8192, 8192) == 384 << 20
+    assert bench.compulsory_bytes("e4m3", 8192, 8192, 8192) == 256 << 20
+    assert bench.compulsory_bytes("e4m3", 8192, 8192, 8192, out_f32=True) == 384 << 20
+    assert bench.compulsory_bytes("bf16", 2047, 3001, 1023) == (2047 * 1023 + 3001 * 1023 +
+                                                                2047 * 3001) * 2
