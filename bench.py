@@ -440,14 +440,9 @@ def fp32_alu_peak_tflops(sms: int, mhz: float) -> float:
     return sms * 128 * 2 * mhz * 1e6 / 1e12
 
 
-def cpu_baseline(kind="f16", M=8192, N=8192, K=8192, seed=2, sigma=0.1, budget_s=12.0):
-    """The oracle, as it stands, on a bounded sample of the workload: random
-    output elements of the same problem, each one K-long FP64 dot product."""
-    import oracle
-    import synthetic_inputs as si
-
-    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=seed, sigma=sigma)
-    a, b = si.codes(ops["A"]), si.codes(ops["B"])
+def _oracle_sample_rate(oracle, si, kind, M, N, K, a, b, seed, budget_s):
+    """Times the oracle on a growing number of random output elements until
+    one timing takes `budget_s`; returns (TFLOP/s, elements, seconds)."""
     count = 512
     elapsed = 0.0
     while True:
@@ -458,10 +453,32 @@ def cpu_baseline(kind="f16", M=8192, N=8192, K=8192, seed=2, sigma=0.1, budget_s
         if elapsed >= budget_s or count >= 1 << 26:
             break
         count = int(count * min(16.0, max(2.0, budget_s / max(elapsed, 1e-3))))
-    tflops = 2.0 * K * count / elapsed / 1e12
-    return {"value": tflops, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+    return 2.0 * K * count / elapsed / 1e12, count, elapsed
+
+
+def cpu_baseline(kind="f16", M=8192, N=8192, K=8192, seed=2, sigma=0.1, budget_s=12.0,
+                 one_core_budget_s=3.0):
+    """The oracle, as it stands, on a bounded sample of the workload: random
+    output elements of the same problem, each one K-long FP64 dot product.
+    Timed on all the cores OpenMP uses, then on one core."""
+    import oracle
+    import synthetic_inputs as si
+
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=seed, sigma=sigma)
+    a, b = si.codes(ops["A"]), si.codes(ops["B"])
+    cores = oracle.num_threads()
+    tflops, count, elapsed = _oracle_sample_rate(oracle, si, kind, M, N, K, a, b, seed, budget_s)
+    oracle.set_num_threads(1)
+    try:
+        one, count1, elapsed1 = _oracle_sample_rate(oracle, si, kind, M, N, K, a, b, seed,
+                                                    one_core_budget_s)
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": tflops, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": "%d random output elements of the %s TN %dx%dx%d problem (each a %d-long "
-                      "FP64 dot product), %.1f s" % (count, kind, M, N, K, K, elapsed)}
+                      "FP64 dot product), %.1f s" % (count, kind, M, N, K, K, elapsed),
+            "one_core": {"value": one, "unit": UNIT, "cores": 1,
+                         "sample": "%d elements, %.1f s" % (count1, elapsed1)}}
 
 
 def run_ours(args):

@@ -69,6 +69,8 @@ def _load():
         lib.oracle_gemm_f32_sampled.restype = i32
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
+        lib.oracle_set_num_threads.argtypes = [i32]
+        lib.oracle_set_num_threads.restype = i32
         _lib = lib
         return lib
 
@@ -95,6 +97,11 @@ def _ptr(a: np.ndarray) -> int:
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> int:
+    """Threads for later oracle calls (n >= 1); returns the count in effect."""
+    return int(_load().oracle_set_num_threads(int(n)))
 
 
 def decode(dtype, codes: np.ndarray) -> np.ndarray:

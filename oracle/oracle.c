@@ -293,3 +293,15 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Sets the number of threads later OpenMP regions here use (n >= 1), so that
+ * the benchmark can also time the oracle on one core.  Returns the count now
+ * in effect. */
+int oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+    return oracle_num_threads();
+}

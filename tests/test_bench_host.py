@@ -115,3 +115,15 @@ def test_compulsory_bytes():
     assert bench.compulsory_bytes("e4m3", 8192, 8192, 8192, out_f32=True) == 384 << 20
     assert bench.compulsory_bytes("bf16", 2047, 3001, 1023) == (2047 * 1023 + 3001 * 1023 +
                                                                 2047 * 3001) * 2
+
+
+def test_cpu_baseline_reports_all_cores_and_one():
+    """The CPU baseline times the oracle on all its threads, then on one, and
+    leaves the thread count as it found it."""
+    import oracle
+
+    before = oracle.num_threads()
+    r = bench.cpu_baseline(M=256, N=256, K=256, budget_s=0.05, one_core_budget_s=0.05)
+    assert r["kind"] == "oracle" and r["cores"] == before and r["value"] > 0
+    assert r["one_core"]["cores"] == 1 and r["one_core"]["value"] > 0
+    assert oracle.num_threads() == before
