@@ -189,3 +189,33 @@ def test_sizes_beyond_any_device_plan_without_overflow(options):
     flags = ALIGNED & ~(capi.PLAN_A_TMA | capi.PLAN_A_128)
     p = plan("bf16", top, top, top, flags=flags, workspace_bytes=(1 << 62))
     assert (p["copy_a"], p["producer"]) == (0, 1)   # A's copy cannot fit either
+
+
+@pytest.mark.parametrize("M,q", [(192, 192), (200, 256), (384, 192), (640, 128)])
+def test_tile_width_by_padding_cost(M, q):
+    """Pair tiles (N = 32768 fills many waves): the width t minimising
+    ceil(M / t) * max(t, 96), ties to the wider tile.  M = 200: 256 and 128
+    both cost 256, so 256; M = 640: 128 costs 640 against 768 for 256 and 192."""
+    p = plan("bf16", M, 32768, 4096)
+    assert p["pair"] == 1 and p["tile_q"] == q
+
+
+def test_repack_threshold_boundary():
+    """Rows 16- but not 128-byte aligned are copied when MN / (M + N) >= 1100 x
+    element size: BF16 M = N = 4400 gives exactly 2200 (copied), 4398 gives
+    2199 (not)."""
+    flags = ALIGNED & ~capi.PLAN_A_128
+    assert plan("bf16", 4400, 4400, 4096, flags=flags, workspace_bytes=WS)["copy_a"] == 1
+    assert plan("bf16", 4398, 4398, 4096, flags=flags, workspace_bytes=WS)["copy_a"] == 0
+
+
+@pytest.mark.parametrize("kind", ["f16", "e4m3"])
+def test_last_wave_cost_model(kind):
+    """86 pair tiles on 76 pair slots leave 10: quarter-width units (one wave
+    at 0.65, or 0.8 for FP8, of a tile's time) beat half-width ones (0.8 / 0.9)
+    and the whole tiles (1.0).  146 tiles leave 70: cut in two they would need
+    two waves (1.6), so the last wave stays whole."""
+    p = plan(kind, 256, 256 * 86, 4096)
+    assert (p["tiles_p"], p["tiles_q"], p["tail_f"], p["tail_ksplit"]) == (86, 1, 4, 0)
+    p = plan(kind, 256, 256 * 146, 4096)
+    assert (p["tiles_p"], p["tail_f"]) == (146, 1)
