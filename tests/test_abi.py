@@ -204,6 +204,15 @@ def test_rasteriser_bijection_and_bands(tiles_m, tiles_n, group):
     assert capi.gemm_tile_coord(tiles_m * tiles_n, tiles_m, tiles_n, group)[0] != 0
 
 
+def test_rasteriser_hand_listed_order():
+    """3 x 2 tiles in bands of 2 rows, listed by hand: the first band walks
+    down its two rows, then moves one column right; the short last band (one
+    row) follows."""
+    expect = [(0, 0), (1, 0), (0, 1), (1, 1), (2, 0), (2, 1)]
+    got = [capi.gemm_tile_coord(t, 3, 2, 2)[1:] for t in range(6)]
+    assert got == expect
+
+
 def test_tuner_shape_parser():
     from dense_gemm_tcgen05_gb300 import tune
 
