@@ -145,7 +145,8 @@ class ClockSampler:
             if len(parts) < 10:
                 continue
             rows.append((ts, parts))
-        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.05 <= r[0] <= self.t1 + 0.15]
+        timed = self.t0 is not None and self.t1 is not None
+        inside = [r for r in rows if timed and self.t0 - 0.05 <= r[0] <= self.t1 + 0.15]
         use = inside or rows
         sm = [float(p[2]) for _, p in use if p[2].replace(".", "").isdigit()]
         mx = [float(p[3]) for _, p in use if p[3].replace(".", "").isdigit()]

@@ -61,6 +61,10 @@ def test_clock_parser():
     out = s.stop()
     assert out["sm_mhz"] == 1900 and out["sm_max_mhz"] == 2070
     assert out["reasons"] == ["sw_power_cap"] and out["samples_in_window"] == 3
+    # a window that was opened but never closed: every sample is used, no error
+    s.t1 = None
+    out = s.stop()
+    assert out["samples_in_window"] == 0 and out["samples"] == 4
 
 
 def test_fp32_alu_peak():
