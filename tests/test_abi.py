@@ -218,3 +218,39 @@ def test_tuner_shape_parser():
 
     assert tune._parse("f16:8192x28672x8192") == ("f16", 8192, 28672, 8192)
     assert all(tune._parse(s)[0] in ("f16", "bf16", "e4m3") for s in tune.DEFAULT_SHAPES)
+
+
+def test_binding_signatures_match_the_prototypes():
+    """Every ctypes signature in the binding has the argument and return types
+    of its prototype in include/gemm.h, position by position."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", open(capi.HEADER).read(), flags=re.S)
+    protos = {}
+    for m in re.finditer(r"^\s*([A-Za-z_][\w ]*?[\w\*])\s*(\**)\s*(gemm_\w+)\s*\(([^)]*)\)\s*;",
+                         text, flags=re.M):
+        ret = (m.group(1) + m.group(2)).replace(" ", "")
+        params = [p.strip() for p in m.group(4).split(",") if p.strip() not in ("", "void")]
+        protos[m.group(3)] = (ret, params)
+    assert set(protos) == set(capi._SIGNATURES)
+
+    def ctype_of(decl):
+        decl = re.sub(r"\b(const)\b", "", decl)
+        decl = re.sub(r"\s+", " ", decl).strip()
+        typ = re.sub(r"\s*\w+$", "", decl) if not decl.endswith("*") else decl
+        typ = typ.replace(" ", "")
+        if typ.endswith("*"):
+            if typ == "char*":
+                return ctypes.c_char_p
+            if typ == "int64_t*":
+                return ctypes.POINTER(ctypes.c_int64)
+            return ctypes.c_void_p
+        return {"int64_t": ctypes.c_int64, "int": ctypes.c_int, "float": ctypes.c_float}[typ]
+
+    for name, (ret, params) in protos.items():
+        args, res = capi._SIGNATURES[name]
+        assert len(args) == len(params), name
+        for a, p in zip(args, params):
+            assert a == ctype_of(p), (name, p)
+        want_ret = {"int": ctypes.c_int, "int64_t": ctypes.c_int64,
+                    "constchar*": ctypes.c_char_p}[ret]
+        assert res == want_ret, (name, ret)
