@@ -3,6 +3,7 @@ builds for sm_103a, loads, exports every function include/gemm.h declares,
 rejects bad arguments before touching the GPU, and its tile rasteriser is a
 bijection with the grouped order the pages describe."""
 import ctypes
+import os
 
 import pytest
 
@@ -254,3 +255,29 @@ def test_binding_signatures_match_the_prototypes():
         want_ret = {"int": ctypes.c_int, "int64_t": ctypes.c_int64,
                     "constchar*": ctypes.c_char_p}[ret]
         assert res == want_ret, (name, ret)
+
+
+def test_product_and_oracle_share_nothing():
+    """The product (the package, its CUDA sources and the header) never imports,
+    loads or includes the oracle, and the oracle includes only the C standard
+    library and OpenMP: the two implementations share no code."""
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    product = []
+    for d in ("dense_gemm_tcgen05_gb300", "include"):
+        for dirpath, _, files in os.walk(os.path.join(root, d)):
+            product += [os.path.join(dirpath, f) for f in files
+                        if f.endswith((".py", ".cu", ".cuh", ".h"))]
+    assert len(product) > 10
+    for path in product:
+        code = open(path).read()
+        if path.endswith(".py"):
+            code = re.sub(r"#[^\n]*", "", code)                      # comments
+        else:
+            code = re.sub(r"//[^\n]*|/\*.*?\*/", "", code, flags=re.S)
+        assert not re.search(r"^\s*(import|from)\s+oracle\b", code, flags=re.M), path
+        assert "liboracle" not in code and "oracle.c" not in code, path
+        assert not re.search(r'#include\s*[<"][^>"]*oracle', code), path
+    includes = re.findall(r'#include\s*[<"]([^>"]+)[>"]',
+                          open(os.path.join(root, "oracle", "oracle.c")).read())
+    assert set(includes) <= {"math.h", "stdint.h", "stdlib.h", "string.h", "omp.h"}, includes
