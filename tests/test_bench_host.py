@@ -77,6 +77,11 @@ def test_reference_arm_line(capsys):
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["metric"] == bench.METRIC
+    # the same workload as this library's arm, which adds its own keys to it
+    cfg = dict(line["config"])
+    assert cfg.pop("accumulate") == "f64 (the oracle)"
+    assert cfg == bench.workload_config(1)
+    assert line["higher_is_better"] is True and line["scaling"] == "weak"
 
 
 def test_traffic_only_while_the_kernel_matches_its_profile(tmp_path, monkeypatch):
