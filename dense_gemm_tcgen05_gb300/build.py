@@ -23,7 +23,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgemm.so")
 
 SOURCES = ["api.cu", "tc_gemm_f16.cu", "tc_gemm_bf16.cu", "tc_gemm_bf16f32.cu", "tc_gemm_fp8.cu",
-           "tc_gemm_mc.cu", "simt_f32.cu", "split_f32.cu", "misc_kernels.cu", "noalloc.cu"]
+           "simt_f32.cu", "split_f32.cu", "misc_kernels.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -50,15 +50,15 @@ _SIGNATURES = {
     "gemm_workspace_bytes": ([_i64, _i64, _i64], _i64),
     "gemm_f32_bf16x6": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp], _int),
     "gemm_f32_bf16x6_workspace_bytes": ([_i64, _i64, _i64], _i64),
-    "gemm_tn_plan": ([_int, _i64, _i64, _i64, _int, _i64, _int, _int, ctypes.POINTER(_i64),
-                      _int], _int),
+    "gemm_tn_plan": ([_int, _i64, _i64, _i64, _int, _i64, _int, ctypes.POINTER(_i64), _int],
+                     _int),
 }
 
 PLAN_KINDS = {"f16": 0, "bf16": 1, "e4m3": 2, "f16_acc16": 3, "e4m3_f32out": 4}
 PLAN_A_TMA, PLAN_B_TMA, PLAN_C_TMA, PLAN_A_128, PLAN_B_128 = 1, 2, 4, 8, 16
 PLAN_ALIGNED = PLAN_A_TMA | PLAN_B_TMA | PLAN_C_TMA | PLAN_A_128 | PLAN_B_128
 PLAN_FIELDS = ("status", "pair", "producer", "tile_q", "half", "splits", "tail_f", "tail_ksplit",
-               "stages", "grid", "copy_a", "copy_b", "multicast", "tiles_p", "tiles_q",
+               "stages", "grid", "copy_a", "copy_b", "tiles_p", "tiles_q",
                "kb_per_split", "tail_kb_per", "stage_bytes")
 
 
@@ -116,11 +116,11 @@ def gemm_f32_bf16x6_workspace_bytes(M: int, N: int, K: int) -> int:
 
 
 def gemm_tn_plan(kind: str, M: int, N: int, K: int, flags: int = PLAN_ALIGNED,
-                 workspace_bytes: int = 0, sms: int = 152, mc_clusters: int = 36):
+                 workspace_bytes: int = 0, sms: int = 152):
     """(status, plan dict) of what a TN call would run (no GPU needed)."""
     out = (_i64 * len(PLAN_FIELDS))()
-    st = lib().gemm_tn_plan(PLAN_KINDS[kind], M, N, K, flags, workspace_bytes, sms, mc_clusters,
-                            out, len(PLAN_FIELDS))
+    st = lib().gemm_tn_plan(PLAN_KINDS[kind], M, N, K, flags, workspace_bytes, sms, out,
+                            len(PLAN_FIELDS))
     return st, dict(zip(PLAN_FIELDS, (int(v) for v in out)))
 
 

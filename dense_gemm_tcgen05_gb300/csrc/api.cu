@@ -79,7 +79,6 @@ std::atomic<int> g_opt_tail{0};
 std::atomic<int> g_opt_tail_k{0};
 std::atomic<int> g_opt_repack{0};
 std::atomic<int> g_opt_f32_tail{0};
-std::atomic<int> g_opt_cluster{0};
 std::atomic<int> g_opt_l2hints{0};
 std::atomic<int> g_opt_half{0};
 std::atomic<int64_t> g_opt_timeout_ns{2000000000LL};
@@ -172,8 +171,6 @@ int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 // size never does, however large the room.
 bool fits(int64_t need, int64_t room) { return need < kSatBytes && need <= room; }
 
-constexpr int kMcStageRegion = 200 * 1024;  // ring of the multicast kernel (tc_gemm_mc.cuh)
-
 // What a TN call is given, for planning: shapes, what TMA can address, the
 // scratch available, and the device.
 struct TnPlanIn {
@@ -187,7 +184,6 @@ struct TnPlanIn {
     int ov_splits;              // -1: option "splits" applies; else the override's value
     bool strict;                // a chosen split that does not fit fails
     int sms;                    // SMs of the device
-    int mc_clusters;            // resident clusters of four of the multicast kernel
 };
 
 // Everything gemm_tn decides before it encodes tensor maps and launches.
@@ -197,7 +193,7 @@ struct TnPlan {
     int64_t dp = 0;             // repacked row pitch in bytes
     int64_t ws_used = 0;        // scratch bytes taken by the repacks
     Producer prod = Producer::Tma;
-    bool pair = false, half = false, mc = false;
+    bool pair = false, half = false;
     int tile_q = 0, load_q = 0;
     TcGeometry g{};
     int64_t tiles_p = 0, tiles_q = 0, tiles = 0, slots = 0;
@@ -431,27 +427,6 @@ TnPlan plan_tn(const TnPlanIn& a) {
             p.grid = static_cast<int>((units < slots ? units : slots) * g.cluster);
         }
     }
-    // Clusters of two pairs sharing P tiles through TMA multicast
-    // (tc_gemm_mc.cuh), option "cluster" = 4: only for pair tiles without
-    // split-K, tail splitting, FP16 accumulation or row-wise stores.
-    const int opt_cl = g_opt_cluster.load();
-    if (p.pair && p.prod == Producer::Tma && a.c_tma && !a.acc16 && p.splits == 1 &&
-        opt_cl == 4 && (a.in == InKind::E4M3 || !a.out_f32) && a.mc_clusters > 0) {
-        p.mc = true;
-        // the multicast kernel's ring: 200 KB of stages of this width
-        const int sb = ((g.load_p + p.load_q) * 128 + 1023) / 1024 * 1024;
-        int st_count = kMcStageRegion / sb;
-        if (st_count > g.max_stages) st_count = g.max_stages;
-        p.stages = st_count;
-        p.stage_bytes = sb;
-        p.tail_f = 1;
-        p.tail_ksplit = false;
-        p.full_units = tiles;
-        const int64_t units = p.tiles_p * ((p.tiles_q + 1) / 2);
-        int64_t clusters = units < a.mc_clusters ? units : a.mc_clusters;
-        if (cap > 0 && cap / 4 < clusters) clusters = cap / 4 > 0 ? cap / 4 : 1;
-        p.grid = static_cast<int>(clusters * 4);
-    }
     return p;
 }
 
@@ -467,20 +442,6 @@ CUresult encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, in
     return g_encode(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-}
-
-// Resident clusters of the multicast kernel per device, input kind and output
-// type, queried once (0 = not yet known).
-std::atomic<int> g_mc_clusters[kMaxDevices][4];
-
-cudaError_t mc_max_clusters(InKind in, bool out_f32, const DeviceInfo* dev, int* n) {
-    const int di = static_cast<int>(dev - g_devices);
-    const int vi = out_f32 ? 3 : static_cast<int>(in);
-    if ((*n = g_mc_clusters[di][vi].load()) > 0) return cudaSuccess;
-    cudaError_t e = tc_mc_max_clusters(in, out_f32, n);
-    if (e != cudaSuccess) return e;
-    g_mc_clusters[di][vi].store(*n);
-    return cudaSuccess;
 }
 
 // `ov`, when given, replaces the registered workspace and the "splits" option:
@@ -596,11 +557,6 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     pin.ov_splits = ov ? ov->splits : -1;
     pin.strict = ov && ov->strict;
     pin.sms = dev->sms;
-    pin.mc_clusters = 0;
-    if (g_opt_cluster.load() == 4 && (in == InKind::E4M3 || !out_f32)) {
-        e = mc_max_clusters(in, out_f32, dev, &pin.mc_clusters);
-        if (e != cudaSuccess) return fail_cuda(e);
-    }
     const TnPlan pl = plan_tn(pin);
     if (pl.status != GEMM_OK) return pl.status;
 
@@ -637,9 +593,7 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     const int tile_q = pl.tile_q, load_q = pl.load_q;
     CUresult r = CUDA_SUCCESS;
     if (prod == Producer::Tma) {
-        // the multicast kernel loads half of each pair's P block per CTA
-        r = encode_2d(&L.map_p, in_dt, B, K, N, ldb * es, g.stage_k,
-                      pl.mc ? g.load_p / 2 : g.load_p);
+        r = encode_2d(&L.map_p, in_dt, B, K, N, ldb * es, g.stage_k, g.load_p);
         if (r == CUDA_SUCCESS)
             r = encode_2d(&L.map_q, in_dt, A, K, M, lda * es, g.stage_k, load_q);
     }
@@ -713,17 +667,16 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
                                       static_cast<uint32_t>(width), d_format);
         L.prm.stage_tx_tail = static_cast<uint32_t>((g.load_p + load_qt) * 128);
     }
-    const bool mc = pl.mc;
     if (std::getenv("GEMM_DEBUG"))
         std::fprintf(stderr,
                      "[gemm] tn in=%d M=%lld N=%lld K=%lld pair=%d producer=%d direct_store=%d "
                      "splits=%d tile_q=%d tail=%d ktail=%d stages=%d tiles=%lldx%lld grid=%d "
-                     "multicast=%d half=%d\n",
+                     "half=%d\n",
                      int(in), (long long)M, (long long)N, (long long)K, int(pair), int(prod),
                      L.prm.direct_store, L.prm.splits, L.prm.tile_q, L.prm.tail_f,
                      L.prm.tail_ksplit, L.prm.stages,
-                     (long long)tiles_q, (long long)tiles_p, L.grid, int(mc), int(L.half));
-    e = mc ? tc_mc_launch(in, out_f32, L) : tc_launch(in, pair, prod, out_f32, L);
+                     (long long)tiles_q, (long long)tiles_p, L.grid, int(L.half));
+    e = tc_launch(in, pair, prod, out_f32, L);
     return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
 }
 
@@ -858,11 +811,11 @@ int gemm_f32_bf16x6(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda
 }
 
 int gemm_tn_plan(int kind, int64_t M, int64_t N, int64_t K, int flags, int64_t workspace_bytes,
-                 int sms, int mc_clusters, int64_t* out, int nout) {
+                 int sms, int64_t* out, int nout) {
     if (kind < GEMM_PLAN_F16 || kind > GEMM_PLAN_FP8_F32OUT || !out || nout < GEMM_PLAN_FIELDS)
         return GEMM_ERR_INVALID_OPTION;
     if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || sms <= 0 ||
-        workspace_bytes < 0 || mc_clusters < 0)
+        workspace_bytes < 0)
         return GEMM_ERR_INVALID_DIM;
     TnPlanIn pin;
     pin.in = kind == GEMM_PLAN_BF16 ? InKind::BF16
@@ -885,7 +838,6 @@ int gemm_tn_plan(int kind, int64_t M, int64_t N, int64_t K, int flags, int64_t w
     pin.ov_splits = -1;
     pin.strict = false;
     pin.sms = sms;
-    pin.mc_clusters = mc_clusters;
     const TnPlan pl = plan_tn(pin);
     const int64_t v[GEMM_PLAN_FIELDS] = {pl.status,
                                          pl.pair,
@@ -899,7 +851,6 @@ int gemm_tn_plan(int kind, int64_t M, int64_t N, int64_t K, int flags, int64_t w
                                          pl.grid,
                                          pl.copy_a,
                                          pl.copy_b,
-                                         pl.mc,
                                          pl.tiles_p,
                                          pl.tiles_q,
                                          pl.kb_per_split,
@@ -980,9 +931,6 @@ int gemm_set_option(const char* name, int64_t value) {
     } else if (!std::strcmp(name, "l2_hints")) {
         if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
         g_opt_l2hints.store(static_cast<int>(value));
-    } else if (!std::strcmp(name, "cluster")) {
-        if (!(value == 0 || value == 2 || value == 4)) return GEMM_ERR_INVALID_OPTION;
-        g_opt_cluster.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "f32_tail")) {
         if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
         g_opt_f32_tail.store(static_cast<int>(value));

@@ -8,13 +8,6 @@
 
 namespace gb300 {
 
-// The tensor-core kernel with clusters of two CTA pairs sharing P tiles
-// through TMA multicast (tc_gemm_mc.cuh): L as for a pair launch, but map_p
-// with 64-row boxes and L.grid a multiple of 4.
-cudaError_t tc_mc_launch(InKind in, bool out_f32, const TcLaunch& L);
-// Most clusters of four of that kernel that can be resident at once.
-cudaError_t tc_mc_max_clusters(InKind in, bool out_f32, int* n);
-
 // CUDA-core fallback for TN operands that TMA cannot address.
 cudaError_t tn_fallback_launch(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K,
                                const void* A, int64_t lda, const void* B, int64_t ldb, float scale,

@@ -3,9 +3,8 @@ library's tuning options on the given shapes and reports the fastest.
 
 The options swept are the ones gemm_set_option exposes -- CTA pairing
 ("pair"), the rasteriser's group size ("group"), the output tile width along M
-("tile_q"), split-K ("splits", with a workspace registered) and, for pairs,
-clusters of two pairs sharing B tiles by TMA multicast ("cluster" = 4) -- so
-a result can be applied directly.  The pages observe that no single tile configuration
+("tile_q") and split-K ("splits", with a workspace registered) -- so a
+result can be applied directly.  The pages observe that no single tile configuration
 is best everywhere ("FP16 GEMM Optimization on AMD RDNA 3 and RDNA 4",
 "Tuning Further"; "FP8 GEMM Optimization on AMD RDNA 4", "Results"); this
 script measures how far the automatic choices are from the best one found.
@@ -81,9 +80,8 @@ def time_config(kind, M, N, K, ops, iters, stream) -> float:
     return 2.0 * M * N * K / (ms * 1e-3) / 1e12
 
 
-def _set(pair, group, tile_q, splits, cluster=0):
-    for name, value in (("pair", pair), ("group", group), ("tile_q", tile_q), ("splits", splits),
-                        ("cluster", cluster)):
+def _set(pair, group, tile_q, splits):
+    for name, value in (("pair", pair), ("group", group), ("tile_q", tile_q), ("splits", splits)):
         st = capi.gemm_set_option(name, value)
         if st != 0:
             raise RuntimeError("option %s=%s: %s" % (name, value, capi.status_text(st)))
@@ -104,12 +102,7 @@ def tune_shape(spec: str, iters: int, quick: bool) -> dict:
         auto = time_config(kind, M, N, K, ops, iters, stream)
         for p, g, t, s in itertools.product(pairs, groups, tile_qs, splits):
             _set(p, g, t, s)
-            rows.append({"pair": p, "group": g, "tile_q": t, "splits": s, "cluster": 2,
-                         "tflops": round(time_config(kind, M, N, K, ops, iters, stream), 1)})
-        # clusters of two pairs (pairs only, no split-K)
-        for g, t in itertools.product(groups, tile_qs):
-            _set(1, g, t, 1, cluster=4)
-            rows.append({"pair": 1, "group": g, "tile_q": t, "splits": 1, "cluster": 4,
+            rows.append({"pair": p, "group": g, "tile_q": t, "splits": s,
                          "tflops": round(time_config(kind, M, N, K, ops, iters, stream), 1)})
         _set(-1, 8, 0, 0)
         auto = max(auto, time_config(kind, M, N, K, ops, iters, stream))  # again, after the sweep

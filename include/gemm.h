@@ -197,16 +197,13 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
  *                    boundaries (base and pitch)
  *   workspace_bytes  the registered workspace (0: none)
  *   sms              the device's SM count (152 on GB300)
- *   mc_clusters      resident clusters of four CTAs of the multicast kernel (36 on
- *                    GB300; used only with option "cluster" = 4)
  *   out[nout]        nout >= GEMM_PLAN_FIELDS; receives, in this order: status
  *                    (GEMM_OK), CTA pairs (0/1), producer (0 TMA, 1 load-based),
  *                    tile width along M, 64-row tiles (0/1), K pieces per tile,
  *                    last-wave units per tile (1: untouched), last wave cut along K
  *                    (0/1; else along M), ring stages, grid (CTAs), A repacked,
- *                    B repacked, multicast kernel (0/1), tiles along N, tiles
- *                    along M, K stages per piece, K stages per last-wave piece,
- *                    ring stage bytes.
+ *                    B repacked, tiles along N, tiles along M, K stages per
+ *                    piece, K stages per last-wave piece, ring stage bytes.
  *
  * Returns GEMM_OK, GEMM_ERR_INVALID_DIM or GEMM_ERR_INVALID_OPTION (kind, out
  * or nout).
@@ -221,9 +218,9 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
 #define GEMM_PLAN_C_TMA 4
 #define GEMM_PLAN_A_128 8
 #define GEMM_PLAN_B_128 16
-#define GEMM_PLAN_FIELDS 18
+#define GEMM_PLAN_FIELDS 17
 int gemm_tn_plan(int kind, int64_t M, int64_t N, int64_t K, int flags, int64_t workspace_bytes,
-                 int sms, int mc_clusters, int64_t* out, int nout);
+                 int sms, int64_t* out, int nout);
 
 /* Human-readable text for a status code.  For GEMM_ERR_LAUNCH it names the
  * last CUDA error this thread saw.  The returned string is static. */
@@ -275,9 +272,6 @@ int gemm_read_watchdog(int reset);
  *                 and "tail" 0 the library takes two pieces by itself when the
  *                 tiles have at least 192 K stages (K >= 12288 for 16-bit inputs,
  *                 24576 for e4m3) and the doubled tail still fits in one wave
- *   "cluster"     0 (default) or 2: CTA pairs as chosen above; 4: clusters of two pairs
- *                 that share B tiles through TMA multicast (TN path with TMA-aligned
- *                 operands and C, no split-K; slower or level on the shapes measured)
  *   "f32_tail"    gemm_f32 only: 0 (default) runs the last partial wave of 128 x 128 tiles
  *                 as 128 x 64 halves where that shortens it, in a second grid started
  *                 early by programmatic dependent launch; 1 keeps whole tiles; 2 is 0

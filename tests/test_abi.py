@@ -134,8 +134,7 @@ def test_options():
     assert capi.gemm_set_option("tile_q", 0) == 0
     assert capi.gemm_set_option("tail", 3) == capi.GEMM_ERR_INVALID_OPTION
     assert capi.gemm_set_option("tail", 0) == 0
-    assert capi.gemm_set_option("cluster", 3) == capi.GEMM_ERR_INVALID_OPTION
-    assert capi.gemm_set_option("cluster", 0) == 0
+    assert capi.gemm_set_option("cluster", 0) == capi.GEMM_ERR_INVALID_OPTION  # removed
     assert capi.gemm_set_option("f32_tail", 3) == capi.GEMM_ERR_INVALID_OPTION
     assert capi.gemm_set_option("f32_tail", 0) == 0
     assert capi.gemm_set_option("tail_k", 1) == capi.GEMM_ERR_INVALID_OPTION

@@ -42,7 +42,7 @@ int main(void) {
     if (gemm_tile_coord(2, 3, 2, 2, &tm, &tn) != GEMM_OK || tm != 0 || tn != 1) return 15;
     if (gemm_tn_plan(GEMM_PLAN_F16, 8192, 8192, 8192,
                      GEMM_PLAN_A_TMA | GEMM_PLAN_B_TMA | GEMM_PLAN_C_TMA | GEMM_PLAN_A_128 |
-                     GEMM_PLAN_B_128, 0, 152, 36, out, GEMM_PLAN_FIELDS) != GEMM_OK) return 16;
+                     GEMM_PLAN_B_128, 0, 152, out, GEMM_PLAN_FIELDS) != GEMM_OK) return 16;
     if (out[0] != GEMM_OK || out[1] != 1 || out[3] != 256) return 17;
     if (gemm_workspace_bytes(0, 1, 1) != 0) return 18;
     printf("ok\n");

@@ -153,17 +153,6 @@ def test_64_row_tiles_only_when_forced(options):
     assert plan("bf16", 4096, 4096, 4096)["half"] == 0          # CTA pairs
 
 
-def test_multicast_only_when_asked(options):
-    assert plan("f16", 8192, 8192, 8192)["multicast"] == 0
-    options("cluster", 4)
-    p = plan("f16", 8192, 8192, 8192, mc_clusters=36)
-    assert (p["multicast"], p["grid"], p["tail_f"]) == (1, 144, 1)
-    assert plan("f16", 8192, 8192, 8192, mc_clusters=0)["multicast"] == 0
-    assert plan("e4m3_f32out", 8192, 8192, 8192, mc_clusters=36)["multicast"] == 1
-    p = plan("f16", 8192, 8192, 8192, flags=ALIGNED & ~capi.PLAN_C_TMA, mc_clusters=36)
-    assert p["multicast"] == 0                                  # row-wise stores
-
-
 def test_persistent_grid_follows_sms_and_cap(options):
     assert plan("f16", 8192, 8192, 8192, sms=148)["grid"] == 148
     options("max_ctas", 64)
@@ -174,8 +163,8 @@ def test_argument_errors():
     assert capi.gemm_tn_plan("f16", 0, 8, 8)[0] == capi.GEMM_ERR_INVALID_DIM
     assert capi.gemm_tn_plan("f16", 8, 8, 8, sms=0)[0] == capi.GEMM_ERR_INVALID_DIM
     lib = capi.lib()
-    assert lib.gemm_tn_plan(9, 8, 8, 8, 0, 0, 152, 36, None, 18) == capi.GEMM_ERR_INVALID_OPTION
-    assert lib.gemm_tn_plan(0, 8, 8, 8, 0, 0, 152, 36, None, 18) == capi.GEMM_ERR_INVALID_OPTION
+    assert lib.gemm_tn_plan(9, 8, 8, 8, 0, 0, 152, None, 17) == capi.GEMM_ERR_INVALID_OPTION
+    assert lib.gemm_tn_plan(0, 8, 8, 8, 0, 0, 152, None, 17) == capi.GEMM_ERR_INVALID_OPTION
 
 
 def test_sizes_beyond_any_device_plan_without_overflow(options):
