@@ -136,3 +136,23 @@ def test_cpu_baseline_reports_all_cores_and_one():
     assert r["kind"] == "oracle" and r["cores"] == before and r["value"] > 0
     assert r["one_core"]["cores"] == 1 and r["one_core"]["value"] > 0
     assert oracle.num_threads() == before
+
+
+def test_tensor_peak_follows_the_window():
+    """Burst for a short window or one without the power cap; sustained only
+    for a window of seconds in which the sampler saw sw_power_cap."""
+    burst, sustained = 1914.3, 1748.8
+    # a driver-style run: 20 launches, 12 ms, clocks at max, no reason
+    peak, regime, why = bench.tensor_peak(12.0, {"reasons": []}, burst, sustained)
+    assert (peak, regime) == (burst, "burst") and "12 ms" in why
+    assert 1837.6 / peak == pytest.approx(0.96, abs=0.001)
+    # short, even if capped
+    assert bench.tensor_peak(500.0, {"reasons": ["sw_power_cap"]}, burst, sustained)[1] == "burst"
+    # long but not capped
+    peak, regime, why = bench.tensor_peak(3000.0, {"reasons": []}, burst, sustained)
+    assert regime == "burst" and "no sw_power_cap" in why
+    # long and capped: a 1000-step loop at the power cap
+    peak, regime, _ = bench.tensor_peak(1600.0, {"reasons": ["sw_power_cap"]}, burst, sustained)
+    assert (peak, regime) == (sustained, "sustained")
+    # no clock record at all
+    assert bench.tensor_peak(5000.0, None, burst, sustained)[1] == "burst"
