@@ -55,7 +55,8 @@ _SIGNATURES = {
 }
 
 PLAN_KINDS = {"f16": 0, "bf16": 1, "e4m3": 2, "f16_acc16": 3, "e4m3_f32out": 4}
-PLAN_A_TMA, PLAN_B_TMA, PLAN_C_TMA, PLAN_A_128, PLAN_B_128 = 1, 2, 4, 8, 16
+PLAN_A_TMA, PLAN_B_TMA, PLAN_C_TMA, PLAN_A_128, PLAN_B_128, PLAN_NOALLOC = 1, 2, 4, 8, 16, 32
+GEMM_NOALLOC_SCRATCH_BYTES = 24 << 20
 PLAN_ALIGNED = PLAN_A_TMA | PLAN_B_TMA | PLAN_C_TMA | PLAN_A_128 | PLAN_B_128
 PLAN_FIELDS = ("status", "pair", "producer", "tile_q", "half", "splits", "tail_f", "tail_ksplit",
                "stages", "grid", "copy_a", "copy_b", "tiles_p", "tiles_q",

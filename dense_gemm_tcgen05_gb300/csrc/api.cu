@@ -182,7 +182,8 @@ struct TnPlanIn {
     bool has_scratch;           // a registered workspace or an override
     int64_t ws_total;           // its bytes for repacks and partial sums
     int ov_splits;              // -1: option "splits" applies; else the override's value
-    bool strict;                // a chosen split that does not fit fails
+    bool strict;                // the no-allocation call's rules (see plan_tn)
+    bool no_copy = false;       // never repack operands into the scratch
     int sms;                    // SMs of the device
 };
 
@@ -211,7 +212,7 @@ struct TnPlan {
 // process-wide options, so that the rules can be checked without a GPU
 // (gemm_tn_plan).  Each rule is measured on GB300; the numbers are with the
 // rules below.
-TnPlan plan_tn(const TnPlanIn& a) {
+TnPlan plan_tn_once(const TnPlanIn& a) {
     TnPlan p;
     const int es = a.in == InKind::E4M3 ? 1 : 2;
     const int os = a.out_f32 ? 4 : 2;
@@ -235,7 +236,7 @@ TnPlan plan_tn(const TnPlanIn& a) {
     const bool copy_a = !a_tma || (heavy && !a.a_al128);
     const bool copy_b = !b_tma || (heavy && !a.b_al128);
     if ((copy_a || copy_b) && g_opt_path.load() == 0 && g_opt_repack.load() == 0 &&
-        a.has_scratch) {
+        a.has_scratch && !a.no_copy) {
         const int64_t rb = K * es;                       // row bytes
         const int64_t dp = (rb + 127) / 128 * 128;       // aligned pitch
         const int64_t need_a = copy_a ? round256(sat_mul(M, dp)) : 0;
@@ -335,14 +336,27 @@ TnPlan plan_tn(const TnPlanIn& a) {
             if (want > 16) want = 16;
         }
         if (want > p.num_kb) want = p.num_kb;
+        // Scratch bytes of a split into `pieces`: counters, then the FP32
+        // partial tiles (32-row slices of 256 columns).
+        const int64_t slices = 4 * g.cluster;                    // 32-row slices per tile
+        const int64_t cnt_bytes = round256(sat_mul(tiles, slices * 4));
+        const int64_t room = a.ws_total - p.ws_used;
+        auto split_bytes = [&](int64_t pieces) {
+            return cnt_bytes + sat_mul(sat_mul(tiles, pieces), slices * 32 * 256 * 4);
+        };
+        // The no-allocation call's automatic split shrinks to what its fixed
+        // array has left after any operand copies (none at all: unsplit).
+        if (a.strict && opt == 0) {
+            while (want >= 2) {
+                const int64_t kb_per = (p.num_kb + want - 1) / want;
+                if (fits(split_bytes((p.num_kb + kb_per - 1) / kb_per), room)) break;
+                --want;
+            }
+        }
         if (want >= 2) {
             const int64_t kb_per = (p.num_kb + want - 1) / want;
             const int64_t pieces = (p.num_kb + kb_per - 1) / kb_per;
-            const int64_t slices = 4 * g.cluster;                    // 32-row slices per tile
-            const int64_t cnt_bytes = round256(sat_mul(tiles, slices * 4));
-            const int64_t part_bytes = sat_mul(sat_mul(tiles, pieces), slices * 32 * 256 * 4);
-            const int64_t room = a.ws_total - p.ws_used;
-            const bool fit = fits(cnt_bytes + part_bytes, room);
+            const bool fit = fits(split_bytes(pieces), room);
             if (a.strict && pieces >= 2 && !fit) {
                 p.status = GEMM_ERR_SCRATCH;
                 return p;
@@ -426,6 +440,21 @@ TnPlan plan_tn(const TnPlanIn& a) {
             const int64_t units = p.full_units + (tiles - p.full_units) * f;
             p.grid = static_cast<int>((units < slots ? units : slots) * g.cluster);
         }
+    }
+    return p;
+}
+
+// The planning half of gemm_tn.  Under the no-allocation call's rules
+// (a.strict) operand copies share the fixed array with the split: a forced
+// split that does not fit beside the copies runs without them (the load-based
+// producer reads the unaligned operand in place) and fails with
+// GEMM_ERR_SCRATCH only when it does not fit the array on its own.
+TnPlan plan_tn(const TnPlanIn& a) {
+    TnPlan p = plan_tn_once(a);
+    if (a.strict && p.status == GEMM_ERR_SCRATCH && (p.copy_a || p.copy_b)) {
+        TnPlanIn b = a;
+        b.no_copy = true;
+        p = plan_tn_once(b);
     }
     return p;
 }
@@ -831,12 +860,14 @@ int gemm_tn_plan(int kind, int64_t M, int64_t N, int64_t K, int flags, int64_t w
     pin.c_tma = (flags & GEMM_PLAN_C_TMA) != 0;
     pin.a_al128 = (flags & GEMM_PLAN_A_128) != 0;
     pin.b_al128 = (flags & GEMM_PLAN_B_128) != 0;
-    // as gemm_tn sees a registered workspace: the counter sets come off the top
+    // as gemm_tn sees a registered workspace (or the no-allocation array): the
+    // counter sets come off the top
     pin.has_scratch = workspace_bytes > 0;
     pin.ws_total = workspace_bytes >= kSplitCounterBytes ? workspace_bytes - kSplitCounterBytes
                                                          : workspace_bytes;
-    pin.ov_splits = -1;
-    pin.strict = false;
+    const bool noalloc = (flags & GEMM_PLAN_NOALLOC) != 0;
+    pin.ov_splits = noalloc ? g_opt_splits.load() : -1;
+    pin.strict = noalloc;
     pin.sms = sms;
     const TnPlan pl = plan_tn(pin);
     const int64_t v[GEMM_PLAN_FIELDS] = {pl.status,

@@ -194,7 +194,10 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
  *   flags            GEMM_PLAN_A_TMA / _B_TMA / _C_TMA: that matrix's base and row
  *                    pitch are 16-byte aligned (TMA can address its rows);
  *                    GEMM_PLAN_A_128 / _B_128: A's or B's rows start on 128-byte
- *                    boundaries (base and pitch)
+ *                    boundaries (base and pitch); GEMM_PLAN_NOALLOC: plan as
+ *                    gemm_bf16_tn_noalloc does, with workspace_bytes standing for
+ *                    its fixed array (pass GEMM_NOALLOC_SCRATCH_BYTES) and the
+ *                    value of option "splits" for its `splits` argument
  *   workspace_bytes  the registered workspace (0: none)
  *   sms              the device's SM count (152 on GB300)
  *   out[nout]        nout >= GEMM_PLAN_FIELDS; receives, in this order: status
@@ -206,7 +209,8 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
  *                    piece, K stages per last-wave piece, ring stage bytes.
  *
  * Returns GEMM_OK, GEMM_ERR_INVALID_DIM or GEMM_ERR_INVALID_OPTION (kind, out
- * or nout).
+ * or nout).  A call that would be refused reports its status in out[0]
+ * (GEMM_ERR_SCRATCH for a forced no-allocation split that cannot fit).
  */
 #define GEMM_PLAN_F16 0
 #define GEMM_PLAN_BF16 1
@@ -218,6 +222,7 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
 #define GEMM_PLAN_C_TMA 4
 #define GEMM_PLAN_A_128 8
 #define GEMM_PLAN_B_128 16
+#define GEMM_PLAN_NOALLOC 32
 #define GEMM_PLAN_FIELDS 17
 int gemm_tn_plan(int kind, int64_t M, int64_t N, int64_t K, int flags, int64_t workspace_bytes,
                  int sms, int64_t* out, int nout);
@@ -330,9 +335,15 @@ int64_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * by the automatic rule (only when the output tiles cannot fill the GPU), 1
  * never splits, 2..64 forces that many K pieces.  The array holds
  * GEMM_NOALLOC_SCRATCH_BYTES (24 MiB) on every GPU that loads the library,
- * until the library is unloaded; a split whose partial sums need more returns
- * GEMM_ERR_SCRATCH without launching anything (the automatic rule needs at
- * most ~20 MiB on a 152-SM GPU).  The first call on a device looks up the
+ * until the library is unloaded.  It serves, in this order, the copies of an
+ * operand whose rows TMA cannot address (or, for compute-heavy shapes, whose
+ * rows are not 128-byte aligned), as gemm_set_workspace describes, and the
+ * split's partial sums.  With splits = 0 the split takes as many K pieces as
+ * fit in what the copies leave (none: the call runs unsplit), so it never
+ * fails for lack of room.  A forced split that does not fit beside the copies
+ * runs without them (the operand is then read in place, more slowly); one
+ * that does not fit the array on its own returns GEMM_ERR_SCRATCH without
+ * launching anything.  The first call on a device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current; make
  * that first call before any stream capture.  All calls share the array and it
  * keeps the last call's contents; its first 128 KiB hold the split counters

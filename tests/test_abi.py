@@ -43,9 +43,11 @@ def test_binding_constants_match_the_header():
              "GEMM_PLAN_F16_ACC16": "f16_acc16", "GEMM_PLAN_FP8_F32OUT": "e4m3_f32out"}
     for name, key in kinds.items():
         assert capi.PLAN_KINDS[key] == defs[name], name
-    for flag in ("A_TMA", "B_TMA", "C_TMA", "A_128", "B_128"):
+    for flag in ("A_TMA", "B_TMA", "C_TMA", "A_128", "B_128", "NOALLOC"):
         assert getattr(capi, "PLAN_" + flag) == defs["GEMM_PLAN_" + flag], flag
     assert len(capi.PLAN_FIELDS) == defs["GEMM_PLAN_FIELDS"]
+    assert "#define GEMM_NOALLOC_SCRATCH_BYTES (24LL << 20)" in open(capi.HEADER).read()
+    assert capi.GEMM_NOALLOC_SCRATCH_BYTES == 24 << 20
 
 
 def test_status_strings():

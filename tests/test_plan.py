@@ -153,6 +153,32 @@ def test_64_row_tiles_only_when_forced(options):
     assert plan("bf16", 4096, 4096, 4096)["half"] == 0          # CTA pairs
 
 
+def test_noalloc_split_rules(options):
+    """The no-allocation call's fixed 24 MiB array serves operand copies first
+    and the split second: an automatic split shrinks to what the copies leave
+    (never failing), a forced split that does not fit beside them runs without
+    them, and one that does not fit the array at all is refused."""
+    na = dict(flags=ALIGNED | capi.PLAN_NOALLOC, workspace_bytes=capi.GEMM_NOALLOC_SCRATCH_BYTES)
+    mis_b = (ALIGNED | capi.PLAN_NOALLOC) & ~(capi.PLAN_B_TMA | capi.PLAN_B_128)
+    nb = dict(na, flags=mis_b)
+    p = plan("bf16", 64, 2048, 4096, **na)                      # aligned: the full automatic split
+    assert (p["splits"], p["copy_b"], p["producer"]) == (8, 0, 0)
+    p = plan("bf16", 64, 2048, 4096, **nb)                      # B copied (16 MiB), split shrinks
+    assert (p["splits"], p["copy_b"], p["producer"]) == (3, 1, 0)
+    # the same inputs with a registered workspace of that size: no shrinking, no split
+    p = plan("bf16", 64, 2048, 4096, flags=mis_b & ~capi.PLAN_NOALLOC,
+             workspace_bytes=capi.GEMM_NOALLOC_SCRATCH_BYTES)
+    assert (p["splits"], p["copy_b"]) == (1, 1)
+    options("splits", 8)                                        # forced: the copy gives way
+    p = plan("bf16", 64, 2048, 4096, **nb)
+    assert (p["splits"], p["copy_b"], p["producer"]) == (8, 0, 1)
+    options("splits", 16)                                       # does not fit at all
+    st, p = capi.gemm_tn_plan("bf16", 4096, 4096, 4096, **na)
+    assert st == capi.GEMM_OK and p["status"] == capi.GEMM_ERR_SCRATCH
+    options("splits", 0)
+    assert plan("bf16", 4096, 4096, 4096, **na)["splits"] == 1  # a full wave: no split
+
+
 def test_persistent_grid_follows_sms_and_cap(options):
     assert plan("f16", 8192, 8192, 8192, sms=148)["grid"] == 148
     options("max_ctas", 64)
