@@ -5,7 +5,8 @@ Default workload (one step = one call of the C ABI): FP16 TN GEMM with
 M = N = K = 8192, A row-major, B column-major, C column-major, FP32
 accumulation, entries N(0,1)*0.1 (seed 2).  The line also reports BF16 and
 FP8-E4M3 at 8192^3 and the FP32 SIMT path at 4096^3, each against its dense
-peak, the end-to-end rate with host buffers, the kernel's roofline fraction,
+peak, every BF16/FP8 configuration shape and the pages' transformer and
+skinny shapes (per_config), the end-to-end rate with host buffers, the kernel's roofline fraction,
 the SM clocks seen while timing, the CPU oracle timed on a bounded sample, and
 the main call's per-launch mean, median and min with L2 warm and flushed.
 
@@ -17,7 +18,7 @@ rank runs its own replica (weak scaling: the GEMM does not need a collective),
 the time is the maximum over ranks and `value` counts every rank's work.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--sweep]
+                  [--no-per-config]
   python bench.py --ncu-case bf16:128x8192x8192   (launches for a profiler capture)
 """
 from __future__ import annotations
@@ -199,6 +200,12 @@ def tn_call(kind, M, N, K, scale_a, scale_b, stream_h, out_f32=False):
 
 def timed_loop(call, sets, steps, warmup, stream, dist=None, sampler=None):
     """W warm-up steps, then K timed steps; returns (total_ms, mean_launch_ms)."""
+    total, launches = timed_launches(call, sets, steps, warmup, stream, dist, sampler)
+    return total, sum(launches) / len(launches)
+
+
+def timed_launches(call, sets, steps, warmup, stream, dist=None, sampler=None):
+    """W warm-up steps, then K timed steps; returns (total_ms, [ms per launch])."""
     import torch
 
     for i in range(warmup):
@@ -224,7 +231,14 @@ def timed_loop(call, sets, steps, warmup, stream, dist=None, sampler=None):
     barrier(dist)
     total = t_begin.elapsed_time(t_end)
     launches = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    return total, sum(launches) / len(launches)
+    return total, launches
+
+
+def spread(launches):
+    """Mean, median, min and max of per-launch times (ms)."""
+    ms = sorted(launches)
+    return {"mean_ms": round(sum(ms) / len(ms), 4), "median_ms": round(statistics.median(ms), 4),
+            "min_ms": round(ms[0], 4), "max_ms": round(ms[-1], 4), "launches": len(ms)}
 
 
 def e2e_loop(kind, M, N, K, ops, steps, warmup, stream, stream_h):
@@ -561,10 +575,11 @@ def run_ours(args):
                            sigma=1.0 if kind == "e4m3" else 0.05, nsets=SETS, device="cuda")
             c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h)
             with torch.cuda.stream(stream):
-                _, lm = timed_loop(c, s, sub_steps, 3, stream)
+                _, ls = timed_launches(c, s, sub_steps, 3, stream)
+            lm = sum(ls) / len(ls)
             tf = flops / (lm * 1e-3) / 1e12
             per[kind + "_tn_8192"] = {"tflops": round(tf, 1), "peak": round(peak, 1),
-                                      "frac": round(tf / peak, 4)}
+                                      "frac": round(tf / peak, 4), **spread(ls)}
             del s
             torch.cuda.empty_cache()
         # FP16 accumulation (the FP16 page's measured mode), same problem
@@ -603,8 +618,10 @@ def run_ours(args):
         per["cublas_context_f32_4096"] = round(cublas_context(4096, 4096, 4096, torch.float32,
                                                               20, stream), 2)
         per["cublas_context_f16_8192"] = round(cublas_context(M, N, K, torch.float16, 20, stream), 1)
-        if args.sweep:
-            per.update(sweep(stream, stream_h, burst, workspace))
+        per_cfg = None
+        if not args.no_per_config:
+            hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+            per_cfg = per_config(stream, stream_h, burst, hbm, workspace)
 
         e2e_steps = max(3, min(args.steps, 20))
         e_ms, serial_ms, h2d, d2h, copy_ms = e2e_loop("f16", M, N, K, ops, e2e_steps, 2, stream,
@@ -653,6 +670,7 @@ def run_ours(args):
             "gpu_launches": args.steps,
             "clocks": clocks,
             "per_dtype": per,
+            "per_config": per_cfg,
             "l2_modes": l2,
         }
         if not args.no_cpu_baseline:
@@ -669,72 +687,88 @@ def compulsory_bytes(kind, M, N, K, out_f32=False) -> int:
     return (M * K + N * K) * es + M * N * (4 if out_f32 else 2)
 
 
-def sweep(stream, stream_h, burst, workspace):
-    """The BF16 and FP8 shape sweeps (configs 4 and 5), one line each.  The
-    first part runs without a registered workspace (the odd shapes' tight
-    leading dimensions then take the load-based producer); the rest, and
-    whatever follows, with the bench's `workspace` registered."""
+L2_BYTES = 129 * 10 ** 6   # GB300 L2 (129 MB)
+
+# The shapes of the BF16 and FP8 configurations, the pages' own transformer
+# shapes ("FP16 GEMM Optimization on AMD RDNA 3 and RDNA 4", "Where That
+# Leaves Us", Table 16; "FP8 GEMM Optimization on AMD RDNA 4", "Results",
+# Tables 1-4, which write FP32 C) and skinny shapes whose time is set by HBM
+# ("Tuning Further").  (kind, (M, N, K), FP32 output, values (seed, sigma),
+# HBM-bound).
+PER_CONFIG = [
+    ("bf16", (4096, 4096, 4096), False, (3, 0.05), False),
+    ("bf16", (4096, 14336, 4096), False, (3, 0.05), False),
+    ("bf16", (4096, 4096, 14336), False, (3, 0.05), False),
+    ("bf16", (2047, 3001, 1023), False, (3, 0.05), False),
+    ("bf16", (8191, 8191, 8191), False, (3, 0.05), False),
+    ("e4m3", (8192, 8192, 8192), False, (4, 1.0), False),
+    ("e4m3", (4096, 14336, 4096), False, (4, 1.0), False),
+    ("e4m3", (16384, 4096, 4096), False, (4, 1.0), False),
+    ("f16", (8192, 28672, 8192), False, (2, 0.1), False),
+    ("e4m3", (8192, 8192, 8192), True, (4, 1.0), False),
+    ("e4m3", (8192, 28672, 8192), True, (4, 1.0), False),
+    ("e4m3", (8192, 10240, 8192), True, (4, 1.0), False),
+    ("e4m3", (3072, 4096, 8192), True, (4, 1.0), False),
+    ("bf16", (16, 8192, 8192), False, (3, 0.05), True),
+    ("bf16", (128, 8192, 8192), False, (3, 0.05), True),
+    ("bf16", (256, 8192, 8192), False, (3, 0.05), True),
+    ("bf16", (64, 14336, 4096), False, (3, 0.05), True),
+    ("bf16", (1024, 1024, 8192), False, (3, 0.05), True),
+    ("e4m3", (128, 8192, 8192), False, (4, 1.0), True),
+]
+
+
+def sets_beyond_l2(kind, M, N, K, out_f32=False):
+    """Rotating input sets whose bytes together exceed twice the L2, so that
+    no launch finds its operands there (at least 3)."""
+    per = compulsory_bytes(kind, M, N, K, out_f32)
+    return max(SETS, min(64, -(-2 * L2_BYTES // per)))
+
+
+def per_config(stream, stream_h, burst, hbm, workspace, launches=20):
+    """Every configuration shape above, timed with the bench's workspace
+    registered (the library's recommended setup): `launches` back-to-back
+    calls after 3 warm-ups over rotating input sets that exceed the L2.  Each
+    entry: TFLOP/s at the mean launch, the fraction of the dtype's burst peak
+    (FP8 = 2x BF16 by the nominal ratio), GB/s of compulsory bytes and the
+    per-launch spread; the HBM-bound shapes add the fraction of the measured
+    copy bandwidth.  The tight-leading-dimension BF16 shapes are timed again
+    without a workspace (the load-based producer reads them in place)."""
     import torch
 
     from dense_gemm_tcgen05_gb300 import capi
 
     out = {}
-    capi.gemm_set_workspace(None, 0)
-    # BF16 and FP8 configurations (tight leading dimensions: the odd shapes take
-    # the load-based producer), then the pages' transformer shapes -- FP16 on
-    # the FP16 page's wide shape, FP8 with FP32 output as the FP8 page measures.
-    shapes = [("bf16", (4096, 4096, 4096), False), ("bf16", (4096, 14336, 4096), False),
-              ("bf16", (4096, 4096, 14336), False), ("bf16", (2047, 3001, 1023), False),
-              ("bf16", (8191, 8191, 8191), False), ("e4m3", (8192, 8192, 8192), False),
-              ("e4m3", (4096, 14336, 4096), False), ("e4m3", (16384, 4096, 4096), False),
-              ("f16", (8192, 28672, 8192), False), ("e4m3", (8192, 8192, 8192), True),
-              ("e4m3", (8192, 28672, 8192), True), ("e4m3", (8192, 10240, 8192), True),
-              ("e4m3", (3072, 4096, 8192), True)]
-    for kind, (M, N, K), f32 in shapes:
-        o, s = tn_sets(kind, M, N, K, seed=4 if kind == "e4m3" else 3,
-                       sigma=1.0 if kind == "e4m3" else 0.05, nsets=SETS, device="cuda",
+
+    def one(kind, M, N, K, f32, seed, sigma, tag=""):
+        nsets = sets_beyond_l2(kind, M, N, K, f32)
+        o, s = tn_sets(kind, M, N, K, seed=seed, sigma=sigma, nsets=nsets, device="cuda",
                        out_f32=f32)
         c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h, out_f32=f32)
         with torch.cuda.stream(stream):
-            _, lm = timed_loop(c, s, 20, 3, stream)
+            _, ls = timed_launches(c, s, launches, 3, stream)
+        del s, o
+        torch.cuda.empty_cache()
+        lm = sum(ls) / len(ls)
         tf = 2.0 * M * N * K / (lm * 1e-3) / 1e12
         peak = burst * (FP8_OVER_BF16 if kind == "e4m3" else 1.0)
-        key = "%s%s_%dx%dx%d" % (kind, "_f32out" if f32 else "", M, N, K)
-        out[key] = {"tflops": round(tf, 1), "frac": round(tf / peak, 4),
-                    "gbs": round(compulsory_bytes(kind, M, N, K, f32) / (lm * 1e-3) / 1e9)}
-        del s
-        torch.cuda.empty_cache()
-    # Skinny and small shapes: HBM-bound, reported in GB/s of compulsory
-    # traffic against the measured copy bandwidth, with the workspace again.
-    peaks, _ = load_peaks()
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    if capi.gemm_set_workspace(workspace.data_ptr(), workspace.numel()) != 0:
-        raise RuntimeError("could not register the workspace")
-    # the tight-leading-dimension BF16 configurations again, now repacked
-    for kind, (M, N, K) in [("bf16", (2047, 3001, 1023)), ("bf16", (8191, 8191, 8191))]:
-        o, s = tn_sets(kind, M, N, K, seed=3, sigma=0.05, nsets=SETS, device="cuda")
-        c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h)
-        with torch.cuda.stream(stream):
-            _, lm = timed_loop(c, s, 20, 3, stream)
-        tf = 2.0 * M * N * K / (lm * 1e-3) / 1e12
-        out["%s_%dx%dx%d_ws" % (kind, M, N, K)] = {
-            "tflops": round(tf, 1), "frac": round(tf / burst, 4),
-            "gbs": round(compulsory_bytes(kind, M, N, K) / (lm * 1e-3) / 1e9)}
-        del s
-        torch.cuda.empty_cache()
-    for kind, (M, N, K) in [("bf16", (16, 8192, 8192)), ("bf16", (128, 8192, 8192)),
-                            ("bf16", (64, 14336, 4096)), ("bf16", (1024, 1024, 8192)),
-                            ("e4m3", (128, 8192, 8192))]:
-        o, s = tn_sets(kind, M, N, K, seed=3, sigma=0.05, nsets=SETS, device="cuda")
-        c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h)
-        with torch.cuda.stream(stream):
-            _, lm = timed_loop(c, s, 30, 3, stream)
-        gbs = compulsory_bytes(kind, M, N, K) / (lm * 1e-3) / 1e9
-        out["%s_skinny_%dx%dx%d" % (kind, M, N, K)] = {
-            "tflops": round(2.0 * M * N * K / (lm * 1e-3) / 1e12, 1), "gbs": round(gbs),
-            "hbm_frac": round(gbs / hbm, 3), "us": round(lm * 1e3, 1)}
-        del s
-        torch.cuda.empty_cache()
+        gbs = compulsory_bytes(kind, M, N, K, f32) / (lm * 1e-3) / 1e9
+        key = "%s%s_%dx%dx%d%s" % (kind, "_f32out" if f32 else "", M, N, K, tag)
+        out[key] = {"tflops": round(tf, 1), "frac": round(tf / peak, 4), "gbs": round(gbs),
+                    "sets": nsets, **spread(ls)}
+        return key, gbs
+
+    for kind, (M, N, K), f32, (seed, sigma), hbm_bound in PER_CONFIG:
+        key, gbs = one(kind, M, N, K, f32, seed, sigma)
+        if hbm_bound:
+            out[key]["hbm_frac"] = round(gbs / hbm, 3)
+    capi.gemm_set_workspace(None, 0)
+    try:
+        for M, N, K in ((2047, 3001, 1023), (8191, 8191, 8191)):
+            one("bf16", M, N, K, False, 3, 0.05, tag="_no_workspace")
+    finally:
+        if capi.gemm_set_workspace(workspace.data_ptr(), workspace.numel()) != 0:
+            raise RuntimeError("could not register the workspace")
     return out
 
 
@@ -852,7 +886,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--sweep", action="store_true", help="add the BF16/FP8 shape sweeps")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-configuration shapes (BF16/FP8 configs, page shapes)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-main", action="store_true",
                     help="time the main workload only (for profiler runs)")

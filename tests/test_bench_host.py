@@ -156,3 +156,27 @@ def test_tensor_peak_follows_the_window():
     assert (peak, regime) == (sustained, "sustained")
     # no clock record at all
     assert bench.tensor_peak(5000.0, None, burst, sustained)[1] == "burst"
+
+
+def test_per_config_sets_exceed_l2():
+    """Every per-configuration shape rotates over input sets whose bytes
+    together exceed twice the 129 MB L2, with at least three sets."""
+    for kind, (M, N, K), f32, _, _ in bench.PER_CONFIG:
+        n = bench.sets_beyond_l2(kind, M, N, K, f32)
+        assert n >= 3 and n * bench.compulsory_bytes(kind, M, N, K, f32) >= 2 * bench.L2_BYTES
+    assert bench.sets_beyond_l2("bf16", 2047, 3001, 1023) == 12    # 22.6 MB a set
+    shapes = {(k, s, f) for k, s, f, _, _ in bench.PER_CONFIG}
+    for shape in [(4096, 4096, 4096), (4096, 14336, 4096), (4096, 4096, 14336),
+                  (2047, 3001, 1023), (8191, 8191, 8191)]:
+        assert ("bf16", shape, False) in shapes                    # the BF16 configuration
+    for shape in [(8192, 8192, 8192), (4096, 14336, 4096), (16384, 4096, 4096)]:
+        assert ("e4m3", shape, False) in shapes                    # the FP8 configuration
+    for shape in [(8192, 8192, 8192), (8192, 28672, 8192), (8192, 10240, 8192),
+                  (3072, 4096, 8192)]:
+        assert ("e4m3", shape, True) in shapes                     # the FP8 page's Tables 1-4
+
+
+def test_spread():
+    s = bench.spread([1.0, 3.0, 2.0, 4.0])
+    assert (s["mean_ms"], s["median_ms"], s["min_ms"], s["max_ms"], s["launches"]) == (
+        2.5, 2.5, 1.0, 4.0, 4)
