@@ -864,6 +864,8 @@ def ncu_case(spec: str):
 
     kind, dims = spec.split(":")
     M, N, K = (int(x) for x in dims.lower().split("x"))
+    if kind == "f32":
+        return ncu_case_f32(M, N, K)
     workspace = torch.empty(WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
     assert capi.gemm_set_workspace(workspace.data_ptr(), workspace.numel()) == 0
     _, sets = tn_sets(kind, M, N, K, 2, 0.1, 2, "cuda")
@@ -880,6 +882,34 @@ def ncu_case(spec: str):
     return {"ncu_case": spec, "launches_each": 3, "cublas": kind != "e4m3"}
 
 
+def ncu_case_f32(M, N, K):
+    """Three gemm_f32 calls (U[-1,1] operands, seed 1) and cuBLAS's FP32 GEMM
+    (TF32 off) on the same operands after each, for profiler captures."""
+    import torch
+
+    import synthetic_inputs as si
+    from dense_gemm_tcgen05_gb300 import capi
+
+    ops = si.f32_operands(M, N, K, dist="uniform", seed=1)
+    a, b = ops["A"].cuda(), ops["B"].cuda()
+    c = torch.empty((M, N), device="cuda")
+    stream = torch.cuda.Stream()
+    tf32 = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                st = capi.gemm_f32(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N,
+                                   stream.cuda_stream)
+                if st != 0:
+                    raise RuntimeError(capi.status_text(st))
+                torch.matmul(a, b, out=c)
+        torch.cuda.synchronize()
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = tf32
+    return {"ncu_case": "f32:%dx%dx%d" % (M, N, K), "launches_each": 3, "cublas": True}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -892,7 +922,8 @@ def main(argv=None):
     ap.add_argument("--only-main", action="store_true",
                     help="time the main workload only (for profiler runs)")
     ap.add_argument("--ncu-case", metavar="KIND:MxNxK",
-                    help="launch one TN shape three times, and cuBLAS beside it, for ncu")
+                    help="launch one shape (f16/bf16/e4m3 TN, or f32) three times, and cuBLAS "
+                         "beside it, for ncu")
     args = ap.parse_args(argv)
     if args.ncu_case:
         print(json.dumps(ncu_case(args.ncu_case)), flush=True)

@@ -43,7 +43,8 @@ _SIGNATURES = {
     "gemm_status_string": ([_int], ctypes.c_char_p),
     "gemm_read_watchdog": ([_int], _int),
     "gemm_set_option": ([ctypes.c_char_p, _i64], _int),
-    "gemm_tile_coord": ([_i64, _i64, _i64, _i64, ctypes.POINTER(_i64), ctypes.POINTER(_i64)], _int),
+    "gemm_tile_coord": ([_i64, _i64, _i64, _i64, _int, ctypes.POINTER(_i64), ctypes.POINTER(_i64)],
+                        _int),
     "gemm_watchdog_selftest": ([_i64, _vp], _int),
     "gemm_set_workspace": ([_vp, _i64], _int),
     "gemm_bf16_tn_noalloc": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i64, _vp], _int),
@@ -159,9 +160,10 @@ def gemm_set_option(name: str, value: int) -> int:
     return lib().gemm_set_option(name.encode(), int(value))
 
 
-def gemm_tile_coord(t: int, tiles_m: int, tiles_n: int, group: int):
+def gemm_tile_coord(t: int, tiles_m: int, tiles_n: int, group: int, snake: int = 0):
     tm, tn = _i64(), _i64()
-    st = lib().gemm_tile_coord(t, tiles_m, tiles_n, group, ctypes.byref(tm), ctypes.byref(tn))
+    st = lib().gemm_tile_coord(t, tiles_m, tiles_n, group, int(snake), ctypes.byref(tm),
+                               ctypes.byref(tn))
     return st, tm.value, tn.value
 
 

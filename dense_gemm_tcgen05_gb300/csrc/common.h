@@ -77,6 +77,12 @@ struct TcParams {
     // tile, a multiple of 1024) in the kernel's fixed stage region.
     int32_t stages;
     uint32_t stage_bytes;
+    // 1: the TMA producer walks the K range of every second unit a CTA runs
+    // backwards, so that the K slices a wave of tiles ends on are the ones the
+    // next wave starts with, while they are still in L2.
+    int32_t k_snake;
+    // 1: odd rasteriser bands walk the tile columns backwards (raster.h).
+    int32_t band_snake;
 };
 
 struct TcLaunch {

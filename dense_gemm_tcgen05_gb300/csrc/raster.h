@@ -16,8 +16,11 @@
 
 namespace gb300 {
 
+// With `snake` set, odd bands walk the tile columns from right to left, so a
+// band starts on the column panels the previous band ended on.
 __host__ __device__ inline void raster_tile(int64_t t, int64_t tiles_m, int64_t tiles_n,
-                                            int64_t group, int64_t* tm, int64_t* tn) {
+                                            int64_t group, int64_t* tm, int64_t* tn,
+                                            bool snake = false) {
     const int64_t per_band = group * tiles_n;      // tiles in one full band
     const int64_t band = t / per_band;
     const int64_t first_row = band * group;
@@ -25,7 +28,8 @@ __host__ __device__ inline void raster_tile(int64_t t, int64_t tiles_m, int64_t 
     const int64_t band_rows = rows_left < group ? rows_left : group;
     const int64_t local = t - band * per_band;      // position inside the band
     *tm = first_row + local % band_rows;
-    *tn = local / band_rows;
+    const int64_t col = local / band_rows;
+    *tn = (snake && (band & 1)) ? tiles_n - 1 - col : col;
 }
 
 }  // namespace gb300

@@ -355,7 +355,8 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF>::kThreads, 1)
                 w.narrow = true;
             }
         }
-        raster_tile(w.tile, prm.tiles_q, prm.tiles_p, prm.group, &w.tq, &w.tp);
+        raster_tile(w.tile, prm.tiles_q, prm.tiles_p, prm.group, &w.tq, &w.tp,
+                    prm.band_snake != 0);
         w.q_off = static_cast<int32_t>(w.tq * prm.tile_q) + part * w.width;
         w.kb_lo = w.piece * kb_per;
         w.kb_hi = w.kb_lo + kb_per < prm.num_kb ? w.kb_lo + kb_per : prm.num_kb;
@@ -371,8 +372,12 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF>::kThreads, 1)
         const uint64_t pol_p = l2_evict_first_policy();
         const uint64_t pol_q = l2_evict_last_policy();
         const bool hints = prm.l2_hints != 0;
-        for (int64_t u = first; ok && u < num_units; u += stride) {
+        uint32_t lu = 0;                     // units this CTA has run
+        for (int64_t u = first; ok && u < num_units; u += stride, ++lu) {
             const Unit w = unit_of(u);
+            // Every second unit reads its K range backwards (the MMA warp sums
+            // the stages in whatever order they arrive).
+            const int32_t k_rev = (prm.k_snake && (lu & 1u)) ? w.kb_lo + w.kb_hi - 1 : -1;
             const int32_t p0 = static_cast<int32_t>(w.tp * Cfg::kTileP + rank * Cfg::kBlockP);
             const int32_t q0 = w.q_off + static_cast<int32_t>(rank) * (w.width / Cfg::kCG);
             const CUtensorMap* mq = w.narrow ? &map_q_tail : &map_q;
@@ -390,7 +395,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF>::kThreads, 1)
                 if (lane == 0) {
                     const uint32_t sp = base + s * stage_bytes;
                     const uint32_t sq = sp + Cfg::kBytesP;
-                    const int32_t kx = kb * Cfg::kStageK;
+                    const int32_t kx = (k_rev >= 0 ? k_rev - kb : kb) * Cfg::kStageK;
                     if constexpr (PAIR) {
                         const uint32_t fb = mapa_shared(full_bar(s), 0);
                         if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * tx);

@@ -92,22 +92,22 @@ def tune_shape(spec: str, iters: int, quick: bool) -> dict:
     ops = _operands(kind, M, N, K)
     stream = torch.cuda.Stream()
     pairs = [0, 1]
-    groups = [8] if quick else [4, 8, 16]
+    groups = [0] if quick else [0, 8, 12, 24]
     tile_qs = [0, 128, 256] if quick else [0, 64, 128, 192, 256]
     splits = [1, 0]
     rows = []
     try:
-        _set(-1, 8, 0, 0)
+        _set(-1, 0, 0, 0)
         time_config(kind, M, N, K, ops, 4 * iters, stream)  # bring clocks up first
         auto = time_config(kind, M, N, K, ops, iters, stream)
         for p, g, t, s in itertools.product(pairs, groups, tile_qs, splits):
             _set(p, g, t, s)
             rows.append({"pair": p, "group": g, "tile_q": t, "splits": s,
                          "tflops": round(time_config(kind, M, N, K, ops, iters, stream), 1)})
-        _set(-1, 8, 0, 0)
+        _set(-1, 0, 0, 0)
         auto = max(auto, time_config(kind, M, N, K, ops, iters, stream))  # again, after the sweep
     finally:
-        _set(-1, 8, 0, 0)
+        _set(-1, 0, 0, 0)
     best = max(rows, key=lambda r: r["tflops"])
     return {"shape": spec, "auto_tflops": round(auto, 1), "best": best,
             "auto_over_best": round(auto / best["tflops"], 4), "configs": rows}

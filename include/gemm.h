@@ -247,7 +247,16 @@ int gemm_read_watchdog(int reset);
  *   "pair"        -1 auto (default: CTA pairs, except when the pair tiles fill less
  *                 than one wave and single-CTA tiles 64 (M <= 128) or 128 wide along
  *                 M fit in one: then those), 0 one CTA per tile, 1 a cta_group::2 pair
- *   "group"       tile-rasteriser group size in tile rows, 1..64 (default 8)
+ *   "group"       tile-rasteriser group size in tile rows, 1..64, or 0 (default):
+ *                 16, chosen for the GB300 L2 (two per-die partitions)
+ *   "band_snake"  1 (default): odd rasteriser groups walk the tile columns backwards
+ *                 (gemm_tile_coord), so a group starts on the column panels the
+ *                 previous one ended on; 0: every group walks forwards
+ *   "k_snake"     1 (default): every second tile a CTA runs reads its K range
+ *                 backwards, so the K slices one wave of tiles ends on are still in
+ *                 L2 when the next wave starts on them; 0: always ascending.  The
+ *                 summation order of those tiles changes, not the result's
+ *                 accuracy; results stay deterministic for a given shape
  *   "path"        0 auto (default), 1 force the CUDA-core kernel, 2 force the
  *                 tensor-core kernel's load-based producer (as for unaligned rows)
  *   "timeout_ns"  device wait limit in ns, 1e6..6e10 (default 2e9).  The longest
@@ -362,10 +371,13 @@ int gemm_bf16_tn_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t
  * rows, walking down the rows of a group before moving to the next tile column;
  * the last group is short when group does not divide tiles_m ("FP16 GEMM
  * Optimization on AMD RDNA 3 and RDNA 4", "Step 6: Block Scheduling for Cache
- * Reuse").  Returns GEMM_OK, or GEMM_ERR_INVALID_DIM for an index out of range.
+ * Reuse").  With snake != 0 the odd groups walk the tile columns from the last
+ * to the first (the tensor-core kernel's order under option "band_snake" = 1,
+ * the default), so each group starts on the columns the previous one ended on.
+ * Returns GEMM_OK, or GEMM_ERR_INVALID_DIM for an index out of range.
  */
-int gemm_tile_coord(int64_t t, int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t* tm,
-                    int64_t* tn);
+int gemm_tile_coord(int64_t t, int64_t tiles_m, int64_t tiles_n, int64_t group, int snake,
+                    int64_t* tm, int64_t* tn);
 
 /*
  * gemm_watchdog_selftest -- launches one block that waits on a shared-memory

@@ -125,8 +125,16 @@ def test_options():
     assert capi.gemm_set_option("pair", 1) == 0
     assert capi.gemm_set_option("pair", -1) == 0
     assert capi.gemm_set_option("pair", 2) == capi.GEMM_ERR_INVALID_OPTION
-    assert capi.gemm_set_option("group", 0) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("group", -1) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("group", 65) == capi.GEMM_ERR_INVALID_OPTION
     assert capi.gemm_set_option("group", 8) == 0
+    assert capi.gemm_set_option("group", 0) == 0
+    assert capi.gemm_set_option("k_snake", 2) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("k_snake", 0) == 0
+    assert capi.gemm_set_option("k_snake", 1) == 0
+    assert capi.gemm_set_option("band_snake", 2) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("band_snake", 0) == 0
+    assert capi.gemm_set_option("band_snake", 1) == 0
     assert capi.gemm_set_option("timeout_ns", 10) == capi.GEMM_ERR_INVALID_OPTION
     assert capi.gemm_set_option("nonsense", 1) == capi.GEMM_ERR_INVALID_OPTION
     assert capi.gemm_set_option("splits", 65) == capi.GEMM_ERR_INVALID_OPTION
@@ -186,24 +194,29 @@ def test_f32_bf16x6_workspace_size():
     assert capi.gemm_f32_bf16x6_workspace_bytes(4, 4, -1) == 0
 
 
+@pytest.mark.parametrize("snake", [0, 1])
 @pytest.mark.parametrize("tiles_m,tiles_n,group", [(1, 1, 8), (32, 64, 8), (16, 12, 8),
-                                                   (17, 5, 8), (7, 9, 3), (5, 5, 64), (64, 3, 1)])
-def test_rasteriser_bijection_and_bands(tiles_m, tiles_n, group):
+                                                   (17, 5, 8), (7, 9, 3), (5, 5, 64), (64, 3, 1),
+                                                   (32, 32, 16)])
+def test_rasteriser_bijection_and_bands(tiles_m, tiles_n, group, snake):
     """Every work index maps to a distinct tile; indices t in one band of
-    `group` tile rows stay in that band and walk down its rows first."""
+    `group` tile rows stay in that band and walk down its rows first, moving
+    one column right (left, for odd bands with snake) after each."""
     seen = set()
     for t in range(tiles_m * tiles_n):
-        st, tm, tn = capi.gemm_tile_coord(t, tiles_m, tiles_n, group)
+        st, tm, tn = capi.gemm_tile_coord(t, tiles_m, tiles_n, group, snake)
         assert st == 0
         assert 0 <= tm < tiles_m and 0 <= tn < tiles_n
         band = t // (group * tiles_n)
         assert tm // group == band
         rows = min(group, tiles_m - band * group)
         local = t - band * group * tiles_n
-        assert tm == band * group + local % rows and tn == local // rows
+        col = local // rows
+        assert tm == band * group + local % rows
+        assert tn == (tiles_n - 1 - col if snake and band % 2 else col)
         seen.add((tm, tn))
     assert len(seen) == tiles_m * tiles_n
-    assert capi.gemm_tile_coord(tiles_m * tiles_n, tiles_m, tiles_n, group)[0] != 0
+    assert capi.gemm_tile_coord(tiles_m * tiles_n, tiles_m, tiles_n, group, snake)[0] != 0
 
 
 def test_rasteriser_hand_listed_order():
@@ -212,6 +225,10 @@ def test_rasteriser_hand_listed_order():
     row) follows."""
     expect = [(0, 0), (1, 0), (0, 1), (1, 1), (2, 0), (2, 1)]
     got = [capi.gemm_tile_coord(t, 3, 2, 2)[1:] for t in range(6)]
+    assert got == expect
+    # snake: the second band walks right to left
+    expect = [(0, 0), (1, 0), (0, 1), (1, 1), (2, 1), (2, 0)]
+    got = [capi.gemm_tile_coord(t, 3, 2, 2, 1)[1:] for t in range(6)]
     assert got == expect
 
 

@@ -39,7 +39,7 @@ int main(void) {
     if (gemm_set_option("no such option", 1) != GEMM_ERR_INVALID_OPTION) return 13;
     if (strcmp(gemm_status_string(GEMM_OK), "ok") != 0) return 14;
     /* host-only queries */
-    if (gemm_tile_coord(2, 3, 2, 2, &tm, &tn) != GEMM_OK || tm != 0 || tn != 1) return 15;
+    if (gemm_tile_coord(2, 3, 2, 2, 0, &tm, &tn) != GEMM_OK || tm != 0 || tn != 1) return 15;
     if (gemm_tn_plan(GEMM_PLAN_F16, 8192, 8192, 8192,
                      GEMM_PLAN_A_TMA | GEMM_PLAN_B_TMA | GEMM_PLAN_C_TMA | GEMM_PLAN_A_128 |
                      GEMM_PLAN_B_128, 0, 152, out, GEMM_PLAN_FIELDS) != GEMM_OK) return 16;

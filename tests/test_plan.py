@@ -25,7 +25,7 @@ def options():
         assert capi.gemm_set_option(name, value) == 0
         touched.append(name)
     yield set_
-    defaults = {"pair": -1, "group": 8}
+    defaults = {"pair": -1, "group": 0, "k_snake": 1, "band_snake": 1}
     for name in touched:
         capi.gemm_set_option(name, defaults.get(name, 0))
 

@@ -270,7 +270,7 @@ def test_group_sizes(group):
     try:
         C = run_tn("bf16", ops, M, N, K)
     finally:
-        capi.gemm_set_option("group", 8)
+        capi.gemm_set_option("group", 0)
     exact = oracle.gemm_tn("bf16", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
     assert_codes_equal(out_codes(C, M, N), exact_codes("bf16", exact))
 
