@@ -83,6 +83,7 @@ std::atomic<int> g_opt_repack{0};
 std::atomic<int> g_opt_f32_tail{0};
 std::atomic<int> g_opt_l2hints{0};
 std::atomic<int> g_opt_half{0};
+std::atomic<int> g_opt_dual{0};
 std::atomic<int64_t> g_opt_timeout_ns{2000000000LL};
 
 thread_local cudaError_t t_last_cuda_error = cudaSuccess;
@@ -210,6 +211,7 @@ struct TnPlan {
     int64_t ws_used = 0;        // scratch bytes taken by the repacks
     Producer prod = Producer::Tma;
     bool pair = false, half = false;
+    bool dual = false;          // two MMA-issuing warps (TcCfg DUAL)
     int tile_q = 0, load_q = 0;
     TcGeometry g{};
     int64_t tiles_p = 0, tiles_q = 0, tiles = 0, slots = 0;
@@ -306,8 +308,37 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
     // 16 x 8192 x 8192: 31.1 against 27.5 us; 16 x 4096 x 8192: 29.7 against
     // 17.4 us), so they run only when forced, and only for one-CTA TMA tiles
     // with FP32 accumulation.
-    p.half = g_opt_half.load() == 1 && !p.pair && p.prod == Producer::Tma && !a.acc16;
+    const int opt_half = g_opt_half.load();
+    p.half = opt_half == 1 && !p.pair && p.prod == Producer::Tma && !a.acc16;
     if (p.half) p.g = tc_geometry(a.in, false, true);
+    // Pairs of 64-row halves (option "half" = 3): a CTA pair computes 128 rows
+    // of N (64 per CTA, MMA M = 128 over the pair) by 128 or 256 columns of M,
+    // each CTA loading its own 64 rows of B and half of the tile's A rows, so
+    // every B row has one reader and a stage is 16 KB (tile width 128).  Each
+    // epilogue warp stores half the tile's columns, so the width must be a
+    // whole number of 64-column chunks per half: 128 or 256.
+    // Automatically (option "half" = 0) for 16-bit inputs with 64 < M <= 256
+    // where one-CTA small tiles were chosen above (the pair tiles of 256 rows
+    // fill less than a wave) and the pairs of halves fit in one wave; they then
+    // run with two MMA issuers (below).  Measured on GB300 against the one-CTA
+    // 64- or 128-column tiles with two issuers (paired A/B): BF16 M x 8192 x 8192
+    // M = 128 30.7 -> 29.6 us, 192 35.0 -> 33.8, 256 35.1 -> 33.6; K = 16384,
+    // M = 128 55.9 -> 54.0, 256 63.2 -> 60.9; FP16 128 x 8192 x 8192 30.0 -> 29.2.
+    // FP8 (1-2 % slower), M <= 64 (level) and two waves (6 % slower) keep the
+    // one-CTA tiles.
+    // They must also fill at least three quarters of the pair slots (64 pairs
+    // on 152 SMs were measured); fewer leave SMs idle where split-K fills them.
+    const int tq_half = (opt_tq == 128 || opt_tq == 256) ? opt_tq : (M <= 128 ? 128 : 256);
+    const int64_t pairs_half = ((N + 127) / 128) * ((M + tq_half - 1) / tq_half);
+    const bool auto_halves = opt_half == 0 && small_q != 0 && a.in != InKind::E4M3 && M > 64 &&
+                             M <= 256 && g_opt_dual.load() != 1 && pairs_half <= a.sms / 2 &&
+                             4 * pairs_half >= 3 * (a.sms / 2);
+    if ((opt_half == 3 || auto_halves) && p.prod == Producer::Tma && !a.acc16) {
+        p.pair = true;
+        p.half = true;
+        p.tile_q = tq_half;
+        p.g = tc_geometry(a.in, true, true);
+    }
     const TcGeometry& g = p.g;
     p.load_q = p.tile_q / g.cluster;
     p.tiles_p = (N + g.tile_p - 1) / g.tile_p;
@@ -414,7 +445,7 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
         auto narrow_ok = [&](int c) {
             return p.tile_q % c == 0 && (p.tile_q / c) % min_w == 0 && p.tile_q / c >= 64;
         };
-        if (p.splits == 1 && rem > 0 && opt_tail != 1) {
+        if (p.splits == 1 && rem > 0 && opt_tail != 1 && !(p.half && p.pair)) {
             if (opt_tail == 2 || opt_tail == 4) {
                 f = narrow_ok(opt_tail) ? opt_tail : 1;
             } else {
@@ -456,6 +487,25 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
             p.grid = static_cast<int>((units < slots ? units : slots) * g.cluster);
         }
     }
+    // Two MMA-issuing warps (TcCfg DUAL): one-CTA TMA tiles of at most 128
+    // columns without K pieces.  Narrow skinny tiles are bound by the MMA issue
+    // rate, so automatically (option "dual" = 0) they run where the tiles are at
+    // most 64 columns wide and fit in one wave.  Measured on GB300 (paired A/B,
+    // 10-launch blocks alternating over 12 rounds): BF16 128 x 8192 x 8192
+    // 32.8 -> 30.5 us, FP16 the same shape 32.8 -> 30.3, FP8 18.9 -> 17.4, BF16
+    // 128 x 8192 x 16384 59.5 -> 56.0, 64 x 14336 x 4096 23.9 -> 23.0; with
+    // 128-column tiles (M = 192, 256) 1.2-1.4 % slower, so not there.
+    const int opt_dual = g_opt_dual.load();
+    if (opt_dual != 1 && !p.pair && !p.half && p.prod == Producer::Tma && !a.acc16 &&
+        p.tile_q <= 128 && p.splits == 1 && !p.tail_ksplit &&
+        (opt_dual == 2 || (p.tile_q <= 64 && p.tiles <= p.slots)))
+        p.dual = true;
+    // ... and for pairs of 64-row halves (accumulators of tile_q / 2 columns
+    // per CTA): automatically whenever they run, since without two issuers they
+    // measured slower than one-CTA tiles on every skinny shape tried (BF16 128 x
+    // 8192 x 8192: 35.0 against 30.7 us)
+    if (opt_dual != 1 && p.pair && p.half && p.prod == Producer::Tma && !a.acc16)
+        p.dual = true;
     return p;
 }
 
@@ -627,6 +677,7 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     TcLaunch L;
     std::memset(&L, 0, sizeof(L));
     L.half = pl.half;
+    L.dual = pl.dual;
     const CUtensorMapDataType in_dt = in == InKind::F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                       : in == InKind::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                            : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -644,7 +695,8 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     // One staged chunk is one 128-byte row per accumulator row of an
     // epilogue warp: a box of 128 / os columns x 32 rows (16 for 64-row tiles).
     if (r == CUDA_SUCCESS && c_tma)
-        r = encode_2d(&L.map_out, out_dt, C, M, N, ldc * os, 128 / os, L.half ? 16 : 32);
+        r = encode_2d(&L.map_out, out_dt, C, M, N, ldc * os, 128 / os,
+                      (L.half && !pair) ? 16 : 32);
     if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
 
     const int64_t tiles_p = pl.tiles_p, tiles_q = pl.tiles_q, tiles = pl.tiles;
@@ -717,11 +769,11 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
         std::fprintf(stderr,
                      "[gemm] tn in=%d M=%lld N=%lld K=%lld pair=%d producer=%d direct_store=%d "
                      "splits=%d tile_q=%d tail=%d ktail=%d stages=%d tiles=%lldx%lld grid=%d "
-                     "half=%d\n",
+                     "half=%d dual=%d\n",
                      int(in), (long long)M, (long long)N, (long long)K, int(pair), int(prod),
                      L.prm.direct_store, L.prm.splits, L.prm.tile_q, L.prm.tail_f,
                      L.prm.tail_ksplit, L.prm.stages,
-                     (long long)tiles_q, (long long)tiles_p, L.grid, int(L.half));
+                     (long long)tiles_q, (long long)tiles_p, L.grid, int(L.half), int(L.dual));
     e = tc_launch(in, pair, prod, out_f32, L);
     return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
 }
@@ -903,7 +955,8 @@ int gemm_tn_plan(int kind, int64_t M, int64_t N, int64_t K, int flags, int64_t w
                                          pl.tiles_q,
                                          pl.kb_per_split,
                                          pl.tail_kb_per,
-                                         pl.stage_bytes};
+                                         pl.stage_bytes,
+                                         pl.dual};
     for (int i = 0; i < GEMM_PLAN_FIELDS; ++i) out[i] = v[i];
     return GEMM_OK;
 }
@@ -991,8 +1044,11 @@ int gemm_set_option(const char* name, int64_t value) {
     } else if (!std::strcmp(name, "repack")) {
         if (value < 0 || value > 1) return GEMM_ERR_INVALID_OPTION;
         g_opt_repack.store(static_cast<int>(value));
-    } else if (!std::strcmp(name, "half")) {
+    } else if (!std::strcmp(name, "dual")) {
         if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
+        g_opt_dual.store(static_cast<int>(value));
+    } else if (!std::strcmp(name, "half")) {
+        if (value < 0 || value > 3) return GEMM_ERR_INVALID_OPTION;
         g_opt_half.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "max_ctas")) {
         if (value < 0 || value > 1 << 20) return GEMM_ERR_INVALID_OPTION;

@@ -90,7 +90,8 @@ struct TcLaunch {
     TcParams prm;
     int grid;
     cudaStream_t stream;
-    bool half;  // one CTA per 64-row tile (MMA M = 64); unsplit TMA launches only
+    bool half;  // 64-row tiles (one CTA, MMA M = 64; or pair halves, MMA M = 128)
+    bool dual;  // two MMA-issuing warps (one CTA, TMA, unsplit, tile_q <= 128)
 };
 
 // Tile geometry of one persistent CTA (or CTA pair), for the host's grid sizing.

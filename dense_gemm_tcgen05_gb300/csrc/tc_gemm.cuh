@@ -51,17 +51,31 @@
 
 namespace gb300 {
 
-// HALF: one CTA per tile of 64 P rows (MMA M = 64).  Its accumulator row
-// 16 q + i sits in TMEM lane 32 q + i (i < 16), so each epilogue warp owns 16
-// rows instead of 32; used for unsplit TMA launches only.
-template <InKind IN, bool PAIR, bool LOADS, bool HALF = false>
+// HALF: 64 P rows per CTA; used for unsplit TMA launches only.
+//   one CTA (MMA M = 64): accumulator row 16 q + i sits in TMEM lane 32 q + i
+//     (i < 16), so each epilogue warp owns 16 rows;
+//   a CTA pair (MMA M = 128, cta_group::2): each CTA holds its 64 rows for all
+//     N columns of the MMA, row r and column n in lane r + 64 (n / (N / 2)),
+//     column n % (N / 2) (measured on GB300 with an in-bounds probe), so each
+//     epilogue warp owns 32 rows of one half of the columns.
+// DUAL: a second MMA-issuing warp (warp 6).  The two issuers take alternate K
+// stages of each unit into accumulators of their own (the second tile_q columns
+// after the first), and the epilogue adds the two.  tcgen05.mma instructions
+// from one issuing thread that commits after every stage complete one at a
+// time, so small MMAs (narrow tiles) are limited by the issue rate; measured
+// on GB300 (one CTA, MMA N = 64, a commit every 4 MMAs) one issuer completes an
+// MMA every ~250 cycles, two issuers one every ~126.  Needs tile_q <= 128 (both
+// accumulators in one 256-column buffer); one CTA, TMA, unsplit.
+template <InKind IN, bool PAIR, bool LOADS, bool HALF = false, bool DUAL = false>
 struct TcCfg {
     static_assert(!(PAIR && LOADS), "the load-based producer runs one CTA per tile");
-    static_assert(!(HALF && (PAIR || LOADS)), "64-row tiles: one CTA, TMA producer");
+    static_assert(!(HALF && LOADS), "64-row tiles: TMA producer");
+    static_assert(!(DUAL && (LOADS || (PAIR != HALF))),
+                  "two issuers: TMA; one CTA with 128-row tiles, or a pair of 64-row halves");
     static constexpr int kCG = PAIR ? 2 : 1;
     static constexpr int kElemBytes = IN == InKind::E4M3 ? 1 : 2;
     static constexpr int kBlockP = HALF ? 64 : 128;  // accumulator rows per CTA
-    static constexpr int kMmaM = PAIR ? 256 : kBlockP;  // M of one MMA instruction
+    static constexpr int kMmaM = kBlockP * kCG;      // M of one MMA instruction
     static constexpr int kMmaN = 256;                // N of one MMA instruction
     static constexpr int kTileP = kMmaM;             // P rows per tile (per pair)
     static constexpr int kMaxLoadQ = kMmaN / (PAIR ? 2 : 1);  // Q rows a CTA loads, at most
@@ -77,12 +91,16 @@ struct TcCfg {
     static_assert(kStages * kStageBytes <= kStageRegion, "widest stages fit the ring");
     static constexpr int kMaxStages = 20;  // narrow tiles: more, smaller stages in the region
     static constexpr int kEpiWarps = 4;
-    static constexpr int kRowsPerWarp = kBlockP / kEpiWarps;  // accumulator rows per epilogue warp
+    // accumulator rows per epilogue warp (a pair of 64-row halves: 32 rows of
+    // one half of the columns)
+    static constexpr int kRowsPerWarp = (PAIR && HALF) ? 32 : kBlockP / kEpiWarps;
+    static constexpr bool kColHalves = PAIR && HALF;
     static constexpr int kEpiBufBytes = 32 * 128;            // 32 rows x one 128-byte row
     static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
     static constexpr int kFirstLoadWarp = 6;
     static constexpr int kLoadWarps = 12;
-    static constexpr int kThreads = LOADS ? (kFirstLoadWarp + kLoadWarps) * 32 : 192;
+    static constexpr int kDualWarp = 6;  // the second MMA issuer (DUAL)
+    static constexpr int kThreads = LOADS ? (kFirstLoadWarp + kLoadWarps) * 32 : (DUAL ? 224 : 192);
     static constexpr int kFullArrivals = LOADS ? kLoadWarps : 1;
     static constexpr int kAccCols = kMmaN;
     static constexpr int kTmemCols = 512;
@@ -241,14 +259,15 @@ __device__ __forceinline__ uint4 mask_chunk(uint4 v, int32_t lim) {
 // SPLIT: the launch cuts tiles into K pieces (split-K or a K-split tail) and
 // combines them through the workspace.  Launches without K pieces run the
 // instantiation without that code.
-template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT, bool HALF>
-__global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF>::kThreads, 1)
+template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT, bool HALF, bool DUAL = false>
+__global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, DUAL>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
                    const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_out,
                    const __grid_constant__ CUtensorMap map_q_tail, const TcParams prm) {
-    using Cfg = TcCfg<IN, PAIR, LOADS, HALF>;
+    using Cfg = TcCfg<IN, PAIR, LOADS, HALF, DUAL>;
     static_assert(!(SPLIT && HALF), "64-row tiles never split K");
+    static_assert(!(SPLIT && DUAL), "two issuers: unsplit launches only");
     constexpr int SM = Cfg::kMaxStages;                 // barrier slots
     const uint32_t S = static_cast<uint32_t>(prm.stages);  // ring depth for this call
     const uint32_t stage_bytes = prm.stage_bytes;
@@ -271,6 +290,9 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF>::kThreads, 1)
 
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
+    // TMEM column of the second issuer's accumulator (DUAL): after the first
+    // one, whose width is tile_q columns (tile_q / 2 for a pair of halves).
+    const uint32_t kAcc2Off = static_cast<uint32_t>(PAIR ? prm.tile_q / 2 : prm.tile_q);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SM; ++s) {
@@ -278,10 +300,10 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF>::kThreads, 1)
             mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(accf_bar(b), 1);
+            mbar_init(accf_bar(b), DUAL ? 2 : 1);   // one commit per issuer
             mbar_init(acce_bar(b), (PAIR ? 2 : 1) * Cfg::kEpiWarps);
         }
-        mbar_init(done_bar, 1);
+        mbar_init(done_bar, DUAL ? 2 : 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -524,8 +546,11 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF>::kThreads, 1)
                 if (lane == 0) mbar_arrive(full_bar(s));
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || (DUAL && warp == Cfg::kDualWarp)) {
         // ------------------------------------------------ MMA issuer
+        // issuer 1 (DUAL only) takes the odd K stages of each unit into the
+        // accumulator tile_q columns after issuer 0's
+        const uint32_t issuer = (DUAL && warp == Cfg::kDualWarp) ? 1u : 0u;
         if (!PAIR || leader) {
             uint32_t lt = 0, rs = 0, rph = 0;   // tiles; ring slot and phase
             const uint64_t adesc0 = sdesc_kmajor_sw128(base);
@@ -538,7 +563,8 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF>::kThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + b * Cfg::kAccCols;
+                const uint32_t d_tmem =
+                    tmem_base + b * Cfg::kAccCols + issuer * kAcc2Off;
                 const Unit w = unit_of(u);
                 const uint32_t idesc = w.narrow ? prm.idesc_tail : prm.idesc;
                 const int32_t kb_lo = w.kb_lo;
@@ -547,6 +573,9 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF>::kThreads, 1)
                     if (++rs == S) {
                         rs = 0;
                         rph ^= 1u;
+                    }
+                    if constexpr (DUAL) {
+                        if (static_cast<uint32_t>((kb - kb_lo) & 1) != issuer) continue;
                     }
                     if (!warp_wait(full_bar(s), ph, wd)) {
                         ok = false;
@@ -563,7 +592,11 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF>::kThreads, 1)
                         for (int kk = 0; kk < Cfg::kMmasPerStage; ++kk) {
                             // advance the start address by 32 bytes of K per MMA
                             const uint64_t off = static_cast<uint64_t>(kk * (Cfg::kMmaKBytes >> 4));
-                            const uint32_t acc = (kb != kb_lo || kk != 0) ? 1u : 0u;
+                            uint32_t acc;
+                            if constexpr (DUAL)
+                                acc = (kb - kb_lo > static_cast<int32_t>(issuer) || kk != 0) ? 1u : 0u;
+                            else
+                                acc = (kb != kb_lo || kk != 0) ? 1u : 0u;
                             if constexpr (IN == InKind::E4M3)
                                 mma_f8<Cfg::kCG>(d_tmem, adesc + off, bdesc + off, idesc, acc);
                             else
@@ -736,14 +769,18 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF>::kThreads, 1)
             const int64_t tp = w.tp;
             // A tile narrower than one chunk (16 or 32 columns) spans all of M, so
             // the chunk's columns past the tile lie past M and are not stored.
-            const int chunks = (w.width + kCols - 1) / kCols;
+            // A pair of 64-row halves: this warp's rows carry half the columns.
+            const int wcols = Cfg::kColHalves ? w.width / 2 : w.width;
+            const int chunks = (wcols + kCols - 1) / kCols;
             const uint32_t b = lt & 1u, aph = (lt >> 1) & 1u;
             if (!warp_wait(accf_bar(b), aph, wd)) break;
             tc_fence_after_sync();
+            const uint32_t wrow = Cfg::kColHalves ? (quarter & 1u) : quarter;
             const int32_t row0 =
                 static_cast<int32_t>(tp * Cfg::kTileP + rank * Cfg::kBlockP +
-                                     quarter * Cfg::kRowsPerWarp);
-            const int32_t col0 = w.q_off;
+                                     wrow * Cfg::kRowsPerWarp);
+            const int32_t col0 =
+                w.q_off + (Cfg::kColHalves ? static_cast<int32_t>(quarter >> 1) * wcols : 0);
             const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + b * Cfg::kAccCols;
             if (!SPLIT || w.pieces == 1) {
 #pragma unroll 1
@@ -752,6 +789,22 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF>::kThreads, 1)
                     tmem_ld_32x32b_x32(t_row + c * kCols, v0);
                     if constexpr (kCols == 64) tmem_ld_32x32b_x32(t_row + c * kCols + 32, v1);
                     tmem_wait_ld();
+                    if constexpr (DUAL) {
+                        // the second issuer's sums (odd K stages), when it had any
+                        if (w.kb_hi - w.kb_lo >= 2) {
+                            uint32_t u0[32], u1[32];
+                            const uint32_t t2 = t_row + kAcc2Off + c * kCols;
+                            tmem_ld_32x32b_x32(t2, u0);
+                            if constexpr (kCols == 64) tmem_ld_32x32b_x32(t2 + 32, u1);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                v0[j] = __float_as_uint(__uint_as_float(v0[j]) + __uint_as_float(u0[j]));
+                                if constexpr (kCols == 64)
+                                    v1[j] = __float_as_uint(__uint_as_float(v1[j]) + __uint_as_float(u1[j]));
+                            }
+                        }
+                    }
                     if (c == chunks - 1) release_acc(b);
                     uint32_t pk[32];
                     if (kOB == 2 && prm.acc16) {
@@ -849,10 +902,11 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF>::kThreads, 1)
     }
 }
 
-template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT, bool HALF = false>
+template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT, bool HALF = false,
+          bool DUAL = false>
 cudaError_t tc_launch_one(const TcLaunch& L) {
-    using Cfg = TcCfg<IN, PAIR, LOADS, HALF>;
-    auto kernel = tc_gemm_kernel<IN, OutT, PAIR, LOADS, SPLIT, HALF>;
+    using Cfg = TcCfg<IN, PAIR, LOADS, HALF, DUAL>;
+    auto kernel = tc_gemm_kernel<IN, OutT, PAIR, LOADS, SPLIT, HALF, DUAL>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -891,12 +945,21 @@ cudaError_t tc_launch_split(bool pair, Producer prod, const TcLaunch& L) {
         if (pair || L.half) return cudaErrorInvalidConfiguration;
         return tc_launch_one<IN, OutT, false, true, SPLIT>(L);
     }
+    if (L.dual) {
+        if constexpr (SPLIT) {
+            return cudaErrorInvalidConfiguration;
+        } else {
+            if (pair != L.half) return cudaErrorInvalidConfiguration;
+            return pair ? tc_launch_one<IN, OutT, true, false, false, true, true>(L)
+                        : tc_launch_one<IN, OutT, false, false, false, false, true>(L);
+        }
+    }
     if (L.half) {
         if constexpr (SPLIT) {
             return cudaErrorInvalidConfiguration;
         } else {
-            if (pair) return cudaErrorInvalidConfiguration;
-            return tc_launch_one<IN, OutT, false, false, false, true>(L);
+            return pair ? tc_launch_one<IN, OutT, true, false, false, true>(L)
+                        : tc_launch_one<IN, OutT, false, false, false, true>(L);
         }
     }
     return pair ? tc_launch_one<IN, OutT, true, false, SPLIT>(L)
@@ -912,6 +975,12 @@ cudaError_t tc_launch_impl(bool pair, Producer prod, const TcLaunch& L) {
 
 template <InKind IN>
 TcGeometry tc_geometry_impl(bool pair, bool half) {
+    if (half && pair) {
+        using Cfg = TcCfg<IN, true, false, true>;
+        return TcGeometry{Cfg::kTileP,  Cfg::kMmaN,    Cfg::kBlockP,      Cfg::kStageK,
+                          2,            Cfg::kMmaM,    Cfg::kFormat,      Cfg::kStageRegion,
+                          Cfg::kMaxStages};
+    }
     if (half) {
         using Cfg = TcCfg<IN, false, false, true>;
         return TcGeometry{Cfg::kTileP,  Cfg::kMmaN,    Cfg::kBlockP,      Cfg::kStageK,

@@ -206,7 +206,8 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
  *                    last-wave units per tile (1: untouched), last wave cut along K
  *                    (0/1; else along M), ring stages, grid (CTAs), A repacked,
  *                    B repacked, tiles along N, tiles along M, K stages per
- *                    piece, K stages per last-wave piece, ring stage bytes.
+ *                    piece, K stages per last-wave piece, ring stage bytes, two
+ *                    MMA-issuing warps (0/1).
  *
  * Returns GEMM_OK, GEMM_ERR_INVALID_DIM or GEMM_ERR_INVALID_OPTION (kind, out
  * or nout).  A call that would be refused reports its status in out[0]
@@ -223,7 +224,7 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
 #define GEMM_PLAN_A_128 8
 #define GEMM_PLAN_B_128 16
 #define GEMM_PLAN_NOALLOC 32
-#define GEMM_PLAN_FIELDS 17
+#define GEMM_PLAN_FIELDS 18
 int gemm_tn_plan(int kind, int64_t M, int64_t N, int64_t K, int flags, int64_t workspace_bytes,
                  int sms, int64_t* out, int nout);
 
@@ -268,9 +269,16 @@ int gemm_read_watchdog(int reset);
  *                 padding cost; 16 or 32 when all of M fits in one such tile and
  *                 single-CTA tiles run), or 16, 32, 64, 128, 192, 256 (16 and 32
  *                 only apply when M fits in one tile and CTAs do not pair; else 64)
- *   "half"        64-row tiles (one CTA per 64 rows of N, MMA M = 64): 0 or 2
- *                 never (default), 1 wherever single-CTA TMA tiles with FP32
- *                 accumulation run; they never split K
+ *   "half"        64-row tiles: 0 or 2 never (default); 1 one CTA per 64 rows of N
+ *                 (MMA M = 64) wherever single-CTA TMA tiles with FP32 accumulation
+ *                 run; 3 CTA pairs of 64-row halves (128 rows of N per pair, MMA
+ *                 M = 128 over the pair, tile width 128 or 256 along M) wherever
+ *                 TMA tiles with FP32 accumulation run.  They never split K
+ *   "dual"        two MMA-issuing warps per CTA, taking alternate K stages into
+ *                 accumulators of their own that the epilogue adds: 0 auto (default:
+ *                 one-CTA TMA tiles of at most 64 columns that run unsplit in one
+ *                 wave), 1 never, 2 wherever one-CTA TMA tiles of at most 128
+ *                 columns run unsplit
  *   "tail"        the last, partial wave of tiles: 0 auto (default) cuts its tiles
  *                 into 2 or 4 narrower ones when that ends it sooner, 1 never, 2 or
  *                 4 always

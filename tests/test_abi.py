@@ -151,7 +151,8 @@ def test_options():
     assert capi.gemm_set_option("tail_k", 0) == 0
     assert capi.gemm_set_option("repack", 2) == capi.GEMM_ERR_INVALID_OPTION
     assert capi.gemm_set_option("repack", 0) == 0
-    assert capi.gemm_set_option("half", 3) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("half", 4) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("half", 3) == 0
     assert capi.gemm_set_option("half", 0) == 0
 
 

@@ -1,0 +1,135 @@
+"""GPU parity of pairs of 64-row halves against the CPU oracle, through the C ABI.
+
+A CTA pair computes 128 rows of N (64 per CTA, tcgen05.mma cta_group::2 with
+M = 128) by 128 or 256 columns of M.  Each CTA holds its 64 rows for all the
+tile's columns, row r and column n in TMEM lane r + 64 (n / (width / 2)),
+column n % (width / 2), so each epilogue warp stores 32 rows of one half of
+the columns.  These cases cover that mapping on every input kind and output
+type, both tile widths, ragged edges in M, N and K (a partial last pair tile,
+and a pair whose second CTA lies past N), leading dimensions that take the
+row-wise store path, +-1 inputs (exact), and few CTA pairs that each walk many
+tiles (ring and accumulator phases)."""
+import pytest
+import torch
+
+import oracle
+import synthetic_inputs as si
+from dense_gemm_tcgen05_gb300 import capi
+from gpu_util import (assert_codes_equal, check_full, check_sampled, exact_codes, out_codes,
+                      run_tn)
+
+pytestmark = pytest.mark.gpu
+KINDS = ["f16", "bf16", "e4m3"]
+
+
+@pytest.fixture
+def pair_halves():
+    touched = []
+
+    def set_(name, value):
+        assert capi.gemm_set_option(name, value) == 0
+        touched.append(name)
+    set_("half", 3)
+    yield set_
+    for name in touched:
+        capi.gemm_set_option(name, -1 if name == "pair" else 0)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("shape", [(128, 8192, 512), (100, 1000, 257), (256, 700, 300),
+                                   (200, 130, 1000), (1, 64, 64), (129, 333, 128)])
+def test_forced_random(kind, shape, pair_halves):
+    M, N, K = shape
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=M + N + K, sigma=0.5)
+    C = run_tn(kind, ops, M, N, K)
+    check_full(kind, ops, M, N, K, C)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("tile_q", [128, 256])
+def test_forced_pm1_bitexact(kind, tile_q, pair_halves):
+    pair_halves("tile_q", tile_q)
+    M, N, K = 250, 1000, 2048
+    ops = si.tn_operands(kind, M, N, K, dist="pm1", seed=7)
+    C = run_tn(kind, ops, M, N, K)
+    exact = oracle.gemm_tn(kind, M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+    assert_codes_equal(out_codes(C, M, N), exact_codes(kind, exact))
+
+
+@pytest.mark.parametrize("ctas", [2, 6])
+def test_few_pairs_walk_many_tiles(ctas, pair_halves):
+    """Two or six CTAs (one or three pairs) each run many tiles: every ring
+    slot and both accumulator buffers cycle through several phases."""
+    pair_halves("max_ctas", ctas)
+    M, N, K = 300, 1200, 700
+    ops = si.tn_operands("bf16", M, N, K, dist="pm1", seed=ctas)
+    C = run_tn("bf16", ops, M, N, K)
+    exact = oracle.gemm_tn("bf16", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+    assert_codes_equal(out_codes(C, M, N), exact_codes("bf16", exact))
+
+
+@pytest.mark.parametrize("ldc_pad", [0, 3])
+def test_forced_row_wise_stores(ldc_pad, pair_halves):
+    """ldc = M + 3 with M odd: C rows are not 16-byte aligned, so the epilogue
+    writes rows itself (32 per warp, half the columns each); the padding must
+    keep its sentinel."""
+    M, N, K = 137, 333, 200
+    ldc = M + ldc_pad
+    ops = si.tn_operands("bf16", M, N, K, dist="normal", seed=11)
+    C = run_tn("bf16", ops, M, N, K, ldc=ldc)
+    check_full("bf16", ops, M, N, K, C)
+    if ldc_pad:
+        assert torch.all(torch.isnan(C[:N, M:].float())), "C padding was written"
+
+
+@pytest.mark.parametrize("M", [64, 128, 192])
+def test_fp8_f32_output(M, pair_halves):
+    """FP32 output: 32-column chunks, two or four per warp; the contract
+    tolerance and the bound of one FP32 rounding plus the accumulation."""
+    import numpy as np
+    from test_fp8_f32out_gpu import run, tols
+
+    N, K = 520, 384
+    ops = si.tn_operands("e4m3", M, N, K, dist="normal", seed=M)
+    C = run(ops, M, N, K)
+    exact = oracle.gemm_tn("e4m3", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K,
+                           ops["scale_a"], ops["scale_b"])
+    a = ops["A"][:, :K].to(torch.float64).numpy() * ops["scale_a"]
+    b = ops["B"][:, :K].to(torch.float64).numpy() * ops["scale_b"]
+    contract, tight = tols(ops, K, exact, np.abs(a) @ np.abs(b).T)
+    err = np.abs(C[:N, :M].double().numpy().T - exact)
+    assert err.max() <= contract and np.all(err <= tight)
+
+
+@pytest.mark.parametrize("kind,shape", [("bf16", (128, 8192, 8192)), ("e4m3", (256, 8192, 8192)),
+                                        ("f16", (128, 16384, 4096))])
+def test_forced_skinny_sampled(kind, shape, pair_halves):
+    M, N, K = shape
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=5, sigma=1.0 if kind == "e4m3"
+                         else 0.05)
+    C = run_tn(kind, ops, M, N, K)
+    check_sampled(kind, ops, M, N, K, C, seed=3)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("shape", [(128, 4100, 700), (256, 900, 2048), (1, 64, 64), (200, 333, 129)])
+def test_two_issuers_random(kind, shape, pair_halves):
+    """Pairs of halves with two MMA-issuing warps in the leader CTA (option
+    "dual" = 2): alternate K stages into accumulators of tile_q / 2 columns
+    each, added by the epilogue; units of one K stage add nothing."""
+    pair_halves("dual", 2)
+    M, N, K = shape
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=M + N + K + 1, sigma=0.5)
+    C = run_tn(kind, ops, M, N, K)
+    check_full(kind, ops, M, N, K, C)
+
+
+@pytest.mark.parametrize("ctas", [2, 6, 0])
+def test_two_issuers_pm1_bitexact(ctas, pair_halves):
+    pair_halves("dual", 2)
+    pair_halves("max_ctas", ctas)
+    M, N, K = 250, 1200, 2048
+    ops = si.tn_operands("bf16", M, N, K, dist="pm1", seed=ctas + 3)
+    C = run_tn("bf16", ops, M, N, K)
+    exact = oracle.gemm_tn("bf16", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+    assert_codes_equal(out_codes(C, M, N), exact_codes("bf16", exact))
