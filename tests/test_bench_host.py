@@ -147,12 +147,12 @@ def test_tensor_peak_follows_the_window():
     assert (peak, regime) == (burst, "burst") and "12 ms" in why
     assert 1837.6 / peak == pytest.approx(0.96, abs=0.001)
     # short, even if capped
-    assert bench.tensor_peak(500.0, {"reasons": ["sw_power_cap"]}, burst, sustained)[1] == "burst"
+    assert bench.tensor_peak(100.0, {"reasons": ["sw_power_cap"]}, burst, sustained)[1] == "burst"
     # long but not capped
     peak, regime, why = bench.tensor_peak(3000.0, {"reasons": []}, burst, sustained)
     assert regime == "burst" and "no sw_power_cap" in why
-    # long and capped: a 1000-step loop at the power cap
-    peak, regime, _ = bench.tensor_peak(1600.0, {"reasons": ["sw_power_cap"]}, burst, sustained)
+    # long and capped: the default 1000-step loop (0.67 s) at the power cap
+    peak, regime, _ = bench.tensor_peak(667.0, {"reasons": ["sw_power_cap"]}, burst, sustained)
     assert (peak, regime) == (sustained, "sustained")
     # no clock record at all
     assert bench.tensor_peak(5000.0, None, burst, sustained)[1] == "burst"
