@@ -12,18 +12,23 @@ script measures how far the automatic choices are from the best one found.
   python -m dense_gemm_tcgen05_gb300.tune [--shapes f16:8192x8192x8192,...]
          [--iters 20] [--quick]
 
-Each timing: 3 warm-up calls, then `iters` calls on the same stream between
-CUDA events, inputs rotating over two sets; each shape starts with a longer
-warm-up run so that clocks have settled, and the automatic choice is timed
-before and after the sweep (the better of the two is reported).  One JSON line
-per shape is printed with every configuration's TFLOP/s, the best one and the
-automatic choice's.
+Each sweep timing: 3 warm-up calls, then `iters` calls on the same stream
+between CUDA events, inputs rotating over two sets; each shape starts with a
+longer warm-up run so that clocks have settled.  A single pass over many
+configurations drifts with the GPU's clock and power (the same configuration
+can differ by several per cent within one sweep), so the automatic choice and
+the three fastest configurations of the sweep are then timed again, paired:
+`rounds` rounds in alternating order, `iters` calls each, and the medians
+decide.  One JSON line per shape is printed with every configuration's sweep
+TFLOP/s, the paired medians, the best configuration and the automatic
+choice's fraction of it.
 """
 from __future__ import annotations
 
 import argparse
 import itertools
 import json
+import statistics
 
 import torch
 
@@ -31,7 +36,7 @@ from . import capi
 
 DEFAULT_SHAPES = ["f16:8192x8192x8192", "bf16:4096x4096x4096", "bf16:4096x14336x4096",
                   "e4m3:8192x8192x8192", "e4m3:3072x4096x8192", "bf16:128x8192x8192",
-                  "bf16:1024x1024x8192"]
+                  "bf16:256x8192x8192", "e4m3:128x8192x8192", "bf16:1024x1024x8192"]
 _DT = {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
 
 
@@ -87,7 +92,21 @@ def _set(pair, group, tile_q, splits):
             raise RuntimeError("option %s=%s: %s" % (name, value, capi.status_text(st)))
 
 
-def tune_shape(spec: str, iters: int, quick: bool) -> dict:
+def paired(kind, M, N, K, ops, configs, iters, rounds, stream) -> list:
+    """Median TFLOP/s of each configuration (None: the automatic choice) over
+    `rounds` rounds in alternating order."""
+    res = [[] for _ in configs]
+    order = list(range(len(configs)))
+    for r in range(rounds):
+        for i in (order if r % 2 == 0 else order[::-1]):
+            c = configs[i]
+            _set(*(c if c is not None else (-1, 0, 0, 0)))
+            res[i].append(time_config(kind, M, N, K, ops, iters, stream))
+    _set(-1, 0, 0, 0)
+    return [statistics.median(v) for v in res]
+
+
+def tune_shape(spec: str, iters: int, quick: bool, rounds: int = 8) -> dict:
     kind, M, N, K = _parse(spec)
     ops = _operands(kind, M, N, K)
     stream = torch.cuda.Stream()
@@ -105,12 +124,18 @@ def tune_shape(spec: str, iters: int, quick: bool) -> dict:
             rows.append({"pair": p, "group": g, "tile_q": t, "splits": s,
                          "tflops": round(time_config(kind, M, N, K, ops, iters, stream), 1)})
         _set(-1, 0, 0, 0)
-        auto = max(auto, time_config(kind, M, N, K, ops, iters, stream))  # again, after the sweep
+        top = sorted(rows, key=lambda r: -r["tflops"])[:3]
+        cands = [None] + [(r["pair"], r["group"], r["tile_q"], r["splits"]) for r in top]
+        med = paired(kind, M, N, K, ops, cands, iters, rounds, stream)
     finally:
         _set(-1, 0, 0, 0)
-    best = max(rows, key=lambda r: r["tflops"])
+    auto = med[0]
+    finals = [dict(r, paired_tflops=round(m, 1)) for r, m in zip(top, med[1:])]
+    best = max(finals, key=lambda r: r["paired_tflops"])
     return {"shape": spec, "auto_tflops": round(auto, 1), "best": best,
-            "auto_over_best": round(auto / best["tflops"], 4), "configs": rows}
+            "auto_over_best": round(min(1.0, auto / best["paired_tflops"]), 4),
+            "auto_over_best_raw": round(auto / best["paired_tflops"], 4),
+            "paired": finals, "configs": rows}
 
 
 def main(argv=None):
@@ -118,6 +143,7 @@ def main(argv=None):
     ap.add_argument("--shapes", default=",".join(DEFAULT_SHAPES))
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--quick", action="store_true", help="fewer group sizes and tile widths")
+    ap.add_argument("--rounds", type=int, default=8, help="paired rounds for the final candidates")
     args = ap.parse_args(argv)
     from . import build
 
@@ -127,7 +153,8 @@ def main(argv=None):
     capi.gemm_set_workspace(ws.data_ptr(), ws.numel())
     try:
         for spec in args.shapes.split(","):
-            print(json.dumps(tune_shape(spec.strip(), args.iters, args.quick)), flush=True)
+            print(json.dumps(tune_shape(spec.strip(), args.iters, args.quick, args.rounds)),
+                  flush=True)
     finally:
         capi.gemm_set_workspace(None, 0)
 
