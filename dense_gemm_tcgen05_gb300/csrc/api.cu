@@ -81,6 +81,7 @@ std::atomic<int> g_opt_tail{0};
 std::atomic<int> g_opt_tail_k{0};
 std::atomic<int> g_opt_repack{0};
 std::atomic<int> g_opt_f32_tail{0};
+std::atomic<int> g_opt_f32_ktail{0};
 std::atomic<int> g_opt_l2hints{0};
 std::atomic<int> g_opt_half{0};
 std::atomic<int> g_opt_dual{0};
@@ -799,9 +800,7 @@ extern "C" {
 
 int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
              int64_t ldb, float* C, int64_t ldc, void* stream_v) {
-    // The SIMT kernel forms K + 7 in 32 bits to count its K slices of 8, so K
-    // stops 7 short of the general limit.
-    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim - 7)
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return GEMM_ERR_INVALID_DIM;
     const int64_t nmin = N > 1 ? N : 1;
     if (lda < (K > 1 ? K : 1) || ldb < nmin || ldc < nmin || lda > kMaxLd || ldb > kMaxLd ||
@@ -817,7 +816,7 @@ int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
     cudaError_t e = K == 0 ? zero_fill_launch(C, M, N, ldc, 4, stream)
                            : f32_launch(M, N, K, A, lda, B, ldb, C, ldc, stream,
-                                        g_opt_f32_tail.load());
+                                        g_opt_f32_tail.load(), g_opt_f32_ktail.load());
     return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
 }
 
@@ -1038,6 +1037,9 @@ int gemm_set_option(const char* name, int64_t value) {
     } else if (!std::strcmp(name, "l2_hints")) {
         if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
         g_opt_l2hints.store(static_cast<int>(value));
+    } else if (!std::strcmp(name, "f32_ktail")) {
+        if (value < 0 || value > 7) return GEMM_ERR_INVALID_OPTION;
+        g_opt_f32_ktail.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "f32_tail")) {
         if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
         g_opt_f32_tail.store(static_cast<int>(value));

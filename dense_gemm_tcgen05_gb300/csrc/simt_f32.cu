@@ -203,6 +203,25 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (dependent && BN != kBN) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// The last k1 - k0 terms of every output's FMA chain: C[m][n] continues from
+// the value the tile kernel stored for terms [0, k0), one fused multiply-add
+// per term in increasing k, so the result is the chain over [0, k1) exactly.
+// Used when K does not fit the tile kernel's 32-bit slice count (K > 2^31 - 8;
+// then k1 - k0 <= 7).
+__global__ void f32_ktail_kernel(int64_t M, int64_t N, int64_t k0, int64_t k1,
+                                 const float* __restrict__ A, int64_t lda,
+                                 const float* __restrict__ B, int64_t ldb, float* __restrict__ C,
+                                 int64_t ldc) {
+    const int64_t total = M * N;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = i / N, n = i - m * N;
+        float acc = C[m * ldc + n];
+        for (int64_t k = k0; k < k1; ++k) acc = fmaf(A[m * lda + k], B[k * ldb + n], acc);
+        C[m * ldc + n] = acc;
+    }
+}
+
 // How many tiles run whole (the rest run as halves), given the SM count and
 // the resident blocks per SM.  Measured on GB300 (two blocks per SM): the time
 // is set by the most tiles any SM runs -- it grows by one step per 152 tiles --
@@ -278,9 +297,36 @@ cudaError_t launch_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t 
 
 }  // namespace
 
+cudaError_t f32_tiles_launch(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                             const float* B, int64_t ldb, float* C, int64_t ldc,
+                             cudaStream_t stream, int tail_mode);
+
 cudaError_t f32_launch(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                        const float* B, int64_t ldb, float* C, int64_t ldc, cudaStream_t stream,
-                       int tail_mode) {
+                       int tail_mode, int ktail) {
+    // The tile kernel counts K slices of 8 as (K + 7) / 8 in 32 bits, so it
+    // takes at most 2^31 - 8 terms; the rest (at most 7) continue each chain
+    // in f32_ktail_kernel.  `ktail` > 0 moves that many terms there for any K
+    // larger than it (to test that path at small sizes).
+    constexpr int64_t kMaxTileK = 0x7fffffffLL - (kBK - 1);
+    int64_t k_main = K > kMaxTileK ? kMaxTileK : K;
+    if (ktail > 0 && K > ktail && K - ktail < k_main) k_main = K - ktail;
+    cudaError_t e = f32_tiles_launch(M, N, k_main, A, lda, B, ldb, C, ldc, stream, tail_mode);
+    if (e != cudaSuccess || k_main == K) return e;
+    int sms = 0, per_sm = 0;
+    e = residency(true, &sms, &per_sm);
+    if (e != cudaSuccess) return e;
+    const int64_t total = M * N;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > static_cast<int64_t>(sms) * 8) blocks = static_cast<int64_t>(sms) * 8;
+    f32_ktail_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(M, N, k_main, K, A, lda,
+                                                                        B, ldb, C, ldc);
+    return cudaGetLastError();
+}
+
+cudaError_t f32_tiles_launch(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                             const float* B, int64_t ldb, float* C, int64_t ldc,
+                             cudaStream_t stream, int tail_mode) {
     const int64_t tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN;
     const int64_t tiles = tiles_m * tiles_n;
     if (tiles > 0x3fffffff) return cudaErrorInvalidValue;

@@ -125,3 +125,32 @@ def test_k_zero_and_empty():
     assert torch.all(C[:M, :N] == 0)
     init = torch.full((M, N), 5.0)
     assert torch.equal(run_f32(ops, 0, N, 1, c_init=init), init)
+
+
+@pytest.mark.parametrize("ktail", [1, 3, 7])
+@pytest.mark.parametrize("shape,lds", [((300, 260, 129), None), ((129, 4, 1000), None),
+                                       ((257, 130, 70), (75, 133, 131)), ((1, 1, 9), None),
+                                       ((2048, 3584, 16), None)])
+def test_k_tail_continues_the_chain(ktail, shape, lds):
+    """K above 2^31 - 8 runs its last terms (at most 7) in a second kernel that
+    continues each output's FMA chain from the value the tile kernel stored.
+    Option "f32_ktail" moves the last 1, 3 or 7 terms there at any K: C must
+    be bit-identical to the one-kernel result (the same chain of FMAs in k
+    order), and match the oracle; with padded leading dimensions too, and
+    with the tile kernel's unchecked variant (the last shape)."""
+    M, N, K = shape
+    lda, ldb, ldc = lds if lds else (K, N, N)
+    ops = si.f32_operands(M, N, K, dist="uniform", seed=M + N + K, lda=lda, ldb=ldb)
+    whole = run_f32(ops, M, N, K, ldc=ldc)
+    assert capi.gemm_set_option("f32_ktail", ktail) == 0
+    try:
+        split = run_f32(ops, M, N, K, ldc=ldc)
+    finally:
+        assert capi.gemm_set_option("f32_ktail", 0) == 0
+    assert torch.equal(whole[:M, :N], split[:M, :N])
+    if ldc > N:
+        assert torch.all(torch.isnan(split[:M, N:])), "C padding was written"
+    exact = oracle.gemm_f32(M, N, K, ops["A"].numpy(), lda, ops["B"].numpy(), ldb)
+    err = np.abs(split[:M, :N].double().numpy() - exact)
+    a, b = ops["A"][:, :K].double().numpy(), ops["B"][:K, :N].double().numpy()
+    assert np.all(err <= tight_f32(a, b, K))
