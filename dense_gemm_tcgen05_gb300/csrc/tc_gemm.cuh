@@ -324,13 +324,6 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, DUAL>::kThreads, 
     if constexpr (PAIR) cluster_sync();
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-    // Launched with programmatic stream serialisation: everything above ran
-    // while the previous grid in the stream may still be finishing; nothing
-    // below may touch global memory before that grid is complete.  Only then
-    // may the next grid be scheduled, so that grids waiting here never hold
-    // SMs an earlier grid still needs.
-    pdl_wait();
-    pdl_trigger();
 
     const Watch wd{abort_flag, prm.watchdog, prm.timeout_ns};
     const int64_t num_tiles = static_cast<int64_t>(prm.tiles_p) * prm.tiles_q;
@@ -386,6 +379,19 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, DUAL>::kThreads, 
     };
     const int64_t first = PAIR ? blockIdx.x / 2 : blockIdx.x;
     const int64_t stride = PAIR ? gridDim.x / 2 : gridDim.x;
+    // The TMA producer's first unit (64-bit divisions, about half a microsecond
+    // on a skinny launch's critical path), worked out from the parameters
+    // alone before the wait below.
+    Unit u_first{};
+    if (warp == 0 && !LOADS && first < num_units) u_first = unit_of(first);
+
+    // Launched with programmatic stream serialisation: everything above ran
+    // while the previous grid in the stream may still be finishing; nothing
+    // below may touch global memory before that grid is complete.  Only then
+    // may the next grid be scheduled, so that grids waiting here never hold
+    // SMs an earlier grid still needs.
+    pdl_wait();
+    pdl_trigger();
 
     if (warp == 0 && !LOADS) {
         // ------------------------------------------------ TMA producer
@@ -396,7 +402,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, DUAL>::kThreads, 
         const bool hints = prm.l2_hints != 0;
         uint32_t lu = 0;                     // units this CTA has run
         for (int64_t u = first; ok && u < num_units; u += stride, ++lu) {
-            const Unit w = unit_of(u);
+            const Unit w = u == first ? u_first : unit_of(u);
             // Every second unit reads its K range backwards (the MMA warp sums
             // the stages in whatever order they arrive).
             const int32_t k_rev = (prm.k_snake && (lu & 1u)) ? w.kb_lo + w.kb_hi - 1 : -1;
@@ -888,7 +894,10 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, DUAL>::kThreads, 
                 release_acc(b);
             }
         }
-        if (!prm.direct_store && lane == 0) bulk_wait_group<0>();
+        // The staging buffers must have been read before the CTA exits; the
+        // stores' global writes complete with the grid, which the next grid
+        // in the stream waits for (griddepcontrol.wait) before it reads C.
+        if (!prm.direct_store && lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
     }
 
