@@ -84,7 +84,7 @@ std::atomic<int> g_opt_f32_tail{0};
 std::atomic<int> g_opt_f32_ktail{0};
 std::atomic<int> g_opt_l2hints{0};
 std::atomic<int> g_opt_half{0};
-std::atomic<int> g_opt_dual{0};
+std::atomic<int> g_opt_issuers{0};
 std::atomic<int64_t> g_opt_timeout_ns{2000000000LL};
 
 thread_local cudaError_t t_last_cuda_error = cudaSuccess;
@@ -212,7 +212,7 @@ struct TnPlan {
     int64_t ws_used = 0;        // scratch bytes taken by the repacks
     Producer prod = Producer::Tma;
     bool pair = false, half = false;
-    bool dual = false;          // two MMA-issuing warps (TcCfg DUAL)
+    int issuers = 1;            // MMA-issuing warps (TcCfg NI)
     int tile_q = 0, load_q = 0;
     TcGeometry g{};
     int64_t tiles_p = 0, tiles_q = 0, tiles = 0, slots = 0;
@@ -332,7 +332,7 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
     const int tq_half = (opt_tq == 128 || opt_tq == 256) ? opt_tq : (M <= 128 ? 128 : 256);
     const int64_t pairs_half = ((N + 127) / 128) * ((M + tq_half - 1) / tq_half);
     const bool auto_halves = opt_half == 0 && small_q != 0 && a.in != InKind::E4M3 && M > 64 &&
-                             M <= 256 && g_opt_dual.load() != 1 && pairs_half <= a.sms / 2 &&
+                             M <= 256 && g_opt_issuers.load() != 1 && pairs_half <= a.sms / 2 &&
                              4 * pairs_half >= 3 * (a.sms / 2);
     if ((opt_half == 3 || auto_halves) && p.prod == Producer::Tma && !a.acc16) {
         p.pair = true;
@@ -488,25 +488,33 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
             p.grid = static_cast<int>((units < slots ? units : slots) * g.cluster);
         }
     }
-    // Two MMA-issuing warps (TcCfg DUAL): one-CTA TMA tiles of at most 128
-    // columns without K pieces.  Narrow skinny tiles are bound by the MMA issue
-    // rate, so automatically (option "dual" = 0) they run where the tiles are at
-    // most 64 columns wide and fit in one wave.  Measured on GB300 (paired A/B,
-    // 10-launch blocks alternating over 12 rounds): BF16 128 x 8192 x 8192
-    // 32.8 -> 30.5 us, FP16 the same shape 32.8 -> 30.3, FP8 18.9 -> 17.4, BF16
-    // 128 x 8192 x 16384 59.5 -> 56.0, 64 x 14336 x 4096 23.9 -> 23.0; with
-    // 128-column tiles (M = 192, 256) 1.2-1.4 % slower, so not there.
-    const int opt_dual = g_opt_dual.load();
-    if (opt_dual != 1 && !p.pair && !p.half && p.prod == Producer::Tma && !a.acc16 &&
-        p.tile_q <= 128 && p.splits == 1 && !p.tail_ksplit &&
-        (opt_dual == 2 || (p.tile_q <= 64 && p.tiles <= p.slots)))
-        p.dual = true;
-    // ... and for pairs of 64-row halves (accumulators of tile_q / 2 columns
-    // per CTA): automatically whenever they run, since without two issuers they
-    // measured slower than one-CTA tiles on every skinny shape tried (BF16 128 x
-    // 8192 x 8192: 35.0 against 30.7 us)
-    if (opt_dual != 1 && p.pair && p.half && p.prod == Producer::Tma && !a.acc16)
-        p.dual = true;
+    // Several MMA-issuing warps (TcCfg NI): one-CTA TMA tiles without K pieces
+    // whose NI accumulators (and the epilogue's 64-column chunk reads past the
+    // last one) fit in one 256-column TMEM buffer.  Narrow skinny tiles are
+    // bound by the MMA issue rate, so automatically (option "issuers" = 0) two
+    // run where the tiles are at most 64 columns wide and fit in one wave.
+    // Measured on GB300 (paired A/B, 10-launch blocks alternating over 12
+    // rounds): BF16 128 x 8192 x 8192 32.8 -> 30.5 us, FP16 the same shape 32.8
+    // -> 30.3, FP8 18.9 -> 17.4, BF16 128 x 8192 x 16384 59.5 -> 56.0, 64 x 14336
+    // x 4096 23.9 -> 23.0; with 128-column tiles (M = 192, 256) 1.2-1.4 %
+    // slower, so not there.
+    const int opt_iss = g_opt_issuers.load();
+    auto issuers_fit = [&](int ni) {
+        return (ni - 1) * p.tile_q + (p.tile_q > 64 ? p.tile_q : 64) <= 256;
+    };
+    if (!p.pair && !p.half && p.prod == Producer::Tma && !a.acc16 && p.splits == 1 &&
+        !p.tail_ksplit) {
+        if (opt_iss == 2) {
+            if (issuers_fit(2)) p.issuers = 2;
+        } else if (opt_iss == 0 && p.tile_q <= 64 && p.tiles <= p.slots) {
+            p.issuers = 2;
+        }
+    }
+    // ... and for pairs of 64-row halves (two accumulators of tile_q / 2
+    // columns per CTA): automatically whenever they run, since without two
+    // issuers they measured slower than one-CTA tiles on every skinny shape
+    // tried (BF16 128 x 8192 x 8192: 35.0 against 30.7 us)
+    if (opt_iss != 1 && p.pair && p.half && p.prod == Producer::Tma && !a.acc16) p.issuers = 2;
     return p;
 }
 
@@ -678,7 +686,7 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     TcLaunch L;
     std::memset(&L, 0, sizeof(L));
     L.half = pl.half;
-    L.dual = pl.dual;
+    L.issuers = pl.issuers;
     const CUtensorMapDataType in_dt = in == InKind::F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                       : in == InKind::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                            : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -770,11 +778,11 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
         std::fprintf(stderr,
                      "[gemm] tn in=%d M=%lld N=%lld K=%lld pair=%d producer=%d direct_store=%d "
                      "splits=%d tile_q=%d tail=%d ktail=%d stages=%d tiles=%lldx%lld grid=%d "
-                     "half=%d dual=%d\n",
+                     "half=%d issuers=%d\n",
                      int(in), (long long)M, (long long)N, (long long)K, int(pair), int(prod),
                      L.prm.direct_store, L.prm.splits, L.prm.tile_q, L.prm.tail_f,
                      L.prm.tail_ksplit, L.prm.stages,
-                     (long long)tiles_q, (long long)tiles_p, L.grid, int(L.half), int(L.dual));
+                     (long long)tiles_q, (long long)tiles_p, L.grid, int(L.half), L.issuers);
     e = tc_launch(in, pair, prod, out_f32, L);
     return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
 }
@@ -955,7 +963,7 @@ int gemm_tn_plan(int kind, int64_t M, int64_t N, int64_t K, int flags, int64_t w
                                          pl.kb_per_split,
                                          pl.tail_kb_per,
                                          pl.stage_bytes,
-                                         pl.dual};
+                                         pl.issuers};
     for (int i = 0; i < GEMM_PLAN_FIELDS; ++i) out[i] = v[i];
     return GEMM_OK;
 }
@@ -1046,9 +1054,9 @@ int gemm_set_option(const char* name, int64_t value) {
     } else if (!std::strcmp(name, "repack")) {
         if (value < 0 || value > 1) return GEMM_ERR_INVALID_OPTION;
         g_opt_repack.store(static_cast<int>(value));
-    } else if (!std::strcmp(name, "dual")) {
+    } else if (!std::strcmp(name, "issuers")) {
         if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
-        g_opt_dual.store(static_cast<int>(value));
+        g_opt_issuers.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "half")) {
         if (value < 0 || value > 3) return GEMM_ERR_INVALID_OPTION;
         g_opt_half.store(static_cast<int>(value));

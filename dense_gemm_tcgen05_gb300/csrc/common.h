@@ -91,7 +91,7 @@ struct TcLaunch {
     int grid;
     cudaStream_t stream;
     bool half;  // 64-row tiles (one CTA, MMA M = 64; or pair halves, MMA M = 128)
-    bool dual;  // two MMA-issuing warps (one CTA, TMA, unsplit, tile_q <= 128)
+    int issuers;  // MMA-issuing warps: 1, 2 or 4 (several: TMA, unsplit)
 };
 
 // Tile geometry of one persistent CTA (or CTA pair), for the host's grid sizing.

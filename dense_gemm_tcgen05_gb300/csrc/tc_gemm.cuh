@@ -58,20 +58,22 @@ namespace gb300 {
 //     N columns of the MMA, row r and column n in lane r + 64 (n / (N / 2)),
 //     column n % (N / 2) (measured on GB300 with an in-bounds probe), so each
 //     epilogue warp owns 32 rows of one half of the columns.
-// DUAL: a second MMA-issuing warp (warp 6).  The two issuers take alternate K
-// stages of each unit into accumulators of their own (the second tile_q columns
-// after the first), and the epilogue adds the two.  tcgen05.mma instructions
-// from one issuing thread that commits after every stage complete one at a
-// time, so small MMAs (narrow tiles) are limited by the issue rate; measured
-// on GB300 (one CTA, MMA N = 64, a commit every 4 MMAs) one issuer completes an
-// MMA every ~250 cycles, two issuers one every ~126.  Needs tile_q <= 128 (both
-// accumulators in one 256-column buffer); one CTA, TMA, unsplit.
-template <InKind IN, bool PAIR, bool LOADS, bool HALF = false, bool DUAL = false>
+// NI: MMA-issuing warps (1 or 2: warp 1, then warp 6).  Issuer j takes
+// the K stages s of each unit with s % NI == j into an accumulator of its own
+// (j * tile_q columns after the first, tile_q / 2 for a pair of halves), and
+// the epilogue adds them.  tcgen05.mma instructions from one issuing thread
+// that commits after every stage complete one at a time, so small MMAs (narrow
+// tiles) are limited by the issue rate; measured on GB300 (one CTA, MMA N = 64,
+// a commit every 4 MMAs) one issuer completes an MMA every ~250 cycles, two
+// issuers one every ~126.  Needs NI accumulators in one 256-column buffer;
+// one CTA, TMA, unsplit (or a pair of halves).
+template <InKind IN, bool PAIR, bool LOADS, bool HALF = false, int NI = 1>
 struct TcCfg {
     static_assert(!(PAIR && LOADS), "the load-based producer runs one CTA per tile");
     static_assert(!(HALF && LOADS), "64-row tiles: TMA producer");
-    static_assert(!(DUAL && (LOADS || (PAIR != HALF))),
-                  "two issuers: TMA; one CTA with 128-row tiles, or a pair of 64-row halves");
+    static_assert(NI == 1 || NI == 2, "one or two MMA issuers");
+    static_assert(NI == 1 || (!LOADS && PAIR == HALF),
+                  "several issuers: TMA; one CTA with 128-row tiles, or a pair of 64-row halves");
     static constexpr int kCG = PAIR ? 2 : 1;
     static constexpr int kElemBytes = IN == InKind::E4M3 ? 1 : 2;
     static constexpr int kBlockP = HALF ? 64 : 128;  // accumulator rows per CTA
@@ -99,8 +101,8 @@ struct TcCfg {
     static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
     static constexpr int kFirstLoadWarp = 6;
     static constexpr int kLoadWarps = 12;
-    static constexpr int kDualWarp = 6;  // the second MMA issuer (DUAL)
-    static constexpr int kThreads = LOADS ? (kFirstLoadWarp + kLoadWarps) * 32 : (DUAL ? 224 : 192);
+    static constexpr int kExtraIssuerWarp = 6;  // issuer 1: warp 6
+    static constexpr int kThreads = LOADS ? (kFirstLoadWarp + kLoadWarps) * 32 : 192 + (NI - 1) * 32;
     static constexpr int kFullArrivals = LOADS ? kLoadWarps : 1;
     static constexpr int kAccCols = kMmaN;
     static constexpr int kTmemCols = 512;
@@ -259,15 +261,15 @@ __device__ __forceinline__ uint4 mask_chunk(uint4 v, int32_t lim) {
 // SPLIT: the launch cuts tiles into K pieces (split-K or a K-split tail) and
 // combines them through the workspace.  Launches without K pieces run the
 // instantiation without that code.
-template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT, bool HALF, bool DUAL = false>
-__global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, DUAL>::kThreads, 1)
+template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT, bool HALF, int NI = 1>
+__global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
                    const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_out,
                    const __grid_constant__ CUtensorMap map_q_tail, const TcParams prm) {
-    using Cfg = TcCfg<IN, PAIR, LOADS, HALF, DUAL>;
+    using Cfg = TcCfg<IN, PAIR, LOADS, HALF, NI>;
     static_assert(!(SPLIT && HALF), "64-row tiles never split K");
-    static_assert(!(SPLIT && DUAL), "two issuers: unsplit launches only");
+    static_assert(!(SPLIT && NI > 1), "several issuers: unsplit launches only");
     constexpr int SM = Cfg::kMaxStages;                 // barrier slots
     const uint32_t S = static_cast<uint32_t>(prm.stages);  // ring depth for this call
     const uint32_t stage_bytes = prm.stage_bytes;
@@ -290,8 +292,8 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, DUAL>::kThreads, 
 
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
-    // TMEM column of the second issuer's accumulator (DUAL): after the first
-    // one, whose width is tile_q columns (tile_q / 2 for a pair of halves).
+    // TMEM columns between the accumulators of consecutive issuers (NI > 1):
+    // tile_q (tile_q / 2 for a pair of halves).
     const uint32_t kAcc2Off = static_cast<uint32_t>(PAIR ? prm.tile_q / 2 : prm.tile_q);
 
     if (threadIdx.x == 0) {
@@ -300,10 +302,10 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, DUAL>::kThreads, 
             mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(accf_bar(b), DUAL ? 2 : 1);   // one commit per issuer
+            mbar_init(accf_bar(b), NI);   // one commit per issuer
             mbar_init(acce_bar(b), (PAIR ? 2 : 1) * Cfg::kEpiWarps);
         }
-        mbar_init(done_bar, DUAL ? 2 : 1);
+        mbar_init(done_bar, NI);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -552,11 +554,12 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, DUAL>::kThreads, 
                 if (lane == 0) mbar_arrive(full_bar(s));
             }
         }
-    } else if (warp == 1 || (DUAL && warp == Cfg::kDualWarp)) {
+    } else if (warp == 1 || (NI > 1 && warp >= Cfg::kExtraIssuerWarp &&
+                             warp < Cfg::kExtraIssuerWarp + NI - 1)) {
         // ------------------------------------------------ MMA issuer
-        // issuer 1 (DUAL only) takes the odd K stages of each unit into the
-        // accumulator tile_q columns after issuer 0's
-        const uint32_t issuer = (DUAL && warp == Cfg::kDualWarp) ? 1u : 0u;
+        // issuer j (NI > 1) takes the K stages s of each unit with s % NI == j
+        // into the accumulator j * kAcc2Off columns after issuer 0's
+        const uint32_t issuer = warp == 1 ? 0u : warp - (Cfg::kExtraIssuerWarp - 1);
         if (!PAIR || leader) {
             uint32_t lt = 0, rs = 0, rph = 0;   // tiles; ring slot and phase
             const uint64_t adesc0 = sdesc_kmajor_sw128(base);
@@ -580,8 +583,8 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, DUAL>::kThreads, 
                         rs = 0;
                         rph ^= 1u;
                     }
-                    if constexpr (DUAL) {
-                        if (static_cast<uint32_t>((kb - kb_lo) & 1) != issuer) continue;
+                    if constexpr (NI > 1) {
+                        if (static_cast<uint32_t>((kb - kb_lo) % NI) != issuer) continue;
                     }
                     if (!warp_wait(full_bar(s), ph, wd)) {
                         ok = false;
@@ -599,7 +602,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, DUAL>::kThreads, 
                             // advance the start address by 32 bytes of K per MMA
                             const uint64_t off = static_cast<uint64_t>(kk * (Cfg::kMmaKBytes >> 4));
                             uint32_t acc;
-                            if constexpr (DUAL)
+                            if constexpr (NI > 1)
                                 acc = (kb - kb_lo > static_cast<int32_t>(issuer) || kk != 0) ? 1u : 0u;
                             else
                                 acc = (kb != kb_lo || kk != 0) ? 1u : 0u;
@@ -795,11 +798,14 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, DUAL>::kThreads, 
                     tmem_ld_32x32b_x32(t_row + c * kCols, v0);
                     if constexpr (kCols == 64) tmem_ld_32x32b_x32(t_row + c * kCols + 32, v1);
                     tmem_wait_ld();
-                    if constexpr (DUAL) {
-                        // the second issuer's sums (odd K stages), when it had any
-                        if (w.kb_hi - w.kb_lo >= 2) {
+                    if constexpr (NI > 1) {
+                        // the other issuers' sums, in issuer order, for those that
+                        // had any of the unit's K stages
+#pragma unroll 1
+                        for (int ij = 1; ij < NI; ++ij) {
+                            if (w.kb_hi - w.kb_lo <= ij) break;
                             uint32_t u0[32], u1[32];
-                            const uint32_t t2 = t_row + kAcc2Off + c * kCols;
+                            const uint32_t t2 = t_row + ij * kAcc2Off + c * kCols;
                             tmem_ld_32x32b_x32(t2, u0);
                             if constexpr (kCols == 64) tmem_ld_32x32b_x32(t2 + 32, u1);
                             tmem_wait_ld();
@@ -912,10 +918,10 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, DUAL>::kThreads, 
 }
 
 template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT, bool HALF = false,
-          bool DUAL = false>
+          int NI = 1>
 cudaError_t tc_launch_one(const TcLaunch& L) {
-    using Cfg = TcCfg<IN, PAIR, LOADS, HALF, DUAL>;
-    auto kernel = tc_gemm_kernel<IN, OutT, PAIR, LOADS, SPLIT, HALF, DUAL>;
+    using Cfg = TcCfg<IN, PAIR, LOADS, HALF, NI>;
+    auto kernel = tc_gemm_kernel<IN, OutT, PAIR, LOADS, SPLIT, HALF, NI>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -954,13 +960,13 @@ cudaError_t tc_launch_split(bool pair, Producer prod, const TcLaunch& L) {
         if (pair || L.half) return cudaErrorInvalidConfiguration;
         return tc_launch_one<IN, OutT, false, true, SPLIT>(L);
     }
-    if (L.dual) {
+    if (L.issuers > 1) {
         if constexpr (SPLIT) {
             return cudaErrorInvalidConfiguration;
         } else {
-            if (pair != L.half) return cudaErrorInvalidConfiguration;
-            return pair ? tc_launch_one<IN, OutT, true, false, false, true, true>(L)
-                        : tc_launch_one<IN, OutT, false, false, false, false, true>(L);
+            if (pair != L.half || L.issuers != 2) return cudaErrorInvalidConfiguration;
+            return pair ? tc_launch_one<IN, OutT, true, false, false, true, 2>(L)
+                        : tc_launch_one<IN, OutT, false, false, false, false, 2>(L);
         }
     }
     if (L.half) {

@@ -208,8 +208,8 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
  *                    last-wave units per tile (1: untouched), last wave cut along K
  *                    (0/1; else along M), ring stages, grid (CTAs), A repacked,
  *                    B repacked, tiles along N, tiles along M, K stages per
- *                    piece, K stages per last-wave piece, ring stage bytes, two
- *                    MMA-issuing warps (0/1).
+ *                    piece, K stages per last-wave piece, ring stage bytes,
+ *                    MMA-issuing warps (1 or 2).
  *
  * Returns GEMM_OK, GEMM_ERR_INVALID_DIM or GEMM_ERR_INVALID_OPTION (kind, out
  * or nout).  A call that would be refused reports its status in out[0]
@@ -276,11 +276,11 @@ int gemm_read_watchdog(int reset);
  *                 run; 3 CTA pairs of 64-row halves (128 rows of N per pair, MMA
  *                 M = 128 over the pair, tile width 128 or 256 along M) wherever
  *                 TMA tiles with FP32 accumulation run.  They never split K
- *   "dual"        two MMA-issuing warps per CTA, taking alternate K stages into
- *                 accumulators of their own that the epilogue adds: 0 auto (default:
- *                 one-CTA TMA tiles of at most 64 columns that run unsplit in one
- *                 wave), 1 never, 2 wherever one-CTA TMA tiles of at most 128
- *                 columns run unsplit
+ *   "issuers"     MMA-issuing warps per CTA, taking alternate K stages into
+ *                 accumulators of their own that the epilogue adds: 0 auto (default: two
+ *                 for one-CTA TMA tiles of at most 64 columns that run unsplit in one
+ *                 wave, and for pairs of 64-row halves), 1 always one, 2 two wherever
+ *                 one-CTA TMA tiles of at most 128 columns run unsplit
  *   "tail"        the last, partial wave of tiles: 0 auto (default) cuts its tiles
  *                 into 2 or 4 narrower ones when that ends it sooner, 1 never, 2 or
  *                 4 always

@@ -1,12 +1,12 @@
-"""GPU parity of two MMA-issuing warps (option "dual" = 2) against the CPU
+"""GPU parity of two MMA-issuing warps (option "issuers" = 2) against the CPU
 oracle, through the C ABI.
 
-The issuers take alternate K stages of each tile into accumulators of their
-own, and the epilogue adds the two.  These cases cover every input kind and
-output type, the tile widths 16 to 128, units of one K stage (the second issuer
-adds nothing), two and three stages, ragged edges, row-wise stores, few CTAs
-walking many tiles, a narrowed last wave, and +-1 inputs (exact: every partial
-sum is an integer)."""
+Issuer j takes the K stages s of each tile with s % 2 == j into an accumulator
+of its own, and the epilogue adds the two.  These
+cases cover every input kind and output type, the tile widths 16 to 128, units
+with fewer K stages than issuers (the idle issuers add nothing), ragged edges,
+row-wise stores, few CTAs walking many tiles, a narrowed last wave, and +-1
+inputs (exact: every partial sum is an integer)."""
 import numpy as np
 import pytest
 import torch
@@ -20,15 +20,16 @@ pytestmark = pytest.mark.gpu
 KINDS = ["f16", "bf16", "e4m3"]
 
 
-@pytest.fixture
-def dual():
+@pytest.fixture(params=[2], ids=["two"])
+def many(request):
     touched = []
 
     def set_(name, value):
         assert capi.gemm_set_option(name, value) == 0
         touched.append(name)
-    set_("dual", 2)
+    set_("issuers", request.param)
     set_("pair", 0)
+    set_.issuers = request.param
     yield set_
     for name in touched:
         capi.gemm_set_option(name, -1 if name == "pair" else 0)
@@ -38,7 +39,7 @@ def dual():
 @pytest.mark.parametrize("shape", [(128, 8192, 512), (100, 1000, 257), (16, 700, 300),
                                    (30, 130, 1000), (1, 64, 64), (129, 333, 128), (64, 500, 65),
                                    (77, 260, 200)])
-def test_forced_random(kind, shape, dual):
+def test_forced_random(kind, shape, many):
     M, N, K = shape
     ops = si.tn_operands(kind, M, N, K, dist="normal", seed=M + N + K, sigma=0.5)
     C = run_tn(kind, ops, M, N, K)
@@ -47,7 +48,7 @@ def test_forced_random(kind, shape, dual):
 
 @pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("M", [16, 32, 64, 128, 200])
-def test_forced_pm1_bitexact(kind, M, dual):
+def test_forced_pm1_bitexact(kind, M, many):
     N, K = 1000, 2048
     ops = si.tn_operands(kind, M, N, K, dist="pm1", seed=M)
     C = run_tn(kind, ops, M, N, K)
@@ -56,12 +57,12 @@ def test_forced_pm1_bitexact(kind, M, dual):
 
 
 @pytest.mark.parametrize("ctas,tail", [(1, 0), (3, 0), (5, 2)])
-def test_few_ctas_many_tiles(ctas, tail, dual):
+def test_few_ctas_many_tiles(ctas, tail, many):
     """One to five CTAs each run many tiles (both issuers cycle every ring slot
     and both accumulator buffers); with tail = 2 the last wave's tiles are cut
     into narrower units."""
-    dual("max_ctas", ctas)
-    dual("tail", tail)
+    many("max_ctas", ctas)
+    many("tail", tail)
     M, N, K = 256, 1100, 700
     ops = si.tn_operands("bf16", M, N, K, dist="pm1", seed=ctas)
     C = run_tn("bf16", ops, M, N, K)
@@ -70,7 +71,7 @@ def test_few_ctas_many_tiles(ctas, tail, dual):
 
 
 @pytest.mark.parametrize("ldc_pad", [0, 3])
-def test_forced_row_wise_stores(ldc_pad, dual):
+def test_forced_row_wise_stores(ldc_pad, many):
     M, N, K = 37, 333, 200
     ldc = M + ldc_pad
     ops = si.tn_operands("bf16", M, N, K, dist="normal", seed=11)
@@ -81,7 +82,7 @@ def test_forced_row_wise_stores(ldc_pad, dual):
 
 
 @pytest.mark.parametrize("M", [16, 64, 128])
-def test_fp8_f32_output(M, dual):
+def test_fp8_f32_output(M, many):
     from test_fp8_f32out_gpu import run, tols
 
     N, K = 520, 384
@@ -96,12 +97,19 @@ def test_fp8_f32_output(M, dual):
     assert err.max() <= contract and np.all(err <= tight)
 
 
-def test_plan_takes_dual_only_where_allowed(dual):
-    """Forced, the second issuer runs on one-CTA TMA tiles of at most 128
-    columns without K pieces, and nowhere else."""
-    st, p = capi.gemm_tn_plan("bf16", 128, 8192, 8192, workspace_bytes=0)
-    assert st == 0 and p["dual"] == 1 and p["pair"] == 0
+def test_plan_takes_issuers_only_where_allowed(many):
+    """Forced, the extra issuers run on one-CTA TMA tiles without K pieces
+    whose accumulators fit in 256 TMEM columns, and nowhere else."""
+    ni = many.issuers
+    many("tile_q", 64)
+    st, p = capi.gemm_tn_plan("bf16", 128, 8192, 8192, workspace_bytes=0)     # 64 columns
+    assert st == 0 and p["issuers"] == ni and p["pair"] == 0
+    many("tile_q", 128)
+    st, p = capi.gemm_tn_plan("bf16", 256, 8192, 8192, workspace_bytes=0)     # 128 columns
+    assert p["issuers"] == 2
+    many("tile_q", 256)
+    st, p = capi.gemm_tn_plan("bf16", 256, 8192, 8192, workspace_bytes=0)     # 256: no room
+    assert p["issuers"] == 1
     capi.gemm_set_option("pair", -1)
-    assert capi.gemm_tn_plan("bf16", 8192, 8192, 8192)[1]["dual"] == 0      # CTA pairs
-    assert capi.gemm_tn_plan("f16_acc16", 128, 8192, 8192)[1]["dual"] == 0  # FP16 accumulation
-    assert capi.gemm_tn_plan("bf16", 128, 8192, 8192, workspace_bytes=1 << 30)[1]["dual"] in (0, 1)
+    assert capi.gemm_tn_plan("bf16", 8192, 8192, 8192)[1]["issuers"] == 1      # CTA pairs
+    assert capi.gemm_tn_plan("f16_acc16", 128, 8192, 8192)[1]["issuers"] == 1  # FP16 accumulation

@@ -115,9 +115,9 @@ def test_forced_skinny_sampled(kind, shape, pair_halves):
 @pytest.mark.parametrize("shape", [(128, 4100, 700), (256, 900, 2048), (1, 64, 64), (200, 333, 129)])
 def test_two_issuers_random(kind, shape, pair_halves):
     """Pairs of halves with two MMA-issuing warps in the leader CTA (option
-    "dual" = 2): alternate K stages into accumulators of tile_q / 2 columns
+    "issuers" = 2): alternate K stages into accumulators of tile_q / 2 columns
     each, added by the epilogue; units of one K stage add nothing."""
-    pair_halves("dual", 2)
+    pair_halves("issuers", 2)
     M, N, K = shape
     ops = si.tn_operands(kind, M, N, K, dist="normal", seed=M + N + K + 1, sigma=0.5)
     C = run_tn(kind, ops, M, N, K)
@@ -126,7 +126,7 @@ def test_two_issuers_random(kind, shape, pair_halves):
 
 @pytest.mark.parametrize("ctas", [2, 6, 0])
 def test_two_issuers_pm1_bitexact(ctas, pair_halves):
-    pair_halves("dual", 2)
+    pair_halves("issuers", 2)
     pair_halves("max_ctas", ctas)
     M, N, K = 250, 1200, 2048
     ops = si.tn_operands("bf16", M, N, K, dist="pm1", seed=ctas + 3)

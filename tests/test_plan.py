@@ -183,40 +183,41 @@ def test_noalloc_split_rules(options):
     assert plan("bf16", 4096, 4096, 4096, **na)["splits"] == 1  # a full wave: no split
 
 
-def test_two_issuers_and_pair_halves_rules(options):
+def test_issuers_and_pair_halves_rules(options):
     """Skinny shapes: 16-bit inputs with 64 < M <= 256 run pairs of 64-row
     halves (128 rows of N per pair) with two MMA issuers when they fit in one
     wave; FP8 and other one-wave skinny shapes run one-CTA tiles, with two
     issuers when the tiles are at most 64 columns wide and unsplit.  Option
-    "dual" = 1 turns both off; "dual" = 2 forces two issuers on one-CTA tiles of
-    up to 128 columns; "half" = 2 keeps one-CTA tiles."""
+    "issuers" = 1 turns both off; 2 forces two on one-CTA tiles of at most 128
+    columns; "half" = 2 keeps one-CTA tiles."""
     for M, tq in ((128, 128), (200, 256), (256, 256)):
         p = plan("bf16", M, 8192, 8192, workspace_bytes=WS)
-        assert (p["pair"], p["half"], p["dual"], p["tile_q"], p["grid"]) == (1, 1, 1, tq, 128), M
+        assert (p["pair"], p["half"], p["issuers"], p["tile_q"], p["grid"]) == (1, 1, 2, tq, 128), M
     p = plan("e4m3", 128, 8192, 8192, workspace_bytes=WS)   # FP8: 128 tiles of 128 x 64
-    assert (p["pair"], p["half"], p["dual"], p["tile_q"], p["splits"]) == (0, 0, 1, 64, 1)
+    assert (p["pair"], p["half"], p["issuers"], p["tile_q"], p["splits"]) == (0, 0, 2, 64, 1)
     assert plan("bf16", 64, 8192, 8192, workspace_bytes=WS)["half"] == 0     # M <= 64
-    assert plan("bf16", 16, 8192, 8192, workspace_bytes=WS)["dual"] == 0     # split K
-    assert plan("bf16", 8192, 8192, 8192)["dual"] == 0                       # CTA pairs
+    assert plan("bf16", 16, 8192, 8192, workspace_bytes=WS)["issuers"] == 1  # split K
+    assert plan("bf16", 8192, 8192, 8192)["issuers"] == 1                    # CTA pairs
     p = plan("f16_acc16", 128, 8192, 8192)                                   # FP16 accumulation
-    assert (p["dual"], p["half"]) == (0, 0)
+    assert (p["issuers"], p["half"]) == (1, 0)
     assert plan("bf16", 128, 16384, 8192)["half"] == 0                       # two waves
     assert plan("bf16", 256, 512, 4096, workspace_bytes=WS)["half"] == 0     # 4 pairs: split-K
     assert plan("bf16", 128, 6144, 8192)["half"] == 0                        # 48 of 76 pairs
-    assert plan("bf16", 64, 131072, 8192)["dual"] == 0                       # several waves
+    assert plan("bf16", 64, 131072, 8192)["issuers"] == 1                    # several waves
     options("half", 2)
     p = plan("bf16", 128, 8192, 8192, workspace_bytes=WS)                    # one-CTA tiles
-    assert (p["pair"], p["half"], p["dual"], p["tile_q"]) == (0, 0, 1, 64)
-    assert plan("bf16", 256, 8192, 8192, workspace_bytes=WS)["dual"] == 0    # 128 columns
-    options("dual", 1)
+    assert (p["pair"], p["half"], p["issuers"], p["tile_q"]) == (0, 0, 2, 64)
+    assert plan("bf16", 256, 8192, 8192, workspace_bytes=WS)["issuers"] == 1  # 128 columns
+    options("issuers", 1)
     p = plan("bf16", 128, 8192, 8192, workspace_bytes=WS)
-    assert (p["dual"], p["half"]) == (0, 0)
+    assert (p["issuers"], p["half"]) == (1, 0)
     options("half", 0)
-    assert plan("bf16", 128, 8192, 8192, workspace_bytes=WS)["half"] == 0    # dual 1: no halves
-    options("dual", 2)
+    assert plan("bf16", 128, 8192, 8192, workspace_bytes=WS)["half"] == 0    # issuers 1: no halves
     options("half", 2)
-    assert plan("bf16", 256, 8192, 8192, workspace_bytes=WS)["dual"] == 1
-    assert plan("bf16", 16, 8192, 8192)["dual"] == 1                         # unsplit here
+    options("issuers", 2)
+    assert plan("bf16", 256, 8192, 8192, workspace_bytes=WS)["issuers"] == 2
+    assert plan("bf16", 16, 8192, 8192)["issuers"] == 2                      # unsplit here
+    assert capi.gemm_set_option("issuers", 4) == capi.GEMM_ERR_INVALID_OPTION
 
 
 def test_persistent_grid_follows_sms_and_cap(options):
