@@ -1046,10 +1046,10 @@ int gemm_set_option(const char* name, int64_t value) {
         if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
         g_opt_l2hints.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "f32_ktail")) {
-        if (value < 0 || value > 7) return GEMM_ERR_INVALID_OPTION;
+        if (value < 0 || value > 15) return GEMM_ERR_INVALID_OPTION;
         g_opt_f32_ktail.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "f32_tail")) {
-        if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
+        if (value < 0 || value > 3) return GEMM_ERR_INVALID_OPTION;
         g_opt_f32_tail.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "repack")) {
         if (value < 0 || value > 1) return GEMM_ERR_INVALID_OPTION;

@@ -59,9 +59,10 @@ cudaError_t f32_split_cols_launch(const float* X, int64_t ldx, int64_t K, int64_
 
 // tail_mode 0: a last wave of whole tiles that is at most half full runs as
 // half-width tiles in a second grid launched with programmatic dependent launch;
-// 1: whole tiles only; 2: as 0 but two plain launches.
+// 1: whole tiles only; 2: as 0 but two plain launches; 3: halves for any last
+// partial wave.
 // ktail > 0: the last ktail terms of K (when K > ktail) run in the chain-
-// continuing kernel that takes the terms past 2^31 - 8 (tests of that path).
+// continuing kernel that takes the terms past 2^31 - 16 (tests of that path).
 cudaError_t f32_launch(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                        const float* B, int64_t ldb, float* C, int64_t ldc, cudaStream_t stream,
                        int tail_mode, int ktail = 0);

@@ -6,28 +6,35 @@
 // Design, following "Optimizing GEMM in HIP" Steps 2-6 (shared-memory tiling,
 // register tiling, double buffering, vectorised loads, register budget), made
 // for a Blackwell SM:
-//   - a 128 x 128 block tile, K slices of 8, 256 threads, 8 x 8 outputs per
-//     thread held in registers (outer products, 64 FMAs per k per thread);
+//   - a 128 x 128 block tile, K slices of 16, 128 threads, 16 x 8 outputs per
+//     thread held in registers (outer products, 128 FMAs per k per thread),
+//     two blocks per SM;
 //   - the FMAs are issued as Blackwell's packed FP32 FMA (__ffma2_rn, two
 //     fused multiply-adds per instruction on adjacent columns, each rounded
-//     once like fmaf): the same results with half the FMA instructions, which
-//     leaves issue slots for the shared-memory loads (measured on GB300 at
-//     8192 x 8192 x 2048: 53 -> 60 TFLOP/s);
-//   - each thread's 8 x 8 outputs are two 4-row by two 4-column groups 64 apart,
-//     so its shared-memory operand reads are float4 and conflict-free;
-//   - A is stored k-major in shared memory (transposed on the way in, rows
-//     padded by 4 floats so the transposing stores do not collide on banks),
-//     B row-major; both are fetched with float4 global loads when the pointers
-//     and leading dimensions allow, with predicated scalar loads otherwise and
-//     on ragged edges (zero-filled);
-//   - two shared-memory buffers: the next slice is fetched into registers while
-//     the current one is multiplied, then stored to the other buffer, so there
-//     is one barrier per slice ("Step 4: Double buffering");
+//     once like fmaf), the A value of a row broadcast to both lanes: half the
+//     FMA instructions, which leaves issue slots for the shared-memory loads;
+//   - slices move from global to shared memory with cp.async (no registers
+//     staged) into a ring of three buffers, one barrier per slice; A is
+//     written k-major (transposed on the way in by 4-byte copies, rows padded
+//     by 4 floats), B row-major by 16-byte copies when its rows allow, 4-byte
+//     copies otherwise; ragged edges are zero-filled by the copies;
+//   - a thread's 8 columns are two groups of 4, 64 apart, and its 16 rows four
+//     groups of 4, 32 apart; a warp's threads are 16 along n by 2 along m, so
+//     every fragment load is one conflict-free float4 per thread, and a B load
+//     of a warp reads 256 distinct bytes (shared-memory wavefronts per k: 15.5
+//     per warp against 19 with 8 x 16 outputs per thread, whose B loads read
+//     128 distinct bytes four times over);
+//   - inside a slice the A fragments of the next k are loaded while the
+//     current ones are multiplied;
 //   - tiles are visited in grouped order (raster.h) for L2 reuse;
 //   - when it shortens the last partial wave (rule at full_tiles), that wave's
-//     tiles are cut into two 128 x 64 halves (8 x 4 outputs per thread), run by
+//     tiles are cut into two 128 x 64 halves (8 x 8 outputs per thread), run by
 //     a second grid that programmatic dependent launch lets start while the
 //     whole-tile grid's last blocks still run.
+// Measured on GB300: 65.2 TFLOP/s at 4096^3 and 68.0 at 8192 x 8192 x 2048
+// (0.81 and 0.84 of 152 SMs x 128 lanes x 2 x 2.07 GHz), against 56 and 59 for
+// the previous design (128 x 128 x 8 tiles, 256 threads of 8 x 8 outputs,
+// register-staged double buffering).
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -38,137 +45,212 @@
 namespace gb300 {
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kBK = 8, kThreads = 256, kPadA = 4;
-constexpr int kLoadsA = kBM * kBK / 4 / kThreads;  // float4 loads of A per thread per slice
-static_assert(kLoadsA == 1, "one float4 of A per thread per slice");
+constexpr int kBM = 128, kBN = 128, kBK = 16, kStages = 3, kThreads = 128, kPadA = 4;
+constexpr int kAS = kBM + kPadA;             // k-major A row stride in shared memory (floats)
+constexpr int kAStage = kBK * kAS;           // floats of A per ring slot
+
+constexpr int kTM = 16;                      // rows per thread: four groups of 4, 32 apart
+constexpr int kRowGroups = kTM / 4, kRowStride = kBM / kRowGroups;
+constexpr int kThreadsN = 16;                 // threads along n
+static_assert(kThreads / kThreadsN * 4 == kRowStride, "row groups tile the block rows");
+
+template <int BN>
+struct SimtShape {
+    static constexpr int kTN = BN / kThreadsN;  // columns per thread
+    static constexpr int kGroups = kTN / 4;     // 4-column groups per thread
+    static constexpr int kGroupStride = BN / kGroups;
+    static constexpr int kStage = kAStage + kBK * BN;           // floats per ring slot
+    static constexpr int kSmemBytes = kStages * kStage * 4;
+    static constexpr int kBChunksPerRow = BN / 4;               // 16-byte chunks of a B row
+    static constexpr int kBRowsPerPass = kThreads / kBChunksPerRow;
+    static constexpr int kBPerThread = kBK / kBRowsPerPass;     // chunks per thread per slice
+    static_assert(kBK % kBRowsPerPass == 0, "B slice rows divide among the threads");
+};
+
+constexpr int kAPerThread = kBM * kBK / kThreads;  // 4-byte A copies per thread per slice
+static_assert(kAPerThread == 16, "a thread's A copies cover 16 rows 4 apart");
+
+// FILL: the form with a source size, whose missing bytes are zero-filled (ragged
+// edges); without it every copy moves all of its bytes.
+template <bool FILL>
+__device__ __forceinline__ void cp_async4(uint32_t dst, const float* src, uint32_t bytes) {
+    if (FILL)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+                     "r"(bytes)
+                     : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+template <bool FILL>
+__device__ __forceinline__ void cp_async16(uint32_t dst, const float* src, uint32_t bytes) {
+    if (FILL)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                     "r"(bytes)
+                     : "memory");
+    else
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// p += step in an opaque add: keeps one running pointer live instead of one
+// precomputed address per copy.
+__device__ __forceinline__ const float* step_ptr(const float* p, int64_t step_bytes) {
+    asm volatile("add.s64 %0, %0, %1;" : "+l"(p) : "l"(step_bytes));
+    return p;
+}
 
 // One output tile of kBM x BN at (m0, n0); BN = 128 (full tile) or 64 (half).
-// EXACT: M and N are multiples of the tile and K of the slice, and the float4
-// path applies (VEC), so no load or store needs a bounds check.
-// The FMAs are issued as packed pairs (__ffma2_rn: two FP32 FMAs per
-// instruction, each rounded once exactly as fmaf), on pairs of adjacent
-// columns: acc[i][p] holds columns 2p and 2p + 1 of row i.
+// VEC: B's rows and C's rows are 16-byte aligned (16-byte B copies, float4
+// stores).  EXACT: M and N are multiples of the tile, K of the slice, and VEC
+// holds, so no copy or store needs a bounds check.
 template <bool VEC, int BN, bool EXACT>
 __device__ __forceinline__ void sgemm_tile(int M, int N, int K, const float* __restrict__ A,
                                            int64_t lda, const float* __restrict__ B, int64_t ldb,
                                            float* __restrict__ C, int64_t ldc, int64_t m0,
-                                           int64_t n0, float (*As)[kBK][kBM + kPadA],
-                                           float (*Bs)[kBK][kBN]) {
-    constexpr int kGroups = BN / 64;                // 4-column groups per thread
-    constexpr int kBVec = kBK * BN / 4;             // float4s of B per slice
-    static_assert(kBVec <= kThreads, "at most one float4 of B per thread per slice");
-    const int tid = threadIdx.x;
-    const int tx = tid & 15, ty = tid >> 4;
+                                           int64_t n0, float* smem) {
+    using S = SimtShape<BN>;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tx = tid % kThreadsN;           // columns g*kGroupStride + tx*4 + 0..3
+    const int ty = tid / kThreadsN;           // rows q*kRowStride + ty*4 + 0..3
 
-    // Global -> register mapping: A tile 128 x kBK (two threads per row, a
-    // float4 each along k), B tile kBK x BN (one float4 along n for each of the
-    // first kBVec threads).
-    const int a_row = tid >> 1, a_k = (tid & 1) * 4;
-    const int b_k = tid / (BN / 4), b_col = (tid % (BN / 4)) * 4;
-    const bool b_loader = tid < kBVec;
-    const int64_t gm = m0 + a_row;
-    const int64_t gn = n0 + b_col;
-
-    auto load_a = [&](int k0) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        const int k = k0 + a_k;
-        if (EXACT) return *reinterpret_cast<const float4*>(A + gm * lda + k);
-        if (gm < M) {
-            const float* p = A + gm * lda + k;
-            if (VEC && k + 3 < K) {
-                v = *reinterpret_cast<const float4*>(p);
-            } else {
-                if (k + 0 < K) v.x = p[0];
-                if (k + 1 < K) v.y = p[1];
-                if (k + 2 < K) v.z = p[2];
-                if (k + 3 < K) v.w = p[3];
-            }
-        }
-        return v;
-    };
-    auto load_b = [&](int k0) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        const int k = k0 + b_k;
-        if (EXACT && kBVec == kThreads)
-            return *reinterpret_cast<const float4*>(B + static_cast<int64_t>(k) * ldb + gn);
-        if (b_loader && (EXACT || k < K)) {
-            const float* p = B + static_cast<int64_t>(k) * ldb + gn;
-            if (EXACT || (VEC && gn + 3 < N)) {
-                v = *reinterpret_cast<const float4*>(p);
-            } else {
-                if (gn + 0 < N) v.x = p[0];
-                if (gn + 1 < N) v.y = p[1];
-                if (gn + 2 < N) v.z = p[2];
-                if (gn + 3 < N) v.w = p[3];
-            }
-        }
-        return v;
-    };
-    auto store_a = [&](int buf, float4 v) {
-        As[buf][a_k + 0][a_row] = v.x;
-        As[buf][a_k + 1][a_row] = v.y;
-        As[buf][a_k + 2][a_row] = v.z;
-        As[buf][a_k + 3][a_row] = v.w;
-    };
-    auto store_b = [&](int buf, float4 v) {
-        if (b_loader) *reinterpret_cast<float4*>(&Bs[buf][b_k][b_col]) = v;
-    };
-
-    float2 acc[8][2 * kGroups];
+    // A copies: instruction j of warp w covers rows r0 + 4 j (r0 = 64 (w & 1)
+    // + lane & 3), k = 8 (w >> 1) + lane >> 2 of the slice: a warp reads 4 rows
+    // x 8 consecutive k (32 bytes each) and writes 32 distinct banks.
+    const int a_row = 64 * (warp & 1) + (lane & 3);
+    const int a_k = 8 * (warp >> 1) + (lane >> 2);
+    const int64_t a_step = 4 * lda * static_cast<int64_t>(sizeof(float));
+    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    const uint32_t a_dst = sbase + 4u * (a_k * kAS + a_row);
+    uint32_t a_rows_ok = 0xffffu;             // bit j: row a_row + 4 j exists
+    if (!EXACT) {
+        a_rows_ok = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+        for (int j = 0; j < kAPerThread; ++j)
+            if (m0 + a_row + 4 * j < M) a_rows_ok |= 1u << j;
+    }
+    const float* a_src = A + (m0 + a_row) * lda + a_k;
+    // B copies: chunk j = row tid / kBChunksPerRow + kBRowsPerPass j, columns
+    // (tid % kBChunksPerRow) * 4 .. + 3.
+    const int b_k = tid / S::kBChunksPerRow;
+    const int b_n = (tid % S::kBChunksPerRow) * 4;
+    const int64_t b_step = S::kBRowsPerPass * ldb * static_cast<int64_t>(sizeof(float));
+    const uint32_t b_dst = sbase + 4u * (kAStage + b_k * BN + b_n);
+    const int64_t gn = n0 + b_n;
+    uint32_t b_bytes = 16;                    // valid bytes of the chunk (VEC)
+    if (!EXACT) {
+        const int64_t left = gn < N ? N - gn : 0;
+        b_bytes = left >= 4 ? 16u : static_cast<uint32_t>(left * 4);
+    }
+    const float* b_src = B + static_cast<int64_t>(b_k) * ldb + gn;
+
+    int k0 = 0;
+    auto issue = [&](int slot) {
+        const uint32_t off = 4u * slot * S::kStage;
+        const bool k_ok = EXACT || k0 + a_k < K;
+        const float* p = a_src;
 #pragma unroll
-        for (int j = 0; j < 2 * kGroups; ++j) acc[i][j] = make_float2(0.f, 0.f);
+        for (int j = 0; j < kAPerThread; ++j) {
+            const bool ok = EXACT || (k_ok && ((a_rows_ok >> j) & 1u));
+            cp_async4<!EXACT>(a_dst + off + 16u * j, ok ? p : A, ok ? 4u : 0u);
+            if (j + 1 < kAPerThread) p = step_ptr(p, a_step);
+        }
+        const float* q = b_src;
+#pragma unroll
+        for (int j = 0; j < S::kBPerThread; ++j) {
+            const uint32_t d = b_dst + off + 4u * S::kBRowsPerPass * BN * j;
+            const bool row_ok = EXACT || k0 + b_k + S::kBRowsPerPass * j < K;
+            if (VEC) {
+                const uint32_t bytes = row_ok ? b_bytes : 0u;
+                cp_async16<!EXACT>(d, bytes ? q : B, bytes);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const bool ok = row_ok && gn + e < N;
+                    cp_async4<true>(d + 4u * e, ok ? q + e : B, ok ? 4u : 0u);
+                }
+            }
+            if (j + 1 < S::kBPerThread) q = step_ptr(q, b_step);
+        }
+        a_src += kBK;
+        b_src += static_cast<int64_t>(kBK) * ldb;
+        k0 += kBK;
+    };
+
+    float2 acc[kTM][S::kTN / 2];
+#pragma unroll
+    for (int i = 0; i < kTM; ++i)
+#pragma unroll
+        for (int j = 0; j < S::kTN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
     const int ktiles = (K + kBK - 1) / kBK;
-    store_a(0, load_a(0));
-    store_b(0, load_b(0));
-    __syncthreads();
-
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) {
+        if (s < ktiles) issue(s);
+        cp_async_commit();
+    }
+    int rd = 0, wr = kStages - 1;
     for (int kt = 0; kt < ktiles; ++kt) {
-        const int cur = kt & 1;
-        const bool more = kt + 1 < ktiles;
-        float4 ra, rb;
-        if (more) {
-            ra = load_a((kt + 1) * kBK);
-            rb = load_b((kt + 1) * kBK);
-        }
+        cp_async_wait<kStages - 2>();         // this thread's copies of slice kt landed
+        __syncthreads();                      // everyone's; and slot wr is no longer read
+        if (kt + kStages - 1 < ktiles) issue(wr);
+        cp_async_commit();
+        const float* As = smem + rd * S::kStage;
+        const float* Bs = As + kAStage;
+        float4 an[kRowGroups], ac[kRowGroups];
+#pragma unroll
+        for (int q = 0; q < kRowGroups; ++q)
+            an[q] = *reinterpret_cast<const float4*>(As + q * kRowStride + 4 * ty);
 #pragma unroll
         for (int k = 0; k < kBK; ++k) {
-            const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][k][ty * 4]);
-            const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][k][64 + ty * 4]);
-            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            float2 b[2 * kGroups];
 #pragma unroll
-            for (int g = 0; g < kGroups; ++g) {
-                const float4 bv = *reinterpret_cast<const float4*>(&Bs[cur][k][g * 64 + tx * 4]);
-                b[2 * g] = make_float2(bv.x, bv.y);
-                b[2 * g + 1] = make_float2(bv.z, bv.w);
+            for (int q = 0; q < kRowGroups; ++q) ac[q] = an[q];
+            if (k + 1 < kBK) {
+#pragma unroll
+                for (int q = 0; q < kRowGroups; ++q)
+                    an[q] = *reinterpret_cast<const float4*>(As + (k + 1) * kAS + q * kRowStride +
+                                                             4 * ty);
             }
+            float4 bq[S::kGroups];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float2 ai = make_float2(a[i], a[i]);
+            for (int g = 0; g < S::kGroups; ++g)
+                bq[g] = *reinterpret_cast<const float4*>(Bs + k * BN + g * S::kGroupStride + 4 * tx);
+            // Column pair outer, rows inner: one B pair feeds 16 FMA pairs in a row.
 #pragma unroll
-                for (int j = 0; j < 2 * kGroups; ++j) acc[i][j] = __ffma2_rn(ai, b[j], acc[i][j]);
+            for (int g = 0; g < S::kGroups; ++g) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float2 b = h ? make_float2(bq[g].z, bq[g].w) : make_float2(bq[g].x, bq[g].y);
+#pragma unroll
+                    for (int q = 0; q < kRowGroups; ++q) {
+                        const float a4[4] = {ac[q].x, ac[q].y, ac[q].z, ac[q].w};
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            acc[4 * q + r][2 * g + h] =
+                                __ffma2_rn(make_float2(a4[r], a4[r]), b, acc[4 * q + r][2 * g + h]);
+                    }
+                }
             }
         }
-        if (more) {
-            store_a(cur ^ 1, ra);
-            store_b(cur ^ 1, rb);
-        }
-        __syncthreads();
+        rd = rd + 1 == kStages ? 0 : rd + 1;
+        wr = wr + 1 == kStages ? 0 : wr + 1;
     }
+    cp_async_wait<0>();
 
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int64_t m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+    for (int i = 0; i < kTM; ++i) {
+        const int64_t m = m0 + (i / 4) * kRowStride + ty * 4 + (i % 4);
         if (!EXACT && m >= M) continue;
 #pragma unroll
-        for (int h = 0; h < kGroups; ++h) {
-            const int64_t n = n0 + h * 64 + tx * 4;
+        for (int g = 0; g < S::kGroups; ++g) {
+            const int64_t n = n0 + g * S::kGroupStride + tx * 4;
             float* p = C + m * ldc + n;
-            const float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x,
-                                acc[i][2 * h + 1].y};
+            const float v[4] = {acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
+                                acc[i][2 * g + 1].y};
             if (EXACT || (VEC && n + 3 < N)) {
                 *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
@@ -180,34 +262,34 @@ __device__ __forceinline__ void sgemm_tile(int M, int N, int K, const float* __r
     }
 }
 
-// Block b takes tile tile_base + b (BN = 128) or one half of tile
+// Block b takes tile tile_base + b (BN = 128) or half b % 2 of tile
 // tile_base + b / 2 (BN = 64), tiles in grouped order.  With `dependent` set
-// (half tiles launched behind the whole-tile grid with programmatic dependent
-// launch), a block first lets the next grid start early and, at the end, waits
-// for the grid before it to finish, so that whatever follows this grid in the
-// stream sees both grids' results.
+// (halves launched behind the whole-tile grid with programmatic dependent
+// launch), a block first lets the next grid start early and, at the end,
+// waits for the grid before it to finish, so that whatever follows this grid
+// in the stream sees both grids' results.
 template <bool VEC, int BN, bool EXACT>
 __global__ void __launch_bounds__(kThreads, 2)
     sgemm_kernel(int M, int N, int K, const float* __restrict__ A, int64_t lda,
                  const float* __restrict__ B, int64_t ldb, float* __restrict__ C, int64_t ldc,
                  int64_t tiles_m, int64_t tiles_n, int64_t tile_base, int dependent) {
-    __shared__ __align__(16) float As[2][kBK][kBM + kPadA];
-    __shared__ __align__(16) float Bs[2][kBK][kBN];
+    extern __shared__ __align__(16) float smem[];
 
     if (dependent) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t b = blockIdx.x;
     int64_t tm, tn;
-    raster_tile(tile_base + (BN == kBN ? b : b / 2), tiles_m, tiles_n, 8, &tm, &tn);
-    const int64_t n0 = tn * kBN + (BN == kBN ? 0 : (b & 1) * BN);
-    sgemm_tile<VEC, BN, EXACT>(M, N, K, A, lda, B, ldb, C, ldc, tm * kBM, n0, As, Bs);
+    constexpr int kPieces = kBN / BN;
+    raster_tile(tile_base + b / kPieces, tiles_m, tiles_n, 8, &tm, &tn);
+    const int64_t n0 = tn * kBN + (b % kPieces) * BN;
+    sgemm_tile<VEC, BN, EXACT>(M, N, K, A, lda, B, ldb, C, ldc, tm * kBM, n0, smem);
     if (dependent && BN != kBN) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // The last k1 - k0 terms of every output's FMA chain: C[m][n] continues from
 // the value the tile kernel stored for terms [0, k0), one fused multiply-add
 // per term in increasing k, so the result is the chain over [0, k1) exactly.
-// Used when K does not fit the tile kernel's 32-bit slice count (K > 2^31 - 8;
-// then k1 - k0 <= 7).
+// Used when K does not fit the tile kernel's 32-bit slice count (K > 2^31 - 16;
+// then k1 - k0 <= 15).
 __global__ void f32_ktail_kernel(int64_t M, int64_t N, int64_t k0, int64_t k1,
                                  const float* __restrict__ A, int64_t lda,
                                  const float* __restrict__ B, int64_t ldb, float* __restrict__ C,
@@ -223,24 +305,52 @@ __global__ void f32_ktail_kernel(int64_t M, int64_t N, int64_t k0, int64_t k1,
 }
 
 // How many tiles run whole (the rest run as halves), given the SM count and
-// the resident blocks per SM.  Measured on GB300 (two blocks per SM): the time
-// is set by the most tiles any SM runs -- it grows by one step per 152 tiles --
-// and a block left alone on its SM runs about twice as fast as one of a pair,
-// while a half tile alone takes nearly as long as a whole one.  Halving the
-// rem = tiles mod (2 x SMs) tiles of the last partial wave therefore only pays
-// when the halves still leave at most one block per SM (rem <= SMs / 2:
-// 0.5-1 % faster); with larger remainders it loses up to 7 %.
+// the resident blocks per SM.  Measured on GB300 (two blocks per SM, 4096-term
+// tiles): a block left alone on its SM takes about half the time of one of a
+// pair (one block's four warps nearly fill the FMA pipes), and two halves
+// sharing an SM take about as long as a lone whole tile.  With rem = tiles mod
+// (2 x SMs) whole tiles left for the last partial wave:
+//   rem <= SMs / 2: every half runs alone on its SM -- halves (64 tiles on 152
+//     SMs: 41.0 against 25.1 TFLOP/s; 20: 51.7 against 44.4);
+//   SMs / 2 < rem <= SMs: whole tiles run alone, halves in pairs -- whole
+//     (112: 64.1 against 63.3; 144: 61.1 against 50.8);
+//   SMs < rem <= 3 SMs / 2: whole tiles end with some SMs running a pair,
+//     halves with one wave of pairs and a few lone halves -- halves (176: 53.3
+//     against 49.2 and 65.1 against 63.8);
+//   larger: two waves of half pairs against one of whole pairs -- whole (256:
+//     53.9 against 48.9; 272: 62.3 against 59.4).
 int64_t full_tiles(int64_t tiles, int sms, int per_sm) {
     const int64_t slots = static_cast<int64_t>(sms) * per_sm;
     if (slots <= 0) return tiles;
     const int64_t rem = tiles % slots;
-    return (rem > 0 && 2 * rem <= sms) ? tiles - rem : tiles;
+    if (rem == 0) return tiles;
+    const bool halve = 2 * rem <= sms || (per_sm == 2 && rem > sms && 2 * rem <= 3 * sms);
+    return halve ? tiles - rem : tiles;
 }
 
 // SM count and resident blocks per SM for each device and variant, queried
 // once; 0 = not yet known.
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices][2], g_per_sm[kMaxDevices][2];
+
+// The whole-tile ring (3 x 16.3 KiB) is above the 48 KiB that a launch may
+// take without opting in; every instantiation opts in to its own size.
+template <bool VEC, int BN, bool EXACT>
+cudaError_t allow_smem() {
+    return cudaFuncSetAttribute(sgemm_kernel<VEC, BN, EXACT>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SimtShape<BN>::kSmemBytes);
+}
+
+cudaError_t allow_smem_all() {
+    cudaError_t e = allow_smem<true, kBN, true>();
+    if (e == cudaSuccess) e = allow_smem<true, kBN, false>();
+    if (e == cudaSuccess) e = allow_smem<false, kBN, false>();
+    if (e == cudaSuccess) e = allow_smem<true, kBN / 2, true>();
+    if (e == cudaSuccess) e = allow_smem<true, kBN / 2, false>();
+    if (e == cudaSuccess) e = allow_smem<false, kBN / 2, false>();
+    return e;
+}
 
 cudaError_t residency(bool vec, int* sms_out, int* per_sm_out) {
     int dev = 0;
@@ -250,13 +360,18 @@ cudaError_t residency(bool vec, int* sms_out, int* per_sm_out) {
         *sms_out = g_sms[dev][vec].load();
         return cudaSuccess;
     }
+    // First use on this device: the opt-in comes before any launch (the
+    // cached residency below is only stored after it succeeded).
+    e = allow_smem_all();
+    if (e != cudaSuccess) return e;
     int sms = 0, per_sm = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
         e = vec ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                      &per_sm, sgemm_kernel<true, kBN, false>, kThreads, 0)
+                      &per_sm, sgemm_kernel<true, kBN, false>, kThreads, SimtShape<kBN>::kSmemBytes)
                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                      &per_sm, sgemm_kernel<false, kBN, false>, kThreads, 0);
+                      &per_sm, sgemm_kernel<false, kBN, false>, kThreads,
+                      SimtShape<kBN>::kSmemBytes);
     if (e != cudaSuccess) return e;
     *sms_out = sms;
     *per_sm_out = per_sm;
@@ -267,32 +382,35 @@ cudaError_t residency(bool vec, int* sms_out, int* per_sm_out) {
     return cudaSuccess;
 }
 
+// Whole tiles [0, full) in one grid, the rest cut into halves in a second.
+// mode 2 launches the second grid plainly; every other mode behind the first
+// with programmatic dependent launch.
 template <bool VEC, bool EXACT>
 cudaError_t launch_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                        const float* B, int64_t ldb, float* C, int64_t ldc, cudaStream_t stream,
                        int64_t tiles_m, int64_t tiles_n, int64_t full, int64_t tiles, int mode) {
-    // mode 0: half tiles behind the whole ones with programmatic dependent
-    // launch; 2: the same as two plain launches.
-    const int dependent = (mode == 0 && full > 0) ? 1 : 0;
+    constexpr int BN = kBN / 2;
+    const int dependent = (mode != 2 && full > 0) ? 1 : 0;
     if (full > 0) {
-        sgemm_kernel<VEC, kBN, EXACT><<<dim3(static_cast<unsigned>(full)), kThreads, 0, stream>>>(
-            int(M), int(N), int(K), A, lda, B, ldb, C, ldc, tiles_m, tiles_n, 0, dependent);
+        sgemm_kernel<VEC, kBN, EXACT>
+            <<<dim3(static_cast<unsigned>(full)), kThreads, SimtShape<kBN>::kSmemBytes, stream>>>(
+                int(M), int(N), int(K), A, lda, B, ldb, C, ldc, tiles_m, tiles_n, 0, dependent);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (tiles == full) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * (tiles - full)));
+    cfg.gridDim = dim3(static_cast<unsigned>((kBN / BN) * (tiles - full)));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = SimtShape<BN>::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = dependent ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, sgemm_kernel<VEC, kBN / 2, EXACT>, int(M), int(N), int(K), A, lda,
-                              B, ldb, C, ldc, tiles_m, tiles_n, full, dependent);
+    return cudaLaunchKernelEx(&cfg, sgemm_kernel<VEC, BN, EXACT>, int(M), int(N), int(K), A, lda, B,
+                              ldb, C, ldc, tiles_m, tiles_n, full, dependent);
 }
 
 }  // namespace
@@ -304,8 +422,8 @@ cudaError_t f32_tiles_launch(int64_t M, int64_t N, int64_t K, const float* A, in
 cudaError_t f32_launch(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                        const float* B, int64_t ldb, float* C, int64_t ldc, cudaStream_t stream,
                        int tail_mode, int ktail) {
-    // The tile kernel counts K slices of 8 as (K + 7) / 8 in 32 bits, so it
-    // takes at most 2^31 - 8 terms; the rest (at most 7) continue each chain
+    // The tile kernel counts K slices of 16 as (K + 15) / 16 in 32 bits, so it
+    // takes at most 2^31 - 16 terms; the rest (at most 15) continue each chain
     // in f32_ktail_kernel.  `ktail` > 0 moves that many terms there for any K
     // larger than it (to test that path at small sizes).
     constexpr int64_t kMaxTileK = 0x7fffffffLL - (kBK - 1);
@@ -330,14 +448,18 @@ cudaError_t f32_tiles_launch(int64_t M, int64_t N, int64_t K, const float* A, in
     const int64_t tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN;
     const int64_t tiles = tiles_m * tiles_n;
     if (tiles > 0x3fffffff) return cudaErrorInvalidValue;
-    const bool vec = (reinterpret_cast<uintptr_t>(A) % 16 == 0) &&
-                     (reinterpret_cast<uintptr_t>(B) % 16 == 0) &&
-                     (reinterpret_cast<uintptr_t>(C) % 16 == 0) && lda % 4 == 0 &&
-                     ldb % 4 == 0 && ldc % 4 == 0;
+    // A moves in 4-byte copies whatever its alignment; B's 16-byte copies and
+    // C's float4 stores need 16-byte rows.
+    const bool vec = (reinterpret_cast<uintptr_t>(B) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ldb % 4 == 0 && ldc % 4 == 0;
     int sms = 0, per_sm = 0;
     const cudaError_t e = residency(vec, &sms, &per_sm);
     if (e != cudaSuccess) return e;
-    const int64_t full = tail_mode == 1 ? tiles : full_tiles(tiles, sms, per_sm);
+    // tail_mode 3 halves the last partial wave whatever its size (tests, tuning).
+    const int64_t slots = static_cast<int64_t>(sms) * per_sm;
+    const int64_t full = tail_mode == 1   ? tiles
+                         : tail_mode == 3 ? (slots > 0 ? tiles - tiles % slots : tiles)
+                                          : full_tiles(tiles, sms, per_sm);
     const bool exact = vec && M % kBM == 0 && N % kBN == 0 && K % kBK == 0;
     if (exact)
         return launch_f32<true, true>(M, N, K, A, lda, B, ldb, C, ldc, stream, tiles_m, tiles_n,

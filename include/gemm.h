@@ -61,9 +61,9 @@ extern "C" {
  *
  * Products and sums in FP32 (fused multiply-add), one rounding per step.
  * A, B and C must be 4-byte aligned.  K may be up to 2^31 - 1: the tile
- * kernel counts K slices of 8 in 32 bits and takes the first 2^31 - 8 terms,
- * and a second kernel continues each output's FMA chain over the rest (at
- * most 7), so the result is the same chain.
+ * kernel counts K slices of 16 in 32 bits and takes the first 2^31 - 16
+ * terms, and a second kernel continues each output's FMA chain over the rest
+ * (at most 15), so the result is the same chain.
  */
 int gemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
              int64_t ldb, float* C, int64_t ldc, void* stream);
@@ -296,13 +296,14 @@ int gemm_read_watchdog(int reset);
  *                 and "tail" 0 the library takes two pieces by itself when the
  *                 tiles have at least 192 K stages (K >= 12288 for 16-bit inputs,
  *                 24576 for e4m3) and the doubled tail still fits in one wave
- *   "f32_ktail"   gemm_f32 only, for tests: 0 (default), or 1..7: the last that
+ *   "f32_ktail"   gemm_f32 only, for tests: 0 (default), or 1..15: the last that
  *                 many terms of K (when K is larger) run in the chain-continuing
- *                 kernel that otherwise takes only the terms past 2^31 - 8
+ *                 kernel that otherwise takes only the terms past 2^31 - 16
  *   "f32_tail"    gemm_f32 only: 0 (default) runs the last partial wave of 128 x 128 tiles
  *                 as 128 x 64 halves where that shortens it, in a second grid started
  *                 early by programmatic dependent launch; 1 keeps whole tiles; 2 is 0
- *                 with a plain second launch.  Results are bit-identical in every mode.
+ *                 with a plain second launch; 3 halves the last partial wave whatever
+ *                 its size.  Results are bit-identical in every mode.
  *   "splits"      K pieces per tile: 0 auto (default, needs a workspace), 1 never
  *                 split, 2..64 split that many ways when the workspace suffices
  * Returns GEMM_OK or GEMM_ERR_INVALID_OPTION.

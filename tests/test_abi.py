@@ -97,7 +97,7 @@ def test_fp8_and_f32_argument_errors_without_gpu():
     assert f6(4, 5, 6, p, 6, p, 5, p, 4) == capi.GEMM_ERR_INVALID_LD
     assert f6(4, 5, 6, p, 6, None, 5, p, 5) == capi.GEMM_ERR_NULL_PTR
     assert f6(4, 5, 6, p, 6, p, 5, p + 2, 5) == capi.GEMM_ERR_MISALIGNED
-    # K up to 2^31 - 1 passes the dimension check (the terms past 2^31 - 8 run in
+    # K up to 2^31 - 1 passes the dimension check (the terms past 2^31 - 16 run in
     # the chain-continuing kernel); 2^31 does not
     assert capi.gemm_f32(4, 5, (1 << 31) - 1, p, 1 << 31, p, 5, p, 4) == capi.GEMM_ERR_INVALID_LD
     assert capi.gemm_f32(4, 5, 1 << 31, p, 1 << 31, p, 5, p, 5) == capi.GEMM_ERR_INVALID_DIM
@@ -146,9 +146,11 @@ def test_options():
     assert capi.gemm_set_option("tail", 3) == capi.GEMM_ERR_INVALID_OPTION
     assert capi.gemm_set_option("tail", 0) == 0
     assert capi.gemm_set_option("cluster", 0) == capi.GEMM_ERR_INVALID_OPTION  # removed
-    assert capi.gemm_set_option("f32_ktail", 8) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("f32_ktail", 16) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("f32_ktail", 15) == 0
     assert capi.gemm_set_option("f32_ktail", 0) == 0
-    assert capi.gemm_set_option("f32_tail", 3) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("f32_tail", 4) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("f32_tail", 3) == 0
     assert capi.gemm_set_option("f32_tail", 0) == 0
     assert capi.gemm_set_option("tail_k", 1) == capi.GEMM_ERR_INVALID_OPTION
     assert capi.gemm_set_option("tail_k", 0) == 0

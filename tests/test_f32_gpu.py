@@ -58,18 +58,19 @@ def test_unaligned_and_padded_ld():
 def test_half_width_tail(shape):
     """On 152 SMs with two blocks each: 324 tiles run as 304 whole + 20 halved
     (with N = 2204 the right halves of the last tile column hold no columns at
-    all); 448 and 480 tiles all whole (remainders 144 and 176); 16 tiles all
-    halved; the last two
+    all); 448 tiles all whole (remainder 144); 480 as 304 whole + 176 halved;
+    16 tiles all halved; the last two
     shapes are multiples of the tile and of the K slice, so they take the
     variant without bounds checks (whole and half tiles).  Every tail mode
     ("f32_tail" 0 = halves behind a dependent launch, 1 = whole tiles, 2 = halves
-    in a plain second launch) must give bit-identical C, since each output is
-    the same chain of FMAs in k order; C's padding columns stay untouched."""
+    in a plain second launch, 3 = halves for any last partial wave) must give
+    bit-identical C, since each output is the same chain of FMAs in k order;
+    C's padding columns stay untouched."""
     M, N, K = shape
     ops = si.f32_operands(M, N, K, dist="uniform", seed=M + K)
     outs = []
     try:
-        for mode in (0, 1, 2):
+        for mode in (0, 1, 2, 3):
             assert capi.gemm_set_option("f32_tail", mode) == 0
             outs.append(run_f32(ops, M, N, K, ldc=N + 7))
     finally:
@@ -83,6 +84,42 @@ def test_half_width_tail(shape):
     for other in outs[1:]:
         assert torch.equal(other[:M, :N], C[:M, :N])
         assert torch.all(torch.isnan(other[:M, N:]))
+
+
+@pytest.mark.parametrize("case", ["ragged_chunk", "odd_lda_unchecked", "a_offset"])
+def test_copy_paths(case):
+    """The copies into shared memory: B's 16-byte copies with a last chunk of
+    N only partly inside (N = 130, ldb = 132: 8 of its 16 bytes are read, the
+    rest zero-filled); A, which always moves in 4-byte copies, with an odd lda
+    on a shape that takes the variant without bounds checks (M, N multiples of
+    128, K of 16); and A starting 4 bytes past a 16-byte boundary."""
+    if case == "ragged_chunk":
+        M, N, K, lda, ldb, ldc = 257, 130, 70, 70, 132, 132
+    elif case == "odd_lda_unchecked":
+        M, N, K, lda, ldb, ldc = 256, 384, 64, 65, 384, 384
+    else:
+        M, N, K, lda, ldb, ldc = 300, 256, 48, 48, 256, 256
+    ops = si.f32_operands(M, N, K, dist="uniform", seed=M + N + lda, lda=lda, ldb=ldb)
+    if case == "a_offset":
+        flat = torch.empty(M * lda + 1, dtype=torch.float32)
+        flat[1:] = ops["A"].reshape(-1)
+        A = flat.cuda()[1:]
+        assert A.data_ptr() % 16 == 4
+    else:
+        A = ops["A"].cuda()
+    B = ops["B"].cuda()
+    C = torch.full((M, ldc), float("nan"), device="cuda")
+    st = capi.gemm_f32(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc,
+                       torch.cuda.current_stream().cuda_stream)
+    assert st == 0, capi.status_text(st)
+    torch.cuda.synchronize()
+    C = C.cpu()
+    exact = oracle.gemm_f32(M, N, K, ops["A"].numpy(), lda, ops["B"].numpy(), ldb)
+    got = C[:M, :N].double().numpy()
+    a, b = ops["A"][:, :K].double().numpy(), ops["B"][:K, :N].double().numpy()
+    assert np.all(np.abs(got - exact) <= tight_f32(a, b, K))
+    if ldc > N:
+        assert torch.all(torch.isnan(C[:M, N:])), "C padding was written"
 
 
 def test_pm1_long_k_exact():
@@ -127,18 +164,21 @@ def test_k_zero_and_empty():
     assert torch.equal(run_f32(ops, 0, N, 1, c_init=init), init)
 
 
-@pytest.mark.parametrize("ktail", [1, 3, 7])
+@pytest.mark.parametrize("ktail", [1, 3, 7, 15])
 @pytest.mark.parametrize("shape,lds", [((300, 260, 129), None), ((129, 4, 1000), None),
-                                       ((257, 130, 70), (75, 133, 131)), ((1, 1, 9), None),
-                                       ((2048, 3584, 16), None)])
+                                       ((257, 130, 70), (75, 133, 131)), ((1, 1, 17), None),
+                                       ((2048, 3584, None), None)])
 def test_k_tail_continues_the_chain(ktail, shape, lds):
-    """K above 2^31 - 8 runs its last terms (at most 7) in a second kernel that
-    continues each output's FMA chain from the value the tile kernel stored.
-    Option "f32_ktail" moves the last 1, 3 or 7 terms there at any K: C must
-    be bit-identical to the one-kernel result (the same chain of FMAs in k
-    order), and match the oracle; with padded leading dimensions too, and
-    with the tile kernel's unchecked variant (the last shape)."""
+    """K above 2^31 - 16 runs its last terms (at most 15) in a second kernel
+    that continues each output's FMA chain from the value the tile kernel
+    stored.  Option "f32_ktail" moves the last 1, 3, 7 or 15 terms there at
+    any K: C must be bit-identical to the one-kernel result (the same chain of
+    FMAs in k order), and match the oracle; with padded leading dimensions too,
+    and with the tile kernel's unchecked variant (the last shape, K = 16 +
+    ktail, so the tile kernel's 16 terms are one whole slice)."""
     M, N, K = shape
+    if K is None:
+        K = 16 + ktail
     lda, ldb, ldc = lds if lds else (K, N, N)
     ops = si.f32_operands(M, N, K, dist="uniform", seed=M + N + K, lda=lda, ldb=ldb)
     whole = run_f32(ops, M, N, K, ldc=ldc)
