@@ -234,6 +234,37 @@ def timed_launches(call, sets, steps, warmup, stream, dist=None, sampler=None):
     return total, launches
 
 
+def graph_time(call, sets, launches, stream, replays=9):
+    """Mean ms per call of `launches` back-to-back calls, rotating over `sets`,
+    captured in one CUDA graph and replayed (median of `replays`): the steady
+    state of a stream of calls, without the host's launch cost and without
+    events between the calls, which keep programmatic dependent launch from
+    overlapping a call's prologue with the end of the one before."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            call(*sets[i % len(sets)])
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(launches):
+                call(*sets[i % len(sets)])
+        g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        per = []
+        for _ in range(replays):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            per.append(e0.elapsed_time(e1) / launches)
+    del g
+    return statistics.median(per)
+
+
 def spread(launches):
     """Mean, median, min and max of per-launch times (ms)."""
     ms = sorted(launches)
@@ -713,6 +744,7 @@ PER_CONFIG = [
     ("e4m3", (3072, 4096, 8192), True, (4, 1.0), False),
     ("bf16", (16, 8192, 8192), False, (3, 0.05), True),
     ("bf16", (128, 8192, 8192), False, (3, 0.05), True),
+    ("bf16", (192, 8192, 8192), False, (3, 0.05), True),
     ("bf16", (256, 8192, 8192), False, (3, 0.05), True),
     ("bf16", (64, 14336, 4096), False, (3, 0.05), True),
     ("bf16", (1024, 1024, 8192), False, (3, 0.05), True),
@@ -734,36 +766,55 @@ def per_config(stream, stream_h, burst, hbm, workspace, launches=20):
     entry: TFLOP/s at the mean launch, the fraction of the dtype's burst peak
     (FP8 = 2x BF16 by the nominal ratio), GB/s of compulsory bytes and the
     per-launch spread; the HBM-bound shapes add the fraction of the measured
-    copy bandwidth.  The tight-leading-dimension BF16 shapes are timed again
-    without a workspace (the load-based producer reads them in place)."""
+    copy bandwidth, and the same calls replayed as a CUDA graph (graph_us,
+    graph_gbs, hbm_frac_graph: the steady state of a stream of calls, where a
+    call's prologue overlaps the end of the one before) with cuBLAS replayed
+    the same way beside them (16-bit inputs).  The tight-leading-dimension
+    BF16 shapes are timed again without a workspace (the load-based producer
+    reads them in place)."""
     import torch
 
     from dense_gemm_tcgen05_gb300 import capi
 
     out = {}
 
-    def one(kind, M, N, K, f32, seed, sigma, tag=""):
+    def one(kind, M, N, K, f32, seed, sigma, tag="", graph=False):
         nsets = sets_beyond_l2(kind, M, N, K, f32)
         o, s = tn_sets(kind, M, N, K, seed=seed, sigma=sigma, nsets=nsets, device="cuda",
                        out_f32=f32)
         c = tn_call(kind, M, N, K, o["scale_a"], o["scale_b"], stream_h, out_f32=f32)
         with torch.cuda.stream(stream):
             _, ls = timed_launches(c, s, launches, 3, stream)
-        del s, o
-        torch.cuda.empty_cache()
         lm = sum(ls) / len(ls)
         tf = 2.0 * M * N * K / (lm * 1e-3) / 1e12
         peak = burst * (FP8_OVER_BF16 if kind == "e4m3" else 1.0)
-        gbs = compulsory_bytes(kind, M, N, K, f32) / (lm * 1e-3) / 1e9
+        byts = compulsory_bytes(kind, M, N, K, f32)
+        gbs = byts / (lm * 1e-3) / 1e9
         key = "%s%s_%dx%dx%d%s" % (kind, "_f32out" if f32 else "", M, N, K, tag)
         out[key] = {"tflops": round(tf, 1), "frac": round(tf / peak, 4), "gbs": round(gbs),
                     "sets": nsets, **spread(ls)}
+        if graph:
+            # The same calls as a replayed CUDA graph, and cuBLAS (torch's
+            # linear on the same operands, 16-bit inputs) replayed the same
+            # way, for context.
+            gm = graph_time(c, s, 2 * len(s) * max(1, 10 // len(s)), stream)
+            out[key]["graph_us"] = round(gm * 1e3, 2)
+            out[key]["graph_gbs"] = round(byts / (gm * 1e-3) / 1e9)
+            if kind != "e4m3" and not f32:
+                def lin(a, b, _c):
+                    torch.nn.functional.linear(a, b)
+                cm = graph_time(lin, s, 2 * len(s) * max(1, 10 // len(s)), stream)
+                out[key]["cublas_graph_us"] = round(cm * 1e3, 2)
+                out[key]["cublas_over_this"] = round(cm / gm, 3)
+        del s, o
+        torch.cuda.empty_cache()
         return key, gbs
 
     for kind, (M, N, K), f32, (seed, sigma), hbm_bound in PER_CONFIG:
-        key, gbs = one(kind, M, N, K, f32, seed, sigma)
+        key, gbs = one(kind, M, N, K, f32, seed, sigma, graph=hbm_bound)
         if hbm_bound:
             out[key]["hbm_frac"] = round(gbs / hbm, 3)
+            out[key]["hbm_frac_graph"] = round(out[key]["graph_gbs"] / hbm, 3)
     capi.gemm_set_workspace(None, 0)
     try:
         for M, N, K in ((2047, 3001, 1023), (8191, 8191, 8191)):
