@@ -82,6 +82,7 @@ std::atomic<int> g_opt_tail_k{0};
 std::atomic<int> g_opt_repack{0};
 std::atomic<int> g_opt_f32_tail{0};
 std::atomic<int> g_opt_f32_ktail{0};
+std::atomic<int> g_opt_atoms{0};
 std::atomic<int> g_opt_l2hints{0};
 std::atomic<int> g_opt_half{0};
 std::atomic<int> g_opt_issuers{0};
@@ -217,6 +218,7 @@ struct TnPlan {
     TcGeometry g{};
     int64_t tiles_p = 0, tiles_q = 0, tiles = 0, slots = 0;
     int num_kb = 0, stages = 0, stage_bytes = 0;
+    int atoms = 1;              // K atoms (128-byte swizzle spans) per ring stage
     int splits = 1, kb_per_split = 0;
     int64_t split_cnt_bytes = 0;  // counter bytes ahead of the split partials
     int tail_f = 1, tail_kb_per = 0;
@@ -350,14 +352,39 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
     if (cap > 0 && cap / g.cluster < p.slots) p.slots = cap / g.cluster > 0 ? cap / g.cluster : 1;
     const int64_t tiles = p.tiles, slots = p.slots;
     p.grid = static_cast<int>((tiles < slots ? tiles : slots) * g.cluster);
-    p.num_kb = static_cast<int>((K + g.stage_k - 1) / g.stage_k);
+    // K atoms per stage (option "atoms"; the load-based producer takes one):
+    // a stage of two atoms carries twice the K of each row and its MMAs end in
+    // one commit instead of two.  The MMA warp's loop costs ~580 cycles per
+    // stage, more than a stage's tensor work in tiles up to 128 columns wide
+    // (at most 256 cycles per SM), so automatically (option 0) those run two
+    // atoms when the ring still holds three stages; wider tiles keep one.
+    // Measured on GB300 against the build without the second atom (same box,
+    // processes alternating; time ratio old / new): one-CTA 128 x 128 tiles
+    // 1024 x 2048 x 4096 1.04, 1024 x 1024 x 8192 1.03; 16-column tiles, K
+    // split in two, 16 x 8192 x 8192 1.03; pairs of 64-row halves 128 wide,
+    // 128 x 8192 x 8192 1.014.  Halves 256 wide lost (192 / 256 x 8192 x 8192
+    // 0.974 / 0.982), and so did 256 x 256 pair tiles on whole waves (2048^3
+    // 0.986, 3072^3 0.986, 2048 x 2048 x 8192 0.984).
+    {
+        const int opt_atoms = g_opt_atoms.load();
+        if (p.prod == Producer::Tma) {
+            if (opt_atoms == 2) {
+                p.atoms = 2;
+            } else if (opt_atoms == 0 && p.tile_q <= 128) {
+                const int rows = g.load_p + p.load_q;
+                const int sb2 = (rows * 128 * 2 + 1023) / 1024 * 1024;
+                if (g.stage_region / sb2 >= 3) p.atoms = 2;
+            }
+        }
+    }
+    p.num_kb = static_cast<int>((K + g.stage_k * p.atoms - 1) / (g.stage_k * p.atoms));
     // Ring: as many stages of this width as the stage region holds (narrow
     // tiles get a deeper ring, i.e. more loads in flight).  The load-based
     // producer's row split assumes the full-width stage.
     {
         const int max_q = g.max_tile_q / g.cluster;
         const int rows = g.load_p + (p.prod == Producer::Loads ? max_q : p.load_q);
-        const int sb = (rows * 128 + 1023) / 1024 * 1024;
+        const int sb = (rows * 128 * p.atoms + 1023) / 1024 * 1024;
         int st_count = g.stage_region / sb;
         if (st_count > g.max_stages) st_count = g.max_stages;
         p.stages = st_count;
@@ -464,7 +491,9 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
                 }
             }
             int want_k = g_opt_tail_k.load();
-            if (want_k == 0 && opt_tail == 0 && p.num_kb >= 192 && 2 * rem <= slots) want_k = 2;
+            // (192 one-atom stages: K >= 12288 for 16-bit inputs, 24576 for e4m3)
+            if (want_k == 0 && opt_tail == 0 && p.num_kb * p.atoms >= 192 && 2 * rem <= slots)
+                want_k = 2;
             if (want_k >= 2 && !a.acc16 && !p.half && a.has_scratch) {
                 const int64_t kb_per = (p.num_kb + want_k - 1) / want_k;
                 const int64_t pieces = (p.num_kb + kb_per - 1) / kb_per;
@@ -730,7 +759,9 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     L.prm.acc16 = acc16 ? 1 : 0;
     L.prm.idesc = make_idesc(g.format, static_cast<uint32_t>(g.mma_m), static_cast<uint32_t>(tile_q),
                              d_format);
-    L.prm.stage_tx_bytes = static_cast<uint32_t>((g.load_p + load_q) * 128);
+    L.prm.stage_tx_bytes = static_cast<uint32_t>((g.load_p + load_q) * 128 * pl.atoms);
+    L.prm.atoms = pl.atoms;
+    L.prm.q_atom_bytes = static_cast<uint32_t>(load_q * 128);
     L.prm.stages = pl.stages;
     L.prm.stage_bytes = static_cast<uint32_t>(pl.stage_bytes);
     L.prm.p_ptr = B;
@@ -772,7 +803,7 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
         }
         L.prm.idesc_tail = make_idesc(g.format, static_cast<uint32_t>(g.mma_m),
                                       static_cast<uint32_t>(width), d_format);
-        L.prm.stage_tx_tail = static_cast<uint32_t>((g.load_p + load_qt) * 128);
+        L.prm.stage_tx_tail = static_cast<uint32_t>((g.load_p + load_qt) * 128 * pl.atoms);
     }
     if (std::getenv("GEMM_DEBUG"))
         std::fprintf(stderr,
@@ -963,7 +994,8 @@ int gemm_tn_plan(int kind, int64_t M, int64_t N, int64_t K, int flags, int64_t w
                                          pl.kb_per_split,
                                          pl.tail_kb_per,
                                          pl.stage_bytes,
-                                         pl.issuers};
+                                         pl.issuers,
+                                         pl.atoms};
     for (int i = 0; i < GEMM_PLAN_FIELDS; ++i) out[i] = v[i];
     return GEMM_OK;
 }
@@ -1060,6 +1092,9 @@ int gemm_set_option(const char* name, int64_t value) {
     } else if (!std::strcmp(name, "half")) {
         if (value < 0 || value > 3) return GEMM_ERR_INVALID_OPTION;
         g_opt_half.store(static_cast<int>(value));
+    } else if (!std::strcmp(name, "atoms")) {
+        if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
+        g_opt_atoms.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "max_ctas")) {
         if (value < 0 || value > 1 << 20) return GEMM_ERR_INVALID_OPTION;
         g_opt_max_ctas.store(static_cast<int>(value));

@@ -83,6 +83,13 @@ struct TcParams {
     int32_t k_snake;
     // 1: odd rasteriser bands walk the tile columns backwards (raster.h).
     int32_t band_snake;
+    // K atoms (128-byte swizzle spans of K) per ring stage, 1 or 2, which
+    // selects the kernel instantiation: a stage of two holds P atom 0, P atom
+    // 1, Q atom 0, Q atom 1 (each atom of Q q_atom_bytes long, the full tile
+    // width), and the MMA warp issues all of a stage's MMAs before one
+    // commit.  The load-based producer takes 1.
+    int32_t atoms;
+    uint32_t q_atom_bytes;
 };
 
 struct TcLaunch {

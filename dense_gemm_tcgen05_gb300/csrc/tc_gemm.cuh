@@ -261,7 +261,8 @@ __device__ __forceinline__ uint4 mask_chunk(uint4 v, int32_t lim) {
 // SPLIT: the launch cuts tiles into K pieces (split-K or a K-split tail) and
 // combines them through the workspace.  Launches without K pieces run the
 // instantiation without that code.
-template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT, bool HALF, int NI = 1>
+template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT, bool HALF, int NI = 1,
+          int AT = 1>
 __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p,
                    const __grid_constant__ CUtensorMap map_q,
@@ -273,6 +274,8 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
     constexpr int SM = Cfg::kMaxStages;                 // barrier slots
     const uint32_t S = static_cast<uint32_t>(prm.stages);  // ring depth for this call
     const uint32_t stage_bytes = prm.stage_bytes;
+    static_assert(AT == 1 || (AT == 2 && !LOADS), "two K atoms per stage: TMA producer only");
+    constexpr int32_t atoms = AT;                          // K atoms per stage
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -403,6 +406,10 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
         const uint64_t pol_q = l2_evict_last_policy();
         const bool hints = prm.l2_hints != 0;
         uint32_t lu = 0;                     // units this CTA has run
+        // stage layout: P atoms, then Q atoms (q_atom bytes each)
+        const uint32_t q_region = atoms > 1 ? 2u * Cfg::kBytesP : Cfg::kBytesP;
+        const uint32_t q_atom = prm.q_atom_bytes;
+        const int32_t stage_k = atoms > 1 ? 2 * Cfg::kStageK : Cfg::kStageK;
         for (int64_t u = first; ok && u < num_units; u += stride, ++lu) {
             const Unit w = u == first ? u_first : unit_of(u);
             // Every second unit reads its K range backwards (the MMA warp sums
@@ -424,8 +431,8 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
                 }
                 if (lane == 0) {
                     const uint32_t sp = base + s * stage_bytes;
-                    const uint32_t sq = sp + Cfg::kBytesP;
-                    const int32_t kx = (k_rev >= 0 ? k_rev - kb : kb) * Cfg::kStageK;
+                    const uint32_t sq = sp + q_region;
+                    const int32_t kx = (k_rev >= 0 ? k_rev - kb : kb) * stage_k;
                     if constexpr (PAIR) {
                         const uint32_t fb = mapa_shared(full_bar(s), 0);
                         if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * tx);
@@ -439,6 +446,10 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
                             tma_load_2d_pair(sp, &map_p, fb, kx, p0);
                             tma_load_2d_pair(sq, mq, fb, kx, q0);
                         }
+                        if (atoms > 1) {   // the stage's second K atom, behind the first
+                            tma_load_2d_pair(sp + Cfg::kBytesP, &map_p, fb, kx + Cfg::kStageK, p0);
+                            tma_load_2d_pair(sq + q_atom, mq, fb, kx + Cfg::kStageK, q0);
+                        }
                     } else {
                         mbar_arrive_expect_tx(full_bar(s), tx);
                         if (hints) {
@@ -450,6 +461,11 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
                         } else {
                             tma_load_2d(sp, &map_p, full_bar(s), kx, p0);
                             tma_load_2d(sq, mq, full_bar(s), kx, q0);
+                        }
+                        if (atoms > 1) {
+                            tma_load_2d(sp + Cfg::kBytesP, &map_p, full_bar(s), kx + Cfg::kStageK,
+                                        p0);
+                            tma_load_2d(sq + q_atom, mq, full_bar(s), kx + Cfg::kStageK, q0);
                         }
                     }
                 }
@@ -563,7 +579,12 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
         if (!PAIR || leader) {
             uint32_t lt = 0, rs = 0, rph = 0;   // tiles; ring slot and phase
             const uint64_t adesc0 = sdesc_kmajor_sw128(base);
-            const uint64_t bdesc0 = sdesc_kmajor_sw128(base + Cfg::kBytesP);
+            const uint64_t bdesc0 =
+                sdesc_kmajor_sw128(base + (atoms > 1 ? 2u * Cfg::kBytesP : Cfg::kBytesP));
+            // descriptor steps to a stage's second K atom (start address in
+            // 16-byte units)
+            const uint64_t a_atom = static_cast<uint64_t>(Cfg::kBytesP >> 4);
+            const uint64_t b_atom = static_cast<uint64_t>(prm.q_atom_bytes >> 4);
             bool ok = true;
             for (int64_t u = first; ok && u < num_units; u += stride, ++lt) {
                 const uint32_t b = lt & 1u, aph = (lt >> 1) & 1u;
@@ -610,6 +631,19 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
                                 mma_f8<Cfg::kCG>(d_tmem, adesc + off, bdesc + off, idesc, acc);
                             else
                                 mma_f16<Cfg::kCG>(d_tmem, adesc + off, bdesc + off, idesc, acc);
+                        }
+                        if (atoms > 1) {   // the second K atom: always accumulates
+#pragma unroll
+                            for (int kk = 0; kk < Cfg::kMmasPerStage; ++kk) {
+                                const uint64_t off =
+                                    static_cast<uint64_t>(kk * (Cfg::kMmaKBytes >> 4));
+                                if constexpr (IN == InKind::E4M3)
+                                    mma_f8<Cfg::kCG>(d_tmem, adesc + a_atom + off,
+                                                     bdesc + b_atom + off, idesc, 1u);
+                                else
+                                    mma_f16<Cfg::kCG>(d_tmem, adesc + a_atom + off,
+                                                      bdesc + b_atom + off, idesc, 1u);
+                            }
                         }
                         commit_to<Cfg::kCG>(empty_bar(s), 0x3);
                     }
@@ -918,10 +952,10 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
 }
 
 template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT, bool HALF = false,
-          int NI = 1>
-cudaError_t tc_launch_one(const TcLaunch& L) {
+          int NI = 1, int AT = 1>
+cudaError_t tc_launch_one_at(const TcLaunch& L) {
     using Cfg = TcCfg<IN, PAIR, LOADS, HALF, NI>;
-    auto kernel = tc_gemm_kernel<IN, OutT, PAIR, LOADS, SPLIT, HALF, NI>;
+    auto kernel = tc_gemm_kernel<IN, OutT, PAIR, LOADS, SPLIT, HALF, NI, AT>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -952,6 +986,20 @@ cudaError_t tc_launch_one(const TcLaunch& L) {
         cfg.numAttrs = 2;
     }
     return cudaLaunchKernelEx(&cfg, kernel, L.map_p, L.map_q, L.map_out, L.map_q_tail, L.prm);
+}
+
+// One or two K atoms per stage (TMA producer only), as the plan says.
+template <InKind IN, typename OutT, bool PAIR, bool LOADS, bool SPLIT, bool HALF = false,
+          int NI = 1>
+cudaError_t tc_launch_one(const TcLaunch& L) {
+    if constexpr (LOADS) {
+        if (L.prm.atoms != 1) return cudaErrorInvalidConfiguration;
+        return tc_launch_one_at<IN, OutT, PAIR, LOADS, SPLIT, HALF, NI, 1>(L);
+    } else {
+        if (L.prm.atoms == 2) return tc_launch_one_at<IN, OutT, PAIR, LOADS, SPLIT, HALF, NI, 2>(L);
+        if (L.prm.atoms != 1) return cudaErrorInvalidConfiguration;
+        return tc_launch_one_at<IN, OutT, PAIR, LOADS, SPLIT, HALF, NI, 1>(L);
+    }
 }
 
 template <InKind IN, typename OutT, bool SPLIT>

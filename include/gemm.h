@@ -209,7 +209,7 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
  *                    (0/1; else along M), ring stages, grid (CTAs), A repacked,
  *                    B repacked, tiles along N, tiles along M, K stages per
  *                    piece, K stages per last-wave piece, ring stage bytes,
- *                    MMA-issuing warps (1 or 2).
+ *                    MMA-issuing warps (1 or 2), K atoms per ring stage (1 or 2).
  *
  * Returns GEMM_OK, GEMM_ERR_INVALID_DIM or GEMM_ERR_INVALID_OPTION (kind, out
  * or nout).  A call that would be refused reports its status in out[0]
@@ -226,7 +226,7 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
 #define GEMM_PLAN_A_128 8
 #define GEMM_PLAN_B_128 16
 #define GEMM_PLAN_NOALLOC 32
-#define GEMM_PLAN_FIELDS 18
+#define GEMM_PLAN_FIELDS 19
 int gemm_tn_plan(int kind, int64_t M, int64_t N, int64_t K, int flags, int64_t workspace_bytes,
                  int sms, int64_t* out, int nout);
 
@@ -281,6 +281,9 @@ int gemm_read_watchdog(int reset);
  *                 for one-CTA TMA tiles of at most 64 columns that run unsplit in one
  *                 wave, and for pairs of 64-row halves), 1 always one, 2 two wherever
  *                 one-CTA TMA tiles of at most 128 columns run unsplit
+ *   "atoms"       K depth of a ring stage in 128-byte swizzle spans: 0 auto
+ *                 (default), 1, or 2 (twice the K per stage and per MMA commit, half
+ *                 as many stages; TMA tiles only)
  *   "tail"        the last, partial wave of tiles: 0 auto (default) cuts its tiles
  *                 into 2 or 4 narrower ones when that ends it sooner, 1 never, 2 or
  *                 4 always

@@ -81,21 +81,48 @@ def test_skinny_single_cta_tiles_and_width(M, q, kind, options):
 
 
 def test_skinny_split_k_needs_a_workspace():
-    """64 tiles on 152 SMs: two K pieces each with a workspace (128 CTAs), one
-    wave of 64 CTAs without."""
+    """64 tiles on 152 SMs: two K pieces each with a workspace (128 CTAs; 32
+    stages of two K atoms each), one wave of 64 CTAs without."""
     p = plan("bf16", 16, 8192, 8192, workspace_bytes=WS)
-    assert (p["splits"], p["kb_per_split"], p["grid"]) == (2, 64, 128)
+    assert (p["splits"], p["kb_per_split"], p["grid"], p["atoms"]) == (2, 32, 128, 2)
     p = plan("bf16", 16, 8192, 8192)
     assert (p["splits"], p["grid"]) == (1, 64)
 
 
-def test_narrow_ring_is_deeper():
-    """A 16-column tile's stage holds 16 KB of B and 2 KB of A: 10 stages of
-    18 KB in the 192 KB ring, against 8 of 24 KB at 64 columns."""
+def test_narrow_ring_is_deeper(options):
+    """A 16-column tile's one-atom stage holds 16 KB of B and 2 KB of A: 10
+    stages of 18 KB in the 192 KB ring, against 8 of 24 KB at 64 columns;
+    with two atoms per stage (the automatic choice there), 5 of 36 KB and 4 of
+    48 KB."""
+    assert (plan("bf16", 16, 8192, 8192)["stages"], plan("bf16", 16, 8192, 8192)["stage_bytes"]) \
+        == (5, 36 * 1024)
+    assert (plan("bf16", 64, 8192, 8192)["stages"], plan("bf16", 64, 8192, 8192)["stage_bytes"]) \
+        == (4, 48 * 1024)
+    options("atoms", 1)
     assert (plan("bf16", 16, 8192, 8192)["stages"], plan("bf16", 16, 8192, 8192)["stage_bytes"]) \
         == (10, 18 * 1024)
     assert (plan("bf16", 64, 8192, 8192)["stages"], plan("bf16", 64, 8192, 8192)["stage_bytes"]) \
         == (8, 24 * 1024)
+
+
+def test_atoms_rule(options):
+    """Two K atoms per stage for tiles at most 128 columns wide whose ring keeps
+    three stages; one for tiles 256 wide (pairs, pairs of halves, one CTA) and
+    for the load-based producer; option 1 / 2 forces it (2 only with TMA)."""
+    assert plan("f16", 8192, 8192, 8192)["atoms"] == 1                       # pairs, 256 wide
+    assert plan("bf16", 1024, 2048, 4096)["atoms"] == 2                      # one CTA, 128 wide
+    p = plan("bf16", 128, 8192, 8192)
+    assert (p["half"], p["atoms"], p["stages"]) == (1, 2, 6)                # pairs of halves
+    assert plan("bf16", 256, 8192, 8192)["atoms"] == 1                       # halves, 256 wide
+    assert plan("e4m3", 128, 8192, 8192)["atoms"] == 2
+    no_tma_a = ALIGNED & ~(capi.PLAN_A_TMA | capi.PLAN_A_128)
+    assert plan("bf16", 1024, 2048, 4096, flags=no_tma_a)["atoms"] == 1     # load producer
+    options("atoms", 2)
+    p = plan("f16", 8192, 8192, 8192)
+    assert (p["atoms"], p["stages"], p["stage_bytes"], p["kb_per_split"]) == (2, 3, 65536, 64)
+    assert plan("bf16", 1024, 2048, 4096, flags=no_tma_a)["atoms"] == 1
+    options("atoms", 1)
+    assert plan("bf16", 1024, 2048, 4096)["atoms"] == 1
 
 
 def test_forced_narrow_width_needs_m_to_fit(options):
