@@ -285,14 +285,31 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
     // stay 10-26 % faster.
     p.pair = p.prod == Producer::Tma && opt_pair != 0;
     int small_q = 0;
+    bool pair_q128 = false;
     if (p.pair && opt_pair < 0) {
         const int64_t pair_tiles = ((N + 255) / 256) * ((M + choose_tile_q(M, 256) - 1) /
                                                         choose_tile_q(M, 256));
         const int q = M <= 16 ? 16 : M <= 32 ? 32 : M <= 128 ? 64 : 128;
         const int64_t small_tiles = ((N + 127) / 128) * ((M + q - 1) / q);
         if (pair_tiles < a.sms / 2 && small_tiles <= a.sms) {
-            p.pair = false;
-            small_q = q;
+            // ... except with long K (16-bit inputs, K >= 8192) and M > 256,
+            // where pair tiles 128 columns wide still fit in one wave: a CTA
+            // of a pair takes in 24 KB per K atom for its 128 x 128 outputs,
+            // one CTA alone 32 KB, and these launches stream operands for
+            // most of their time.  Measured on GB300 (graph-replayed, BF16,
+            // one-CTA -> pair 128 wide): 1024 x 1536 x 8192 30.2 -> 26.8 us,
+            // 1024 x 1024 x 8192 20.9 -> 20.0, 512 x 512 x 16384 21.4 -> 20.9,
+            // 768 x 1024 x 8192 18.0 -> 17.8; with K <= 4096 the one-CTA tiles
+            // stay ahead (2048 x 1024 x 2048 9.2 against 10.5, 512 x 2048 x
+            // 4096 14.1 against 14.4).
+            const int64_t pair128_tiles = ((N + 255) / 256) * ((M + 127) / 128);
+            if (q == 128 && M > 256 && a.in != InKind::E4M3 && K >= 8192 &&
+                pair128_tiles <= a.sms / 2 && g_opt_tile_q.load() == 0) {
+                pair_q128 = true;
+            } else {
+                p.pair = false;
+                small_q = q;
+            }
         }
     }
     p.g = tc_geometry(a.in, p.pair);
@@ -302,7 +319,10 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
     // (the TMA store clips it), and never for CTA pairs.
     const int opt_tq = g_opt_tile_q.load();
     {
-        const int t = opt_tq ? opt_tq : small_q ? small_q : choose_tile_q(M, p.g.max_tile_q);
+        const int t = opt_tq      ? opt_tq
+                      : small_q   ? small_q
+                      : pair_q128 ? 128
+                                  : choose_tile_q(M, p.g.max_tile_q);
         p.tile_q = t < 64 && (p.pair || M > t) ? 64 : t;
     }
     // 64-row tiles (one CTA each, MMA M = 64), option "half" = 1: they cover

@@ -184,3 +184,32 @@ def test_large_sampled(kind, shape, atoms2):
                          sigma=1.0 if kind == "e4m3" else 0.05)
     C = run_tn(kind, ops, M, N, K)
     check_sampled(kind, ops, M, N, K, C, seed=6)
+
+
+@pytest.mark.parametrize("kind", ["f16", "bf16"])
+def test_long_k_sub_wave_pairs_auto(kind):
+    """The automatic plan for long K below a wave of tiles (M > 256, K >= 8192):
+    CTA pairs 128 columns wide, two K atoms per stage, K cut into pieces through
+    the workspace; +-1 inputs, exact."""
+    ws = torch.empty(1 << 27, dtype=torch.uint8, device="cuda")
+    assert capi.gemm_set_workspace(ws.data_ptr(), ws.numel()) == 0
+    try:
+        M, N, K = 300, 512, 8200
+        p = planned(kind, M, N, K, ws=ws.numel())
+        assert (p["pair"], p["tile_q"], p["atoms"]) == (1, 128, 2) and p["splits"] >= 2, p
+        ops = si.tn_operands(kind, M, N, K, dist="pm1", seed=17)
+        C = run_tn(kind, ops, M, N, K)
+        exact = oracle.gemm_tn(kind, M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+        assert_codes_equal(out_codes(C, M, N), exact_codes(kind, exact))
+    finally:
+        capi.gemm_set_workspace(None, 0)
+
+
+def test_long_k_sub_wave_pairs_unsplit_sampled():
+    """1024 x 1536 x 8192: 48 pair tiles 128 wide, one K piece each."""
+    M, N, K = 1024, 1536, 8192
+    p = planned("bf16", M, N, K)
+    assert (p["pair"], p["tile_q"], p["splits"]) == (1, 128, 1), p
+    ops = si.tn_operands("bf16", M, N, K, dist="normal", seed=21, sigma=0.05)
+    C = run_tn("bf16", ops, M, N, K)
+    check_sampled("bf16", ops, M, N, K, C, seed=8)

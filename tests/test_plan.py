@@ -135,11 +135,19 @@ def test_forced_narrow_width_needs_m_to_fit(options):
 
 def test_sub_wave_rule():
     """Pair tiles filling less than a wave give way to single-CTA tiles that
-    fit in one (1024 x 1024 x 8192: 64 tiles of 128 x 128, two K pieces with a
-    workspace); where those would need a second wave (2048^2) pairs stay."""
-    p = plan("bf16", 1024, 1024, 8192, workspace_bytes=WS)
+    fit in one (1024 x 1024 x 4096: 64 tiles of 128 x 128, two K pieces with a
+    workspace); where those would need a second wave (2048^2) pairs stay.  With
+    K >= 8192, 16-bit inputs and M > 256, pair tiles 128 wide run instead when
+    they fit in one wave (1024 x 1024 x 8192: 32 pair tiles, two K pieces);
+    FP8 and M <= 256 keep their rules."""
+    p = plan("bf16", 1024, 1024, 4096, workspace_bytes=WS)
     assert (p["pair"], p["tile_q"], p["splits"], p["grid"]) == (0, 128, 2, 128)
     assert plan("bf16", 2048, 2048, 8192)["pair"] == 1
+    p = plan("bf16", 1024, 1024, 8192, workspace_bytes=WS)
+    assert (p["pair"], p["tile_q"], p["splits"], p["grid"]) == (1, 128, 2, 128)
+    assert (plan("e4m3", 1024, 1024, 8192)["pair"], plan("bf16", 1024, 1024, 8192)["pair"]) \
+        == (0, 1)
+    assert plan("bf16", 256, 8192, 8192)["half"] == 1
 
 
 def test_unaligned_operands_repacked_or_load_producer():
