@@ -337,9 +337,14 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
     // Pairs of 64-row halves (option "half" = 3): a CTA pair computes 128 rows
     // of N (64 per CTA, MMA M = 128 over the pair) by 128 or 256 columns of M,
     // each CTA loading its own 64 rows of B and half of the tile's A rows, so
-    // every B row has one reader and a stage is 16 KB (tile width 128).  Each
-    // epilogue warp stores half the tile's columns, so the width must be a
-    // whole number of 64-column chunks per half: 128 or 256.
+    // every B row has one reader and a stage is 16 KB (tile width 128).  The
+    // width is M rounded up to a multiple of 32 (160 to 256; 128 for M <= 128:
+    // width 96 measured level with 128 at M = 80 and 96),
+    // or 128, 192 or 256 when option "tile_q" says so: a pair streams in
+    // lockstep, so every A row a CTA loads past M would cost time (BF16 192 x
+    // 8192 x 8192, graph-replayed on GB300: 30.2 us at width 256, 28.7 at 192).
+    // Each epilogue warp stores half the tile's columns; a half that ends
+    // inside a 64-column chunk has that chunk stored by the lanes.
     // Automatically (option "half" = 0) for 16-bit inputs with 64 < M <= 256
     // where one-CTA small tiles were chosen above (the pair tiles of 256 rows
     // fill less than a wave) and the pairs of halves fit in one wave; they then
@@ -351,7 +356,10 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
     // one-CTA tiles.
     // They must also fill at least three quarters of the pair slots (64 pairs
     // on 152 SMs were measured); fewer leave SMs idle where split-K fills them.
-    const int tq_half = (opt_tq == 128 || opt_tq == 256) ? opt_tq : (M <= 128 ? 128 : 256);
+    const int tq_half = (opt_tq == 128 || opt_tq == 192 || opt_tq == 256) ? opt_tq
+                        : M <= 128                                        ? 128
+                        : M >= 256                                        ? 256
+                                    : static_cast<int>((M + 31) / 32 * 32);
     const int64_t pairs_half = ((N + 127) / 128) * ((M + tq_half - 1) / tq_half);
     const bool auto_halves = opt_half == 0 && small_q != 0 && a.in != InKind::E4M3 && M > 64 &&
                              M <= 256 && g_opt_issuers.load() != 1 && pairs_half <= a.sms / 2 &&
@@ -387,7 +395,11 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
     // 0.986, 3072^3 0.986, 2048 x 2048 x 8192 0.984).
     {
         const int opt_atoms = g_opt_atoms.load();
-        if (p.prod == Producer::Tma) {
+        // Pairs of halves wider than 128 columns keep one atom even when
+        // forced: one such configuration (width 160, two atoms, two issuers,
+        // a five-stage ring) faulted on GB300 with no cause found by reading.
+        const bool wide_halves = p.half && p.pair && p.tile_q > 128;
+        if (p.prod == Producer::Tma && !wide_halves) {
             if (opt_atoms == 2) {
                 p.atoms = 2;
             } else if (opt_atoms == 0 && p.tile_q <= 128) {

@@ -712,29 +712,44 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
             }
         };
 
-        // Writes this warp's packed chunk (rows row0 + lane, columns [x, x + kCols)).
-        auto emit = [&](const uint32_t (&pk)[32], int32_t x, int32_t row0) {
-            const bool in_range = x < prm.rows_q && row0 < prm.rows_p;
+        // Writes this warp's packed chunk: rows row0 + lane, columns [x, x + kCols)
+        // that lie below xlim (min(M, end of the warp's columns): a pair of
+        // halves 192 wide gives each warp 96 columns, so its second chunk ends
+        // halfway, where the other half's columns begin).
+        auto emit = [&](const uint32_t (&pk)[32], int32_t x, int32_t row0, int32_t xlim) {
+            const bool in_range = x < xlim && row0 < prm.rows_p;
             const uint32_t buf = stage0 + (chunk & 1u) * Cfg::kEpiBufBytes;
             ++chunk;
-            if (!prm.direct_store && in_range && x + kCols > prm.rows_q &&
-                (prm.rows_q % kGran) != 0) {
-                // A TMA store writes whole 16-byte granules of the contiguous
-                // dimension, so a chunk that ends inside a granule would spill
-                // into the caller's padding between rows_q and ld_out: store it
-                // element by element.
+            if (!prm.direct_store && in_range && x + kCols > xlim &&
+                (xlim < prm.rows_q || (prm.rows_q % kGran) != 0)) {
+                // A TMA store writes the whole box up to M, and whole 16-byte
+                // granules of the contiguous dimension, so a chunk cut short
+                // by xlim, or one that ends inside a granule (it would spill into
+                // the caller's padding between M and ld_out), is stored by the
+                // lanes: whole granules where they are aligned, the rest element
+                // by element.
                 const int32_t r = row0 + static_cast<int32_t>(lane);
                 if (static_cast<int>(lane) < Cfg::kRowsPerWarp && r < prm.rows_p) {
                     uint8_t* dst = out8 + (static_cast<int64_t>(r) * prm.ld_out + x) * kOB;
-                    const int32_t ncols = prm.rows_q - x;
+                    const int32_t ncols = xlim - x;
+                    const bool al16 = (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        if constexpr (kOB == 2) {
-                            uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
-                            if (2 * j < ncols) d16[2 * j] = static_cast<uint16_t>(pk[j] & 0xFFFFu);
-                            if (2 * j + 1 < ncols) d16[2 * j + 1] = static_cast<uint16_t>(pk[j] >> 16);
-                        } else {
-                            if (j < ncols) reinterpret_cast<uint32_t*>(dst)[j] = pk[j];
+                    for (int gi = 0; gi < 8; ++gi) {
+                        if (al16 && (gi + 1) * kGran <= ncols) {
+                            *reinterpret_cast<uint4*>(dst + 16 * gi) =
+                                make_uint4(pk[4 * gi], pk[4 * gi + 1], pk[4 * gi + 2], pk[4 * gi + 3]);
+                            continue;
+                        }
+#pragma unroll
+                        for (int j = 4 * gi; j < 4 * gi + 4; ++j) {
+                            if constexpr (kOB == 2) {
+                                uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+                                if (2 * j < ncols) d16[2 * j] = static_cast<uint16_t>(pk[j] & 0xFFFFu);
+                                if (2 * j + 1 < ncols)
+                                    d16[2 * j + 1] = static_cast<uint16_t>(pk[j] >> 16);
+                            } else {
+                                if (j < ncols) reinterpret_cast<uint32_t*>(dst)[j] = pk[j];
+                            }
                         }
                     }
                 }
@@ -778,14 +793,14 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
                     const uint32_t v = ld_shared_u32(
                         buf + r * 128u + (lane_off ^ ((static_cast<uint32_t>(r) & 7u) << 4)));
                     uint8_t* dst = out8 + (static_cast<int64_t>(grow) * prm.ld_out + m) * kOB;
-                    if (m + kPerLane - 1 < prm.rows_q) {
+                    if (m + kPerLane - 1 < xlim) {
                         if ((reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
                             *reinterpret_cast<uint32_t*>(dst) = v;
                         } else {
                             reinterpret_cast<uint16_t*>(dst)[0] = static_cast<uint16_t>(v & 0xFFFFu);
                             reinterpret_cast<uint16_t*>(dst)[1] = static_cast<uint16_t>(v >> 16);
                         }
-                    } else if (m < prm.rows_q) {  // 16-bit output only
+                    } else if (m < xlim) {  // 16-bit output only
                         reinterpret_cast<uint16_t*>(dst)[0] = static_cast<uint16_t>(v & 0xFFFFu);
                     }
                 }
@@ -824,6 +839,8 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
                                      wrow * Cfg::kRowsPerWarp);
             const int32_t col0 =
                 w.q_off + (Cfg::kColHalves ? static_cast<int32_t>(quarter >> 1) * wcols : 0);
+            const int32_t xlim = Cfg::kColHalves && col0 + wcols < prm.rows_q ? col0 + wcols
+                                                                              : prm.rows_q;
             const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + b * Cfg::kAccCols;
             if (!SPLIT || w.pieces == 1) {
 #pragma unroll 1
@@ -868,7 +885,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
                             f[j] = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
                         pack(f, pk);
                     }
-                    emit(pk, col0 + c * kCols, row0);
+                    emit(pk, col0 + c * kCols, row0, xlim);
                 }
             } else if constexpr (SPLIT) {
                 // This K piece's partial sums -> workspace, column-major within
@@ -929,7 +946,7 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
                     }
                     uint32_t pk[32];
                     pack(f, pk);
-                    emit(pk, col0 + c * kCols, row0);
+                    emit(pk, col0 + c * kCols, row0, xlim);
                 }
                 release_acc(b);
             }

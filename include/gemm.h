@@ -274,8 +274,10 @@ int gemm_read_watchdog(int reset);
  *   "half"        64-row tiles: 0 or 2 never (default); 1 one CTA per 64 rows of N
  *                 (MMA M = 64) wherever single-CTA TMA tiles with FP32 accumulation
  *                 run; 3 CTA pairs of 64-row halves (128 rows of N per pair, MMA
- *                 M = 128 over the pair, tile width 128 or 256 along M) wherever
- *                 TMA tiles with FP32 accumulation run.  They never split K
+ *                 M = 128 over the pair, tile width along M: "tile_q" when that is
+ *                 128, 192 or 256, else M rounded up to a multiple of 32, from 160
+ *                 to 256, and 128 for M <= 128) wherever TMA tiles with FP32
+ *                 accumulation run.  They never split K
  *   "issuers"     MMA-issuing warps per CTA, taking alternate K stages into
  *                 accumulators of their own that the epilogue adds: 0 auto (default: two
  *                 for one-CTA TMA tiles of at most 64 columns that run unsplit in one
@@ -283,7 +285,8 @@ int gemm_read_watchdog(int reset);
  *                 one-CTA TMA tiles of at most 128 columns run unsplit
  *   "atoms"       K depth of a ring stage in 128-byte swizzle spans: 0 auto
  *                 (default), 1, or 2 (twice the K per stage and per MMA commit, half
- *                 as many stages; TMA tiles only)
+ *                 as many stages; TMA tiles only, and not pairs of 64-row halves
+ *                 wider than 128 columns, which keep 1)
  *   "tail"        the last, partial wave of tiles: 0 auto (default) cuts its tiles
  *                 into 2 or 4 narrower ones when that ends it sooner, 1 never, 2 or
  *                 4 always

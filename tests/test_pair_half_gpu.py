@@ -1,14 +1,15 @@
 """GPU parity of pairs of 64-row halves against the CPU oracle, through the C ABI.
 
 A CTA pair computes 128 rows of N (64 per CTA, tcgen05.mma cta_group::2 with
-M = 128) by 128 or 256 columns of M.  Each CTA holds its 64 rows for all the
-tile's columns, row r and column n in TMEM lane r + 64 (n / (width / 2)),
+M = 128) by 128, 192 or 256 columns of M.  Each CTA holds its 64 rows for all
+the tile's columns, row r and column n in TMEM lane r + 64 (n / (width / 2)),
 column n % (width / 2), so each epilogue warp stores 32 rows of one half of
-the columns.  These cases cover that mapping on every input kind and output
-type, both tile widths, ragged edges in M, N and K (a partial last pair tile,
-and a pair whose second CTA lies past N), leading dimensions that take the
-row-wise store path, +-1 inputs (exact), and few CTA pairs that each walk many
-tiles (ring and accumulator phases)."""
+the columns (96 for width 192: one whole 64-column chunk and one cut at the
+half's end, which the lanes store).  These cases cover that mapping on every
+input kind and output type, all three tile widths, ragged edges in M, N and K
+(a partial last pair tile, and a pair whose second CTA lies past N or past M),
+leading dimensions that take the row-wise store path, +-1 inputs (exact), and
+few CTA pairs that each walk many tiles (ring and accumulator phases)."""
 import pytest
 import torch
 
@@ -133,3 +134,130 @@ def test_two_issuers_pm1_bitexact(ctas, pair_halves):
     C = run_tn("bf16", ops, M, N, K)
     exact = oracle.gemm_tn("bf16", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
     assert_codes_equal(out_codes(C, M, N), exact_codes("bf16", exact))
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("issuers", [1, 2])
+@pytest.mark.parametrize("M", [192, 150, 97, 250])
+def test_width_192_pm1_bitexact(kind, issuers, M, pair_halves):
+    """Width 192: 96 columns per half.  M = 150 ends inside a 16-byte granule
+    of the second half; M = 97 leaves the second CTA one row of A; M = 250
+    adds a second column of tiles 58 wide.  N = 1000 ends inside a pair."""
+    pair_halves("tile_q", 192)
+    pair_halves("issuers", issuers)
+    N, K = 1000, 2048
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, p = capi.gemm_tn_plan(kind, M, N, K, sms=sms)
+    assert st == 0 and (p["pair"], p["half"], p["tile_q"], p["atoms"]) == (1, 1, 192, 1), p
+    assert p["issuers"] == issuers, p
+    ops = si.tn_operands(kind, M, N, K, dist="pm1", seed=M + issuers)
+    C = run_tn(kind, ops, M, N, K)
+    exact = oracle.gemm_tn(kind, M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+    assert_codes_equal(out_codes(C, M, N), exact_codes(kind, exact))
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("shape", [(192, 8192, 512), (180, 700, 300), (129, 130, 1000)])
+def test_width_192_random(kind, shape, pair_halves):
+    pair_halves("tile_q", 192)
+    M, N, K = shape
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=M + N + K + 2, sigma=0.5)
+    C = run_tn(kind, ops, M, N, K)
+    check_full(kind, ops, M, N, K, C)
+
+
+@pytest.mark.parametrize("M,ldc", [(192, 200), (137, 140), (191, 194)])
+def test_width_192_padding_and_row_wise_stores(M, ldc, pair_halves):
+    """ldc = 200 keeps C rows 16-byte aligned (TMA stores, lanes for the cut
+    chunk); 140 and 194 with 16-bit output do not (row-wise stores).  The
+    padding between M and ldc keeps its sentinel."""
+    pair_halves("tile_q", 192)
+    N, K = 333, 200
+    ops = si.tn_operands("bf16", M, N, K, dist="normal", seed=ldc)
+    C = run_tn("bf16", ops, M, N, K, ldc=ldc)
+    check_full("bf16", ops, M, N, K, C)
+    assert torch.all(torch.isnan(C[:N, M:].float())), "C padding was written"
+
+
+@pytest.mark.parametrize("ctas", [2, 6])
+def test_width_192_few_pairs_walk_many_tiles(ctas, pair_halves):
+    pair_halves("tile_q", 192)
+    pair_halves("max_ctas", ctas)
+    M, N, K = 400, 1200, 700
+    ops = si.tn_operands("f16", M, N, K, dist="pm1", seed=ctas + 20)
+    C = run_tn("f16", ops, M, N, K)
+    exact = oracle.gemm_tn("f16", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+    assert_codes_equal(out_codes(C, M, N), exact_codes("f16", exact))
+
+
+def test_width_192_fp8_f32_output(pair_halves):
+    """FP32 output: three whole 32-column chunks per half, nothing cut."""
+    import numpy as np
+    from test_fp8_f32out_gpu import run, tols
+
+    pair_halves("tile_q", 192)
+    M, N, K = 170, 520, 384
+    ops = si.tn_operands("e4m3", M, N, K, dist="normal", seed=M)
+    C = run(ops, M, N, K)
+    exact = oracle.gemm_tn("e4m3", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K,
+                           ops["scale_a"], ops["scale_b"])
+    a = ops["A"][:, :K].to(torch.float64).numpy() * ops["scale_a"]
+    b = ops["B"][:, :K].to(torch.float64).numpy() * ops["scale_b"]
+    contract, tight = tols(ops, K, exact, np.abs(a) @ np.abs(b).T)
+    err = np.abs(C[:N, :M].double().numpy().T - exact)
+    assert err.max() <= contract and np.all(err <= tight)
+
+
+def test_width_192_skinny_sampled(pair_halves):
+    pair_halves("tile_q", 192)
+    M, N, K = 192, 8192, 8192
+    ops = si.tn_operands("bf16", M, N, K, dist="normal", seed=9, sigma=0.05)
+    C = run_tn("bf16", ops, M, N, K)
+    check_sampled("bf16", ops, M, N, K, C, seed=4)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("issuers", [1, 2])
+@pytest.mark.parametrize("M,width", [(100, 128), (140, 160), (160, 160), (210, 224),
+                                     (224, 224)])
+def test_width_from_m_pm1_bitexact(kind, issuers, M, width, pair_halves):
+    """Without a tile_q option the width is M rounded up to a multiple of 32
+    (128 for M <= 128): halves of 80 and 112 columns end 16 or 48 columns into
+    their last 64-column chunk."""
+    pair_halves("issuers", issuers)
+    N, K = 1000, 1000
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, p = capi.gemm_tn_plan(kind, M, N, K, sms=sms)
+    assert st == 0 and (p["pair"], p["half"], p["tile_q"], p["issuers"]) == (1, 1, width, issuers), p
+    ops = si.tn_operands(kind, M, N, K, dist="pm1", seed=M + issuers)
+    C = run_tn(kind, ops, M, N, K)
+    exact = oracle.gemm_tn(kind, M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
+    assert_codes_equal(out_codes(C, M, N), exact_codes(kind, exact))
+
+
+@pytest.mark.parametrize("M,ldc", [(150, 152), (150, 153), (211, 216), (211, 213), (137, 138)])
+def test_width_from_m_padding_and_row_wise_stores(M, ldc, pair_halves):
+    N, K = 300, 300
+    ops = si.tn_operands("f16", M, N, K, dist="normal", seed=ldc + 1)
+    C = run_tn("f16", ops, M, N, K, ldc=ldc)
+    check_full("f16", ops, M, N, K, C)
+    assert torch.all(torch.isnan(C[:N, M:].float())), "C padding was written"
+
+
+@pytest.mark.parametrize("M", [150, 220])
+def test_width_from_m_fp8_f32_output(M, pair_halves):
+    """FP32 output, 32-column chunks: halves of 80 and 112 columns end 16
+    columns into their last chunk."""
+    import numpy as np
+    from test_fp8_f32out_gpu import run, tols
+
+    N, K = 520, 384
+    ops = si.tn_operands("e4m3", M, N, K, dist="normal", seed=M + 1)
+    C = run(ops, M, N, K)
+    exact = oracle.gemm_tn("e4m3", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K,
+                           ops["scale_a"], ops["scale_b"])
+    a = ops["A"][:, :K].to(torch.float64).numpy() * ops["scale_a"]
+    b = ops["B"][:, :K].to(torch.float64).numpy() * ops["scale_b"]
+    contract, tight = tols(ops, K, exact, np.abs(a) @ np.abs(b).T)
+    err = np.abs(C[:N, :M].double().numpy().T - exact)
+    assert err.max() <= contract and np.all(err <= tight)

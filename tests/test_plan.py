@@ -220,14 +220,32 @@ def test_noalloc_split_rules(options):
 
 def test_issuers_and_pair_halves_rules(options):
     """Skinny shapes: 16-bit inputs with 64 < M <= 256 run pairs of 64-row
-    halves (128 rows of N per pair) with two MMA issuers when they fit in one
-    wave; FP8 and other one-wave skinny shapes run one-CTA tiles, with two
+    halves (128 rows of N per pair, tile width M rounded up to a multiple of
+    32) with two MMA issuers when they fit in one wave; an explicit tile_q of
+    128, 192 or 256 sets the width.  FP8 and other one-wave skinny shapes run
+    one-CTA tiles, with two
     issuers when the tiles are at most 64 columns wide and unsplit.  Option
     "issuers" = 1 turns both off; 2 forces two on one-CTA tiles of at most 128
     columns; "half" = 2 keeps one-CTA tiles."""
-    for M, tq in ((128, 128), (200, 256), (256, 256)):
+    for M, tq in ((65, 128), (100, 128), (128, 128), (129, 160), (192, 192),
+                  (200, 224), (225, 256), (256, 256)):
         p = plan("bf16", M, 8192, 8192, workspace_bytes=WS)
         assert (p["pair"], p["half"], p["issuers"], p["tile_q"], p["grid"]) == (1, 1, 2, tq, 128), M
+    for forced in (128, 192, 256):
+        options("tile_q", forced)
+        assert plan("bf16", 150, 8192, 8192, workspace_bytes=WS)["tile_q"] == forced
+    options("tile_q", 0)
+    # two K atoms per stage: halves up to 128 wide take them by themselves;
+    # wider halves keep one atom even when forced
+    assert plan("bf16", 128, 8192, 8192, workspace_bytes=WS)["atoms"] == 2
+    assert plan("bf16", 160, 8192, 8192, workspace_bytes=WS)["atoms"] == 1
+    options("atoms", 2)
+    for M, atoms in ((100, 2), (160, 1), (192, 1), (256, 1)):
+        assert plan("bf16", M, 8192, 8192, workspace_bytes=WS)["atoms"] == atoms, M
+    options("half", 2)
+    assert plan("bf16", 256, 8192, 8192, workspace_bytes=WS)["atoms"] == 2  # one-CTA tiles
+    options("half", 0)
+    options("atoms", 0)
     p = plan("e4m3", 128, 8192, 8192, workspace_bytes=WS)   # FP8: 128 tiles of 128 x 64
     assert (p["pair"], p["half"], p["issuers"], p["tile_q"], p["splits"]) == (0, 0, 2, 64, 1)
     assert plan("bf16", 64, 8192, 8192, workspace_bytes=WS)["half"] == 0     # M <= 64
