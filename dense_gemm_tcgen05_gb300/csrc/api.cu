@@ -338,15 +338,15 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
     // of N (64 per CTA, MMA M = 128 over the pair) by 128 or 256 columns of M,
     // each CTA loading its own 64 rows of B and half of the tile's A rows, so
     // every B row has one reader and a stage is 16 KB (tile width 128).  The
-    // width is M rounded up to a multiple of 32 (160 to 256; 128 for M <= 128:
-    // width 96 measured level with 128 at M = 80 and 96),
+    // width is 32 or 64 for M up to that, 128 for M <= 128 (width 96 measured
+    // level with 128 at M = 80 and 96), else M rounded up to a multiple of 32,
     // or 128, 192 or 256 when option "tile_q" says so: a pair streams in
     // lockstep, so every A row a CTA loads past M would cost time (BF16 192 x
     // 8192 x 8192, graph-replayed on GB300: 30.2 us at width 256, 28.7 at 192).
     // Each epilogue warp stores half the tile's columns; a half that ends
     // inside a 64-column chunk has that chunk stored by the lanes.
     // Automatically (option "half" = 0) for 16-bit inputs with 64 < M <= 256
-    // where one-CTA small tiles were chosen above (the pair tiles of 256 rows
+    // (M <= 64: below) where one-CTA small tiles were chosen above (the pair tiles of 256 rows
     // fill less than a wave) and the pairs of halves fit in one wave; they then
     // run with two MMA issuers (below).  Measured on GB300 against the one-CTA
     // 64- or 128-column tiles with two issuers (paired A/B): BF16 M x 8192 x 8192
@@ -357,12 +357,21 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
     // They must also fill at least three quarters of the pair slots (64 pairs
     // on 152 SMs were measured); fewer leave SMs idle where split-K fills them.
     const int tq_half = (opt_tq == 128 || opt_tq == 192 || opt_tq == 256) ? opt_tq
+                        : M <= 32                                         ? 32
+                        : M <= 64                                         ? 64
                         : M <= 128                                        ? 128
                         : M >= 256                                        ? 256
                                     : static_cast<int>((M + 31) / 32 * 32);
     const int64_t pairs_half = ((N + 127) / 128) * ((M + tq_half - 1) / tq_half);
-    const bool auto_halves = opt_half == 0 && small_q != 0 && a.in != InKind::E4M3 && M > 64 &&
-                             M <= 256 && g_opt_issuers.load() != 1 && pairs_half <= a.sms / 2 &&
+    // For M <= 64 (halves 32 or 64 wide) only without a workspace: then K
+    // cannot be split and the one-CTA tiles fill half the SMs (BF16 16 x 8192 x
+    // 8192 27.3 -> 25.0 us, 64 x 8192 x 8192 28.4 -> 25.6); with one, the
+    // split one-CTA tiles are level at K = 8192 and 6 % faster at K = 16384.
+    // (A forced tile width they cannot take, 16 to 64, keeps one-CTA tiles.)
+    const bool auto_halves = opt_half == 0 && small_q != 0 && a.in != InKind::E4M3 &&
+                             (opt_tq == 0 || opt_tq >= 128) &&
+                             (M > 64 || !a.has_scratch) && M <= 256 &&
+                             g_opt_issuers.load() != 1 && pairs_half <= a.sms / 2 &&
                              4 * pairs_half >= 3 * (a.sms / 2);
     if ((opt_half == 3 || auto_halves) && p.prod == Producer::Tma && !a.acc16) {
         p.pair = true;
@@ -395,11 +404,11 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
     // 0.986, 3072^3 0.986, 2048 x 2048 x 8192 0.984).
     {
         const int opt_atoms = g_opt_atoms.load();
-        // Pairs of halves wider than 128 columns keep one atom even when
-        // forced: one such configuration (width 160, two atoms, two issuers,
-        // a five-stage ring) faulted on GB300 with no cause found by reading.
-        const bool wide_halves = p.half && p.pair && p.tile_q > 128;
-        if (p.prod == Producer::Tma && !wide_halves) {
+        // Pairs of halves other than 128 wide keep one atom even when forced:
+        // one such configuration (width 160, two atoms, two issuers, a
+        // five-stage ring) faulted on GB300 with no cause found by reading.
+        const bool one_atom_halves = p.half && p.pair && p.tile_q != 128;
+        if (p.prod == Producer::Tma && !one_atom_halves) {
             if (opt_atoms == 2) {
                 p.atoms = 2;
             } else if (opt_atoms == 0 && p.tile_q <= 128) {
@@ -576,6 +585,13 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
     // issuers they measured slower than one-CTA tiles on every skinny shape
     // tried (BF16 128 x 8192 x 8192: 35.0 against 30.7 us)
     if (opt_iss != 1 && p.pair && p.half && p.prod == Producer::Tma && !a.acc16) p.issuers = 2;
+    // Two issuers with two K atoms per stage get an even ring depth, so that
+    // every ring slot is always consumed (and released) by the same issuer.
+    // Both faults this configuration family raised on GB300 (unspecified
+    // launch failures, no cause found by reading) ran five-stage rings, where
+    // consecutive uses of a slot alternate between the issuers; the same
+    // alternation with one atom per stage ran thousands of launches clean.
+    if (p.issuers > 1 && p.atoms == 2 && (p.stages & 1) && p.stages > 2) --p.stages;
     return p;
 }
 

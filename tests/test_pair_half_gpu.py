@@ -218,24 +218,28 @@ def test_width_192_skinny_sampled(pair_halves):
 
 @pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("issuers", [1, 2])
-@pytest.mark.parametrize("M,width", [(100, 128), (140, 160), (160, 160), (210, 224),
+@pytest.mark.parametrize("M,width", [(1, 32), (16, 32), (20, 32), (32, 32), (33, 64), (48, 64),
+                                     (64, 64), (100, 128), (140, 160), (160, 160), (210, 224),
                                      (224, 224)])
 def test_width_from_m_pm1_bitexact(kind, issuers, M, width, pair_halves):
-    """Without a tile_q option the width is M rounded up to a multiple of 32
-    (128 for M <= 128): halves of 80 and 112 columns end 16 or 48 columns into
-    their last 64-column chunk."""
+    """Without a tile_q option the width is 32 or 64 for M up to that, 128 up
+    to 128, else M rounded up to a multiple of 32: halves of 16, 32, 80 and
+    112 columns end inside their only or last 64-column chunk (16-bit output);
+    widths 32 and 64 run one K atom per stage."""
     pair_halves("issuers", issuers)
     N, K = 1000, 1000
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     st, p = capi.gemm_tn_plan(kind, M, N, K, sms=sms)
     assert st == 0 and (p["pair"], p["half"], p["tile_q"], p["issuers"]) == (1, 1, width, issuers), p
+    assert p["atoms"] == (2 if width == 128 else 1), p
     ops = si.tn_operands(kind, M, N, K, dist="pm1", seed=M + issuers)
     C = run_tn(kind, ops, M, N, K)
     exact = oracle.gemm_tn(kind, M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K)
     assert_codes_equal(out_codes(C, M, N), exact_codes(kind, exact))
 
 
-@pytest.mark.parametrize("M,ldc", [(150, 152), (150, 153), (211, 216), (211, 213), (137, 138)])
+@pytest.mark.parametrize("M,ldc", [(150, 152), (150, 153), (211, 216), (211, 213), (137, 138),
+                                   (20, 24), (20, 21), (40, 48), (57, 59)])
 def test_width_from_m_padding_and_row_wise_stores(M, ldc, pair_halves):
     N, K = 300, 300
     ops = si.tn_operands("f16", M, N, K, dist="normal", seed=ldc + 1)
@@ -244,10 +248,10 @@ def test_width_from_m_padding_and_row_wise_stores(M, ldc, pair_halves):
     assert torch.all(torch.isnan(C[:N, M:].float())), "C padding was written"
 
 
-@pytest.mark.parametrize("M", [150, 220])
+@pytest.mark.parametrize("M", [20, 50, 150, 220])
 def test_width_from_m_fp8_f32_output(M, pair_halves):
-    """FP32 output, 32-column chunks: halves of 80 and 112 columns end 16
-    columns into their last chunk."""
+    """FP32 output, 32-column chunks: halves of 16, 80 and 112 columns end 16
+    columns into their only or last chunk; halves of 32 fill one."""
     import numpy as np
     from test_fp8_f32out_gpu import run, tols
 
@@ -261,3 +265,12 @@ def test_width_from_m_fp8_f32_output(M, pair_halves):
     contract, tight = tols(ops, K, exact, np.abs(a) @ np.abs(b).T)
     err = np.abs(C[:N, :M].double().numpy().T - exact)
     assert err.max() <= contract and np.all(err <= tight)
+
+
+@pytest.mark.parametrize("kind,M", [("bf16", 16), ("f16", 64), ("e4m3", 32)])
+def test_narrow_widths_skinny_sampled(kind, M, pair_halves):
+    N, K = 8192, 8192
+    ops = si.tn_operands(kind, M, N, K, dist="normal", seed=M, sigma=1.0 if kind == "e4m3"
+                         else 0.05)
+    C = run_tn(kind, ops, M, N, K)
+    check_sampled(kind, ops, M, N, K, C, seed=5)

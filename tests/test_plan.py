@@ -72,32 +72,40 @@ def test_tail_options(options):
                                  (129, 128)])
 def test_skinny_single_cta_tiles_and_width(M, q, kind, options):
     """Decode-like shapes: single-CTA 128-row tiles, 16/32 columns when M fits
-    in one such tile, else 64 (M <= 128) or 128.  (16-bit inputs with M > 64
-    run pairs of 64-row halves instead unless option "half" = 2.)"""
-    if kind == "bf16" and M > 64:
+    in one such tile, else 64 (M <= 128) or 128.  (16-bit inputs with M > 64,
+    or M <= 64 without a workspace, run pairs of 64-row halves instead unless
+    option "half" = 2.)"""
+    if kind == "bf16":
         options("half", 2)
     p = plan(kind, M, 8192, 8192)
     assert p["pair"] == 0 and p["tile_q"] == q and p["tiles_p"] == 64
 
 
-def test_skinny_split_k_needs_a_workspace():
+def test_skinny_split_k_needs_a_workspace(options):
     """64 tiles on 152 SMs: two K pieces each with a workspace (128 CTAs; 32
-    stages of two K atoms each), one wave of 64 CTAs without."""
+    stages of two K atoms each); without one, 64 pairs of 64-row halves 32
+    wide (128 CTAs, K whole), or 64 one-CTA tiles when halves are off."""
     p = plan("bf16", 16, 8192, 8192, workspace_bytes=WS)
     assert (p["splits"], p["kb_per_split"], p["grid"], p["atoms"]) == (2, 32, 128, 2)
     p = plan("bf16", 16, 8192, 8192)
-    assert (p["splits"], p["grid"]) == (1, 64)
+    assert (p["splits"], p["pair"], p["half"], p["tile_q"], p["grid"]) == (1, 1, 1, 32, 128)
+    options("half", 2)
+    p = plan("bf16", 16, 8192, 8192)
+    assert (p["splits"], p["pair"], p["grid"]) == (1, 0, 64)
 
 
 def test_narrow_ring_is_deeper(options):
-    """A 16-column tile's one-atom stage holds 16 KB of B and 2 KB of A: 10
-    stages of 18 KB in the 192 KB ring, against 8 of 24 KB at 64 columns;
-    with two atoms per stage (the automatic choice there), 5 of 36 KB and 4 of
-    48 KB."""
-    assert (plan("bf16", 16, 8192, 8192)["stages"], plan("bf16", 16, 8192, 8192)["stage_bytes"]) \
-        == (5, 36 * 1024)
-    assert (plan("bf16", 64, 8192, 8192)["stages"], plan("bf16", 64, 8192, 8192)["stage_bytes"]) \
-        == (4, 48 * 1024)
+    """A 16-column one-CTA tile's one-atom stage holds 16 KB of B and 2 KB of
+    A: 10 stages of 18 KB in the 192 KB ring, against 8 of 24 KB at 64
+    columns; with two atoms per stage (the automatic choice there), 5 of 36 KB
+    and 4 of 48 KB (K split, one issuer)."""
+    def ring(M):
+        p = plan("bf16", M, 8192, 8192, workspace_bytes=WS)
+        assert p["pair"] == 0 and p["issuers"] == 1, p
+        return p["stages"], p["stage_bytes"]
+    assert ring(16) == (5, 36 * 1024)
+    assert ring(64) == (4, 48 * 1024)
+    options("half", 2)
     options("atoms", 1)
     assert (plan("bf16", 16, 8192, 8192)["stages"], plan("bf16", 16, 8192, 8192)["stage_bytes"]) \
         == (10, 18 * 1024)
@@ -184,7 +192,11 @@ def test_fp8_stages_and_tail():
 
 
 def test_64_row_tiles_only_when_forced(options):
-    assert plan("bf16", 16, 8192, 8192)["half"] == 0
+    """One CTA per 64 rows of N (MMA M = 64) only with option "half" = 1;
+    pairs of 64-row halves (pair = 1) are another plan."""
+    assert plan("bf16", 16, 8192, 8192, workspace_bytes=WS)["half"] == 0
+    p = plan("bf16", 16, 8192, 8192)
+    assert p["half"] == 0 or p["pair"] == 1
     options("half", 1)
     p = plan("bf16", 16, 8192, 8192, workspace_bytes=WS)
     assert (p["half"], p["tiles_p"], p["splits"], p["grid"]) == (1, 128, 1, 128)
@@ -248,7 +260,12 @@ def test_issuers_and_pair_halves_rules(options):
     options("atoms", 0)
     p = plan("e4m3", 128, 8192, 8192, workspace_bytes=WS)   # FP8: 128 tiles of 128 x 64
     assert (p["pair"], p["half"], p["issuers"], p["tile_q"], p["splits"]) == (0, 0, 2, 64, 1)
-    assert plan("bf16", 64, 8192, 8192, workspace_bytes=WS)["half"] == 0     # M <= 64
+    assert plan("bf16", 64, 8192, 8192, workspace_bytes=WS)["half"] == 0     # M <= 64: split
+    for M, tq in ((1, 32), (16, 32), (32, 32), (48, 64), (64, 64)):           # no workspace
+        p = plan("bf16", M, 8192, 8192)
+        assert (p["pair"], p["half"], p["tile_q"], p["issuers"], p["atoms"]) == (1, 1, tq, 2, 1), M
+    assert plan("e4m3", 16, 8192, 8192)["half"] == 0                         # FP8
+    assert plan("bf16", 16, 4096, 8192)["half"] == 0                         # half a wave
     assert plan("bf16", 16, 8192, 8192, workspace_bytes=WS)["issuers"] == 1  # split K
     assert plan("bf16", 8192, 8192, 8192)["issuers"] == 1                    # CTA pairs
     p = plan("f16_acc16", 128, 8192, 8192)                                   # FP16 accumulation
@@ -328,3 +345,28 @@ def test_last_wave_cost_model(kind):
     assert (p["tiles_p"], p["tiles_q"], p["tail_f"], p["tail_ksplit"]) == (86, 1, 4, 0)
     p = plan(kind, 256, 256 * 146, 4096)
     assert (p["tiles_p"], p["tail_f"]) == (146, 1)
+
+
+def test_two_issuers_with_two_atoms_get_an_even_ring(options):
+    """Two MMA issuers with two K atoms per stage: the ring depth is rounded
+    down to an even count, so each slot always belongs to one issuer."""
+    shapes = [("bf16", 16, 16384, 8192), ("bf16", 16, 8192, 8192), ("bf16", 64, 14336, 4096),
+              ("e4m3", 16, 16384, 8192), ("f16", 128, 8192, 8192), ("bf16", 32, 16384, 8192)]
+    seen = 0
+    for kind, M, N, K in shapes:
+        for ws in (0, WS):
+            p = plan(kind, M, N, K, workspace_bytes=ws)
+            if p["issuers"] == 2 and p["atoms"] == 2:
+                assert p["stages"] % 2 == 0, (kind, M, N, K, p)
+                seen += 1
+    assert seen >= 6
+    # one-CTA 16-wide tiles: 36 KB stages, five fit; the two-issuer plan keeps four
+    p = plan("bf16", 16, 16384, 8192, workspace_bytes=WS)
+    assert (p["pair"], p["tile_q"], p["issuers"], p["atoms"], p["stages"]) == (0, 16, 2, 2, 4)
+    # one issuer (the split plan) keeps all five
+    p = plan("bf16", 16, 8192, 8192, workspace_bytes=WS)
+    assert (p["splits"], p["issuers"], p["atoms"], p["stages"]) == (2, 1, 2, 5)
+    options("issuers", 2)
+    options("pair", 0)
+    p = plan("bf16", 100, 1100, 1000)                   # 64 KB stages: three fit, two run
+    assert (p["tile_q"], p["issuers"], p["atoms"], p["stages"]) == (128, 2, 2, 2)
