@@ -777,7 +777,9 @@ def per_config(stream, stream_h, burst, hbm, workspace, launches=20):
     copy bandwidth, and the same calls replayed as a CUDA graph (graph_us,
     graph_gbs, hbm_frac_graph: the steady state of a stream of calls, where a
     call's prologue overlaps the end of the one before) with cuBLAS replayed
-    the same way beside them (16-bit inputs).  The tight-leading-dimension
+    the same way beside them (16-bit inputs: torch's linear, whose M x N
+    row-major output is the transpose of this library's layout, and matmul
+    into this library's layout).  The tight-leading-dimension
     BF16 shapes are timed again without a workspace (the load-based producer
     reads them in place)."""
     import torch
@@ -809,11 +811,21 @@ def per_config(stream, stream_h, burst, hbm, workspace, launches=20):
             out[key]["graph_us"] = round(gm * 1e3, 2)
             out[key]["graph_gbs"] = round(byts / (gm * 1e-3) / 1e9)
             if kind != "e4m3" and not f32:
+                # linear writes C as M x N row-major, the transpose of this
+                # library's layout, and cuBLAS then picks its kernel for that
+                # problem; matmul into the (N, M) buffer keeps this library's
+                # layout (C = B A^T row-major, i.e. column-major M x N).
                 def lin(a, b, _c):
                     torch.nn.functional.linear(a, b)
+
+                def same_layout(a, b, c):
+                    torch.matmul(b, a.t(), out=c)
                 cm = graph_time(lin, s, 2 * len(s) * max(1, 10 // len(s)), stream)
                 out[key]["cublas_graph_us"] = round(cm * 1e3, 2)
                 out[key]["cublas_over_this"] = round(cm / gm, 3)
+                cs = graph_time(same_layout, s, 2 * len(s) * max(1, 10 // len(s)), stream)
+                out[key]["cublas_same_layout_graph_us"] = round(cs * 1e3, 2)
+                out[key]["cublas_same_layout_over_this"] = round(cs / gm, 3)
         del s, o
         torch.cuda.empty_cache()
         return key, gbs

@@ -72,6 +72,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<int> g_opt_pair{-1};
 std::atomic<int> g_opt_group{0};
 std::atomic<int> g_opt_k_snake{1};
+std::atomic<int> g_opt_k_rotate{0};
 std::atomic<int> g_opt_band_snake{1};
 std::atomic<int> g_opt_path{0};
 std::atomic<int> g_opt_max_ctas{0};
@@ -793,6 +794,21 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
     L.prm.tiles_q = static_cast<int32_t>(tiles_q);
     L.prm.group = g_opt_group.load() > 0 ? g_opt_group.load() : kDefaultGroup;
     L.prm.k_snake = g_opt_k_snake.load();
+    // K rotation (option "k_rotate"): automatically for the unsplit skinny
+    // plans that run two MMA issuers (one-CTA tiles up to 64 wide in one wave,
+    // pairs of 64-row halves), whose units all stream their own rows of B at
+    // once.  Measured on GB300 (graph-replayed BF16, paired A/B, in order ->
+    // rotated): 128 x 8192 x 8192 26.65 -> 26.18 us, 192x 29.36 -> 28.78, 256x
+    // 31.42 -> 31.00, 64 x 14336 x 4096 21.91 -> 21.36, 256 x 8192 x 16384
+    // 56.89 -> 56.14; split plans level (16 x 8192 x 8192) or slower (1024 x
+    // 1024 x 8192 pairs, 19.64 -> 20.21).
+    {
+        const int opt_rot = g_opt_k_rotate.load();
+        L.prm.k_rotate =
+            opt_rot == 2 || (opt_rot == 0 && pl.issuers > 1 && pl.splits == 1 && !pl.tail_ksplit)
+                ? 1
+                : 0;
+    }
     L.prm.band_snake = g_opt_band_snake.load();
     L.prm.scale = scale;
     L.prm.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
@@ -857,11 +873,12 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
         std::fprintf(stderr,
                      "[gemm] tn in=%d M=%lld N=%lld K=%lld pair=%d producer=%d direct_store=%d "
                      "splits=%d tile_q=%d tail=%d ktail=%d stages=%d tiles=%lldx%lld grid=%d "
-                     "half=%d issuers=%d\n",
+                     "half=%d issuers=%d atoms=%d k_rotate=%d\n",
                      int(in), (long long)M, (long long)N, (long long)K, int(pair), int(prod),
                      L.prm.direct_store, L.prm.splits, L.prm.tile_q, L.prm.tail_f,
                      L.prm.tail_ksplit, L.prm.stages,
-                     (long long)tiles_q, (long long)tiles_p, L.grid, int(L.half), L.issuers);
+                     (long long)tiles_q, (long long)tiles_p, L.grid, int(L.half), L.issuers,
+                     L.prm.atoms, L.prm.k_rotate);
     e = tc_launch(in, pair, prod, out_f32, L);
     return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
 }
@@ -1099,6 +1116,9 @@ int gemm_set_option(const char* name, int64_t value) {
     } else if (!std::strcmp(name, "k_snake")) {
         if (value < 0 || value > 1) return GEMM_ERR_INVALID_OPTION;
         g_opt_k_snake.store(static_cast<int>(value));
+    } else if (!std::strcmp(name, "k_rotate")) {
+        if (value < 0 || value > 2) return GEMM_ERR_INVALID_OPTION;
+        g_opt_k_rotate.store(static_cast<int>(value));
     } else if (!std::strcmp(name, "band_snake")) {
         if (value < 0 || value > 1) return GEMM_ERR_INVALID_OPTION;
         g_opt_band_snake.store(static_cast<int>(value));

@@ -83,6 +83,11 @@ struct TcParams {
     int32_t k_snake;
     // 1: odd rasteriser bands walk the tile columns backwards (raster.h).
     int32_t band_snake;
+    // 1: the TMA producer starts each unit's K range at a stage of its own,
+    // spaced over the range by the unit's tile row (tp * stages / tiles_p),
+    // and wraps around, so that concurrent units do not read the same K
+    // offset at the same time (the MMA warp sums stages in any order).
+    int32_t k_rotate;
     // K atoms (128-byte swizzle spans of K) per ring stage, 1 or 2, which
     // selects the kernel instantiation: a stage of two holds P atom 0, P atom
     // 1, Q atom 0, Q atom 1 (each atom of Q q_atom_bytes long, the full tile

@@ -414,7 +414,12 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
             const Unit w = u == first ? u_first : unit_of(u);
             // Every second unit reads its K range backwards (the MMA warp sums
             // the stages in whatever order they arrive).
-            const int32_t k_rev = (prm.k_snake && (lu & 1u)) ? w.kb_lo + w.kb_hi - 1 : -1;
+            const bool k_rev = prm.k_snake && (lu & 1u);
+            const int32_t nkb = w.kb_hi - w.kb_lo;
+            const int32_t k_rot =
+                prm.k_rotate && nkb > 1
+                    ? static_cast<int32_t>(w.tp * static_cast<int64_t>(nkb) / prm.tiles_p % nkb)
+                    : 0;
             const int32_t p0 = static_cast<int32_t>(w.tp * Cfg::kTileP + rank * Cfg::kBlockP);
             const int32_t q0 = w.q_off + static_cast<int32_t>(rank) * (w.width / Cfg::kCG);
             const CUtensorMap* mq = w.narrow ? &map_q_tail : &map_q;
@@ -432,7 +437,9 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
                 if (lane == 0) {
                     const uint32_t sp = base + s * stage_bytes;
                     const uint32_t sq = sp + q_region;
-                    const int32_t kx = (k_rev >= 0 ? k_rev - kb : kb) * stage_k;
+                    int32_t ki = kb - w.kb_lo + k_rot;   // the unit's ki-th K stage
+                    if (ki >= nkb) ki -= nkb;
+                    const int32_t kx = (k_rev ? w.kb_hi - 1 - ki : w.kb_lo + ki) * stage_k;
                     if constexpr (PAIR) {
                         const uint32_t fb = mapa_shared(full_bar(s), 0);
                         if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * tx);

@@ -260,6 +260,13 @@ int gemm_read_watchdog(int reset);
  *                 L2 when the next wave starts on them; 0: always ascending.  The
  *                 summation order of those tiles changes, not the result's
  *                 accuracy; results stay deterministic for a given shape
+ *   "k_rotate"    2: the TMA producer starts each unit at the K stage
+ *                 tp * stages / tiles_p of its range (tp: the unit's tile row)
+ *                 and wraps around; 1: every unit reads its K range in order (or
+ *                 backwards, "k_snake"); 0 (default): 2 for unsplit plans with
+ *                 two MMA issuers (the skinny shapes), else 1.  The summation
+ *                 order changes, not the accuracy; results stay deterministic
+ *                 for a given shape
  *   "path"        0 auto (default), 1 force the CUDA-core kernel, 2 force the
  *                 tensor-core kernel's load-based producer (as for unaligned rows)
  *   "timeout_ns"  device wait limit in ns, 1e6..6e10 (default 2e9).  The longest

@@ -136,6 +136,10 @@ def test_options():
     assert capi.gemm_set_option("band_snake", 2) == capi.GEMM_ERR_INVALID_OPTION
     assert capi.gemm_set_option("band_snake", 0) == 0
     assert capi.gemm_set_option("band_snake", 1) == 0
+    assert capi.gemm_set_option("k_rotate", 3) == capi.GEMM_ERR_INVALID_OPTION
+    assert capi.gemm_set_option("k_rotate", -1) == capi.GEMM_ERR_INVALID_OPTION
+    for v in (2, 1, 0):
+        assert capi.gemm_set_option("k_rotate", v) == 0
     assert capi.gemm_set_option("timeout_ns", 10) == capi.GEMM_ERR_INVALID_OPTION
     assert capi.gemm_set_option("nonsense", 1) == capi.GEMM_ERR_INVALID_OPTION
     assert capi.gemm_set_option("splits", 65) == capi.GEMM_ERR_INVALID_OPTION
