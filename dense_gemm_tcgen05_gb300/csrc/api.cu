@@ -586,13 +586,14 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
     // issuers they measured slower than one-CTA tiles on every skinny shape
     // tried (BF16 128 x 8192 x 8192: 35.0 against 30.7 us)
     if (opt_iss != 1 && p.pair && p.half && p.prod == Producer::Tma && !a.acc16) p.issuers = 2;
-    // Two issuers with two K atoms per stage get an even ring depth, so that
-    // every ring slot is always consumed (and released) by the same issuer.
-    // Both faults this configuration family raised on GB300 (unspecified
-    // launch failures, no cause found by reading) ran five-stage rings, where
-    // consecutive uses of a slot alternate between the issuers; the same
-    // alternation with one atom per stage ran thousands of launches clean.
-    if (p.issuers > 1 && p.atoms == 2 && (p.stages & 1) && p.stages > 2) --p.stages;
+    // Two issuers get an even ring depth, so that every ring slot is always
+    // consumed (and released) by the same issuer.  The three unspecified launch
+    // failures seen on GB300 with several issuers (no cause found by reading)
+    // all ran odd rings, where consecutive uses of a slot alternate between the
+    // issuers and both commit to its barrier: five stages with two K atoms
+    // (twice), nine with one atom and split K.  A ring one stage shorter costs
+    // nothing measurable at these depths.
+    if (p.issuers > 1 && (p.stages & 1) && p.stages > 2) --p.stages;
     return p;
 }
 

@@ -347,19 +347,25 @@ def test_last_wave_cost_model(kind):
     assert (p["tiles_p"], p["tail_f"]) == (146, 1)
 
 
-def test_two_issuers_with_two_atoms_get_an_even_ring(options):
-    """Two MMA issuers with two K atoms per stage: the ring depth is rounded
-    down to an even count, so each slot always belongs to one issuer."""
+def test_two_issuers_get_an_even_ring(options):
+    """Two MMA issuers: the ring depth is rounded down to an even count, so
+    each slot always belongs to one issuer (with one or two K atoms)."""
     shapes = [("bf16", 16, 16384, 8192), ("bf16", 16, 8192, 8192), ("bf16", 64, 14336, 4096),
-              ("e4m3", 16, 16384, 8192), ("f16", 128, 8192, 8192), ("bf16", 32, 16384, 8192)]
-    seen = 0
+              ("e4m3", 16, 16384, 8192), ("f16", 128, 8192, 8192), ("bf16", 32, 16384, 8192),
+              ("bf16", 192, 8192, 8192), ("bf16", 160, 8192, 8192), ("bf16", 250, 8192, 8192),
+              ("f16", 48, 8192, 8192)]
+    seen = {1: 0, 2: 0}
     for kind, M, N, K in shapes:
         for ws in (0, WS):
             p = plan(kind, M, N, K, workspace_bytes=ws)
-            if p["issuers"] == 2 and p["atoms"] == 2:
+            if p["issuers"] == 2:
                 assert p["stages"] % 2 == 0, (kind, M, N, K, p)
-                seen += 1
-    assert seen >= 6
+                seen[p["atoms"]] += 1
+    assert seen[1] >= 4 and seen[2] >= 6, seen
+    p = plan("bf16", 192, 8192, 8192, workspace_bytes=WS)   # 20 KB stages: nine fit, eight run
+    assert (p["half"], p["tile_q"], p["atoms"], p["stages"]) == (1, 192, 1, 8)
+    p = plan("bf16", 16, 8192, 8192)                         # halves 32 wide: 19 fit, 18 run
+    assert (p["half"], p["tile_q"], p["atoms"], p["stages"]) == (1, 32, 1, 18)
     # one-CTA 16-wide tiles: 36 KB stages, five fit; the two-issuer plan keeps four
     p = plan("bf16", 16, 16384, 8192, workspace_bytes=WS)
     assert (p["pair"], p["tile_q"], p["issuers"], p["atoms"], p["stages"]) == (0, 16, 2, 2, 4)
