@@ -61,7 +61,7 @@ GEMM_NOALLOC_SCRATCH_BYTES = 24 << 20
 PLAN_ALIGNED = PLAN_A_TMA | PLAN_B_TMA | PLAN_C_TMA | PLAN_A_128 | PLAN_B_128
 PLAN_FIELDS = ("status", "pair", "producer", "tile_q", "half", "splits", "tail_f", "tail_ksplit",
                "stages", "grid", "copy_a", "copy_b", "tiles_p", "tiles_q",
-               "kb_per_split", "tail_kb_per", "stage_bytes", "issuers", "atoms")
+               "kb_per_split", "tail_kb_per", "stage_bytes", "issuers", "atoms", "ring_epi")
 
 
 class GemmError(RuntimeError):

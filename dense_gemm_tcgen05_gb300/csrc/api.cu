@@ -220,6 +220,7 @@ struct TnPlan {
     int64_t tiles_p = 0, tiles_q = 0, tiles = 0, slots = 0;
     int num_kb = 0, stages = 0, stage_bytes = 0;
     int atoms = 1;              // K atoms (128-byte swizzle spans) per ring stage
+    bool ring_epi = false;      // the ring extends over the epilogue's staging area
     int splits = 1, kb_per_split = 0;
     int64_t split_cnt_bytes = 0;  // counter bytes ahead of the split partials
     int tail_f = 1, tail_kb_per = 0;
@@ -591,9 +592,25 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
     // failures seen on GB300 with several issuers (no cause found by reading)
     // all ran odd rings, where consecutive uses of a slot alternate between the
     // issuers and both commit to its barrier: five stages with two K atoms
-    // (twice), nine with one atom and split K.  A ring one stage shorter costs
-    // nothing measurable at these depths.
+    // (twice), nine with one atom and split K.  The stage given up costs up to
+    // 3 % (pairs of halves 192 wide, 9 -> 8 stages: 28.9 -> 29.9 us), which the
+    // ring wins back below where it can.
     if (p.issuers > 1 && (p.stages & 1) && p.stages > 2) --p.stages;
+    // Where every CTA (or pair) runs one unit, its epilogue starts only after
+    // the ring has drained, so the ring may run on over the epilogue's staging
+    // area (224 KB instead of 192).  These launches stream operands for most
+    // of their time and gain from the loads in flight (the even-ring
+    // measurement above: 12 % fewer bytes in flight cost 3 %).
+    if (p.prod == Producer::Tma && p.tail_f == 1 && !p.tail_ksplit &&
+        p.tiles * p.splits <= p.slots) {
+        int st = (g.stage_region + g.epi_region) / p.stage_bytes;
+        if (st > g.max_stages) st = g.max_stages;
+        if (p.issuers > 1 && (st & 1) && st > 2) --st;
+        if (st > p.stages) {
+            p.stages = st;
+            p.ring_epi = true;
+        }
+    }
     return p;
 }
 
@@ -826,6 +843,7 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
                              d_format);
     L.prm.stage_tx_bytes = static_cast<uint32_t>((g.load_p + load_q) * 128 * pl.atoms);
     L.prm.atoms = pl.atoms;
+    L.prm.ring_epi = pl.ring_epi ? 1 : 0;
     L.prm.q_atom_bytes = static_cast<uint32_t>(load_q * 128);
     L.prm.stages = pl.stages;
     L.prm.stage_bytes = static_cast<uint32_t>(pl.stage_bytes);
@@ -874,12 +892,12 @@ int gemm_tn(InKind in, bool out_f32, int64_t M, int64_t N, int64_t K, const void
         std::fprintf(stderr,
                      "[gemm] tn in=%d M=%lld N=%lld K=%lld pair=%d producer=%d direct_store=%d "
                      "splits=%d tile_q=%d tail=%d ktail=%d stages=%d tiles=%lldx%lld grid=%d "
-                     "half=%d issuers=%d atoms=%d k_rotate=%d\n",
+                     "half=%d issuers=%d atoms=%d k_rotate=%d ring_epi=%d\n",
                      int(in), (long long)M, (long long)N, (long long)K, int(pair), int(prod),
                      L.prm.direct_store, L.prm.splits, L.prm.tile_q, L.prm.tail_f,
                      L.prm.tail_ksplit, L.prm.stages,
                      (long long)tiles_q, (long long)tiles_p, L.grid, int(L.half), L.issuers,
-                     L.prm.atoms, L.prm.k_rotate);
+                     L.prm.atoms, L.prm.k_rotate, L.prm.ring_epi);
     e = tc_launch(in, pair, prod, out_f32, L);
     return e == cudaSuccess ? GEMM_OK : fail_cuda(e);
 }
@@ -1061,7 +1079,8 @@ int gemm_tn_plan(int kind, int64_t M, int64_t N, int64_t K, int flags, int64_t w
                                          pl.tail_kb_per,
                                          pl.stage_bytes,
                                          pl.issuers,
-                                         pl.atoms};
+                                         pl.atoms,
+                                         pl.ring_epi ? 1 : 0};
     for (int i = 0; i < GEMM_PLAN_FIELDS; ++i) out[i] = v[i];
     return GEMM_OK;
 }

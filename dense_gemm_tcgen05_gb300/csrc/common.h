@@ -10,8 +10,10 @@ namespace gb300 {
 
 enum class InKind : int { F16 = 0, BF16 = 1, E4M3 = 2 };
 
-// Watchdog status bits recorded by kernels whose bounded waits ran out.
+// Watchdog status bits recorded by kernels whose bounded waits ran out, or
+// that refused launch parameters breaking one of their invariants.
 constexpr unsigned int kWatchTimeout = 1u;
+constexpr unsigned int kWatchBadParams = 2u;
 
 // Parameters of the persistent tensor-core kernel.  "P" is the operand whose
 // rows become TMEM lanes (the API's B, rows n), "Q" the operand whose rows
@@ -95,6 +97,12 @@ struct TcParams {
     // commit.  The load-based producer takes 1.
     int32_t atoms;
     uint32_t q_atom_bytes;
+    // 1: the ring extends over the epilogue's staging area.  Only for launches
+    // in which every CTA (or pair) runs at most one unit: its epilogue then
+    // starts after the ring has drained (the accumulator-full barrier waits
+    // for every MMA, and every load was consumed by one).  The kernel checks
+    // the unit count and refuses the launch otherwise.
+    int32_t ring_epi;
 };
 
 struct TcLaunch {
@@ -117,6 +125,7 @@ struct TcGeometry {
     uint32_t format;       // A/B format code of the instruction descriptor
     int stage_region;      // shared-memory bytes for the stage ring
     int max_stages;        // barrier slots
+    int epi_region;        // the epilogue's staging bytes, right after the ring
 };
 
 // Operand producer of the tensor-core kernel: TMA tensor copies, or (for rows

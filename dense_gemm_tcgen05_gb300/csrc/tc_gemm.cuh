@@ -107,7 +107,7 @@ struct TcCfg {
     static constexpr int kAccCols = kMmaN;
     static constexpr int kTmemCols = 512;
     static constexpr int kNumBars = 2 * kMaxStages + 4 + 1;
-    static constexpr int kOffEpi = kStageRegion;
+    static constexpr int kOffEpi = kStageRegion;  // a ring with ring_epi runs on into it
     static constexpr int kOffBars = kOffEpi + kEpiBytes;
     static constexpr int kOffTmemSlot = kOffBars + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -277,6 +277,21 @@ __global__ void __launch_bounds__(TcCfg<IN, PAIR, LOADS, HALF, NI>::kThreads, 1)
     static_assert(AT == 1 || (AT == 2 && !LOADS), "two K atoms per stage: TMA producer only");
     constexpr int32_t atoms = AT;                          // K atoms per stage
 
+    // A ring over the epilogue's staging area (ring_epi) needs every CTA (or
+    // pair) to run at most one unit; the planner only asks for it then.  The
+    // check is uniform over the grid, so all CTAs leave together, before any
+    // barrier, tensor-memory or cluster operation.
+    if (prm.ring_epi) {
+        const int64_t tiles = static_cast<int64_t>(prm.tiles_p) * prm.tiles_q;
+        const int64_t units = prm.full_units + (tiles - prm.full_units / prm.splits) * prm.tail_f;
+        const int64_t slots = PAIR ? gridDim.x / 2 : gridDim.x;
+        if (LOADS || units > slots ||
+            static_cast<int64_t>(prm.stages) * prm.stage_bytes >
+                static_cast<int64_t>(TcCfg<IN, PAIR, LOADS, HALF, NI>::kOffBars)) {
+            if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(prm.watchdog, kWatchBadParams);
+            return;
+        }
+    }
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1066,24 +1081,24 @@ TcGeometry tc_geometry_impl(bool pair, bool half) {
         using Cfg = TcCfg<IN, true, false, true>;
         return TcGeometry{Cfg::kTileP,  Cfg::kMmaN,    Cfg::kBlockP,      Cfg::kStageK,
                           2,            Cfg::kMmaM,    Cfg::kFormat,      Cfg::kStageRegion,
-                          Cfg::kMaxStages};
+                          Cfg::kMaxStages, Cfg::kEpiBytes};
     }
     if (half) {
         using Cfg = TcCfg<IN, false, false, true>;
         return TcGeometry{Cfg::kTileP,  Cfg::kMmaN,    Cfg::kBlockP,      Cfg::kStageK,
                           1,            Cfg::kMmaM,    Cfg::kFormat,      Cfg::kStageRegion,
-                          Cfg::kMaxStages};
+                          Cfg::kMaxStages, Cfg::kEpiBytes};
     }
     if (pair) {
         using Cfg = TcCfg<IN, true, false>;
         return TcGeometry{Cfg::kTileP,  Cfg::kMmaN,    Cfg::kBlockP,      Cfg::kStageK,
                           2,            Cfg::kMmaM,    Cfg::kFormat,      Cfg::kStageRegion,
-                          Cfg::kMaxStages};
+                          Cfg::kMaxStages, Cfg::kEpiBytes};
     }
     using Cfg = TcCfg<IN, false, false>;
     return TcGeometry{Cfg::kTileP,  Cfg::kMmaN,    Cfg::kBlockP,      Cfg::kStageK,
                       1,            Cfg::kMmaM,    Cfg::kFormat,      Cfg::kStageRegion,
-                      Cfg::kMaxStages};
+                      Cfg::kMaxStages, Cfg::kEpiBytes};
 }
 
 }  // namespace gb300

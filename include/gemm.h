@@ -209,7 +209,9 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
  *                    (0/1; else along M), ring stages, grid (CTAs), A repacked,
  *                    B repacked, tiles along N, tiles along M, K stages per
  *                    piece, K stages per last-wave piece, ring stage bytes,
- *                    MMA-issuing warps (1 or 2), K atoms per ring stage (1 or 2).
+ *                    MMA-issuing warps (1 or 2), K atoms per ring stage (1 or 2),
+ *                    ring over the epilogue's staging area (0/1: only where every
+ *                    CTA or CTA pair runs one unit).
  *
  * Returns GEMM_OK, GEMM_ERR_INVALID_DIM or GEMM_ERR_INVALID_OPTION (kind, out
  * or nout).  A call that would be refused reports its status in out[0]
@@ -226,7 +228,7 @@ int gemm_fp8_tn_f32(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
 #define GEMM_PLAN_A_128 8
 #define GEMM_PLAN_B_128 16
 #define GEMM_PLAN_NOALLOC 32
-#define GEMM_PLAN_FIELDS 19
+#define GEMM_PLAN_FIELDS 20
 int gemm_tn_plan(int kind, int64_t M, int64_t N, int64_t K, int flags, int64_t workspace_bytes,
                  int sms, int64_t* out, int nout);
 
@@ -239,8 +241,10 @@ const char* gemm_status_string(int status);
  * a time limit (gemm_set_option "timeout_ns"), records GEMM_ERR_TIMEOUT in a
  * per-device status word and lets its kernel exit cleanly instead of hanging.
  * This call synchronises the current device, returns GEMM_OK when no wait has
- * run out since the last reset, GEMM_ERR_TIMEOUT when one has, and
- * GEMM_ERR_LAUNCH on a CUDA error.  reset != 0 clears the word.
+ * run out since the last reset, GEMM_ERR_TIMEOUT when one has (or when a
+ * kernel refused launch parameters that break one of its invariants, which
+ * the library's planner does not produce), and GEMM_ERR_LAUNCH on a CUDA
+ * error.  reset != 0 clears the word.
  */
 int gemm_read_watchdog(int reset);
 

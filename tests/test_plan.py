@@ -98,19 +98,28 @@ def test_narrow_ring_is_deeper(options):
     """A 16-column one-CTA tile's one-atom stage holds 16 KB of B and 2 KB of
     A: 10 stages of 18 KB in the 192 KB ring, against 8 of 24 KB at 64
     columns; with two atoms per stage (the automatic choice there), 5 of 36 KB
-    and 4 of 48 KB (K split, one issuer)."""
-    def ring(M):
-        p = plan("bf16", M, 8192, 8192, workspace_bytes=WS)
+    and 4 of 48 KB (K split, one issuer).  With one unit per CTA the ring also
+    takes the epilogue's staging area (224 KB): 6 of 36 KB, still 4 of 48 KB;
+    with one atom and two issuers (unsplit) 12 of 18 KB and 8 of 24 KB."""
+    def ring(M, **kw):
+        p = plan("bf16", M, 8192, 8192, workspace_bytes=WS, **kw)
         assert p["pair"] == 0 and p["issuers"] == 1, p
         return p["stages"], p["stage_bytes"]
-    assert ring(16) == (5, 36 * 1024)
+    assert ring(16) == (6, 36 * 1024)
     assert ring(64) == (4, 48 * 1024)
+    options("max_ctas", 32)                     # 64 tiles on 32 CTAs: 192 KB
+    p = plan("bf16", 16, 8192, 8192, workspace_bytes=WS)
+    assert (p["ring_epi"], p["issuers"], p["stages"], p["stage_bytes"]) == (0, 1, 5, 36 * 1024)
+    options("max_ctas", 0)
     options("half", 2)
     options("atoms", 1)
     assert (plan("bf16", 16, 8192, 8192)["stages"], plan("bf16", 16, 8192, 8192)["stage_bytes"]) \
-        == (10, 18 * 1024)
+        == (12, 18 * 1024)
     assert (plan("bf16", 64, 8192, 8192)["stages"], plan("bf16", 64, 8192, 8192)["stage_bytes"]) \
         == (8, 24 * 1024)
+    options("max_ctas", 32)                     # two units per CTA: the 192 KB ring
+    assert (plan("bf16", 16, 8192, 8192)["stages"], plan("bf16", 16, 8192, 8192)["stage_bytes"]) \
+        == (10, 18 * 1024)
 
 
 def test_atoms_rule(options):
@@ -362,17 +371,58 @@ def test_two_issuers_get_an_even_ring(options):
                 assert p["stages"] % 2 == 0, (kind, M, N, K, p)
                 seen[p["atoms"]] += 1
     assert seen[1] >= 4 and seen[2] >= 6, seen
+    options("max_ctas", 64)      # 64 pairs on 32 pair slots: the 192 KB ring
     p = plan("bf16", 192, 8192, 8192, workspace_bytes=WS)   # 20 KB stages: nine fit, eight run
-    assert (p["half"], p["tile_q"], p["atoms"], p["stages"]) == (1, 192, 1, 8)
-    p = plan("bf16", 16, 8192, 8192)                         # halves 32 wide: 19 fit, 18 run
-    assert (p["half"], p["tile_q"], p["atoms"], p["stages"]) == (1, 32, 1, 18)
-    # one-CTA 16-wide tiles: 36 KB stages, five fit; the two-issuer plan keeps four
+    assert (p["half"], p["tile_q"], p["atoms"], p["stages"], p["ring_epi"]) == (1, 192, 1, 8, 0)
+    options("max_ctas", 0)       # one pair tile each: 224 KB, eleven fit, ten run
+    p = plan("bf16", 192, 8192, 8192, workspace_bytes=WS)
+    assert (p["half"], p["tile_q"], p["atoms"], p["stages"], p["ring_epi"]) == (1, 192, 1, 10, 1)
+    p = plan("bf16", 16, 8192, 8192)                         # halves 32 wide: 20 barrier slots
+    assert (p["half"], p["tile_q"], p["atoms"], p["stages"]) == (1, 32, 1, 20)
+    # one-CTA 16-wide tiles: 36 KB stages, six fit in 224 KB (one tile per CTA)
     p = plan("bf16", 16, 16384, 8192, workspace_bytes=WS)
-    assert (p["pair"], p["tile_q"], p["issuers"], p["atoms"], p["stages"]) == (0, 16, 2, 2, 4)
-    # one issuer (the split plan) keeps all five
+    assert (p["pair"], p["tile_q"], p["issuers"], p["atoms"], p["stages"]) == (0, 16, 2, 2, 6)
+    # one issuer (the split plan) takes all six
     p = plan("bf16", 16, 8192, 8192, workspace_bytes=WS)
-    assert (p["splits"], p["issuers"], p["atoms"], p["stages"]) == (2, 1, 2, 5)
+    assert (p["splits"], p["issuers"], p["atoms"], p["stages"]) == (2, 1, 2, 6)
+    # two tiles per CTA: five fit in the 192 KB ring; one issuer takes them
+    # all, two (forced) keep four
+    options("max_ctas", 64)
+    p = plan("bf16", 16, 16384, 8192, workspace_bytes=WS)
+    assert (p["tile_q"], p["atoms"], p["ring_epi"], p["issuers"], p["stages"]) == (16, 2, 0, 1, 5)
+    options("issuers", 2)
+    p = plan("bf16", 16, 16384, 8192, workspace_bytes=WS)
+    assert (p["tile_q"], p["atoms"], p["ring_epi"], p["issuers"], p["stages"]) == (16, 2, 0, 2, 4)
+    options("issuers", 0)
+    options("max_ctas", 0)
     options("issuers", 2)
     options("pair", 0)
     p = plan("bf16", 100, 1100, 1000)                   # 64 KB stages: three fit, two run
     assert (p["tile_q"], p["issuers"], p["atoms"], p["stages"]) == (128, 2, 2, 2)
+
+
+def test_ring_over_the_epilogue_area(options):
+    """Where every CTA (or pair) runs one unit, the ring also takes the
+    epilogue's 32 KB staging area (224 KB instead of 192), still rounded to an
+    even depth with two issuers; plans with several units per CTA, a cut last
+    wave or the load-based producer keep 192 KB."""
+    def ring(kind, M, N, K, **kw):
+        p = plan(kind, M, N, K, workspace_bytes=WS, **kw)
+        return p["ring_epi"], p["stages"], p["stage_bytes"]
+    assert ring("bf16", 192, 8192, 8192) == (1, 10, 20 * 1024)     # halves 192 wide: 8 -> 10
+    assert ring("bf16", 160, 8192, 8192) == (1, 12, 18 * 1024)     # 10 -> 12
+    assert ring("bf16", 16, 8192, 8192) == (1, 6, 36 * 1024)       # split, one issuer: 5 -> 6
+    assert ring("bf16", 2048, 2048, 2048) == (1, 7, 32 * 1024)     # 64 pair tiles: 6 -> 7
+    assert ring("bf16", 128, 8192, 8192)[0] == 0                   # 7 rounds down to 6
+    assert ring("bf16", 256, 8192, 8192)[0] == 0                   # 9 rounds down to 8
+    assert ring("f16", 8192, 8192, 8192)[0] == 0                   # several tiles per pair
+    assert ring("bf16", 4096, 4096, 4096)[0] == 0
+    options("max_ctas", 64)
+    assert ring("bf16", 192, 8192, 8192)[0] == 0                   # 64 tiles on 32 pairs
+    options("max_ctas", 0)
+    options("tail", 2)
+    assert ring("bf16", 512, 8192, 4096)[0] == 0                   # narrowed last wave
+    options("tail", 0)
+    flags = ALIGNED & ~(capi.PLAN_A_TMA | capi.PLAN_A_128)
+    p = plan("bf16", 130, 300, 257, flags=flags)                   # load-based producer
+    assert p["producer"] == 1 and p["ring_epi"] == 0
