@@ -598,10 +598,12 @@ TnPlan plan_tn_once(const TnPlanIn& a) {
     if (p.issuers > 1 && (p.stages & 1) && p.stages > 2) --p.stages;
     // Where every CTA (or pair) runs one unit, its epilogue starts only after
     // the ring has drained, so the ring may run on over the epilogue's staging
-    // area (224 KB instead of 192).  These launches stream operands for most
-    // of their time and gain from the loads in flight (the even-ring
-    // measurement above: 12 % fewer bytes in flight cost 3 %).
-    if (p.prod == Producer::Tma && p.tail_f == 1 && !p.tail_ksplit &&
+    // area (224 KB instead of 192).  Pairs of 64-row halves gain from the
+    // loads in flight (graph-replayed BF16 on GB300, 192 KB -> 224 KB: width
+    // 192 29.9 -> 28.5 us, 160 28.0 -> 27.6, 224 30.5 -> 29.0, 192 x 8192 x
+    // 16384 54.2 -> 51.6); the split one-CTA 16-wide tiles (25.6 -> 26.0) and
+    // 2048^3 pairs (15.3 -> 15.6) lost, so only pairs of halves take it.
+    if (p.prod == Producer::Tma && p.pair && p.half && p.tail_f == 1 && !p.tail_ksplit &&
         p.tiles * p.splits <= p.slots) {
         int st = (g.stage_region + g.epi_region) / p.stage_bytes;
         if (st > g.max_stages) st = g.max_stages;

@@ -1,15 +1,15 @@
 """GPU parity of rings that run on over the epilogue's staging area (plan field
 ring_epi = 1) against the CPU oracle, through the C ABI.
 
-Where every CTA (or CTA pair) runs one unit, the ring takes the epilogue's 32
-KB of staging buffers as well; the epilogue writes them only after the
-accumulator-full barrier, when every load has been consumed and every MMA has
-completed.  These cases cover the plans that do so -- pairs of 64-row halves
-(widths 160 and 192, one and two issuers), CTA pairs 256 wide, one-CTA tiles,
-split K through the workspace -- on every input kind, with K from one ring's
-worth to many ring cycles, TMA and row-wise stores, FP32 output, and +-1
-inputs (exact: a stage overwritten by the epilogue while still in use, or a
-staged chunk overwritten by a load, would show)."""
+Where every CTA pair of a plan of 64-row halves runs one unit, the ring takes
+the epilogue's 32 KB of staging buffers as well; the epilogue writes them only
+after the accumulator-full barrier, when every load has been consumed and every
+MMA has completed.  These cases cover that on every input kind, at widths 32,
+64, 160, 192 and 224 with one and two issuers, with K from less than one ring
+to many ring cycles, TMA and row-wise stores, FP32 output, and +-1 inputs
+(exact: a stage overwritten by the epilogue while still in use, or a staged
+chunk overwritten by a load, would show); and that the other plans keep the
+192 KB ring."""
 import numpy as np
 import pytest
 import torch
@@ -55,13 +55,13 @@ def exact(kind, M, N, K, seed, ldc=None):
 
 
 PLANS = {
-    # name: (options, M, N) -- each plan runs one unit per CTA or pair
+    # name: (options, M, N) -- pairs of halves, one unit per pair
     "halves_192": ({"half": 3, "tile_q": 192}, 190, 2000),
     "halves_160_one_issuer": ({"half": 3, "issuers": 1}, 150, 2000),
     "halves_160": ({"half": 3}, 160, 1000),
-    "pairs_256": ({"pair": 1}, 700, 1000),
-    "one_cta_128": ({"pair": 0}, 300, 1500),
-    "split_16": ({}, 16, 2048),
+    "halves_224": ({"half": 3}, 210, 1500),
+    "halves_32": ({"half": 3}, 20, 2000),
+    "halves_64": ({"half": 3}, 48, 1000),
 }
 
 
@@ -70,23 +70,30 @@ PLANS = {
 @pytest.mark.parametrize("K", [200, 2048, 8200])
 def test_pm1_bitexact(kind, name, K, opts):
     o, M, N = PLANS[name]
-    if kind == "e4m3" and name.startswith("halves"):
-        o = dict(o, tile_q=0) if "tile_q" in o else o
     for k, v in o.items():
         opts(k, v)
     p = planned(kind, M, N, K, opts.ws)
-    # a last wave cut into narrower units (short K on CTA pairs) gives some
-    # CTAs two units: then the ring stays short
-    assert p["ring_epi"] == (1 if p["tail_f"] == 1 else 0), (name, p)
-    if name == "split_16" and K >= 2048:
-        assert p["splits"] > 1, p
+    assert (p["pair"], p["half"], p["ring_epi"]) == (1, 1, 1), (name, p)
     exact(kind, M, N, K, seed=M + K)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("M,N,K,pair", [(16, 2048, 2048, -1), (700, 1000, 2048, 1),
+                                        (300, 1500, 1000, 0)])
+def test_other_plans_keep_the_short_ring(kind, M, N, K, pair, opts):
+    """Split one-CTA tiles, CTA pairs 256 wide and one-CTA tiles 128 wide run
+    one unit per CTA too, but measured slower with the longer ring."""
+    opts("pair", pair)
+    p = planned(kind, M, N, K, opts.ws)
+    assert p["half"] == 0 and p["ring_epi"] == 0, p
+    exact(kind, M, N, K, seed=M)
 
 
 @pytest.mark.parametrize("ldc_pad", [3, 8])
 def test_row_wise_and_padded_stores(ldc_pad, opts):
     """ldc = M + 3: row-wise stores through the staging buffers; ldc = M + 8:
-    TMA stores; the padding keeps its sentinel."""
+    TMA stores (and lane stores for the halves' cut chunks); the padding keeps
+    its sentinel."""
     opts("half", 3)
     M, N, K = 171, 900, 1024
     p = planned("bf16", M, N, K, opts.ws)
@@ -98,10 +105,11 @@ def test_row_wise_and_padded_stores(ldc_pad, opts):
 def test_fp8_f32_output(opts):
     from test_fp8_f32out_gpu import run, tols
 
-    M, N, K = 16, 2048, 1024
+    opts("half", 3)
+    M, N, K = 150, 2048, 1024
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     st, p = capi.gemm_tn_plan("e4m3_f32out", M, N, K, workspace_bytes=opts.ws.numel(), sms=sms)
-    assert st == 0 and p["ring_epi"] == 1, p
+    assert st == 0 and (p["half"], p["tile_q"], p["ring_epi"]) == (1, 160, 1), p
     ops = si.tn_operands("e4m3", M, N, K, dist="normal", seed=M)
     C = run(ops, M, N, K)
     ref = oracle.gemm_tn("e4m3", M, N, K, si.codes(ops["A"]), K, si.codes(ops["B"]), K,
@@ -114,9 +122,11 @@ def test_fp8_f32_output(opts):
 
 
 @pytest.mark.parametrize("kind,shape", [("bf16", (192, 8192, 8192)), ("f16", (160, 8192, 16384)),
-                                        ("bf16", (16, 8192, 8192)), ("bf16", (2048, 2048, 2048))])
+                                        ("bf16", (224, 8192, 8192)), ("e4m3", (200, 8192, 8192))])
 def test_full_size_sampled(kind, shape, opts):
     M, N, K = shape
+    if kind == "e4m3":
+        opts("half", 3)
     assert planned(kind, M, N, K, opts.ws)["ring_epi"] == 1
     ops = si.tn_operands(kind, M, N, K, dist="normal", seed=5, sigma=0.05)
     C = run_tn(kind, ops, M, N, K)
