@@ -117,16 +117,23 @@ def test_automatic_choice(capfd):
     """64-row tiles run only when forced (measured slower than 128-row tiles
     with K split in two on every skinny shape tried).  Skinny shapes whose M
     fits in 16 or 32 columns take that narrower tile instead, which leaves room
-    for more ring stages of B."""
+    for more ring stages of B.  Without a workspace (no split) 16-bit skinny
+    shapes with M <= 64 run pairs of 64-row halves 32 or 64 wide."""
+    ws = torch.empty(1 << 26, dtype=torch.uint8, device="cuda")
+    assert capi.gemm_set_workspace(ws.data_ptr(), ws.numel()) == 0
     assert capi.gemm_set_option("half", 0) == 0
-    line = _chosen(capfd, 16, 8192, 1024)
-    assert "half=0" in line and "tile_q=16" in line, line
-    assert "tile_q=32" in _chosen(capfd, 20, 8192, 1024)
-    assert "tile_q=64" in _chosen(capfd, 48, 8192, 1024)
-    assert capi.gemm_set_option("half", 1) == 0
     try:
+        line = _chosen(capfd, 16, 8192, 1024)
+        assert "pair=0" in line and "half=0" in line and "tile_q=16" in line, line
+        assert "tile_q=32" in _chosen(capfd, 20, 8192, 1024)
+        assert "tile_q=64" in _chosen(capfd, 48, 8192, 1024)
+        assert capi.gemm_set_option("half", 1) == 0
         line = _chosen(capfd, 16, 8192, 1024)
         assert "half=1" in line and "splits=1" in line and "grid=128" in line, line
         assert "half=0" in _chosen(capfd, 2048, 2048, 1024)   # CTA pairs: not applied
     finally:
         capi.gemm_set_option("half", 0)
+        capi.gemm_set_workspace(None, 0)
+    for M, width in ((16, 32), (48, 64)):
+        line = _chosen(capfd, M, 8192, 1024)
+        assert "pair=1" in line and "half=1" in line and f"tile_q={width}" in line, line
