@@ -19,7 +19,8 @@ the time is the maximum over ranks and `value` counts every rank's work.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--no-per-config]
-  python bench.py --ncu-case bf16:128x8192x8192   (launches for a profiler capture)
+  python bench.py --ncu-case bf16:128x8192x8192[:half=3,workspace=0]
+                  (launches for a profiler capture, with library options if given)
 """
 from __future__ import annotations
 
@@ -926,21 +927,50 @@ def run_reference(args):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def parse_ncu_case(spec: str):
+    """KIND:MxNxK[:name=value,...] -> (kind, M, N, K, options, workspace).  The
+    optional third field sets library options (gemm_set_option) for the
+    case; workspace=0 runs it without the bench workspace."""
+    parts = spec.split(":")
+    if len(parts) not in (2, 3):
+        raise ValueError("expected KIND:MxNxK[:name=value,...], got %r" % spec)
+    kind = parts[0]
+    M, N, K = (int(x) for x in parts[1].lower().split("x"))
+    options, workspace = {}, True
+    if len(parts) == 3 and parts[2]:
+        for item in parts[2].split(","):
+            name, value = item.split("=")
+            if name == "workspace":
+                workspace = int(value) != 0
+            else:
+                options[name] = int(value)
+    return kind, M, N, K, options, workspace
+
+
 def ncu_case(spec: str):
     """A few launches of one TN shape for profiler captures: three rounds of
     this library's call followed by cuBLAS's (torch.matmul) on the same
-    operands, with the bench workspace registered.  Nothing is timed; the
-    line only names the case.  FP8 runs this library's call alone."""
+    operands, with the bench workspace registered (unless the spec says
+    workspace=0) and any options the spec names set for the case.  Nothing is
+    timed; the line only names the case and the plan.  FP8 runs this
+    library's call alone."""
     import torch
 
     from dense_gemm_tcgen05_gb300 import capi
 
-    kind, dims = spec.split(":")
-    M, N, K = (int(x) for x in dims.lower().split("x"))
+    kind, M, N, K, options, use_ws = parse_ncu_case(spec)
     if kind == "f32":
         return ncu_case_f32(M, N, K)
-    workspace = torch.empty(WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
-    assert capi.gemm_set_workspace(workspace.data_ptr(), workspace.numel()) == 0
+    for name, value in options.items():
+        if capi.gemm_set_option(name, value) != 0:
+            raise ValueError("invalid option %s=%d" % (name, value))
+    workspace = torch.empty(WORKSPACE_BYTES, dtype=torch.uint8, device="cuda") if use_ws else None
+    if use_ws:
+        assert capi.gemm_set_workspace(workspace.data_ptr(), workspace.numel()) == 0
+    plan_kind = {"f16": "f16", "bf16": "bf16", "e4m3": "e4m3"}[kind]
+    st, plan = capi.gemm_tn_plan(plan_kind, M, N, K,
+                                 workspace_bytes=workspace.numel() if use_ws else 0,
+                                 sms=torch.cuda.get_device_properties(0).multi_processor_count)
     _, sets = tn_sets(kind, M, N, K, 2, 0.1, 2, "cuda")
     stream = torch.cuda.Stream()
     call = tn_call(kind, M, N, K, 1.0, 1.0, stream.cuda_stream)
@@ -951,8 +981,11 @@ def ncu_case(spec: str):
             if kind != "e4m3":
                 torch.matmul(b, a.T, out=c)      # C column-major = (B A^T) row-major
     torch.cuda.synchronize()
-    assert capi.gemm_set_workspace(None, 0) == 0
-    return {"ncu_case": spec, "launches_each": 3, "cublas": kind != "e4m3"}
+    if use_ws:
+        assert capi.gemm_set_workspace(None, 0) == 0
+    for name in options:
+        capi.gemm_set_option(name, -1 if name == "pair" else 0)
+    return {"ncu_case": spec, "launches_each": 3, "cublas": kind != "e4m3", "plan": plan}
 
 
 def ncu_case_f32(M, N, K):
@@ -994,9 +1027,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-main", action="store_true",
                     help="time the main workload only (for profiler runs)")
-    ap.add_argument("--ncu-case", metavar="KIND:MxNxK",
+    ap.add_argument("--ncu-case", metavar="KIND:MxNxK[:name=value,...]",
                     help="launch one shape (f16/bf16/e4m3 TN, or f32) three times, and cuBLAS "
-                         "beside it, for ncu")
+                         "beside it, for ncu; the optional third field sets library options "
+                         "(workspace=0: no workspace)")
     args = ap.parse_args(argv)
     if args.ncu_case:
         print(json.dumps(ncu_case(args.ncu_case)), flush=True)

@@ -180,3 +180,16 @@ def test_spread():
     s = bench.spread([1.0, 3.0, 2.0, 4.0])
     assert (s["mean_ms"], s["median_ms"], s["min_ms"], s["max_ms"], s["launches"]) == (
         2.5, 2.5, 1.0, 4.0, 4)
+
+
+def test_ncu_case_spec():
+    """--ncu-case: KIND:MxNxK with an optional third field of library options;
+    workspace=0 drops the bench workspace."""
+    assert bench.parse_ncu_case("bf16:128x8192x8192") == ("bf16", 128, 8192, 8192, {}, True)
+    assert bench.parse_ncu_case("f16:16x8192x8192:half=3,workspace=0") == \
+        ("f16", 16, 8192, 8192, {"half": 3}, False)
+    assert bench.parse_ncu_case("e4m3:64X512X256:tile_q=192,pair=1") == \
+        ("e4m3", 64, 512, 256, {"tile_q": 192, "pair": 1}, True)
+    for bad in ("bf16", "bf16:1x2", "bf16:1x2x3:half", "bf16:1x2x3:a=1:b=2"):
+        with pytest.raises(ValueError):
+            bench.parse_ncu_case(bad)
