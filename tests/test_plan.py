@@ -422,3 +422,59 @@ def test_ring_over_the_epilogue_area(options):
     flags = ALIGNED & ~(capi.PLAN_A_TMA | capi.PLAN_A_128)
     p = plan("bf16", 130, 300, 257, flags=flags)                   # load-based producer
     assert p["producer"] == 1 and p["ring_epi"] == 0
+
+
+def _sweep_shapes():
+    Ms = (1, 7, 16, 17, 32, 33, 48, 64, 65, 96, 100, 128, 129, 150, 160, 176, 192, 200, 224,
+          225, 255, 256, 257, 384, 1000, 2048, 8192)
+    Ns = (64, 1000, 4096, 8192, 9728, 16384)
+    Ks = (64, 200, 2048, 8192)
+    for M in Ms:
+        for N in Ns:
+            for K in Ks:
+                yield M, N, K
+
+
+@pytest.mark.parametrize("kind", ["f16", "bf16", "e4m3", "e4m3_f32out"])
+def test_ring_layout_invariants(kind, options):
+    """Over a grid of shapes, with and without a workspace, automatic and with
+    pairs of halves forced: the ring fits its region (192 KB, or 224 KB when it
+    runs on over the epilogue's staging area), stays within the 20 barrier
+    slots, keeps 1024-byte stages, is even with two issuers, and runs over the
+    staging area only for pairs of halves whose pairs run one unit each."""
+    for forced in (0, 3):
+        options("half", forced)
+        for M, N, K in _sweep_shapes():
+            for ws in (0, WS):
+                p = plan(kind, M, N, K, workspace_bytes=ws)
+                if p["status"] != 0:
+                    continue
+                region = (224 if p["ring_epi"] else 192) * 1024
+                assert p["stages"] * p["stage_bytes"] <= region, (M, N, K, ws, p)
+                assert 2 <= p["stages"] <= 20 and p["stage_bytes"] % 1024 == 0, p
+                if p["issuers"] == 2:
+                    assert p["stages"] % 2 == 0, (M, N, K, ws, p)
+                if p["ring_epi"]:
+                    units = p["tiles_p"] * p["tiles_q"] * p["splits"]
+                    slots = p["grid"] // 2
+                    assert (p["pair"], p["half"], p["producer"], p["tail_f"]) == (1, 1, 0, 1), p
+                    assert units <= slots, (M, N, K, ws, p)
+                if p["atoms"] == 2 and p["pair"] and p["half"]:
+                    assert p["tile_q"] == 128, p
+    options("half", 0)
+
+
+@pytest.mark.parametrize("kind,out_bytes", [("bf16", 2), ("f16", 2), ("e4m3", 2), ("e4m3_f32out", 4)])
+def test_halves_widths_keep_stores_aligned(kind, out_bytes, options):
+    """Pairs of 64-row halves: the width is a multiple of 32 from 32 to 256, so
+    each half starts 16 * k bytes into the tile (its TMA stores need a 16-byte
+    aligned innermost coordinate), and a CTA's A box is at most 128 rows."""
+    options("half", 3)
+    for M in range(1, 300):
+        p = plan(kind, M, 8192, 2048)
+        if not (p["pair"] and p["half"]):
+            continue
+        w = p["tile_q"]
+        assert w % 32 == 0 and 32 <= w <= 256, (M, p)
+        assert (w // 2 * out_bytes) % 16 == 0 and (w * out_bytes) % 16 == 0, (M, p)
+        assert M > 256 or w >= M, (M, p)                      # one column of tiles
